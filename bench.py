@@ -1,0 +1,437 @@
+"""Benchmark of the IBP gather-decompression hot path on GB300.
+
+Default workload (the headline): sparse GNN features, 2,000,000 rows x 128
+fp32 (512 B rows, 1 GB) compressed in place into pinned host slots (chunk
+1 KB, Mask/Bitval from a 1 % sample at T = 0.95).  One step = one
+ibp_gather_decompress of 200,000 uniform-random row ids: every stored byte is
+read zero-copy over the host link by the kernel and 102.4 MB of rows are
+written to HBM.
+
+Reported (one JSON line on rank 0): delivered decompressed GB/s (value), its
+fraction of the roofline min(HBM peak, link GB/s / ratio) where the link
+bandwidth is measured in the same run by the aligned zero-copy copy kernel,
+the end-to-end number through the C ABI with host buffers, the raw-gather
+baseline, clocks, and the CPU oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload sparse|tiny]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": PEAKS_FALLBACK["hbm_gbs"], "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) over the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload setup
+class SparseStore:
+    """Sparse-GNN feature store compressed into pinned host slots by the GPU."""
+
+    def __init__(self, torch, ibp, wl, dev, n_rows=2_000_000, dim=128, chunk=1024,
+                 per_mille=10, num=95, den=100, seed=0, keep_raw=True):
+        self.n_rows, self.R, self.C = n_rows, dim * 4, chunk
+        t0 = time.time()
+        rows = np.empty((n_rows, dim), np.float32)
+        wl.sparse_gnn_rows(n_rows, dim, seed=seed, out=rows)
+        log("generated %d x %d rows in %.1fs" % (n_rows, dim, time.time() - t0))
+        self.rows_np = rows
+        self.st = ibp.ibp_store_create(self.R, chunk, n_rows, 0)
+        self.slot = ibp.ibp_store_get_info(self.st).slot_bytes
+        self.slots = torch.empty((n_rows, self.slot), dtype=torch.uint8, pin_memory=True)
+        d_rows = torch.from_numpy(rows.view(np.uint8)).to(dev)
+        sample = wl.sample_ids(n_rows, per_mille, seed=seed)
+        self.sample = sample
+        d_sample = torch.from_numpy(sample).to(dev)
+        ibp.ibp_build_meta(self.st, d_rows, self.R, d_sample, len(sample), num, den)
+        self.stored = torch.empty(n_rows, dtype=torch.int32, device=dev)
+        ibp.ibp_compress(self.st, self.slots, d_rows, self.R, None, n_rows, self.stored)
+        torch.cuda.synchronize()
+        assert ibp.ibp_stream_status(self.st, reset=True) == ibp.IBP_OK
+        self.raw_host = None
+        if keep_raw:  # uncompressed host copy: the raw-gather baseline
+            self.raw_host = torch.empty((n_rows, self.slot), dtype=torch.uint8, pin_memory=True)
+            self.raw_host[:, :self.R].copy_(torch.from_numpy(rows.view(np.uint8)))
+        del d_rows
+        torch.cuda.empty_cache()
+        self.stored_np = self.stored.cpu().numpy().astype(np.int64)
+        log("store ready in %.1fs (ratio over all rows %.4f)" % (
+            time.time() - t0, self.stored_np.sum() / (n_rows * self.R)))
+
+    def close(self, ibp):
+        ibp.ibp_store_destroy(self.st)
+
+
+def cpu_oracle_decode(store, ids, mask, bitval, bitmap, threads):
+    from oracle import ref_c
+    slots = store.slots.numpy()
+    out, bad = ref_c.decompress_batch(slots, bitmap, store.R, store.C, mask, bitval, ids=ids,
+                                      slot_stride=store.slot, nthreads=threads)
+    return out, bad
+
+
+# ------------------------------------------------------------------ arms
+def run_ours(args, rank, world, torch, dist):
+    from lossless_invariant_bit_gb300 import ibp
+    from lossless_invariant_bit_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks = measured_peaks()
+    store = SparseStore(torch, ibp, wl, dev, seed=args.seed)
+    R, n = store.R, args.batch
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    # --- link probe: aligned zero-copy host -> HBM copy of 1 GB (best of 5)
+    probe_bytes = (store.slots.numel() // 16) * 16
+    probe_dst = torch.empty(probe_bytes, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        ibp.ibp_link_copy(probe_dst, store.slots, probe_bytes, sp)
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ibp.ibp_link_copy(probe_dst, store.slots, probe_bytes, sp)
+        e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3
+        best = t if best is None else min(best, t)
+    link_gbs = probe_bytes / best / 1e9
+    del probe_dst
+    torch.cuda.empty_cache()
+    log("link probe: %.1f GB/s host->HBM" % link_gbs)
+
+    # --- batches (each rank its own ids: weak scaling)
+    total = args.warmup + args.steps
+    ids_np = [wl.uniform_ids(n, store.n_rows, seed=args.seed, batch=rank * 100000 + b)
+              for b in range(total)]
+    ids_dev = [torch.from_numpy(x).to(dev) for x in ids_np]
+    out = torch.empty((n, R), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ratios = [float(store.stored_np[x].sum()) / (n * R) for x in ids_np]
+
+    def step_device(b):
+        ibp.ibp_gather_decompress(store.st, out, store.slots, None, ids_dev[b], n, sp)
+
+    def timed(fn, steps_from, count, pre=None):
+        evs = []
+        for b in range(steps_from, steps_from + count):
+            flush.zero_()  # L2 flush, outside the timed events
+            if pre:
+                pre(b)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(b)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(c) / 1e3 for a, c in evs]
+
+    for b in range(args.warmup):
+        step_device(b)
+    torch.cuda.synchronize()
+    assert ibp.ibp_stream_status(store.st, reset=True) == ibp.IBP_OK
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        times = timed(step_device, args.warmup, args.steps)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    assert ibp.ibp_stream_status(store.st, reset=True) == ibp.IBP_OK
+    t_total = sum(times)
+    if dist:
+        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_total = float(tt.item())
+    rows_all = n * args.steps * world
+    value = rows_all * R / t_total / 1e9
+    t_launch = statistics.mean(times)
+    ratio = statistics.mean(ratios[args.warmup:])
+
+    # parity spot check of the last timed batch against the oracle (rows sampled)
+    last = args.warmup + args.steps - 1
+    ibp.ibp_gather_decompress(store.st, out, store.slots, None, ids_dev[last], n, sp)
+    torch.cuda.synchronize()
+    pick = np.random.default_rng(1).choice(n, size=2000, replace=False)
+    got = out[torch.from_numpy(pick).to(dev)].cpu().numpy()
+    want = store.rows_np.view(np.uint8)[ids_np[last][pick]]
+    parity_ok = bool(np.array_equal(got, want))
+
+    # --- raw gather baseline (uncompressed rows over the same link)
+    raw_times = timed(lambda b: ibp.ibp_gather_copy(out, store.raw_host, store.slot, R,
+                                                    ids_dev[b], n, store.n_rows, sp),
+                      args.warmup, args.steps)
+    raw_gbs = n * R * len(raw_times) / sum(raw_times) / 1e9
+
+    # --- end to end through the C ABI with host buffers: ids H2D, kernel, rows D2H
+    ids_host = [torch.from_numpy(x).pin_memory() for x in ids_np]
+    out_host = torch.empty((n, R), dtype=torch.uint8, pin_memory=True)
+    ids_buf = torch.empty(n, dtype=torch.int64, device=dev)
+
+    def step_e2e(b):
+        ids_buf.copy_(ids_host[b], non_blocking=True)
+        ibp.ibp_gather_decompress(store.st, out, store.slots, None, ids_buf, n, sp)
+        out_host.copy_(out, non_blocking=True)
+
+    for b in range(args.warmup):
+        step_e2e(b)
+    e2e_times = timed(step_e2e, args.warmup, args.steps)
+    t_e2e = sum(e2e_times)
+    if dist:
+        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e_gbs = n * R * args.steps * world / t_e2e / 1e9
+
+    # --- the dominant kernel's roofline
+    hbm = peaks["hbm_gbs"]
+    roof = min(hbm, link_gbs / ratio)
+    delivered_per_launch = n * R / t_launch / 1e9
+    algo_bytes = sum(float(store.stored_np[x].sum()) + n * R + 8 * n
+                     for x in ids_np[args.warmup:]) / args.steps
+    result = {
+        "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
+        "value": round(value, 3),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_total / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u32",
+        "data": "synthetic (seeded numpy: sparse GNN features, 1.0 w.p. 0.01 else 0.0)",
+        "config": {
+            "workload": "sparse GNN gather-decompress: 2,000,000 x 128 fp32 rows in pinned "
+                        "host slots, chunk 1 KB, 1% sample, T=0.95, batches of 200,000 "
+                        "uniform ids",
+            "rows": store.n_rows, "row_bytes": R, "chunk_bytes": store.C,
+            "batch_ids": n, "source": "pinned host (zero-copy)",
+            "l2": "flushed between steps (256 MB write, outside the timed events)",
+            "parallelism": "dp%d (id batches sharded, no collective)" % world,
+        },
+        "ratio": round(ratio, 5),
+        "link_gbs": round(link_gbs, 2),
+        "raw_gather_gbs": round(raw_gbs, 2),
+        "speedup_vs_raw_gather": round(value / world / raw_gbs, 3),
+        "parity_sampled_rows_ok": parity_ok,
+        "roofline": {
+            "bound": "link",
+            "achieved": round(delivered_per_launch, 2),
+            "peak": round(roof, 2),
+            "unit": "GB/s",
+            "frac": round(delivered_per_launch / roof, 4),
+            "traffic": None,
+            "peak_is": "min(HBM %s %.0f GB/s, link %.1f GB/s measured in this run / ratio %.4f)"
+                       % (peaks["source"], hbm, link_gbs, ratio),
+            "kernel": "k_decode<true> (ibp_gather_decompress)",
+            "algorithmic_bytes_per_launch": int(algo_bytes),
+            "link_bytes_achieved_gbs": round(ratio * delivered_per_launch, 2),
+        },
+        "e2e": {"value": round(e2e_gbs, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": 8 * n, "d2h_bytes_per_step": n * R},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+
+    # --- CPU baseline: the oracle on the host cores, one batch (rank 0, N = 1)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(store, ids_np[last], ibp, sample=n)
+    store.close(ibp)
+    return result
+
+
+def cpu_baseline(store, ids, ibp, sample):
+    from oracle import ref_c
+    mask = np.zeros(store.R // 4, np.uint32)
+    bitval = np.zeros(store.R // 4, np.uint32)
+    ibp.ibp_meta_get(store.st, mask, bitval)
+    bitmap = np.zeros((store.n_rows + 31) // 32, np.uint32)
+    ibp.ibp_bitmap_get(store.st, bitmap)
+    threads = len(os.sched_getaffinity(0))
+    ids = ids[:sample]
+    cpu_oracle_decode(store, ids[:1000], mask, bitval, bitmap, threads)  # warm
+    t0 = time.perf_counter()
+    out, bad = cpu_oracle_decode(store, ids, mask, bitval, bitmap, threads)
+    dt = time.perf_counter() - t0
+    assert bad == 0
+    return {"value": round(len(ids) * store.R / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "one batch of %d ids of the same workload, oracle C decoder, OpenMP "
+                      "over rows" % len(ids)}
+
+
+def run_reference(args, rank, world, torch):
+    """The oracle as it stands, on the host cores, same workload and metric."""
+    from lossless_invariant_bit_gb300 import workloads as wl
+    from oracle import ref_c
+
+    n_rows, dim, R, C = 2_000_000, 128, 512, 1024
+    rows = np.empty((n_rows, dim), np.float32)
+    wl.sparse_gnn_rows(n_rows, dim, seed=args.seed, out=rows)
+    rb = rows.view(np.uint8)
+    sample = wl.sample_ids(n_rows, 10, seed=args.seed)
+    threads = len(os.sched_getaffinity(0))
+    mask, bitval = ref_c.build_meta(rb, 95, 100, sample_ids=sample)
+    slot = 512
+    slots = np.zeros((n_rows, slot), np.uint8)
+    bitmap = np.zeros((n_rows + 31) // 32, np.uint32)
+    ref_c.compress_batch(rb, C, mask, bitval, slots, bitmap, nthreads=threads)
+    n = args.batch
+    times = []
+    for b in range(args.warmup + args.steps):
+        ids = wl.uniform_ids(n, n_rows, seed=args.seed, batch=b)
+        t0 = time.perf_counter()
+        _, bad = ref_c.decompress_batch(slots, bitmap, R, C, mask, bitval, ids=ids,
+                                        slot_stride=slot, nthreads=threads)
+        dt = time.perf_counter() - t0
+        assert bad == 0
+        if b >= args.warmup:
+            times.append(dt)
+    value = n * R * len(times) / sum(times) / 1e9
+    return {
+        "impl": "reference",
+        "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sum(times) / len(times) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (seeded numpy: sparse GNN features)",
+        "config": {"workload": "sparse GNN gather-decompress: 2,000,000 x 128 fp32 rows, "
+                               "chunk 1 KB, 1% sample, T=0.95, batches of 200,000 uniform ids",
+                   "source": "host memory (CPU oracle)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "%d steps of %d ids, oracle C decoder" % (args.steps, n)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=200_000)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 alone runs it; other ranks exit without work
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world, torch)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+
+    from lossless_invariant_bit_gb300 import build as libbuild
+    if rank == 0 or world == 1:
+        libbuild.build()
+    if dist:
+        dist.barrier()
+    res = run_ours(args, rank, world, torch, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * ibp.h -- C ABI of the GB300 Invariant Bit Packing (IBP) library (libibp.so).
+ *
+ * IBP is the lossless scheme of "Reducing the GPU Memory Bottleneck with
+ * Lossless Compression for ML -- Extended" (Kamath, Krishnamurthy, Canini,
+ * Peter).  The gist.science explainer, Technical Summary, Methodology > Core
+ * Algorithm defines the three operations exposed here (preprocessing into a
+ * Mask/Bitval pair, chunked compression with participation bits, warp-parallel
+ * decompression); its System Integration section defines the two storage
+ * layouts (a compressed GPU cache, and in-place fixed-size host buffers with a
+ * GPU bitmask of compressed tensors).
+ *
+ * Stream format (the pages fix the idea, not the bits; this library's choice):
+ *   - a row of R bytes is R/4 little-endian 32-bit words; Mask and Bitval have
+ *     one bit per row bit position;
+ *   - chunk k covers words [k*C/4, min((k+1)*C/4, R/4)); nch = ceil(R/C);
+ *   - chunk k participates (p_k = 1) iff every word w in it satisfies
+ *     (x_w & Mask_w) == Bitval_w and the chunk has at least one invariant bit;
+ *   - the stream is LSB-first 32-bit words: nch participation bits, then per
+ *     chunk the non-Mask bits of each word (p_k = 1) or all its bits (p_k = 0);
+ *   - a row whose stream needs 4*ceil(bits/32) >= R bytes is stored raw (its
+ *     R bytes unchanged) and its raw-bitmap bit is set.
+ *
+ * Conventions shared by every call:
+ *   - All device work is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  A synchronous return covers argument errors
+ *     only.  Data errors found by a kernel (row id out of range, corrupt
+ *     stream, misaligned offset) set the store's device status word and the
+ *     affected output row is zero-filled; read it with ibp_stream_status.
+ *   - Pointers marked "device" may be device memory or pinned, mapped host
+ *     memory (cudaHostAlloc / torch pin_memory) -- the kernels read and write
+ *     host memory zero-copy over the host link.  The caller owns every buffer
+ *     it passes; the store owns its metadata, derived tables, raw bitmap and
+ *     status word.
+ *   - Limits: R = row_bytes is a multiple of 16 and <= IBP_MAX_ROW_BYTES;
+ *     C = chunk_bytes is a multiple of 4; nch <= IBP_MAX_CHUNKS.  Row, slot
+ *     and destination base addresses are 16-byte aligned.
+ *   - No call traps, asserts or spins without bound on the device.
+ */
+#ifndef IBP_H_
+#define IBP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define IBP_API __attribute__((visibility("default")))
+#else
+#define IBP_API
+#endif
+
+#define IBP_MAX_ROW_BYTES 32768u
+#define IBP_MAX_CHUNKS 256u
+
+typedef enum {
+  IBP_OK = 0,
+  IBP_EINVAL = 1,   /* bad argument (NULL, size, threshold, geometry) */
+  IBP_EALIGN = 2,   /* a pointer, stride or offset is not 16-byte aligned */
+  IBP_ERANGE = 3,   /* a row / slot id outside [0, n_rows) */
+  IBP_ECORRUPT = 4, /* a stored stream that cannot be a valid IBP stream */
+  IBP_ENOMEM = 5,   /* device allocation failed (store creation only) */
+  IBP_ECUDA = 6,    /* a CUDA runtime call failed */
+  IBP_ETIMEOUT = 7  /* reserved: a bounded device wait gave up */
+} ibp_status;
+
+/* Opaque store: geometry, Mask/Bitval, tables derived from them, the raw
+ * bitmap of its n_rows slots and a device status word, all in HBM. */
+typedef struct ibp_store ibp_store;
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* ibp_stream_t;
+
+typedef struct {
+  uint32_t row_bytes;   /* R */
+  uint32_t chunk_bytes; /* C */
+  uint32_t n_chunks;    /* nch = ceil(R / C) */
+  uint32_t min_bits;    /* nch + sum of kept bits: shortest possible stream */
+  uint64_t n_rows;      /* slots the raw bitmap covers */
+  uint64_t slot_bytes;  /* host-store slot stride S (>= R, multiple of 16) */
+  uint32_t meta_valid;  /* 1 once a Mask/Bitval has been built or set */
+  uint32_t max_runs;    /* most runs of kept bits in one word of ~Mask */
+} ibp_store_info;
+
+/* Create a store for rows of `row_bytes` bytes cut into `chunk_bytes`
+ * chunks, with a raw bitmap for `n_rows` slots of stride `slot_bytes`
+ * (0 = roundup(row_bytes, 128), the 128-byte line the host link moves).
+ * Allocates device memory; *out receives the store.  Mask and Bitval start
+ * as all-zero (every row would be stored raw).  Synchronous.
+ * Errors: IBP_EINVAL (geometry outside the limits), IBP_EALIGN (slot_bytes
+ * not a multiple of 16 or < row_bytes), IBP_ENOMEM, IBP_ECUDA. */
+IBP_API ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_bytes,
+                            uint64_t n_rows, uint64_t slot_bytes);
+
+/* Free a store and its device memory (synchronises the device). NULL is a no-op. */
+IBP_API ibp_status ibp_store_destroy(ibp_store* store);
+
+/* Fill *info (host struct).  Synchronous: waits for the last derive kernel. */
+IBP_API ibp_status ibp_store_get_info(const ibp_store* store, ibp_store_info* info);
+
+/* Preprocessing (Core Algorithm > Preprocessing; the review's sampling
+ * experiment: 1/5/10 % samples): count, for every row bit position j, the
+ * ones over the analysed rows -- rows[sample_ids[i]] for i < n, or rows[0..n)
+ * when sample_ids is NULL -- and mark j invariant when
+ * ones*den >= num*n (Bitval bit 1) or (n-ones)*den >= num*n (Bitval bit 0),
+ * i.e. threshold T = num/den with 1/2 < T <= 1.  Then derives the store's
+ * decode tables.
+ *   rows        device/host-mapped, row r at rows + r*row_stride (R bytes)
+ *   row_stride  bytes, multiple of 16
+ *   sample_ids  device int64[n] or NULL; ids must lie in [0, 2^40)
+ *   n           analysed rows, 1 <= n < 2^32
+ * Errors: IBP_EINVAL (n, threshold), IBP_EALIGN, IBP_ECUDA. */
+IBP_API ibp_status ibp_build_meta(ibp_store* store, const void* rows, uint64_t row_stride,
+                          const int64_t* sample_ids, uint64_t n, uint32_t thr_num,
+                          uint32_t thr_den, ibp_stream_t stream);
+
+/* Compression (Core Algorithm > Compression; System Integration: in-place
+ * compression into fixed-size buffers, GPU bitmask of compressed tensors):
+ * compress row i (src_rows + i*src_stride, i < n) into slot slot_ids[i]
+ * (NULL: slot i) at dst_slots + slot*slot_bytes: the stored bytes go to the
+ * slot start (16-byte granules; the slot tail is not defined), and the slot's
+ * raw-bitmap bit is set or cleared.  stored_bytes_out (optional, device
+ * uint32[n]) receives each row's stored size (R for a raw row).  dst_slots may
+ * be pinned host memory (zero-copy writes over the host link).  Rows whose
+ * slot ids collide race.  Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA;
+ * a slot id out of range sets IBP_ERANGE in the status word. */
+IBP_API ibp_status ibp_compress(ibp_store* store, void* dst_slots, const void* src_rows,
+                        uint64_t src_stride, const int64_t* slot_ids, uint64_t n,
+                        uint32_t* stored_bytes_out, ibp_stream_t stream);
+
+/* Decompression of rows 0..n-1 (Core Algorithm > Decompression):
+ * row i's stored bytes start at src + offsets[i] (a packed HBM cache; offsets
+ * device uint64[n], multiples of 16) or, with offsets NULL, at
+ * src + i*slot_bytes (a slot store).  dst receives n rows of R bytes,
+ * contiguous.  Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA; corrupt streams and
+ * misaligned offsets set the status word. */
+IBP_API ibp_status ibp_decompress(const ibp_store* store, void* dst, const void* src,
+                          const uint64_t* offsets, uint64_t n, ibp_stream_t stream);
+
+/* Gather-decompression (the hot path): row i of dst (R bytes, contiguous) is
+ * the decompressed row ids[i] of the store, read from host_or_dev_src +
+ * offsets[id] (offsets may be NULL: + id*slot_bytes).  ids: device int64[n].
+ * With a pinned host source every stored byte crosses the host link inside
+ * the kernel (GPU-initiated zero-copy reads, 16-byte vectors, 128-byte lines).
+ * Errors: as ibp_decompress; an id outside [0, n_rows) sets IBP_ERANGE. */
+IBP_API ibp_status ibp_gather_decompress(const ibp_store* store, void* dst, const void* host_or_dev_src,
+                                 const uint64_t* offsets, const int64_t* ids, uint64_t n,
+                                 ibp_stream_t stream);
+
+/* As ibp_gather_decompress, with row i written to dst + i*dst_stride_bytes
+ * (dst_stride_bytes >= R, multiple of 16): e.g. one table's column of a
+ * [batch, tables, dim] embedding output. */
+IBP_API ibp_status ibp_gather_decompress_strided(const ibp_store* store, void* dst,
+                                         uint64_t dst_stride_bytes,
+                                         const void* host_or_dev_src, const uint64_t* offsets,
+                                         const int64_t* ids, uint64_t n, ibp_stream_t stream);
+
+/* Build a packed HBM cache (System Integration: compressed GPU software
+ * cache) from compressed slots: row i's stored_bytes[i] bytes at
+ * src_slots + i*slot_bytes are copied to dst_packed + offsets_out[i], where
+ * offsets_out[i] = sum over i' < i of roundup(stored_bytes[i'], 16) and
+ * offsets_out[n] is the total.  With dst_packed NULL only the offsets are
+ * written (size query).  offsets_out: device uint64[n+1]; stored_bytes:
+ * device uint32[n] as written by ibp_compress.  The raw bitmap of the slots
+ * applies unchanged to the packed rows.  Errors: IBP_EINVAL, IBP_EALIGN,
+ * IBP_ECUDA. */
+IBP_API ibp_status ibp_pack(const ibp_store* store, void* dst_packed, uint64_t* offsets_out,
+                            const void* src_slots, const uint32_t* stored_bytes, uint64_t n,
+                            ibp_stream_t stream);
+
+/* Copy the store's Mask and Bitval (R/4 words each) to host arrays.  Synchronous. */
+IBP_API ibp_status ibp_meta_get(const ibp_store* store, uint32_t* mask_host, uint32_t* bitval_host);
+
+/* Install a Mask/Bitval from host arrays (R/4 words each; Bitval bits outside
+ * the Mask must be zero, else IBP_EINVAL) and derive the decode tables.  Synchronous. */
+IBP_API ibp_status ibp_meta_set(ibp_store* store, const uint32_t* mask_host, const uint32_t* bitval_host);
+
+/* Copy the raw bitmap (ceil(n_rows/32) words; bit id%32 of word id/32) to the host.  Synchronous. */
+IBP_API ibp_status ibp_bitmap_get(const ibp_store* store, uint32_t* bitmap_host);
+
+/* Install a raw bitmap from the host (e.g. for streams compressed elsewhere).  Synchronous. */
+IBP_API ibp_status ibp_bitmap_set(ibp_store* store, const uint32_t* bitmap_host);
+
+/* Synchronise `stream`, then report the store's device status word (IBP_OK
+ * or the first data error a kernel recorded) in *out; reset != 0 clears it. */
+IBP_API ibp_status ibp_stream_status(const ibp_store* store, ibp_stream_t stream, ibp_status* out,
+                             int reset);
+
+/* Aligned zero-copy copy of `bytes` (multiple of 16, 16-byte aligned ends)
+ * from src to dst by GPU warps issuing 16-byte loads that cover whole
+ * 128-byte lines (the review's "GPU aligned transfer", Figure 5).  Used as the
+ * host-link bandwidth probe.  Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA. */
+IBP_API ibp_status ibp_link_copy(void* dst, const void* src, uint64_t bytes, ibp_stream_t stream);
+
+/* Uncompressed gather: row i of dst (row_bytes, contiguous) = the row_bytes
+ * at src + ids[i]*slot_bytes.  The raw-transfer baseline of the review's
+ * Table 1 speedups.  row_bytes and slot_bytes are multiples of 16; a row whose
+ * id lies outside [0, n_rows) is zero-filled (no status word: no store). */
+IBP_API ibp_status ibp_gather_copy(void* dst, const void* src, uint64_t slot_bytes, uint32_t row_bytes,
+                           const int64_t* ids, uint64_t n, uint64_t n_rows,
+                           ibp_stream_t stream);
+
+/* Static text of a status code. */
+IBP_API const char* ibp_status_str(ibp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* IBP_H_ */

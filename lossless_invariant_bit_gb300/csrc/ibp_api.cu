@@ -1,0 +1,364 @@
+// C-ABI of the IBP library: store objects, argument checks, launches.
+// The operations are those of "Reducing the GPU Memory Bottleneck with
+// Lossless Compression for ML -- Extended" (gist.science explainer, Technical
+// Summary, Methodology > Core Algorithm and System Integration); see ibp.h
+// for the contract of each entry point.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "ibp_internal.cuh"
+
+struct ibp_store {
+  uint32_t R, C, W, wpc, nch;
+  uint64_t n_rows, slot;
+  int device;
+  int sm_count;
+  void* base;  // one device allocation, carved below
+  uint32_t *mask, *bitval, *nm, *pre, *kr, *mv, *ckeep, *scal, *counts, *bitmap, *status;
+  uint64_t bitmap_words;
+};
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline ibp_status cu(cudaError_t e) { return e == cudaSuccess ? IBP_OK : IBP_ECUDA; }
+
+// Calls on a store run on the device it was created on.
+ibp_status on_device(const ibp_store* s) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) return IBP_ECUDA;
+  return d == s->device ? IBP_OK : IBP_EINVAL;
+}
+
+ibp::MetaView view(const ibp_store* s) {
+  ibp::MetaView m;
+  m.mask = s->mask;
+  m.bitval = s->bitval;
+  m.nm = s->nm;
+  m.pre = s->pre;
+  m.kr = s->kr;
+  m.mv = s->mv;
+  m.ckeep = s->ckeep;
+  m.scal = s->scal;
+  m.R = s->R;
+  m.W = s->W;
+  m.wpc = s->wpc;
+  m.nch = s->nch;
+  return m;
+}
+
+ibp_status derive(ibp_store* s, cudaStream_t st) {
+  return cu(ibp::launch_derive(s->mask, s->bitval, s->nm, s->pre, s->kr, s->mv, s->ckeep,
+                               s->scal, s->W, s->wpc, s->nch, st));
+}
+
+ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void* src,
+                  const uint64_t* offsets, const int64_t* ids, uint64_t n, cudaStream_t st) {
+  if (!s) return IBP_EINVAL;
+  if (n == 0) return IBP_OK;
+  if (!dst || !src) return IBP_EINVAL;
+  if (!aligned16(dst) || !aligned16(src) || (dst_stride & 15u) || dst_stride < s->R)
+    return IBP_EALIGN;
+  if (!ids && n > s->n_rows) return IBP_ERANGE;
+  ibp_status e = on_device(s);
+  if (e != IBP_OK) return e;
+  ibp::DecodeArgs a;
+  a.m = view(s);
+  a.bitmap = s->bitmap;
+  a.status = s->status;
+  a.src = static_cast<const uint8_t*>(src);
+  a.offsets = offsets;
+  a.slot = s->slot;
+  a.avail = offsets ? s->R : s->slot;
+  a.ids = ids;
+  a.n = n;
+  a.n_rows = s->n_rows;
+  a.dst = static_cast<uint8_t*>(dst);
+  a.dst_stride = dst_stride;
+  return cu(ibp::launch_decode(a, s->sm_count, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ibp_status_str(ibp_status s) {
+  switch (s) {
+    case IBP_OK: return "IBP_OK";
+    case IBP_EINVAL: return "IBP_EINVAL: invalid argument";
+    case IBP_EALIGN: return "IBP_EALIGN: pointer, stride or offset not 16-byte aligned";
+    case IBP_ERANGE: return "IBP_ERANGE: row or slot id out of range";
+    case IBP_ECORRUPT: return "IBP_ECORRUPT: stored stream is not a valid IBP stream";
+    case IBP_ENOMEM: return "IBP_ENOMEM: device allocation failed";
+    case IBP_ECUDA: return "IBP_ECUDA: CUDA runtime error";
+    case IBP_ETIMEOUT: return "IBP_ETIMEOUT: bounded device wait gave up";
+  }
+  return "IBP: unknown status";
+}
+
+ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_bytes,
+                            uint64_t n_rows, uint64_t slot_bytes) {
+  if (!out) return IBP_EINVAL;
+  *out = nullptr;
+  if (row_bytes == 0 || row_bytes > IBP_MAX_ROW_BYTES || (row_bytes & 15u)) return IBP_EINVAL;
+  if (chunk_bytes == 0 || (chunk_bytes & 3u) || n_rows == 0) return IBP_EINVAL;
+  const uint32_t W = row_bytes / 4, wpc = chunk_bytes / 4;
+  const uint32_t nch = (W + wpc - 1) / wpc;
+  if (nch > IBP_MAX_CHUNKS) return IBP_EINVAL;
+  if (slot_bytes == 0) slot_bytes = ((uint64_t)row_bytes + 127u) & ~(uint64_t)127u;
+  if ((slot_bytes & 15u) || slot_bytes < row_bytes) return IBP_EALIGN;
+  if (n_rows > (1ull << 40)) return IBP_EINVAL;
+
+  ibp_store* s = new (std::nothrow) ibp_store();
+  if (!s) return IBP_ENOMEM;
+  s->R = row_bytes;
+  s->C = chunk_bytes;
+  s->W = W;
+  s->wpc = wpc;
+  s->nch = nch;
+  s->n_rows = n_rows;
+  s->slot = slot_bytes;
+  s->bitmap_words = (n_rows + 31) / 32;
+  if (cudaGetDevice(&s->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&s->sm_count, cudaDevAttrMultiProcessorCount, s->device) !=
+          cudaSuccess) {
+    delete s;
+    return IBP_ECUDA;
+  }
+  // words: mask, bitval, nm, pre, kr (5W) + mv (5W) + ckeep (nch) + scal (4)
+  //        + counts (32W) + status (4) + bitmap, each piece 16-byte aligned
+  auto r4 = [](uint64_t x) { return (x + 3u) & ~(uint64_t)3u; };
+  const uint64_t words = 10ull * r4(W) + r4(nch) + 4 + 32ull * W + 4 + r4(s->bitmap_words);
+  if (cudaMalloc(&s->base, words * 4) != cudaSuccess) {
+    cudaGetLastError();
+    delete s;
+    return IBP_ENOMEM;
+  }
+  uint32_t* p = static_cast<uint32_t*>(s->base);
+  auto take = [&](uint64_t n) {
+    uint32_t* q = p;
+    p += r4(n);
+    return q;
+  };
+  s->mask = take(W);
+  s->bitval = take(W);
+  s->nm = take(W);
+  s->pre = take(W);
+  s->kr = take(W);
+  s->mv = take(5ull * W);
+  s->ckeep = take(nch);
+  s->scal = take(4);
+  s->counts = take(32ull * W);
+  s->status = take(4);
+  s->bitmap = take(s->bitmap_words);
+  ibp_status e = cu(cudaMemset(s->base, 0, words * 4));
+  if (e == IBP_OK) e = derive(s, 0);  // all-zero Mask: tables for "everything raw"
+  if (e == IBP_OK) e = cu(cudaDeviceSynchronize());
+  if (e != IBP_OK) {
+    cudaFree(s->base);
+    delete s;
+    return e;
+  }
+  // derive() sets the valid flag; a fresh store has no built Mask yet
+  uint32_t zero = 0;
+  if (cudaMemcpy(s->scal + 2, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(s->base);
+    delete s;
+    return IBP_ECUDA;
+  }
+  *out = s;
+  return IBP_OK;
+}
+
+ibp_status ibp_store_destroy(ibp_store* s) {
+  if (!s) return IBP_OK;
+  cudaDeviceSynchronize();
+  const cudaError_t e = cudaFree(s->base);
+  delete s;
+  return cu(e);
+}
+
+ibp_status ibp_store_get_info(const ibp_store* s, ibp_store_info* info) {
+  if (!s || !info) return IBP_EINVAL;
+  uint32_t sc[4];
+  if (cudaDeviceSynchronize() != cudaSuccess) return IBP_ECUDA;
+  if (cudaMemcpy(sc, s->scal, sizeof sc, cudaMemcpyDeviceToHost) != cudaSuccess) return IBP_ECUDA;
+  info->row_bytes = s->R;
+  info->chunk_bytes = s->C;
+  info->n_chunks = s->nch;
+  info->min_bits = sc[0];
+  info->max_runs = sc[1];
+  info->meta_valid = sc[2];
+  info->n_rows = s->n_rows;
+  info->slot_bytes = s->slot;
+  return IBP_OK;
+}
+
+ibp_status ibp_build_meta(ibp_store* s, const void* rows, uint64_t row_stride,
+                          const int64_t* sample_ids, uint64_t n, uint32_t thr_num,
+                          uint32_t thr_den, ibp_stream_t stream) {
+  if (!s || !rows) return IBP_EINVAL;
+  if (n == 0 || n >= (1ull << 32)) return IBP_EINVAL;
+  if (thr_den == 0 || thr_num > thr_den || 2ull * thr_num <= thr_den) return IBP_EINVAL;
+  if (!aligned16(rows) || (row_stride & 15u) || row_stride < s->R) return IBP_EALIGN;
+  ibp_status e = on_device(s);
+  if (e != IBP_OK) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  e = cu(cudaMemsetAsync(s->counts, 0, 32ull * s->W * 4, st));
+  if (e != IBP_OK) return e;
+  ibp::CountArgs a;
+  a.rows = static_cast<const uint8_t*>(rows);
+  a.row_stride = row_stride;
+  a.ids = sample_ids;
+  a.n = n;
+  a.W = s->W;
+  a.counts = s->counts;
+  e = cu(ibp::launch_count_ones(a, s->sm_count, st));
+  if (e != IBP_OK) return e;
+  e = cu(ibp::launch_finish_meta(s->counts, s->W, n, thr_num, thr_den, s->mask, s->bitval, st));
+  if (e != IBP_OK) return e;
+  return derive(s, st);
+}
+
+ibp_status ibp_compress(ibp_store* s, void* dst_slots, const void* src_rows, uint64_t src_stride,
+                        const int64_t* slot_ids, uint64_t n, uint32_t* stored_bytes_out,
+                        ibp_stream_t stream) {
+  if (!s) return IBP_EINVAL;
+  if (n == 0) return IBP_OK;
+  if (!dst_slots || !src_rows) return IBP_EINVAL;
+  if (!aligned16(dst_slots) || !aligned16(src_rows) || (src_stride & 15u) || src_stride < s->R)
+    return IBP_EALIGN;
+  if (!slot_ids && n > s->n_rows) return IBP_ERANGE;
+  ibp_status e = on_device(s);
+  if (e != IBP_OK) return e;
+  ibp::EncodeArgs a;
+  a.m = view(s);
+  a.bitmap = s->bitmap;
+  a.status = s->status;
+  a.src = static_cast<const uint8_t*>(src_rows);
+  a.src_stride = src_stride;
+  a.slot_ids = slot_ids;
+  a.n = n;
+  a.n_rows = s->n_rows;
+  a.dst = static_cast<uint8_t*>(dst_slots);
+  a.slot = s->slot;
+  a.stored_out = stored_bytes_out;
+  return cu(ibp::launch_encode(a, s->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ibp_status ibp_decompress(const ibp_store* s, void* dst, const void* src, const uint64_t* offsets,
+                          uint64_t n, ibp_stream_t stream) {
+  return decode(s, dst, s ? s->R : 0, src, offsets, nullptr, n,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+ibp_status ibp_gather_decompress(const ibp_store* s, void* dst, const void* src,
+                                 const uint64_t* offsets, const int64_t* ids, uint64_t n,
+                                 ibp_stream_t stream) {
+  if (!ids && n) return IBP_EINVAL;
+  return decode(s, dst, s ? s->R : 0, src, offsets, ids, n,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+ibp_status ibp_gather_decompress_strided(const ibp_store* s, void* dst, uint64_t dst_stride,
+                                         const void* src, const uint64_t* offsets,
+                                         const int64_t* ids, uint64_t n, ibp_stream_t stream) {
+  if (!ids && n) return IBP_EINVAL;
+  return decode(s, dst, dst_stride, src, offsets, ids, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ibp_status ibp_pack(const ibp_store* s, void* dst_packed, uint64_t* offsets_out,
+                    const void* src_slots, const uint32_t* stored_bytes, uint64_t n,
+                    ibp_stream_t stream) {
+  if (!s || !offsets_out) return IBP_EINVAL;
+  if (n && (!src_slots || !stored_bytes)) return IBP_EINVAL;
+  if ((dst_packed && !aligned16(dst_packed)) || (src_slots && !aligned16(src_slots)))
+    return IBP_EALIGN;
+  ibp_status e = on_device(s);
+  if (e != IBP_OK) return e;
+  return cu(ibp::launch_pack(static_cast<uint8_t*>(dst_packed), offsets_out,
+                             static_cast<const uint8_t*>(src_slots), s->slot, stored_bytes, n,
+                             s->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ibp_status ibp_meta_get(const ibp_store* s, uint32_t* mask_host, uint32_t* bitval_host) {
+  if (!s || !mask_host || !bitval_host) return IBP_EINVAL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return IBP_ECUDA;
+  if (cudaMemcpy(mask_host, s->mask, 4ull * s->W, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return IBP_ECUDA;
+  return cu(cudaMemcpy(bitval_host, s->bitval, 4ull * s->W, cudaMemcpyDeviceToHost));
+}
+
+ibp_status ibp_meta_set(ibp_store* s, const uint32_t* mask_host, const uint32_t* bitval_host) {
+  if (!s || !mask_host || !bitval_host) return IBP_EINVAL;
+  for (uint32_t w = 0; w < s->W; ++w)
+    if (bitval_host[w] & ~mask_host[w]) return IBP_EINVAL;
+  ibp_status e = on_device(s);
+  if (e != IBP_OK) return e;
+  if (cudaDeviceSynchronize() != cudaSuccess) return IBP_ECUDA;
+  if (cudaMemcpy(s->mask, mask_host, 4ull * s->W, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(s->bitval, bitval_host, 4ull * s->W, cudaMemcpyHostToDevice) != cudaSuccess)
+    return IBP_ECUDA;
+  e = derive(s, 0);
+  if (e != IBP_OK) return e;
+  return cu(cudaDeviceSynchronize());
+}
+
+ibp_status ibp_bitmap_get(const ibp_store* s, uint32_t* host) {
+  if (!s || !host) return IBP_EINVAL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return IBP_ECUDA;
+  return cu(cudaMemcpy(host, s->bitmap, 4ull * s->bitmap_words, cudaMemcpyDeviceToHost));
+}
+
+ibp_status ibp_bitmap_set(ibp_store* s, const uint32_t* host) {
+  if (!s || !host) return IBP_EINVAL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return IBP_ECUDA;
+  return cu(cudaMemcpy(s->bitmap, host, 4ull * s->bitmap_words, cudaMemcpyHostToDevice));
+}
+
+ibp_status ibp_stream_status(const ibp_store* s, ibp_stream_t stream, ibp_status* out,
+                             int reset) {
+  if (!s || !out) return IBP_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return IBP_ECUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, s->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return IBP_ECUDA;
+  *out = static_cast<ibp_status>(v);
+  if (reset && v) {
+    if (cudaMemset(s->status, 0, 4) != cudaSuccess) return IBP_ECUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return IBP_ECUDA;
+  }
+  return IBP_OK;
+}
+
+ibp_status ibp_link_copy(void* dst, const void* src, uint64_t bytes, ibp_stream_t stream) {
+  if (bytes == 0) return IBP_OK;
+  if (!dst || !src) return IBP_EINVAL;
+  if (!aligned16(dst) || !aligned16(src) || (bytes & 15u)) return IBP_EALIGN;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return IBP_ECUDA;
+  return cu(ibp::launch_link_copy(static_cast<uint4*>(dst), static_cast<const uint4*>(src),
+                                  bytes / 16, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ibp_status ibp_gather_copy(void* dst, const void* src, uint64_t slot_bytes, uint32_t row_bytes,
+                           const int64_t* ids, uint64_t n, uint64_t n_rows,
+                           ibp_stream_t stream) {
+  if (n == 0) return IBP_OK;
+  if (!dst || !src || !ids || row_bytes == 0) return IBP_EINVAL;
+  if (!aligned16(dst) || !aligned16(src) || (row_bytes & 15u) || (slot_bytes & 15u))
+    return IBP_EALIGN;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return IBP_ECUDA;
+  return cu(ibp::launch_gather_copy(static_cast<uint8_t*>(dst), static_cast<const uint8_t*>(src),
+                                    slot_bytes, row_bytes, ids, n, n_rows, sms,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// Internal declarations shared by the IBP kernels and the C-ABI host code.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ibp.h"
+
+namespace ibp {
+
+// Read-only views of a store's metadata and the tables derived from it.
+//   mask, bitval  W words each (the Mask / Bitval of the Core Algorithm)
+//   nm            ~mask: the positions whose bits are kept in a packed chunk
+//   pre           kept bits of the earlier words of the same chunk
+//   kr            chunk index (bits 0..15) | word index inside the chunk (16..31)
+//   mv            5 x W move masks of the bit-gather network of nm (stage i at i*W)
+//   ckeep         nch words: kept bits per chunk
+//   scal          [0] min_bits = nch + sum(ckeep), [1] max runs of one word's nm,
+//                 [2] meta valid flag
+struct MetaView {
+  const uint32_t* mask;
+  const uint32_t* bitval;
+  const uint32_t* nm;
+  const uint32_t* pre;
+  const uint32_t* kr;
+  const uint32_t* mv;
+  const uint32_t* ckeep;
+  const uint32_t* scal;
+  uint32_t R, W, wpc, nch;
+};
+
+struct DecodeArgs {
+  MetaView m;
+  const uint32_t* bitmap;
+  uint32_t* status;
+  const uint8_t* src;
+  const uint64_t* offsets;  // NULL: slot layout
+  uint64_t slot;            // slot stride (slot layout)
+  uint64_t avail;           // bytes of a row's storage the decoder may read
+  const int64_t* ids;       // NULL: row i
+  uint64_t n;
+  uint64_t n_rows;
+  uint8_t* dst;
+  uint64_t dst_stride;
+};
+
+struct EncodeArgs {
+  MetaView m;
+  uint32_t* bitmap;
+  uint32_t* status;
+  const uint8_t* src;
+  uint64_t src_stride;
+  const int64_t* slot_ids;
+  uint64_t n;
+  uint64_t n_rows;
+  uint8_t* dst;
+  uint64_t slot;
+  uint32_t* stored_out;
+};
+
+struct CountArgs {
+  const uint8_t* rows;
+  uint64_t row_stride;
+  const int64_t* ids;
+  uint64_t n;
+  uint32_t W;
+  uint32_t* counts;  // 32 * W
+};
+
+// Shared-memory layout of one warp in the decode / encode kernels (in words).
+struct WarpSmem {
+  uint32_t sbuf_words;  // stream (decode) or packed output (encode) buffer
+  uint32_t xbuf_words;  // raw row (encode only)
+  uint32_t cinfo_words; // per chunk start | p << 31
+  uint32_t total_words; // per warp
+};
+
+WarpSmem decode_smem(uint32_t W, uint32_t nch);
+WarpSmem encode_smem(uint32_t W, uint32_t nch);
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_count_ones(const CountArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_finish_meta(const uint32_t* counts, uint32_t W, uint64_t n, uint32_t num,
+                               uint32_t den, uint32_t* mask, uint32_t* bitval, cudaStream_t st);
+cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32_t* pre,
+                          uint32_t* kr, uint32_t* mv, uint32_t* ckeep, uint32_t* scal,
+                          uint32_t W, uint32_t wpc, uint32_t nch, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_encode(const EncodeArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,
+                        const uint32_t* stored, uint64_t n, int sm_count, cudaStream_t st);
+cudaError_t launch_link_copy(uint4* dst, const uint4* src, uint64_t nvec, int sm_count,
+                             cudaStream_t st);
+cudaError_t launch_gather_copy(uint8_t* dst, const uint8_t* src, uint64_t slot,
+                               uint32_t row_bytes, const int64_t* ids, uint64_t n,
+                               uint64_t n_rows, int sm_count, cudaStream_t st);
+
+}  // namespace ibp

@@ -1,0 +1,634 @@
+// IBP kernels for sm_103a: Mask/Bitval builder, table derivation, compressor,
+// decompressor (dense and gather, HBM or zero-copy host source) and the
+// aligned zero-copy copy used as the host-link probe.
+//
+// Method: "Reducing the GPU Memory Bottleneck with Lossless Compression for
+// ML -- Extended", gist.science explainer, Technical Summary, Methodology >
+// Core Algorithm (Preprocessing, Compression, Decompression) and System
+// Integration; juhe.plus review (one warp per tensor with only warp-local
+// communication, 128-byte aligned GPU-initiated transfers).
+//
+// Nothing here is a dense contraction, so there are no tensor-core paths: the
+// decoder is bound by the host link (zero-copy source) or by HBM (cache
+// source), the builder by the bandwidth of the rows it reads, and the bit
+// work runs on the integer pipes.
+#include "ibp_internal.cuh"
+
+namespace ibp {
+namespace {
+
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ void set_status(uint32_t* st, uint32_t code) {
+  atomicCAS(st, 0u, code);
+}
+
+__device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v, uint32_t lane) {
+#pragma unroll
+  for (uint32_t d = 1; d < 32; d <<= 1) {
+    const uint32_t t = __shfl_up_sync(kFull, v, d);
+    if (lane >= d) v += t;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) { return __ldg(p); }
+
+__device__ __forceinline__ void st_smem_v4(uint32_t* s, const uint4& v) {
+  *reinterpret_cast<uint4*>(s) = v;
+}
+
+// Scatter network of a kept-bit mask: the low popcount(nm) bits of v move to
+// the set positions of nm, in order (5 stages of shifts by 16, 8, 4, 2, 1,
+// the inverse of the gather below).  Bits of v above popcount(nm) may be
+// anything; the caller masks the result with nm.
+__device__ __forceinline__ uint32_t scatter_bits(uint32_t v, const uint32_t* mv, uint32_t W,
+                                                 uint32_t w) {
+#pragma unroll
+  for (int i = 4; i >= 0; --i) {
+    const uint32_t m = __ldg(mv + (uint32_t)i * W + w);
+    v = (v & ~m) | ((v << (1u << i)) & m);
+  }
+  return v;
+}
+
+// Gather network: the bits of x at the set positions of nm, packed to the
+// low end in order (x must already be masked with nm).
+__device__ __forceinline__ uint32_t gather_bits(uint32_t x, const uint32_t* mv, uint32_t W,
+                                                uint32_t w) {
+#pragma unroll
+  for (int i = 0; i < 5; ++i) {
+    const uint32_t t = x & __ldg(mv + (uint32_t)i * W + w);
+    x = (x ^ t) | (t >> (1u << i));
+  }
+  return x;
+}
+
+// ------------------------------------------------------------------------
+// Builder (Core Algorithm > Preprocessing): ones count per row bit position.
+// Thread = one word position; block.x tiles words, grid.x splits the rows.
+// Each thread adds its words into 8 bit-plane counters (a vertical
+// ripple-carry adder: 16 logic ops per word per row) and spills them into 32
+// per-bit counts every 255 rows, then adds those into the global counts.
+// ------------------------------------------------------------------------
+__device__ __forceinline__ void vadd(uint32_t (&c)[8], uint32_t x) {
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t t = c[p] & x;
+    c[p] ^= x;
+    x = t;
+  }
+}
+
+__device__ __forceinline__ void vspill(uint32_t (&c)[8], uint32_t (&ones)[32]) {
+#pragma unroll
+  for (int b = 0; b < 32; ++b) {
+    uint32_t s = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) s += ((c[p] >> b) & 1u) << p;
+    ones[b] += s;
+  }
+#pragma unroll
+  for (int p = 0; p < 8; ++p) c[p] = 0;
+}
+
+__global__ void __launch_bounds__(128) k_count_ones(CountArgs a) {
+  const uint32_t w = blockIdx.y * blockDim.x + threadIdx.x;
+  if (w >= a.W) return;
+  uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint32_t ones[32];
+#pragma unroll
+  for (int b = 0; b < 32; ++b) ones[b] = 0;
+  uint32_t inplanes = 0;
+  const uint64_t step = gridDim.x;
+  uint64_t r = blockIdx.x;
+  // four rows per trip: their loads are independent and overlap
+  for (; r + 3 * step < a.n; r += 4 * step) {
+    uint32_t x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint64_t i = r + (uint64_t)u * step;
+      const uint64_t row = a.ids ? (uint64_t)__ldg(a.ids + i) : i;
+      x[u] = __ldg(reinterpret_cast<const uint32_t*>(a.rows + row * a.row_stride) + w);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) vadd(c, x[u]);
+    inplanes += 4;
+    if (inplanes > 255 - 4) {
+      vspill(c, ones);
+      inplanes = 0;
+    }
+  }
+  for (; r < a.n; r += step) {
+    const uint64_t row = a.ids ? (uint64_t)__ldg(a.ids + r) : r;
+    vadd(c, __ldg(reinterpret_cast<const uint32_t*>(a.rows + row * a.row_stride) + w));
+    if (++inplanes == 255) {
+      vspill(c, ones);
+      inplanes = 0;
+    }
+  }
+  vspill(c, ones);
+#pragma unroll
+  for (int b = 0; b < 32; ++b)
+    if (ones[b]) atomicAdd(a.counts + 32u * w + b, ones[b]);
+}
+
+// Threshold: bit j is invariant when ones*den >= num*n (value 1) or
+// (n-ones)*den >= num*n (value 0); 64-bit integer arithmetic.
+__global__ void k_finish_meta(const uint32_t* counts, uint32_t W, uint64_t n, uint32_t num,
+                              uint32_t den, uint32_t* mask, uint32_t* bitval) {
+  const uint32_t w = blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= W) return;
+  const uint64_t lim = (uint64_t)num * n;
+  uint32_t m = 0, bv = 0;
+  for (uint32_t b = 0; b < 32; ++b) {
+    const uint64_t o = counts[32u * w + b];
+    const bool inv1 = o * den >= lim;
+    const bool inv0 = (n - o) * den >= lim;
+    m |= (uint32_t)(inv1 || inv0) << b;
+    bv |= (uint32_t)inv1 << b;
+  }
+  mask[w] = m;
+  bitval[w] = bv;
+}
+
+// Decode tables from the Mask (one block).  The move masks are those of the
+// classic 5-stage bit gather (H. S. Warren, Hacker's Delight, sec. 7-4 and
+// 7-5): at stage i, the bits of the current mask with an odd number of
+// not-yet-consumed zeros below them (parallel suffix parity) move right by
+// 2^i.
+__device__ void move_masks(uint32_t m, uint32_t (&mv)[5]) {
+  uint32_t zeros_below = ~m << 1;
+#pragma unroll
+  for (int i = 0; i < 5; ++i) {
+    uint32_t par = zeros_below ^ (zeros_below << 1);
+    par ^= par << 2;
+    par ^= par << 4;
+    par ^= par << 8;
+    par ^= par << 16;
+    const uint32_t mov = par & m;
+    mv[i] = mov;
+    m = (m ^ mov) | (mov >> (1u << i));
+    zeros_below &= ~par;
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm,
+                                                 uint32_t* pre, uint32_t* kr, uint32_t* mv,
+                                                 uint32_t* ckeep, uint32_t* scal, uint32_t W,
+                                                 uint32_t wpc, uint32_t nch) {
+  __shared__ uint32_t s_sum, s_runs;
+  if (threadIdx.x == 0) {
+    s_sum = 0;
+    s_runs = 0;
+  }
+  __syncthreads();
+  for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
+    const uint32_t keepm = ~mask[w];
+    bitval[w] &= mask[w];
+    nm[w] = keepm;
+    uint32_t m5[5];
+    move_masks(keepm, m5);
+#pragma unroll
+    for (int i = 0; i < 5; ++i) mv[(uint32_t)i * W + w] = m5[i];
+    kr[w] = (w / wpc) | ((w % wpc) << 16);
+    atomicMax(&s_runs, (uint32_t)__popc(keepm & ~(keepm << 1)));
+  }
+  for (uint32_t k = threadIdx.x; k < nch; k += blockDim.x) {
+    const uint32_t e = min((k + 1) * wpc, W);
+    uint32_t acc = 0;
+    for (uint32_t w = k * wpc; w < e; ++w) {
+      pre[w] = acc;
+      acc += __popc(~mask[w]);
+    }
+    ckeep[k] = acc;
+    atomicAdd(&s_sum, acc);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    scal[0] = nch + s_sum;
+    scal[1] = s_runs;
+    scal[2] = 1;
+  }
+}
+
+// ------------------------------------------------------------------------
+// Decompression.  One warp per row (the pages' "one warp per tensor"), but
+// the lanes split the row's output words rather than its chunks, so a row
+// with fewer than 32 chunks still keeps all lanes busy.  Per row:
+//   resolve   id, raw bit, source address;
+//   fetch     the shortest stream any compressed row can have (min_bits) in
+//             16-byte vectors, staged in the warp's shared memory;
+//   scan      participation bits -> chunk sizes -> exclusive warp scan;
+//   fetch     the rest of the stream when raw chunks made it longer;
+//   re-insert each lane builds 4 output words at a time: a funnel shift
+//             pulls the word's bits out of the staged stream, the scatter
+//             network spreads them over ~Mask, Bitval fills the rest; one
+//             coalesced 16-byte store.
+// A raw row is a straight 16-byte vector copy.
+// ------------------------------------------------------------------------
+__device__ __forceinline__ void zero_row(uint4* drow, uint32_t nvec, uint32_t lane) {
+  for (uint32_t v = lane; v < nvec; v += 32) drow[v] = make_uint4(0, 0, 0, 0);
+}
+
+template <bool kIds>
+__global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
+  extern __shared__ __align__(16) uint32_t smem[];
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t wid = threadIdx.x >> 5;
+  uint32_t* sbuf = smem + wid * L.total_words;
+  uint32_t* cinfo = sbuf + L.sbuf_words;
+  const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
+  const uint32_t nvec = R >> 4;
+  const uint32_t min_words = (__ldg(a.m.scal) + 31u) >> 5;
+  const uint32_t min_vec = (4u * min_words + 15u) >> 4;
+  const uint64_t wpb = blockDim.x >> 5;
+  const uint64_t stride = (uint64_t)gridDim.x * wpb;
+
+  for (uint64_t i = (uint64_t)blockIdx.x * wpb + wid; i < a.n; i += stride) {
+    uint4* drow = reinterpret_cast<uint4*>(a.dst + i * a.dst_stride);
+    const int64_t id = kIds ? __ldg(a.ids + i) : (int64_t)i;
+    if (id < 0 || (uint64_t)id >= a.n_rows) {
+      if (lane == 0) set_status(a.status, IBP_ERANGE);
+      zero_row(drow, nvec, lane);
+      continue;
+    }
+    const uint64_t off = a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
+    if (off & 15u) {
+      if (lane == 0) set_status(a.status, IBP_EALIGN);
+      zero_row(drow, nvec, lane);
+      continue;
+    }
+    const uint4* srow = reinterpret_cast<const uint4*>(a.src + off);
+    const bool raw = (__ldg(a.bitmap + (id >> 5)) >> (id & 31)) & 1u;
+    if (raw) {
+      for (uint32_t v = lane; v < nvec; v += 32) drow[v] = ld_nc_v4(srow + v);
+      continue;
+    }
+    if (4u * min_words >= R) {  // no compressed row can exist for this Mask
+      if (lane == 0) set_status(a.status, IBP_ECORRUPT);
+      zero_row(drow, nvec, lane);
+      continue;
+    }
+    for (uint32_t v = lane; v < min_vec; v += 32) st_smem_v4(sbuf + 4u * v, ld_nc_v4(srow + v));
+    __syncwarp();
+    // chunk starts: exclusive scan of the chunk sizes, 32 chunks per pass
+    uint32_t run = nch;
+    for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
+      const uint32_t k = k0 + lane;
+      uint32_t size = 0, p = 0;
+      if (k < nch) {
+        p = (sbuf[k >> 5] >> (k & 31u)) & 1u;
+        size = p ? __ldg(a.m.ckeep + k) : 32u * min(wpc, W - k * wpc);
+      }
+      const uint32_t incl = warp_inclusive_scan(size, lane);
+      if (k < nch) cinfo[k] = (run + incl - size) | (p << 31);
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    const uint32_t words = (run + 31u) >> 5;
+    if (4u * words >= R || 4ull * words > a.avail) {
+      if (lane == 0) set_status(a.status, IBP_ECORRUPT);
+      __syncwarp();
+      zero_row(drow, nvec, lane);
+      continue;
+    }
+    const uint32_t need_vec = (4u * words + 15u) >> 4;
+    for (uint32_t v = min_vec + lane; v < need_vec; v += 32)
+      st_smem_v4(sbuf + 4u * v, ld_nc_v4(srow + v));
+    __syncwarp();
+    for (uint32_t v = lane; v < nvec; v += 32) {
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t w = 4u * v + (uint32_t)e;
+        const uint32_t krw = __ldg(a.m.kr + w);
+        const uint32_t ci = cinfo[krw & 0xFFFFu];
+        const bool packed = (ci >> 31) != 0u;
+        const uint32_t bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
+        const uint32_t q = bit >> 5;
+        uint32_t x = __funnelshift_r(sbuf[q], sbuf[q + 1], bit & 31u);
+        if (packed)
+          x = (scatter_bits(x, a.m.mv, W, w) & __ldg(a.m.nm + w)) | __ldg(a.m.bitval + w);
+        o[e] = x;
+      }
+      drow[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------------
+// Compression (Core Algorithm > Compression).  One warp per row: stage the
+// row in shared memory, flag chunks with a Mask mismatch, decide the
+// participation bits, scan the chunk sizes, then every lane gathers the kept
+// bits of its words (or takes the whole word of a raw chunk) and ORs them
+// into the packed buffer at their stream offset with shared-memory atomics.
+// A row that would not shrink is written raw and flagged in the bitmap.
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
+  extern __shared__ __align__(16) uint32_t smem[];
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t wid = threadIdx.x >> 5;
+  uint32_t* obuf = smem + wid * L.total_words;
+  uint32_t* xbuf = obuf + L.sbuf_words;
+  uint32_t* cinfo = xbuf + L.xbuf_words;
+  const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
+  const uint32_t nvec = R >> 4;
+  const uint64_t wpb = blockDim.x >> 5;
+  const uint64_t stride = (uint64_t)gridDim.x * wpb;
+
+  for (uint64_t i = (uint64_t)blockIdx.x * wpb + wid; i < a.n; i += stride) {
+    const int64_t slot = a.slot_ids ? __ldg(a.slot_ids + i) : (int64_t)i;
+    if (slot < 0 || (uint64_t)slot >= a.n_rows) {
+      if (lane == 0) set_status(a.status, IBP_ERANGE);
+      if (a.stored_out && lane == 0) a.stored_out[i] = 0;
+      continue;
+    }
+    const uint4* srow = reinterpret_cast<const uint4*>(a.src + i * a.src_stride);
+    for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
+    for (uint32_t k = lane; k < nch; k += 32) cinfo[k] = 0;
+    __syncwarp();
+    for (uint32_t w = lane; w < W; w += 32)
+      if ((xbuf[w] & __ldg(a.m.mask + w)) != __ldg(a.m.bitval + w))
+        cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
+    __syncwarp();
+    uint32_t run = nch;
+    for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
+      const uint32_t k = k0 + lane;
+      uint32_t size = 0, p = 0;
+      if (k < nch) {
+        const uint32_t full = 32u * min(wpc, W - k * wpc);
+        const uint32_t keep = __ldg(a.m.ckeep + k);
+        p = (cinfo[k] == 0u && keep < full) ? 1u : 0u;
+        size = p ? keep : full;
+      }
+      const uint32_t incl = warp_inclusive_scan(size, lane);
+      __syncwarp();
+      if (k < nch) cinfo[k] = (run + incl - size) | (p << 31);
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    const uint32_t words = (run + 31u) >> 5;
+    const bool raw = 4u * words >= R;
+    uint4* dslot = reinterpret_cast<uint4*>(a.dst + (uint64_t)slot * a.slot);
+    if (raw) {
+      for (uint32_t v = lane; v < nvec; v += 32)
+        dslot[v] = *reinterpret_cast<const uint4*>(xbuf + 4u * v);
+    } else {
+      const uint32_t padded = (words + 3u) & ~3u;
+      for (uint32_t j = lane; j < padded + 4u; j += 32) obuf[j] = 0;
+      __syncwarp();
+      for (uint32_t k = lane; k < nch; k += 32)
+        if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
+      for (uint32_t w = lane; w < W; w += 32) {
+        const uint32_t krw = __ldg(a.m.kr + w);
+        const uint32_t ci = cinfo[krw & 0xFFFFu];
+        const bool packed = (ci >> 31) != 0u;
+        const uint32_t bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
+        uint32_t v = xbuf[w];
+        uint32_t nbits = 32;
+        if (packed) {
+          const uint32_t keepm = __ldg(a.m.nm + w);
+          v = gather_bits(v & keepm, a.m.mv, W, w);
+          nbits = __popc(keepm);
+        }
+        if (nbits) {
+          const uint32_t q = bit >> 5, sh = bit & 31u;
+          atomicOr(obuf + q, v << sh);
+          if (sh != 0u && sh + nbits > 32u) atomicOr(obuf + q + 1, v >> (32u - sh));
+        }
+      }
+      __syncwarp();
+      for (uint32_t v = lane; 4u * v < padded; v += 32)
+        dslot[v] = *reinterpret_cast<const uint4*>(obuf + 4u * v);
+    }
+    if (lane == 0) {
+      const uint32_t bitm = 1u << ((uint64_t)slot & 31u);
+      if (raw)
+        atomicOr(a.bitmap + ((uint64_t)slot >> 5), bitm);
+      else
+        atomicAnd(a.bitmap + ((uint64_t)slot >> 5), ~bitm);
+      if (a.stored_out) a.stored_out[i] = raw ? R : 4u * words;
+    }
+    __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------------
+// Aligned zero-copy copy (the review's GPU aligned transfer): consecutive
+// lanes take consecutive 16-byte vectors, so every warp load covers four
+// whole 128-byte lines; eight loads per thread are in flight before the
+// first store.
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(512) k_link_copy(uint4* __restrict__ dst,
+                                                   const uint4* __restrict__ src,
+                                                   uint64_t nvec) {
+  const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t T = (uint64_t)gridDim.x * blockDim.x;
+  uint64_t v = t;
+  for (; v + 7 * T < nvec; v += 8 * T) {
+    uint4 r[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) r[u] = ld_nc_v4(src + v + (uint64_t)u * T);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) dst[v + (uint64_t)u * T] = r[u];
+  }
+  for (; v < nvec; v += T) dst[v] = ld_nc_v4(src + v);
+}
+
+__global__ void __launch_bounds__(256) k_gather_copy(uint8_t* dst, const uint8_t* src,
+                                                     uint64_t slot, uint32_t row_bytes,
+                                                     const int64_t* ids, uint64_t n,
+                                                     uint64_t n_rows) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t wpb = blockDim.x >> 5;
+  const uint32_t nvec = row_bytes >> 4;
+  for (uint64_t i = (uint64_t)blockIdx.x * wpb + (threadIdx.x >> 5); i < n;
+       i += (uint64_t)gridDim.x * wpb) {
+    const int64_t id = __ldg(ids + i);
+    uint4* d = reinterpret_cast<uint4*>(dst + i * row_bytes);
+    if (id < 0 || (uint64_t)id >= n_rows) {
+      zero_row(d, nvec, lane);
+      continue;
+    }
+    const uint4* s = reinterpret_cast<const uint4*>(src + (uint64_t)id * slot);
+    for (uint32_t v = lane; v < nvec; v += 32) d[v] = ld_nc_v4(s + v);
+  }
+}
+
+// Packed-cache offsets: exclusive scan of roundup(stored, 16) in one block.
+// Thread t owns a contiguous range; range sums are scanned in shared memory.
+__global__ void __launch_bounds__(1024) k_pack_offsets(const uint32_t* stored, uint64_t n,
+                                                       uint64_t* offsets) {
+  __shared__ uint64_t part[1024];
+  const uint64_t per = (n + blockDim.x - 1) / blockDim.x;
+  const uint64_t b = (uint64_t)threadIdx.x * per;
+  const uint64_t e = min(b + per, n);
+  uint64_t sum = 0;
+  for (uint64_t i = b; i < e; ++i) sum += (__ldg(stored + i) + 15u) & ~15u;
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  for (uint32_t d = 1; d < blockDim.x; d <<= 1) {
+    const uint64_t t = threadIdx.x >= d ? part[threadIdx.x - d] : 0;
+    __syncthreads();
+    part[threadIdx.x] += t;
+    __syncthreads();
+  }
+  uint64_t run = part[threadIdx.x] - sum;
+  for (uint64_t i = b; i < e; ++i) {
+    offsets[i] = run;
+    run += (__ldg(stored + i) + 15u) & ~15u;
+  }
+  if (threadIdx.x == blockDim.x - 1) offsets[n] = part[threadIdx.x];
+}
+
+// Copy each row's stored bytes (16-byte granules) from its slot to the cache.
+__global__ void __launch_bounds__(256) k_pack_copy(uint8_t* dst, const uint64_t* offsets,
+                                                   const uint8_t* src, uint64_t slot,
+                                                   const uint32_t* stored, uint64_t n) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t wpb = blockDim.x >> 5;
+  for (uint64_t i = (uint64_t)blockIdx.x * wpb + (threadIdx.x >> 5); i < n;
+       i += (uint64_t)gridDim.x * wpb) {
+    const uint32_t nv = (__ldg(stored + i) + 15u) >> 4;
+    const uint4* s = reinterpret_cast<const uint4*>(src + i * slot);
+    uint4* d = reinterpret_cast<uint4*>(dst + __ldg(offsets + i));
+    for (uint32_t v = lane; v < nv; v += 32) d[v] = ld_nc_v4(s + v);
+  }
+}
+
+template <typename K>
+int blocks_per_sm(K kernel, int threads, size_t smem) {
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, smem) != cudaSuccess)
+    return 1;
+  return b > 0 ? b : 1;
+}
+
+uint32_t warps_for(uint32_t per_warp_bytes) {
+  uint32_t w = (96u * 1024u) / per_warp_bytes;
+  if (w > 8u) w = 8u;
+  if (w < 1u) w = 1u;
+  return w;
+}
+
+}  // namespace
+
+WarpSmem decode_smem(uint32_t W, uint32_t nch) {
+  WarpSmem L;
+  L.sbuf_words = ((W + 8u) + 3u) & ~3u;
+  L.xbuf_words = 0;
+  L.cinfo_words = (nch + 3u) & ~3u;
+  L.total_words = L.sbuf_words + L.cinfo_words;
+  return L;
+}
+
+WarpSmem encode_smem(uint32_t W, uint32_t nch) {
+  WarpSmem L;
+  L.sbuf_words = ((W + 8u) + 3u) & ~3u;
+  L.xbuf_words = (W + 3u) & ~3u;
+  L.cinfo_words = (nch + 3u) & ~3u;
+  L.total_words = L.sbuf_words + L.xbuf_words + L.cinfo_words;
+  return L;
+}
+
+cudaError_t launch_count_ones(const CountArgs& a, int sm_count, cudaStream_t st) {
+  const uint32_t tpb = 128;
+  const uint32_t gy = (a.W + tpb - 1) / tpb;
+  // enough CTAs for ~4 per SM over the word tiles; each covers n/gx rows
+  uint64_t gx = ((uint64_t)sm_count * 4 + gy - 1) / gy;
+  const uint64_t max_gx = (a.n + 63) / 64;  // at least 64 rows per CTA
+  if (gx > max_gx) gx = max_gx;
+  if (gx < 1) gx = 1;
+  if (gx > 65535) gx = 65535;
+  k_count_ones<<<dim3((uint32_t)gx, gy), tpb, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finish_meta(const uint32_t* counts, uint32_t W, uint64_t n, uint32_t num,
+                               uint32_t den, uint32_t* mask, uint32_t* bitval, cudaStream_t st) {
+  k_finish_meta<<<(W + 127) / 128, 128, 0, st>>>(counts, W, n, num, den, mask, bitval);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32_t* pre,
+                          uint32_t* kr, uint32_t* mv, uint32_t* ckeep, uint32_t* scal,
+                          uint32_t W, uint32_t wpc, uint32_t nch, cudaStream_t st) {
+  k_derive<<<1, 1024, 0, st>>>(mask, bitval, nm, pre, kr, mv, ckeep, scal, W, wpc, nch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, int sm_count, cudaStream_t st) {
+  if (a.n == 0) return cudaSuccess;
+  const WarpSmem L = decode_smem(a.m.W, a.m.nch);
+  const uint32_t warps = warps_for(4u * L.total_words);
+  const int threads = (int)(32u * warps);
+  const size_t smem = (size_t)4u * L.total_words * warps;
+  int bps;
+  if (a.ids) {
+    cudaFuncSetAttribute(k_decode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    bps = blocks_per_sm(k_decode<true>, threads, smem);
+  } else {
+    cudaFuncSetAttribute(k_decode<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    bps = blocks_per_sm(k_decode<false>, threads, smem);
+  }
+  uint64_t blocks = (uint64_t)sm_count * bps;
+  const uint64_t need = (a.n + warps - 1) / warps;
+  if (blocks > need) blocks = need;
+  if (a.ids)
+    k_decode<true><<<(uint32_t)blocks, threads, smem, st>>>(a, L);
+  else
+    k_decode<false><<<(uint32_t)blocks, threads, smem, st>>>(a, L);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode(const EncodeArgs& a, int sm_count, cudaStream_t st) {
+  if (a.n == 0) return cudaSuccess;
+  const WarpSmem L = encode_smem(a.m.W, a.m.nch);
+  const uint32_t warps = warps_for(4u * L.total_words);
+  const int threads = (int)(32u * warps);
+  const size_t smem = (size_t)4u * L.total_words * warps;
+  cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int bps = blocks_per_sm(k_encode, threads, smem);
+  uint64_t blocks = (uint64_t)sm_count * bps;
+  const uint64_t need = (a.n + warps - 1) / warps;
+  if (blocks > need) blocks = need;
+  k_encode<<<(uint32_t)blocks, threads, smem, st>>>(a, L);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,
+                        const uint32_t* stored, uint64_t n, int sm_count, cudaStream_t st) {
+  k_pack_offsets<<<1, 1024, 0, st>>>(stored, n, offsets);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || dst == nullptr || n == 0) return e;
+  uint64_t blocks = (uint64_t)sm_count * blocks_per_sm(k_pack_copy, 256, 0);
+  const uint64_t need = (n + 7) / 8;
+  if (blocks > need) blocks = need;
+  k_pack_copy<<<(uint32_t)blocks, 256, 0, st>>>(dst, offsets, src, slot, stored, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_link_copy(uint4* dst, const uint4* src, uint64_t nvec, int sm_count,
+                             cudaStream_t st) {
+  if (nvec == 0) return cudaSuccess;
+  const int threads = 512;
+  uint64_t blocks = (uint64_t)sm_count * blocks_per_sm(k_link_copy, threads, 0);
+  const uint64_t need = (nvec + threads - 1) / threads;
+  if (blocks > need) blocks = need;
+  k_link_copy<<<(uint32_t)blocks, threads, 0, st>>>(dst, src, nvec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_copy(uint8_t* dst, const uint8_t* src, uint64_t slot,
+                               uint32_t row_bytes, const int64_t* ids, uint64_t n,
+                               uint64_t n_rows, int sm_count, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  uint64_t blocks = (uint64_t)sm_count * blocks_per_sm(k_gather_copy, threads, 0);
+  const uint64_t need = (n + 7) / 8;
+  if (blocks > need) blocks = need;
+  k_gather_copy<<<(uint32_t)blocks, threads, 0, st>>>(dst, src, slot, row_bytes, ids, n, n_rows);
+  return cudaGetLastError();
+}
+
+}  // namespace ibp

@@ -163,3 +163,16 @@ def decompress_batch(src: np.ndarray, bitmap: np.ndarray, R: int, C: int, mask: 
 
 def max_threads() -> int:
     return int(lib().ibp_ref_max_threads())
+
+
+def pack_slots(slots: np.ndarray, stored: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Packed cache layout (System Integration: compressed GPU cache): row i's
+    stored bytes at offsets[i] = sum_{i'<i} roundup(stored[i'], 16); offsets has
+    n+1 entries, the last being the total.  Returns (packed uint8, offsets uint64)."""
+    sizes = (stored.astype(np.uint64) + np.uint64(15)) & ~np.uint64(15)
+    offsets = np.zeros(len(stored) + 1, np.uint64)
+    offsets[1:] = np.cumsum(sizes)
+    packed = np.zeros(int(offsets[-1]), np.uint8)
+    for i in range(len(stored)):
+        packed[int(offsets[i]):int(offsets[i]) + int(stored[i])] = slots[i, :int(stored[i])]
+    return packed, offsets

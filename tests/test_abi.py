@@ -1,0 +1,73 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point include/ibp.h declares, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+
+import pytest
+
+from lossless_invariant_bit_gb300 import ibp
+from lossless_invariant_bit_gb300 import build as libbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return ibp._lib_handle()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = ibp.declared_symbols()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding wraps each of them under the same name
+    for n in names:
+        assert callable(getattr(ibp, n)), n
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(ibp.STATUS_NAMES):
+        assert ibp.ibp_status_str(code).startswith(name)
+    assert "unknown" in ibp.ibp_status_str(99)
+
+
+def test_host_side_argument_checks(lib):
+    out = ctypes.c_void_p()
+    # geometry outside the limits is rejected before any device call
+    assert lib.ibp_store_create(ctypes.byref(out), 0, 256, 10, 0) == ibp.IBP_EINVAL
+    assert lib.ibp_store_create(ctypes.byref(out), 1000, 256, 10, 0) == ibp.IBP_EINVAL  # R % 16
+    assert lib.ibp_store_create(ctypes.byref(out), 65536, 256, 10, 0) == ibp.IBP_EINVAL  # > max
+    assert lib.ibp_store_create(ctypes.byref(out), 1024, 6, 10, 0) == ibp.IBP_EINVAL  # C % 4
+    assert lib.ibp_store_create(ctypes.byref(out), 8192, 4, 10, 0) == ibp.IBP_EINVAL  # nch > max
+    assert lib.ibp_store_create(ctypes.byref(out), 1024, 256, 0, 0) == ibp.IBP_EINVAL  # no rows
+    assert lib.ibp_store_create(ctypes.byref(out), 1024, 256, 10, 1000) == ibp.IBP_EALIGN
+    assert lib.ibp_store_create(ctypes.byref(out), 1024, 256, 10, 512) == ibp.IBP_EALIGN
+    assert lib.ibp_store_create(None, 1024, 256, 10, 0) == ibp.IBP_EINVAL
+    # NULL store
+    assert lib.ibp_build_meta(None, 16, 16, None, 1, 95, 100, None) == ibp.IBP_EINVAL
+    assert lib.ibp_compress(None, 16, 16, 16, None, 1, None, None) == ibp.IBP_EINVAL
+    assert lib.ibp_decompress(None, 16, 16, None, 1, None) == ibp.IBP_EINVAL
+    assert lib.ibp_gather_decompress(None, 16, 16, None, 16, 1, None) == ibp.IBP_EINVAL
+    assert lib.ibp_gather_decompress_strided(None, 16, 16, 16, None, 16, 1, None) == ibp.IBP_EINVAL
+    assert lib.ibp_pack(None, None, 16, None, None, 0, None) == ibp.IBP_EINVAL
+    assert lib.ibp_meta_get(None, 16, 16) == ibp.IBP_EINVAL
+    assert lib.ibp_meta_set(None, 16, 16) == ibp.IBP_EINVAL
+    assert lib.ibp_bitmap_get(None, 16) == ibp.IBP_EINVAL
+    assert lib.ibp_bitmap_set(None, 16) == ibp.IBP_EINVAL
+    assert lib.ibp_store_get_info(None, None) == ibp.IBP_EINVAL
+    st = ctypes.c_int()
+    assert lib.ibp_stream_status(None, None, ctypes.byref(st), 0) == ibp.IBP_EINVAL
+    assert lib.ibp_store_destroy(None) == ibp.IBP_OK
+    # copies: alignment and size checked on the host
+    assert lib.ibp_link_copy(16, 16, 0, None) == ibp.IBP_OK
+    assert lib.ibp_link_copy(None, 16, 16, None) == ibp.IBP_EINVAL
+    assert lib.ibp_link_copy(17, 16, 16, None) == ibp.IBP_EALIGN
+    assert lib.ibp_link_copy(16, 16, 24, None) == ibp.IBP_EALIGN
+    assert lib.ibp_gather_copy(16, 16, 512, 500, 16, 4, 10, None) == ibp.IBP_EALIGN
+    assert lib.ibp_gather_copy(16, 16, 512, 512, None, 4, 10, None) == ibp.IBP_EINVAL
+
+
+def test_binding_raises_on_error(lib):
+    with pytest.raises(ibp.IbpError) as ei:
+        ibp.ibp_store_create(1000, 256, 10)
+    assert ei.value.status == ibp.IBP_EINVAL

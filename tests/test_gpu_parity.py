@@ -1,0 +1,347 @@
+"""GPU path vs CPU oracle, through the C ABI.  Integer work: bit-exact.
+
+Covered: builder (all rows, sampled ids, host-mapped rows, thresholds),
+compressor (stored bytes, sizes, raw bitmap; HBM and host slots), decoder
+(dense slots, packed cache, gather with duplicates, strided output, host
+source), the pack step, geometry edges (R from 16 B to the 32 KB maximum, C
+above R and not dividing R, up to 256 chunks, ragged batch sizes, n = 0 and
+1), degenerate metadata (empty Mask, full Mask with rows equal to the
+Bitval), and the kernel-detected data errors.
+"""
+import numpy as np
+import pytest
+import torch
+
+from lossless_invariant_bit_gb300 import ibp
+from lossless_invariant_bit_gb300 import workloads as wl
+from oracle import ref_c
+from tests.gpu_util import (DEV, Store, assert_streams_equal, oracle_slots, rows_u8, to_dev,
+                            to_pinned)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def stores():
+    made = []
+
+    def make(*a, **k):
+        s = Store(*a, **k)
+        made.append(s)
+        return s
+
+    yield make
+    for s in made:
+        s.close()
+
+
+def gpu_compress(st, d_rows, n, slot_ids=None, host=False):
+    slots = (torch.zeros((st.n_rows, st.slot), dtype=torch.uint8, pin_memory=True) if host
+             else torch.zeros((st.n_rows, st.slot), dtype=torch.uint8, device=DEV))
+    stored = torch.zeros(n, dtype=torch.int32, device=DEV)
+    ids = None if slot_ids is None else to_dev(slot_ids.astype(np.int64))
+    ibp.ibp_compress(st.h, slots, d_rows, d_rows.stride(0) * d_rows.element_size(), ids, n,
+                     stored)
+    torch.cuda.synchronize()
+    return slots, stored.cpu().numpy().astype(np.uint32)
+
+
+# ---------------------------------------------------------------- builder
+@pytest.mark.parametrize("where", ["hbm", "host"])
+def test_build_meta_tiny(stores, where):
+    rows, _ = wl.tiny_rows(seed=0)
+    b = rows_u8(rows)
+    st = stores(1024, 256, len(b))
+    d = to_dev(b) if where == "hbm" else to_pinned(b)
+    ibp.ibp_build_meta(st.h, d, 1024, None, len(b), 95, 100)
+    m, bv = st.meta()
+    mr, br = ref_c.build_meta(b, 95, 100)
+    assert np.array_equal(m, mr) and np.array_equal(bv, br)
+    assert np.all(m == 0xFF801FFF) and np.all(bv == 0x3F800000)
+    info = ibp.ibp_store_get_info(st.h)
+    assert info.meta_valid == 1 and info.min_bits == 4 + 4 * 640 and info.max_runs == 1
+
+
+@pytest.mark.parametrize("R,num,den,per_mille", [
+    (64, 3, 4, 0), (512, 95, 100, 100), (2048, 9, 10, 50), (8192, 999, 1000, 0),
+    (32768, 1, 1, 0), (112, 51, 100, 300)])
+def test_build_meta_fuzz(stores, R, num, den, per_mille):
+    n = 3000 if R <= 8192 else 700
+    b = wl.fuzz_rows(n, R, seed=R + num)
+    ids = wl.sample_ids(n, per_mille, seed=1) if per_mille else None
+    st = stores(R, 256, n)
+    d = to_dev(b)
+    d_ids = None if ids is None else to_dev(ids)
+    ibp.ibp_build_meta(st.h, d, R, d_ids, n if ids is None else len(ids), num, den)
+    m, bv = st.meta()
+    mr, br = ref_c.build_meta(b, num, den, sample_ids=ids)
+    assert np.array_equal(m, mr) and np.array_equal(bv, br)
+
+
+def test_build_meta_many_rows_spill(stores):
+    """More rows per thread than the 8 bit-plane counters hold (255): exercises the spill."""
+    n = 400_000
+    b = wl.fuzz_rows(n, 64, seed=5)
+    st = stores(64, 16, n)
+    ibp.ibp_build_meta(st.h, to_dev(b), 64, None, n, 7, 8)
+    m, bv = st.meta()
+    mr, br = ref_c.build_meta(b, 7, 8)
+    assert np.array_equal(m, mr) and np.array_equal(bv, br)
+
+
+def test_build_meta_rejects_bad_threshold(stores):
+    st = stores(64, 16, 4)
+    d = torch.zeros((4, 64), dtype=torch.uint8, device=DEV)
+    for num, den in [(1, 2), (2, 1), (0, 0)]:
+        with pytest.raises(ibp.IbpError) as e:
+            ibp.ibp_build_meta(st.h, d, 64, None, 4, num, den)
+        assert e.value.status == ibp.IBP_EINVAL
+
+
+# ---------------------------------------------------------------- compressor + decoder
+GEOMS = [(16, 4), (16, 8), (64, 16), (112, 12), (512, 1024), (512, 256), (1024, 256),
+         (2048, 1024), (8192, 256), (4096, 4096), (8192, 8192), (32768, 128), (4096, 16),
+         (1024, 100)]
+
+
+@pytest.mark.parametrize("R,C", GEOMS)
+def test_compress_and_decompress_fuzz(stores, R, C):
+    n = 777 if R <= 8192 else 133  # ragged: not a multiple of the warps per block
+    b = wl.fuzz_rows(n, R, seed=R * 7 + C)
+    mr, br = ref_c.build_meta(b, 9, 10)
+    st = stores(R, C, n)
+    st.set_meta(mr, br)
+    d = to_dev(b)
+    slots, stored = gpu_compress(st, d, n)
+    ref_sl, ref_bm, ref_st = oracle_slots(b, C, mr, br, st.slot)
+    assert np.array_equal(stored, ref_st)
+    assert np.array_equal(st.bitmap(), ref_bm)
+    assert_streams_equal(slots.cpu().numpy(), ref_sl, ref_st)
+    assert 0 < ref_bm.sum() or True
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, slots, None, n)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
+
+
+@pytest.mark.parametrize("R,C", [(1024, 256), (8192, 256), (512, 1024)])
+def test_decompress_oracle_streams_from_host(stores, R, C):
+    """Decoder input written by the oracle, read zero-copy from pinned host memory."""
+    n = 1500
+    b = wl.fuzz_rows(n, R, seed=R + 3)
+    mr, br = ref_c.build_meta(b, 95, 100)
+    st = stores(R, C, n)
+    st.set_meta(mr, br)
+    ref_sl, ref_bm, ref_st = oracle_slots(b, C, mr, br, st.slot)
+    st.set_bitmap(ref_bm)
+    src = to_pinned(ref_sl)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, src, None, n)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
+
+
+def test_compress_into_host_slots_with_ids(stores):
+    R, C, N = 512, 256, 4000
+    n = 1000
+    b = wl.fuzz_rows(n, R, seed=77)
+    mr, br = ref_c.build_meta(b, 95, 100)
+    st = stores(R, C, N)
+    st.set_meta(mr, br)
+    slot_ids = np.random.default_rng(3).permutation(N)[:n].astype(np.int64)
+    slots, stored = gpu_compress(st, to_dev(b), n, slot_ids=slot_ids, host=True)
+    ref_sl, ref_bm, ref_st = oracle_slots(b, C, mr, br, st.slot)
+    assert np.array_equal(stored, ref_st)
+    sl = slots.numpy()[slot_ids]
+    assert_streams_equal(sl, ref_sl, ref_st)
+    bm = st.bitmap()
+    raw = np.unpackbits(bm.view(np.uint8), bitorder="little")[:N].astype(bool)
+    assert np.array_equal(np.nonzero(raw)[0], np.sort(slot_ids[ref_st == R]))
+    # gather them back through the host link, duplicates included
+    ids = np.concatenate([slot_ids, slot_ids[:300]])
+    out = torch.empty((len(ids), R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress(st.h, out, slots, None, to_dev(ids), len(ids))
+    assert st.status() == ibp.IBP_OK
+    inv = np.empty(N, np.int64)
+    inv[slot_ids] = np.arange(n)
+    assert np.array_equal(out.cpu().numpy(), b[inv[ids]])
+
+
+def test_gather_strided(stores):
+    R, C, N, T = 1024, 1024, 5000, 3
+    b = wl.fuzz_rows(N, R, seed=8)
+    mr, br = ref_c.build_meta(b, 95, 100)
+    st = stores(R, C, N)
+    st.set_meta(mr, br)
+    slots, stored = gpu_compress(st, to_dev(b), N, host=True)
+    ids = np.random.default_rng(4).integers(0, N, size=2049)
+    out = torch.full((len(ids), T, R), 0xAB, dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress_strided(st.h, out[:, 1], T * R, slots, None, to_dev(ids), len(ids))
+    assert st.status() == ibp.IBP_OK
+    o = out.cpu().numpy()
+    assert np.array_equal(o[:, 1], b[ids])
+    assert np.all(o[:, 0] == 0xAB) and np.all(o[:, 2] == 0xAB)
+
+
+def test_packed_cache_tiny(stores):
+    """Cache path: oracle-packed bytes decode on the GPU, and GPU compress + pack
+    reproduces the oracle's packed cache and offsets byte for byte."""
+    rows, pick = wl.tiny_rows(seed=0)
+    b = rows_u8(rows)
+    n, R, C = len(b), 1024, 256
+    st = stores(R, C, n, R)
+    d = to_dev(b)
+    ibp.ibp_build_meta(st.h, d, R, None, n, 95, 100)
+    mr, br = st.meta()
+    ref_sl, ref_bm, ref_st = oracle_slots(b, C, mr, br, R)
+    packed_ref, offs_ref = ref_c.pack_slots(ref_sl, ref_st)
+    assert int(ref_st.sum()) == 1_355_104
+    # decode the oracle's cache
+    st.set_bitmap(ref_bm)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, to_dev(packed_ref), to_dev(offs_ref[:-1]), n)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
+    # GPU compress + pack
+    slots, stored = gpu_compress(st, d, n)
+    d_stored = to_dev(stored.astype(np.int32))
+    offs = torch.zeros(n + 1, dtype=torch.int64, device=DEV)
+    ibp.ibp_pack(st.h, None, offs, slots, d_stored, n)
+    total = int(offs[-1].item())
+    assert total == int(offs_ref[-1])
+    packed = torch.zeros(total, dtype=torch.uint8, device=DEV)
+    ibp.ibp_pack(st.h, packed, offs, slots, d_stored, n)
+    torch.cuda.synchronize()
+    assert np.array_equal(offs.cpu().numpy().astype(np.uint64), offs_ref)
+    pk = packed.cpu().numpy()
+    for i in range(n):
+        o, s = int(offs_ref[i]), int(ref_st[i])
+        assert np.array_equal(pk[o:o + s], packed_ref[o:o + s]), i
+
+
+# ---------------------------------------------------------------- degenerate metadata, sizes
+def test_empty_mask_all_raw(stores):
+    R, C, n = 256, 64, 100
+    b = wl.fuzz_rows(n, R, seed=12)
+    st = stores(R, C, n)
+    slots, stored = gpu_compress(st, to_dev(b), n)  # fresh store: Mask all zero
+    assert np.all(stored == R)
+    assert np.all(np.unpackbits(st.bitmap().view(np.uint8), bitorder="little")[:n] == 1)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, slots, None, n)
+    assert st.status() == ibp.IBP_OK and np.array_equal(out.cpu().numpy(), b)
+
+
+def test_full_mask_rows_equal_bitval(stores):
+    R, C, n = 4096, 256, 64
+    bitval = np.random.default_rng(2).integers(0, 1 << 32, size=R // 4, dtype=np.uint64)
+    bitval = bitval.astype(np.uint32)
+    rows = np.repeat(bitval[None, :], n, axis=0).view(np.uint8)
+    st = stores(R, C, n)
+    ibp.ibp_build_meta(st.h, to_dev(rows), R, None, n, 95, 100)
+    m, bv = st.meta()
+    assert np.all(m == 0xFFFFFFFF) and np.array_equal(bv, bitval)
+    slots, stored = gpu_compress(st, to_dev(rows), n)
+    assert np.all(stored == 4)  # 16 participation bits in one word
+    assert np.all(slots.cpu().numpy()[:, :4].view(np.uint32) == 0xFFFF)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, slots, None, n)
+    assert np.array_equal(out.cpu().numpy(), rows)
+
+
+def test_zero_and_one_rows(stores):
+    R, C = 512, 256
+    b = wl.fuzz_rows(1, R, seed=1)
+    st = stores(R, C, 1)
+    mr, br = ref_c.build_meta(b, 1, 1)
+    st.set_meta(mr, br)
+    out = torch.empty((1, R), dtype=torch.uint8, device=DEV)
+    d = to_dev(b)
+    ibp.ibp_compress(st.h, out, d, R, None, 0)   # n = 0: no-op
+    ibp.ibp_decompress(st.h, out, d, None, 0)
+    slots, stored = gpu_compress(st, d, 1)
+    ibp.ibp_decompress(st.h, out, slots, None, 1)
+    assert st.status() == ibp.IBP_OK and np.array_equal(out.cpu().numpy(), b)
+
+
+# ---------------------------------------------------------------- data errors
+def test_out_of_range_ids_flagged_and_zeroed(stores):
+    R, C, N = 512, 256, 100
+    b = wl.fuzz_rows(N, R, seed=21)
+    mr, br = ref_c.build_meta(b, 95, 100)
+    st = stores(R, C, N)
+    st.set_meta(mr, br)
+    slots, _ = gpu_compress(st, to_dev(b), N)
+    ids = np.array([0, 5, N, -1, 7], np.int64)
+    out = torch.full((len(ids), R), 0x55, dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress(st.h, out, slots, None, to_dev(ids), len(ids))
+    assert st.status() == ibp.IBP_ERANGE
+    assert st.status() == ibp.IBP_OK  # reset by the previous read
+    o = out.cpu().numpy()
+    assert np.array_equal(o[[0, 1, 4]], b[[0, 5, 7]])
+    assert np.all(o[[2, 3]] == 0)
+
+
+def test_corrupt_stream_flagged_and_zeroed(stores):
+    """A row flagged compressed whose header says every chunk is raw needs more
+    than R bytes: the decoder reports it and writes zeros (the stream is built on
+    the host; every read stays inside the slot)."""
+    R, C, n = 1024, 256, 4
+    rows, _ = wl.tiny_rows(seed=0, n_rows=64, raw_frac=0.0)
+    b = rows_u8(rows)[:n]
+    mr, br = ref_c.build_meta(rows_u8(rows), 95, 100)
+    st = stores(R, C, n)
+    st.set_meta(mr, br)
+    ref_sl, ref_bm, ref_st = oracle_slots(b, C, mr, br, R)
+    assert ref_bm.sum() == 0
+    ref_sl[2, 0] &= 0xF0  # clear the 4 participation bits of row 2
+    st.set_bitmap(ref_bm)
+    out = torch.full((n, R), 0x55, dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, to_dev(ref_sl), None, n)
+    assert st.status() == ibp.IBP_ECORRUPT
+    o = out.cpu().numpy()
+    assert np.all(o[2] == 0)
+    assert np.array_equal(o[[0, 1, 3]], b[[0, 1, 3]])
+
+
+def test_misaligned_offset_flagged(stores):
+    R, C, n = 512, 256, 3
+    b = wl.fuzz_rows(n, R, seed=4)
+    st = stores(R, C, n)
+    slots, stored = gpu_compress(st, to_dev(b), n)  # all raw (empty Mask)
+    flat = slots.reshape(-1)
+    offs = np.array([0, 2 * st.slot + 8, st.slot], np.uint64)
+    out = torch.full((n, R), 0x55, dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, flat, to_dev(offs), n)
+    assert st.status() == ibp.IBP_EALIGN
+    o = out.cpu().numpy()
+    assert np.array_equal(o[0], b[0]) and np.all(o[1] == 0) and np.array_equal(o[2], b[1])
+
+
+def test_host_checks_alignment(stores):
+    st = stores(512, 256, 8)
+    d = torch.zeros(8 * 512 + 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(ibp.IbpError) as e:
+        ibp.ibp_decompress(st.h, d[1:], d, None, 1)
+    assert e.value.status == ibp.IBP_EALIGN
+    with pytest.raises(ibp.IbpError) as e:
+        ibp.ibp_decompress(st.h, d, d, None, 9)  # more rows than slots
+    assert e.value.status == ibp.IBP_ERANGE
+
+
+# ---------------------------------------------------------------- copies
+def test_link_copy_and_gather_copy():
+    n = (1 << 22) + 48
+    src = torch.randint(0, 256, (n,), dtype=torch.uint8).pin_memory()
+    dst = torch.empty(n, dtype=torch.uint8, device=DEV)
+    ibp.ibp_link_copy(dst, src, n)
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu(), src)
+    R, S, N = 512, 640, 1000
+    store = torch.randint(0, 256, (N, S), dtype=torch.uint8).pin_memory()
+    ids = torch.tensor([3, 999, 0, 3, 1000, -2], dtype=torch.int64, device=DEV)
+    out = torch.full((6, R), 7, dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_copy(out, store, S, R, ids, 6, N)
+    o = out.cpu()
+    assert torch.equal(o[:4], store[[3, 999, 0, 3], :R])
+    assert torch.all(o[4:] == 0)
