@@ -161,7 +161,7 @@ def run_ours(args, rank, world, torch, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     peaks = measured_peaks()
-    store = SparseStore(torch, ibp, wl, dev, seed=args.seed)
+    store = SparseStore(torch, ibp, wl, dev, n_rows=args.rows, seed=args.seed)
     R, n = store.R, args.batch
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -185,17 +185,17 @@ def run_ours(args, rank, world, torch, dist):
     torch.cuda.empty_cache()
     log("link probe: %.1f GB/s host->HBM" % link_gbs)
 
-    # --- batches (each rank its own ids: weak scaling)
-    total = args.warmup + args.steps
+    # --- a pool of distinct id batches, cycled (each rank its own: weak scaling)
+    pool = min(args.pool, args.warmup + args.steps)
     ids_np = [wl.uniform_ids(n, store.n_rows, seed=args.seed, batch=rank * 100000 + b)
-              for b in range(total)]
+              for b in range(pool)]
     ids_dev = [torch.from_numpy(x).to(dev) for x in ids_np]
     out = torch.empty((n, R), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ratios = [float(store.stored_np[x].sum()) / (n * R) for x in ids_np]
 
     def step_device(b):
-        ibp.ibp_gather_decompress(store.st, out, store.slots, None, ids_dev[b], n, sp)
+        ibp.ibp_gather_decompress(store.st, out, store.slots, None, ids_dev[b % pool], n, sp)
 
     def timed(fn, steps_from, count, pre=None):
         evs = []
@@ -232,10 +232,10 @@ def run_ours(args, rank, world, torch, dist):
     rows_all = n * args.steps * world
     value = rows_all * R / t_total / 1e9
     t_launch = statistics.mean(times)
-    ratio = statistics.mean(ratios[args.warmup:])
+    ratio = statistics.mean(ratios[(args.warmup + b) % pool] for b in range(args.steps))
 
     # parity spot check of the last timed batch against the oracle (rows sampled)
-    last = args.warmup + args.steps - 1
+    last = (args.warmup + args.steps - 1) % pool
     ibp.ibp_gather_decompress(store.st, out, store.slots, None, ids_dev[last], n, sp)
     torch.cuda.synchronize()
     pick = np.random.default_rng(1).choice(n, size=2000, replace=False)
@@ -245,7 +245,7 @@ def run_ours(args, rank, world, torch, dist):
 
     # --- raw gather baseline (uncompressed rows over the same link)
     raw_times = timed(lambda b: ibp.ibp_gather_copy(out, store.raw_host, store.slot, R,
-                                                    ids_dev[b], n, store.n_rows, sp),
+                                                    ids_dev[b % pool], n, store.n_rows, sp),
                       args.warmup, args.steps)
     raw_gbs = n * R * len(raw_times) / sum(raw_times) / 1e9
 
@@ -255,7 +255,7 @@ def run_ours(args, rank, world, torch, dist):
     ids_buf = torch.empty(n, dtype=torch.int64, device=dev)
 
     def step_e2e(b):
-        ids_buf.copy_(ids_host[b], non_blocking=True)
+        ids_buf.copy_(ids_host[b % pool], non_blocking=True)
         ibp.ibp_gather_decompress(store.st, out, store.slots, None, ids_buf, n, sp)
         out_host.copy_(out, non_blocking=True)
 
@@ -273,8 +273,8 @@ def run_ours(args, rank, world, torch, dist):
     hbm = peaks["hbm_gbs"]
     roof = min(hbm, link_gbs / ratio)
     delivered_per_launch = n * R / t_launch / 1e9
-    algo_bytes = sum(float(store.stored_np[x].sum()) + n * R + 8 * n
-                     for x in ids_np[args.warmup:]) / args.steps
+    algo_bytes = statistics.mean(float(store.stored_np[ids_np[(args.warmup + b) % pool]].sum())
+                                 + n * R + 8 * n for b in range(args.steps))
     result = {
         "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
         "value": round(value, 3),
@@ -293,7 +293,7 @@ def run_ours(args, rank, world, torch, dist):
                         "host slots, chunk 1 KB, 1% sample, T=0.95, batches of 200,000 "
                         "uniform ids",
             "rows": store.n_rows, "row_bytes": R, "chunk_bytes": store.C,
-            "batch_ids": n, "source": "pinned host (zero-copy)",
+            "batch_ids": n, "distinct_batches": pool, "source": "pinned host (zero-copy)",
             "l2": "flushed between steps (256 MB write, outside the timed events)",
             "parallelism": "dp%d (id batches sharded, no collective)" % world,
         },
@@ -323,29 +323,33 @@ def run_ours(args, rank, world, torch, dist):
 
     # --- CPU baseline: the oracle on the host cores, one batch (rank 0, N = 1)
     if rank == 0 and world == 1 and not args.no_cpu:
-        result["cpu_baseline"] = cpu_baseline(store, ids_np[last], ibp, sample=n)
+        result["cpu_baseline"] = cpu_baseline(store, ids_np, ibp)
     store.close(ibp)
     return result
 
 
-def cpu_baseline(store, ids, ibp, sample):
-    from oracle import ref_c
+def cpu_baseline(store, batches, ibp, seconds=1.5):
+    """The oracle's decoder on the host cores over whole batches of this workload,
+    until about `seconds` of wall time (x cores of CPU work) have been spent."""
     mask = np.zeros(store.R // 4, np.uint32)
     bitval = np.zeros(store.R // 4, np.uint32)
     ibp.ibp_meta_get(store.st, mask, bitval)
     bitmap = np.zeros((store.n_rows + 31) // 32, np.uint32)
     ibp.ibp_bitmap_get(store.st, bitmap)
     threads = len(os.sched_getaffinity(0))
-    ids = ids[:sample]
-    cpu_oracle_decode(store, ids[:1000], mask, bitval, bitmap, threads)  # warm
-    t0 = time.perf_counter()
-    out, bad = cpu_oracle_decode(store, ids, mask, bitval, bitmap, threads)
-    dt = time.perf_counter() - t0
-    assert bad == 0
-    return {"value": round(len(ids) * store.R / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+    cpu_oracle_decode(store, batches[0][:1000], mask, bitval, bitmap, threads)  # warm
+    rows, dt, k = 0, 0.0, 0
+    while dt < seconds and k < len(batches):
+        t0 = time.perf_counter()
+        _, bad = cpu_oracle_decode(store, batches[k], mask, bitval, bitmap, threads)
+        dt += time.perf_counter() - t0
+        assert bad == 0
+        rows += len(batches[k])
+        k += 1
+    return {"value": round(rows * store.R / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": "one batch of %d ids of the same workload, oracle C decoder, OpenMP "
-                      "over rows" % len(ids)}
+            "sample": "%d batches of %d ids of the same workload (%.1f s wall), oracle C "
+                      "decoder, OpenMP over rows" % (k, len(batches[0]), dt)}
 
 
 def run_reference(args, rank, world, torch):
@@ -366,8 +370,10 @@ def run_reference(args, rank, world, torch):
     ref_c.compress_batch(rb, C, mask, bitval, slots, bitmap, nthreads=threads)
     n = args.batch
     times = []
+    pool = [wl.uniform_ids(n, n_rows, seed=args.seed, batch=b)
+            for b in range(min(args.pool, args.warmup + args.steps))]
     for b in range(args.warmup + args.steps):
-        ids = wl.uniform_ids(n, n_rows, seed=args.seed, batch=b)
+        ids = pool[b % len(pool)]
         t0 = time.perf_counter()
         _, bad = ref_c.decompress_batch(slots, bitmap, R, C, mask, bitval, ids=ids,
                                         slot_stride=slot, nthreads=threads)
@@ -397,8 +403,10 @@ def run_reference(args, rank, world, torch):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--rows", type=int, default=2_000_000)
+    ap.add_argument("--pool", type=int, default=20, help="distinct id batches, cycled")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch", type=int, default=200_000)
     ap.add_argument("--seed", type=int, default=0)

@@ -54,6 +54,7 @@ extern "C" {
 
 #define IBP_MAX_ROW_BYTES 32768u
 #define IBP_MAX_CHUNKS 256u
+#define IBP_NOALLOC_MAX_ROW_BYTES 8192u
 
 typedef enum {
   IBP_OK = 0,
@@ -115,6 +116,30 @@ IBP_API ibp_status ibp_store_get_info(const ibp_store* store, ibp_store_info* in
 IBP_API ibp_status ibp_build_meta(ibp_store* store, const void* rows, uint64_t row_stride,
                           const int64_t* sample_ids, uint64_t n, uint32_t thr_num,
                           uint32_t thr_den, ibp_stream_t stream);
+
+/* Allocation-free builder.  The paper has no counterpart: this entry point
+ * exists for callers that cannot allocate device memory when they build a
+ * Mask/Bitval -- code inside another framework's memory pool, whose allocator
+ * must own every device allocation, or a latency-sensitive loop where
+ * cudaMalloc's implicit device synchronisation would stall other streams.
+ * It computes exactly what ibp_build_meta computes (same arguments and
+ * threshold rule) but needs no store and calls no allocating routine: the
+ * per-bit ones counters live in a fixed 256 KiB array of device memory that
+ * the library holds on every GPU that loads it, until the process exits.
+ *   rows, row_stride, sample_ids, n, thr_num, thr_den  as for ibp_build_meta
+ *   row_bytes    R, a multiple of 16, at most IBP_NOALLOC_MAX_ROW_BYTES
+ *                (larger rows are rejected with IBP_EINVAL)
+ *   mask_out, bitval_out  device uint32[R/4] each, written by the call
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call clears and reuses the same array, so calls whose work
+ * overlaps on the GPU (other streams, other host threads) race and give wrong
+ * results: serialise them.  Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA. */
+IBP_API ibp_status ibp_build_meta_noalloc(const void* rows, uint64_t row_stride,
+                                          uint32_t row_bytes, const int64_t* sample_ids,
+                                          uint64_t n, uint32_t thr_num, uint32_t thr_den,
+                                          uint32_t* mask_out, uint32_t* bitval_out,
+                                          ibp_stream_t stream);
 
 /* Compression (Core Algorithm > Compression; System Integration: in-place
  * compression into fixed-size buffers, GPU bitmask of compressed tensors):

@@ -47,6 +47,7 @@ _SIGS = {
     "ibp_store_destroy": [_P],
     "ibp_store_get_info": [_P, ctypes.POINTER(ibp_store_info)],
     "ibp_build_meta": [_P, _P, _U64, _P, _U64, _U32, _U32, _P],
+    "ibp_build_meta_noalloc": [_P, _U64, _U32, _P, _U64, _U32, _U32, _P, _P, _P],
     "ibp_compress": [_P, _P, _P, _U64, _P, _U64, _P, _P],
     "ibp_decompress": [_P, _P, _P, _P, _U64, _P],
     "ibp_gather_decompress": [_P, _P, _P, _P, _P, _U64, _P],
@@ -138,6 +139,15 @@ def ibp_build_meta(store: int, rows, row_stride: int, sample_ids, n: int, thr_nu
                    thr_den: int, stream=None) -> None:
     _check(_lib_handle().ibp_build_meta(store, _ptr(rows), row_stride, _ptr(sample_ids), n,
                                         thr_num, thr_den, _stream(stream)), "ibp_build_meta")
+
+
+def ibp_build_meta_noalloc(rows, row_stride: int, row_bytes: int, sample_ids, n: int,
+                           thr_num: int, thr_den: int, mask_out, bitval_out, stream=None) -> None:
+    """Builder that allocates nothing: Mask/Bitval into the caller's device arrays."""
+    _check(_lib_handle().ibp_build_meta_noalloc(_ptr(rows), row_stride, row_bytes,
+                                                _ptr(sample_ids), n, thr_num, thr_den,
+                                                _ptr(mask_out), _ptr(bitval_out),
+                                                _stream(stream)), "ibp_build_meta_noalloc")
 
 
 def ibp_compress(store: int, dst_slots, src_rows, src_stride: int, slot_ids, n: int,
