@@ -16,6 +16,8 @@ struct ibp_store {
   int sm_count;
   void* base;  // one device allocation, carved below
   uint32_t *mask, *bitval, *nm, *pre, *kr, *mv, *ckeep, *scal, *counts, *bitmap, *status;
+  uint4 *t2, *t5;  // fast-decoder descriptors
+  uint32_t* gtab;
   uint64_t bitmap_words;
 };
 
@@ -51,7 +53,7 @@ ibp::MetaView view(const ibp_store* s) {
 
 ibp_status derive(ibp_store* s, cudaStream_t st) {
   return cu(ibp::launch_derive(s->mask, s->bitval, s->nm, s->pre, s->kr, s->mv, s->ckeep,
-                               s->scal, s->W, s->wpc, s->nch, st));
+                               s->scal, s->t2, s->t5, s->gtab, s->W, s->wpc, s->nch, st));
 }
 
 ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void* src,
@@ -66,6 +68,9 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   if (e != IBP_OK) return e;
   ibp::DecodeArgs a;
   a.m = view(s);
+  a.t2 = s->t2;
+  a.t5 = s->t5;
+  a.gtab = s->gtab;
   a.bitmap = s->bitmap;
   a.status = s->status;
   a.src = static_cast<const uint8_t*>(src);
@@ -128,9 +133,11 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
     return IBP_ECUDA;
   }
   // words: mask, bitval, nm, pre, kr (5W) + mv (5W) + ckeep (nch) + scal (4)
-  //        + counts (32W) + status (4) + bitmap, each piece 16-byte aligned
+  //        + counts (32W) + status (4) + t2 (4W) + t5 (8W) + gtab (W/4) + bitmap,
+  //        each piece 16-byte aligned
   auto r4 = [](uint64_t x) { return (x + 3u) & ~(uint64_t)3u; };
-  const uint64_t words = 10ull * r4(W) + r4(nch) + 4 + 32ull * W + 4 + r4(s->bitmap_words);
+  const uint64_t words = 10ull * r4(W) + r4(nch) + 4 + 32ull * W + 4 + 12ull * W +
+                         r4(W / 4 + 1) + r4(s->bitmap_words);
   if (cudaMalloc(&s->base, words * 4) != cudaSuccess) {
     cudaGetLastError();
     delete s;
@@ -152,6 +159,9 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
   s->scal = take(4);
   s->counts = take(32ull * W);
   s->status = take(4);
+  s->t2 = reinterpret_cast<uint4*>(take(4ull * W));
+  s->t5 = reinterpret_cast<uint4*>(take(8ull * W));
+  s->gtab = take(W / 4 + 1);
   s->bitmap = take(s->bitmap_words);
   ibp_status e = cu(cudaMemset(s->base, 0, words * 4));
   if (e == IBP_OK) e = derive(s, 0);  // all-zero Mask: tables for "everything raw"

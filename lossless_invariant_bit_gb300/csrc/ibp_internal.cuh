@@ -31,6 +31,9 @@ struct MetaView {
 
 struct DecodeArgs {
   MetaView m;
+  const uint4* t2;          // fast-decoder descriptors (two-run form), W entries
+  const uint4* t5;          // fast-decoder descriptors (network form), 2W entries
+  const uint32_t* gtab;     // fast-decoder group table, W/4 entries
   const uint32_t* bitmap;
   uint32_t* status;
   const uint8_t* src;
@@ -75,6 +78,15 @@ struct WarpSmem {
   uint32_t total_words; // per warp
 };
 
+// Shared-memory layout of the fast decoder (in words): descriptor table and
+// group table per CTA, then per warp P stream buffers and the chunk starts.
+struct FastLayout {
+  uint32_t table_words;
+  uint32_t gtab_words;
+  uint32_t sbuf_words;
+  uint32_t warp_words;
+};
+
 WarpSmem decode_smem(uint32_t W, uint32_t nch);
 WarpSmem encode_smem(uint32_t W, uint32_t nch);
 
@@ -84,7 +96,8 @@ cudaError_t launch_finish_meta(const uint32_t* counts, uint32_t W, uint64_t n, u
                                uint32_t den, uint32_t* mask, uint32_t* bitval, cudaStream_t st);
 cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32_t* pre,
                           uint32_t* kr, uint32_t* mv, uint32_t* ckeep, uint32_t* scal,
-                          uint32_t W, uint32_t wpc, uint32_t nch, cudaStream_t st);
+                          uint4* t2, uint4* t5, uint32_t* gtab, uint32_t W, uint32_t wpc,
+                          uint32_t nch, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_encode(const EncodeArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,
