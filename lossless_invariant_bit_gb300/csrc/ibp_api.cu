@@ -82,6 +82,12 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.n_rows = s->n_rows;
   a.dst = static_cast<uint8_t*>(dst);
   a.dst_stride = dst_stride;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, src) != cudaSuccess) {
+    cudaGetLastError();
+    return IBP_EINVAL;
+  }
+  a.src_on_device = attr.type == cudaMemoryTypeDevice;
   return cu(ibp::launch_decode(a, s->sm_count, st));
 }
 
@@ -136,8 +142,8 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
   //        + counts (32W) + status (4) + t2 (4W) + t5 (8W) + gtab (W/4) + bitmap,
   //        each piece 16-byte aligned
   auto r4 = [](uint64_t x) { return (x + 3u) & ~(uint64_t)3u; };
-  const uint64_t words = 10ull * r4(W) + r4(nch) + 4 + 32ull * W + 4 + 12ull * W +
-                         r4(W / 4 + 1) + r4(s->bitmap_words);
+  const uint64_t words = 10ull * r4(W) + r4(nch) + 16 + 32ull * W + 4 + 12ull * W +
+                         r4(W / 4) + r4(nch) + r4(s->bitmap_words);
   if (cudaMalloc(&s->base, words * 4) != cudaSuccess) {
     cudaGetLastError();
     delete s;
@@ -156,12 +162,12 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
   s->kr = take(W);
   s->mv = take(5ull * W);
   s->ckeep = take(nch);
-  s->scal = take(4);
+  s->scal = take(16);
   s->counts = take(32ull * W);
   s->status = take(4);
   s->t2 = reinterpret_cast<uint4*>(take(4ull * W));
   s->t5 = reinterpret_cast<uint4*>(take(8ull * W));
-  s->gtab = take(W / 4 + 1);
+  s->gtab = take(r4(W / 4) + r4(nch));
   s->bitmap = take(s->bitmap_words);
   ibp_status e = cu(cudaMemset(s->base, 0, words * 4));
   if (e == IBP_OK) e = derive(s, 0);  // all-zero Mask: tables for "everything raw"

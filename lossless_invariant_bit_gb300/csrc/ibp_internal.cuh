@@ -16,7 +16,9 @@ namespace ibp {
 //   mv            5 x W move masks of the bit-gather network of nm (stage i at i*W)
 //   ckeep         nch words: kept bits per chunk
 //   scal          [0] min_bits = nch + sum(ckeep), [1] max runs of one word's nm,
-//                 [2] meta valid flag
+//                 [2] meta valid flag, [3] uniform flag (all words share ~Mask
+//                 and Bitval, <= 2 runs), [4] run0, [5] run1, [6] s0 | s1 << 8,
+//                 [7] Bitval, [8] kept bits per word (of the uniform word)
 struct MetaView {
   const uint32_t* mask;
   const uint32_t* bitval;
@@ -45,6 +47,7 @@ struct DecodeArgs {
   uint64_t n_rows;
   uint8_t* dst;
   uint64_t dst_stride;
+  bool src_on_device;       // src is device (HBM) memory, not host-mapped memory
 };
 
 struct EncodeArgs {

@@ -213,19 +213,36 @@ __global__ void __launch_bounds__(1024) k_derive(uint32_t* mask, uint32_t* bitva
 }
 
 // Shared-memory decode descriptors for the fast decoder (one block; runs
-// after k_derive, whose nm/pre/mv it reads):
-//   t2 = {run0, run1, Bitval, pre | s0 << 20 | s1 << 25} -- ~Mask as at most
+// after k_derive, whose nm/pre/mv/ckeep it reads).  soff[w] is word w's bit
+// offset in a stream whose chunks all participate: nch + the kept bits of
+// every earlier word.
+//   t2 = {run0, run1, Bitval, soff | s0 << 20 | s1 << 25} -- ~Mask as at most
 //        two runs of kept bits: run r takes the next len_r stream bits, shifted
 //        left by s_r (its start minus the kept bits before it); valid when
 //        every word has <= 2 runs
-//   t5 = {mv0, mv1, mv2, mv3}, {mv4, ~Mask, Bitval, pre} -- scatter network
-//   gtab[g] = chunk of words 4g..4g+3 | (4g - first word of that chunk) << 16
+//   t5 = {mv0, mv1, mv2, mv3}, {mv4, ~Mask, Bitval, soff} -- scatter network
+//   gtab[g] = chunk of words 4g..4g+3 | (4g - first word of that chunk) << 16,
+//   then (from word roundup(W/4, 4)) the all-packed start of each chunk
 // Word w = 4g + e sits at t2[e*G + g] and t5[(2e + h)*G + g] (G = W/4): the
 // lanes of a warp read consecutive 16-byte entries, free of bank conflicts.
 __global__ void __launch_bounds__(1024) k_derive_fast(const uint32_t* nm, const uint32_t* bitval,
                                                       const uint32_t* pre, const uint32_t* mv,
-                                                      uint4* t2, uint4* t5, uint32_t* gtab,
-                                                      uint32_t W, uint32_t wpc) {
+                                                      const uint32_t* ckeep, uint4* t2, uint4* t5,
+                                                      uint32_t* gtab, uint32_t* scal, uint32_t W,
+                                                      uint32_t wpc, uint32_t nch) {
+  __shared__ uint32_t s_start[IBP_MAX_CHUNKS];
+  __shared__ uint32_t s_same;
+  if (threadIdx.x == 0) {
+    s_same = 1;
+    uint32_t run = nch;
+    for (uint32_t k = 0; k < nch; ++k) {
+      s_start[k] = run;
+      run += ckeep[k];
+    }
+  }
+  __syncthreads();
+  const uint32_t G = W >> 2;
+  const uint32_t G4 = (G + 3u) & ~3u;
   for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
     const uint32_t keepm = nm[w];
     const uint32_t r0 = keepm & ~(keepm + (keepm & (0u - keepm)));
@@ -233,16 +250,37 @@ __global__ void __launch_bounds__(1024) k_derive_fast(const uint32_t* nm, const 
     const uint32_t r1 = rest & ~(rest + (rest & (0u - rest)));
     const uint32_t s0 = r0 ? (uint32_t)(__ffs(r0) - 1) : 0u;
     const uint32_t s1 = r1 ? (uint32_t)(__ffs(r1) - 1) - (uint32_t)__popc(r0) : 0u;
-    const uint32_t G = W >> 2, g = w >> 2, e = w & 3u;
+    const uint32_t soff = s_start[w / wpc] + pre[w];
+    const uint32_t g = w >> 2, e = w & 3u;
     if (g < G) {
-      t2[e * G + g] = make_uint4(r0, r1, bitval[w], pre[w] | (s0 << 20) | (s1 << 25));
+      t2[e * G + g] = make_uint4(r0, r1, bitval[w], soff | (s0 << 20) | (s1 << 25));
       t5[2 * e * G + g] = make_uint4(mv[w], mv[W + w], mv[2 * W + w], mv[3 * W + w]);
-      t5[(2 * e + 1) * G + g] = make_uint4(mv[4 * W + w], keepm, bitval[w], pre[w]);
+      t5[(2 * e + 1) * G + g] = make_uint4(mv[4 * W + w], keepm, bitval[w], soff);
     }
   }
-  for (uint32_t g = threadIdx.x; 4 * g < W; g += blockDim.x) {
+  for (uint32_t g = threadIdx.x; g < G; g += blockDim.x) {
     const uint32_t k = (4 * g) / wpc;
     gtab[g] = k | ((4 * g - k * wpc) << 16);
+  }
+  for (uint32_t k = threadIdx.x; k < nch; k += blockDim.x) gtab[G4 + k] = s_start[k];
+  // uniform store: every word has the same ~Mask and Bitval, with <= 2 runs
+  for (uint32_t w = threadIdx.x; w < W; w += blockDim.x)
+    if (nm[w] != nm[0] || bitval[w] != bitval[0]) atomicAnd(&s_same, 0u);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t keepm = nm[0];
+    const uint32_t r0 = keepm & ~(keepm + (keepm & (0u - keepm)));
+    const uint32_t rest = keepm & ~r0;
+    const uint32_t r1 = rest & ~(rest + (rest & (0u - rest)));
+    const uint32_t s0 = r0 ? (uint32_t)(__ffs(r0) - 1) : 0u;
+    const uint32_t s1 = r1 ? (uint32_t)(__ffs(r1) - 1) - (uint32_t)__popc(r0) : 0u;
+    const bool two = (rest & ~r1) == 0u;
+    scal[3] = (s_same && two) ? 1u : 0u;
+    scal[4] = r0;
+    scal[5] = r1;
+    scal[6] = s0 | (s1 << 8);
+    scal[7] = bitval[0];
+    scal[8] = (uint32_t)__popc(keepm);
   }
 }
 
@@ -355,20 +393,70 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
 // Fast decompression for rows of at most 2 KB whose chunks hold whole groups
 // of 4 words (C % 16 == 0): the common geometries (512 B - 2 KB rows, chunks
 // of 256 B / 1 KB / 4 KB).  Differences from k_decode:
+//   - a warp takes P rows per batch and keeps the next batch in flight while
+//     it decodes the current one: cp.async copies land each batch in one of
+//     two shared-memory stages, so the bytes in flight cost no registers; the
+//     batch after that is resolved (id -> offset, raw bit) one step ahead, so
+//     the dependent id -> slot -> data loads overlap too;
+//   - a row whose chunks all participate (the usual case) needs no scan: word
+//     w's kept bits sit at a static offset (for a uniform store, one whose
+//     words all share the same ~Mask and Bitval, nch + w*keep);
 //   - the per-word decode descriptors sit in shared memory, staged once per
-//     persistent CTA, and a lane decodes a group of 4 words per descriptor
-//     lookup of its chunk;
-//   - where no word of ~Mask has more than two runs of kept bits (fp32
-//     sign/exponent masks), the scatter is two shift-and-mask steps instead
-//     of the 5-stage network;
-//   - a warp takes P rows per batch and keeps the next batch's loads in
-//     flight (registers) while it decodes the current one from shared
-//     memory; the batch after that is resolved (id -> offset, raw bit) one
-//     iteration ahead, so the dependent id -> slot -> data loads overlap.
-// Raw rows go from registers straight to the output.
+//     persistent CTA; where no word of ~Mask has more than two runs of kept
+//     bits (fp32 sign/exponent masks), the scatter is two shift-and-mask
+//     steps instead of the 5-stage network.
 // ------------------------------------------------------------------------
-template <bool kIds, int P, int V>
-__global__ void __launch_bounds__(256, 3) k_decode_fast(DecodeArgs a, FastLayout L) {
+__device__ __forceinline__ void cp_async16(uint32_t* sdst, const void* gsrc) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(sdst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_prev() {  // all but the newest group done
+  asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+}
+
+// Four output words 4g..4g+3 of a row whose chunk participates: their kept
+// bits start at the static offsets plus `delta` (the extra bits of raw chunks
+// earlier in the row).
+__device__ __forceinline__ uint4 decode_group(const uint4* tab, const uint32_t* sb, uint32_t g,
+                                              uint32_t G, uint32_t delta, bool net5) {
+  uint32_t o[4];
+  if (!net5) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint4 t = tab[(uint32_t)e * G + g];
+      const uint32_t bit = (t.w & 0xFFFFFu) + delta;
+      const uint32_t q = bit >> 5;
+      const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
+      o[e] = ((x << ((t.w >> 20) & 31u)) & t.x) | ((x << (t.w >> 25)) & t.y) | t.z;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint4 t0 = tab[2u * (uint32_t)e * G + g];
+      const uint4 t1 = tab[(2u * (uint32_t)e + 1u) * G + g];
+      const uint32_t bit = t1.w + delta;
+      const uint32_t q = bit >> 5;
+      uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
+      x = (x & ~t1.x) | ((x << 16) & t1.x);
+      x = (x & ~t0.w) | ((x << 8) & t0.w);
+      x = (x & ~t0.z) | ((x << 4) & t0.z);
+      x = (x & ~t0.y) | ((x << 2) & t0.y);
+      x = (x & ~t0.x) | ((x << 1) & t0.x);
+      o[e] = (x & t1.y) | t1.z;
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+#ifndef IBP_FAST_MIN_BLOCKS
+#define IBP_FAST_MIN_BLOCKS 3  // 8-warp CTAs per SM the register budget allows
+#endif
+
+template <bool kIds, int P>
+__global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS) k_decode_fast(DecodeArgs a, FastLayout L) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
@@ -379,24 +467,30 @@ __global__ void __launch_bounds__(256, 3) k_decode_fast(DecodeArgs a, FastLayout
   const uint32_t min_words = (__ldg(a.m.scal) + 31u) >> 5;
   const bool can_pack = 4u * min_words < R;
   const uint32_t min_vec = min((4u * min_words + 15u) >> 4, nvec);
+  const bool uni = __ldg(a.m.scal + 3) != 0u;
 
   uint4* tab = reinterpret_cast<uint4*>(smem);
   uint32_t* gtab = smem + L.table_words;
-  uint32_t* wbase = gtab + L.gtab_words + wid * L.warp_words;
-  uint32_t* cinfo = wbase + P * L.sbuf_words;
+  uint32_t* uparm = gtab + L.gtab_words;  // uniform-store parameters
+  uint32_t* wbase = uparm + 8 + wid * L.warp_words;
+  uint32_t* cinfo = wbase + 2u * P * L.sbuf_words;
   {
     const uint4* t = net5 ? a.t5 : a.t2;
     const uint32_t nv = net5 ? 2u * W : W;
-    for (uint32_t v = threadIdx.x; v < nv; v += blockDim.x) tab[v] = __ldg(t + v);
-    for (uint32_t g = threadIdx.x; g < G; g += blockDim.x) gtab[g] = __ldg(a.gtab + g);
+    if (!uni)
+      for (uint32_t v = threadIdx.x; v < nv; v += blockDim.x) tab[v] = __ldg(t + v);
+    for (uint32_t g = threadIdx.x; g < L.gtab_words; g += blockDim.x) gtab[g] = __ldg(a.gtab + g);
+    if (threadIdx.x < 8) uparm[threadIdx.x] = __ldg(a.m.scal + 4 + threadIdx.x);
   }
   __syncthreads();
+  const uint32_t* cstat = gtab + ((G + 3u) & ~3u);  // all-packed start of each chunk
+  const uint32_t nhw = (nch + 31u) >> 5;             // header words
 
   const uint64_t nb = (a.n + P - 1) / P;
   const uint64_t wstride = (uint64_t)gridDim.x * (blockDim.x >> 5);
   uint64_t b = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
 
-  // lane p < P resolves row b*P + p.  flags: 1 present, 2 raw, 4 bad id, 8 misaligned
+  // lane p < P resolves row bat*P + p.  flags: 1 present, 2 raw, 4 bad id, 8 misaligned
   auto resolve = [&](uint64_t bat, uint64_t& off, uint32_t& fl) {
     off = 0;
     fl = 0;
@@ -416,74 +510,83 @@ __global__ void __launch_bounds__(256, 3) k_decode_fast(DecodeArgs a, FastLayout
       }
     }
   };
-  auto fetch = [&](uint64_t off_l, uint32_t fl_l, uint4 (&d)[P][V]) {
+  // copy the stored bytes of a resolved batch into stage `stg` (one commit group)
+  auto issue = [&](uint64_t off_l, uint32_t fl_l, uint32_t stg) {
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-      const uint64_t off = __shfl_sync(kFull, off_l, p);
       const uint32_t fl = __shfl_sync(kFull, fl_l, p);
-      const bool ok = (fl & 13u) == 1u;
-      const uint32_t nv = (fl & 2u) ? nvec : min_vec;
-      const uint4* s = reinterpret_cast<const uint4*>(a.src + off);
-#pragma unroll
-      for (int j = 0; j < V; ++j) {
-        const uint32_t v = lane + 32u * (uint32_t)j;
-        if (ok && v < nv) d[p][j] = ld_nc_v4(s + v);
+      const uint64_t off = __shfl_sync(kFull, off_l, p);
+      if ((fl & 13u) == 1u) {
+        const uint32_t nv = (fl & 2u) ? nvec : min_vec;
+        const uint4* src = reinterpret_cast<const uint4*>(a.src + off);
+        uint32_t* sb = wbase + (stg * P + (uint32_t)p) * L.sbuf_words;
+        for (uint32_t v = lane; v < nv; v += 32) cp_async16(sb + 4u * v, src + v);
       }
     }
+    cp_async_commit();
   };
 
-  uint4 d[P][V];
   uint64_t offA, offB;
   uint32_t flA, flB;
   resolve(b, offA, flA);
-  fetch(offA, flA, d);
+  issue(offA, flA, 0);
   resolve(b + wstride, offB, flB);
-  for (; b < nb; b += wstride) {
-    // 1. land batch b: raw rows straight out, compressed streams into shared memory
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      const uint32_t fl = __shfl_sync(kFull, flA, p);
-      if (!(fl & 1u)) continue;
-      uint4* drow = reinterpret_cast<uint4*>(a.dst + (b * P + p) * a.dst_stride);
-      if (fl & 12u) {
-        if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
-        zero_row(drow, nvec, lane);
-      } else if (fl & 2u) {
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-          const uint32_t v = lane + 32u * (uint32_t)j;
-          if (v < nvec) drow[v] = d[p][j];
-        }
-      } else {
-        uint32_t* sb = wbase + (uint32_t)p * L.sbuf_words;
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-          const uint32_t v = lane + 32u * (uint32_t)j;
-          if (v < min_vec) st_smem_v4(sb + 4u * v, d[p][j]);
-        }
-      }
-    }
-    __syncwarp();
+  uint32_t stg = 0;
+  for (; b < nb; b += wstride, stg ^= 1u) {
     const uint64_t offC = offA;
     const uint32_t flC = flA;
-    // 2. next batch's loads go out now; the one after is resolved
     offA = offB;
     flA = flB;
-    fetch(offA, flA, d);
-    resolve(b + 2 * wstride, offB, flB);
-    // 3. decode the compressed rows of batch b
+    issue(offA, flA, stg ^ 1u);           // next batch in flight
+    resolve(b + 2 * wstride, offB, flB);  // the one after: addresses
+    cp_async_wait_prev();                 // batch b has landed
+    __syncwarp();
 #pragma unroll 1
     for (int p = 0; p < P; ++p) {
       const uint32_t fl = __shfl_sync(kFull, flC, p);
-      if ((fl & 15u) != 1u) continue;
-      const uint64_t off = __shfl_sync(kFull, offC, p);
-      uint4* drow = reinterpret_cast<uint4*>(a.dst + (b * P + p) * a.dst_stride);
-      uint32_t* sb = wbase + (uint32_t)p * L.sbuf_words;
+      if (!(fl & 1u)) continue;
+      uint4* drow = reinterpret_cast<uint4*>(a.dst + (b * P + (uint64_t)p) * a.dst_stride);
+      uint32_t* sb = wbase + (stg * P + (uint32_t)p) * L.sbuf_words;
+      if (fl & 12u) {
+        if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
+        zero_row(drow, nvec, lane);
+        continue;
+      }
+      if (fl & 2u) {  // raw row
+        for (uint32_t v = lane; v < nvec; v += 32)
+          drow[v] = *reinterpret_cast<const uint4*>(sb + 4u * v);
+        continue;
+      }
       if (!can_pack) {
         if (lane == 0) set_status(a.status, IBP_ECORRUPT);
         zero_row(drow, nvec, lane);
         continue;
       }
+      const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
+                                                                     : ((1u << (nch & 31u)) - 1u);
+      if (__all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp)) {
+        // every chunk participates: static offsets, no scan
+        if (uni) {
+          const uint32_t um0 = uparm[0], um1 = uparm[1], ush = uparm[2], ubv = uparm[3];
+          const uint32_t ukeep = uparm[4];
+          for (uint32_t g = lane; g < G; g += 32) {
+            uint32_t bit = nch + 4u * g * ukeep;
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t q = bit >> 5;
+              const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
+              o[e] = ((x << (ush & 31u)) & um0) | ((x << (ush >> 8)) & um1) | ubv;
+              bit += ukeep;
+            }
+            drow[g] = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        } else {
+          for (uint32_t g = lane; g < G; g += 32) drow[g] = decode_group(tab, sb, g, G, 0u, net5);
+        }
+        continue;
+      }
+      // some chunks are raw: scan the chunk sizes
       uint32_t run = nch;
       for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
         const uint32_t k = k0 + lane;
@@ -504,53 +607,48 @@ __global__ void __launch_bounds__(256, 3) k_decode_fast(DecodeArgs a, FastLayout
         continue;
       }
       const uint32_t need_vec = (4u * words + 15u) >> 4;
-      if (need_vec > min_vec) {  // raw chunks made the stream longer: second fetch
-        const uint4* s = reinterpret_cast<const uint4*>(a.src + off);
-        for (uint32_t v = min_vec + lane; v < need_vec; v += 32) st_smem_v4(sb + 4u * v, ld_nc_v4(s + v));
+      if (need_vec > min_vec) {  // the raw chunks made the stream longer: second fetch
+        const uint64_t off = __shfl_sync(kFull, offC, p);
+        const uint4* src = reinterpret_cast<const uint4*>(a.src + off);
+        for (uint32_t v = min_vec + lane; v < need_vec; v += 32) st_smem_v4(sb + 4u * v, ld_nc_v4(src + v));
       }
       __syncwarp();
       for (uint32_t g = lane; g < G; g += 32) {
         const uint32_t gd = gtab[g];
-        const uint32_t ci = cinfo[gd & 0xFFFFu];
+        const uint32_t k = gd & 0xFFFFu;
+        const uint32_t ci = cinfo[k];
         const uint32_t start = ci & 0x7FFFFFFFu;
-        uint32_t o[4];
         if (ci >> 31) {
-          if (!net5) {
+          if (uni) {
+            const uint32_t um0 = uparm[0], um1 = uparm[1], ush = uparm[2], ubv = uparm[3];
+            const uint32_t ukeep = uparm[4];
+            uint32_t bit = nch + 4u * g * ukeep + (start - cstat[k]);
+            uint32_t o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const uint4 t = tab[(uint32_t)e * G + g];
-              const uint32_t bit = start + (t.w & 0xFFFFFu);
               const uint32_t q = bit >> 5;
               const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
-              o[e] = ((x << ((t.w >> 20) & 31u)) & t.x) | ((x << (t.w >> 25)) & t.y) | t.z;
+              o[e] = ((x << (ush & 31u)) & um0) | ((x << (ush >> 8)) & um1) | ubv;
+              bit += ukeep;
             }
+            drow[g] = make_uint4(o[0], o[1], o[2], o[3]);
           } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint4 t0 = tab[2u * (uint32_t)e * G + g];
-              const uint4 t1 = tab[(2u * (uint32_t)e + 1u) * G + g];
-              const uint32_t bit = start + t1.w;
-              const uint32_t q = bit >> 5;
-              uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
-              x = (x & ~t1.x) | ((x << 16) & t1.x);
-              x = (x & ~t0.w) | ((x << 8) & t0.w);
-              x = (x & ~t0.z) | ((x << 4) & t0.z);
-              x = (x & ~t0.y) | ((x << 2) & t0.y);
-              x = (x & ~t0.x) | ((x << 1) & t0.x);
-              o[e] = (x & t1.y) | t1.z;
-            }
+            drow[g] = decode_group(tab, sb, g, G, start - cstat[k], net5);
           }
         } else {
           const uint32_t bit = start + ((gd >> 16) << 5);
           const uint32_t q = bit >> 5;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[e] = __funnelshift_r(sb[q + e], sb[q + e + 1], bit);
+          drow[g] = make_uint4(__funnelshift_r(sb[q], sb[q + 1], bit),
+                               __funnelshift_r(sb[q + 1], sb[q + 2], bit),
+                               __funnelshift_r(sb[q + 2], sb[q + 3], bit),
+                               __funnelshift_r(sb[q + 3], sb[q + 4], bit));
         }
-        drow[g] = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      __syncwarp();
     }
+    __syncwarp();  // stage stg is refilled two steps from now
   }
+  cp_async_wait_prev();
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
 // ------------------------------------------------------------------------
@@ -793,7 +891,7 @@ cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32
   k_derive<<<1, 1024, 0, st>>>(mask, bitval, nm, pre, kr, mv, ckeep, scal, W, wpc, nch);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_derive_fast<<<1, 1024, 0, st>>>(nm, bitval, pre, mv, t2, t5, gtab, W, wpc);
+  k_derive_fast<<<1, 1024, 0, st>>>(nm, bitval, pre, mv, ckeep, t2, t5, gtab, scal, W, wpc, nch);
   return cudaGetLastError();
 }
 
@@ -802,18 +900,19 @@ bool fast_geometry(uint32_t R, uint32_t C) { return R <= 2048u && (C % 16u) == 0
 FastLayout fast_layout(uint32_t W, uint32_t nch, int P) {
   FastLayout L;
   L.table_words = 8u * W;
-  L.gtab_words = ((W >> 2) + 3u) & ~3u;
+  L.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
   L.sbuf_words = ((W + 8u) + 3u) & ~3u;
-  L.warp_words = (uint32_t)P * L.sbuf_words + ((nch + 3u) & ~3u);
+  L.warp_words = 2u * (uint32_t)P * L.sbuf_words + ((nch + 3u) & ~3u);
   return L;
 }
 
-template <bool kIds, int P, int V>
+template <bool kIds, int P>
 cudaError_t launch_fast(const DecodeArgs& a, int sm_count, cudaStream_t st) {
   const FastLayout L = fast_layout(a.m.W, a.m.nch, P);
   const int warps = 8;
-  const size_t smem = 4ull * (L.table_words + L.gtab_words + (uint64_t)warps * L.warp_words);
-  auto kern = k_decode_fast<kIds, P, V>;
+  const size_t smem =
+      4ull * (L.table_words + L.gtab_words + 8 + (uint64_t)warps * L.warp_words);
+  auto kern = k_decode_fast<kIds, P>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
@@ -824,18 +923,19 @@ cudaError_t launch_fast(const DecodeArgs& a, int sm_count, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// rows per warp batch: about 2 KB of stored bytes per stage
 template <bool kIds>
 cudaError_t launch_fast_v(const DecodeArgs& a, int sm_count, cudaStream_t st) {
-  const uint32_t V = (a.m.R + 511u) / 512u;
-  if (V == 1) return launch_fast<kIds, 4, 1>(a, sm_count, st);
-  if (V == 2) return launch_fast<kIds, 2, 2>(a, sm_count, st);
-  if (V == 3) return launch_fast<kIds, 1, 3>(a, sm_count, st);
-  return launch_fast<kIds, 1, 4>(a, sm_count, st);
+  if (a.m.R <= 512u) return launch_fast<kIds, 4>(a, sm_count, st);
+  if (a.m.R <= 1024u) return launch_fast<kIds, 2>(a, sm_count, st);
+  return launch_fast<kIds, 1>(a, sm_count, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int sm_count, cudaStream_t st) {
   if (a.n == 0) return cudaSuccess;
-  if (a.t2 && fast_geometry(a.m.R, a.m.wpc * 4u))
+  // cp.async staging pays off from HBM; reads of host memory over the link go
+  // faster as plain 16-byte register loads (measured), so they take k_decode
+  if (a.src_on_device && a.t2 && fast_geometry(a.m.R, a.m.wpc * 4u))
     return a.ids ? launch_fast_v<true>(a, sm_count, st) : launch_fast_v<false>(a, sm_count, st);
   const WarpSmem L = decode_smem(a.m.W, a.m.nch);
   const uint32_t warps = warps_for(4u * L.total_words);
