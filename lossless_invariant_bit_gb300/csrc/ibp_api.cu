@@ -18,6 +18,8 @@ struct ibp_store {
   uint32_t *mask, *bitval, *nm, *pre, *kr, *mv, *ckeep, *scal, *counts, *bitmap, *status;
   uint4 *t2, *t5;  // fast-decoder descriptors
   uint32_t* gtab;
+  uint32_t* h_scal;       // pinned host mirror of scal, filled after each derive
+  cudaEvent_t props_ev;   // completes when h_scal is current
   uint64_t bitmap_words;
 };
 
@@ -51,9 +53,36 @@ ibp::MetaView view(const ibp_store* s) {
   return m;
 }
 
+// Derive the decode tables, then mirror the store's properties to the host
+// (asynchronously: a decode launched before the copy lands uses the kernel
+// that reads them on the device).
 ibp_status derive(ibp_store* s, cudaStream_t st) {
-  return cu(ibp::launch_derive(s->mask, s->bitval, s->nm, s->pre, s->kr, s->mv, s->ckeep,
-                               s->scal, s->t2, s->t5, s->gtab, s->W, s->wpc, s->nch, st));
+  ibp_status e = cu(ibp::launch_derive(s->mask, s->bitval, s->nm, s->pre, s->kr, s->mv,
+                                       s->ckeep, s->scal, s->t2, s->t5, s->gtab, s->W, s->wpc,
+                                       s->nch, st));
+  if (e != IBP_OK) return e;
+  e = cu(cudaMemcpyAsync(s->h_scal, s->scal, 16 * sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
+  if (e != IBP_OK) return e;
+  return cu(cudaEventRecord(s->props_ev, st));
+}
+
+ibp::HostProps host_props(const ibp_store* s) {
+  ibp::HostProps hp = {};
+  if (cudaEventQuery(s->props_ev) != cudaSuccess) {
+    cudaGetLastError();  // cudaErrorNotReady: not known yet
+    return hp;
+  }
+  const volatile uint32_t* h = s->h_scal;
+  hp.known = true;
+  hp.min_bits = h[0];
+  hp.max_runs = h[1];
+  hp.uniform = h[3] != 0;
+  hp.um0 = h[4];
+  hp.um1 = h[5];
+  hp.ush = h[6];
+  hp.ubv = h[7];
+  hp.ukeep = h[8];
+  return hp;
 }
 
 ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void* src,
@@ -88,7 +117,7 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
     return IBP_EINVAL;
   }
   a.src_on_device = attr.type == cudaMemoryTypeDevice;
-  return cu(ibp::launch_decode(a, s->sm_count, st));
+  return cu(ibp::launch_decode(a, host_props(s), s->sm_count, st));
 }
 
 }  // namespace
@@ -149,6 +178,15 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
     delete s;
     return IBP_ENOMEM;
   }
+  if (cudaHostAlloc(reinterpret_cast<void**>(&s->h_scal), 16 * sizeof(uint32_t),
+                    cudaHostAllocDefault) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s->props_ev, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (s->h_scal) cudaFreeHost(s->h_scal);
+    cudaFree(s->base);
+    delete s;
+    return IBP_ENOMEM;
+  }
   uint32_t* p = static_cast<uint32_t*>(s->base);
   auto take = [&](uint64_t n) {
     uint32_t* q = p;
@@ -172,17 +210,16 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
   ibp_status e = cu(cudaMemset(s->base, 0, words * 4));
   if (e == IBP_OK) e = derive(s, 0);  // all-zero Mask: tables for "everything raw"
   if (e == IBP_OK) e = cu(cudaDeviceSynchronize());
+  // derive() sets the valid flag; a fresh store has no built Mask yet
+  uint32_t zero = 0;
+  if (e == IBP_OK) e = cu(cudaMemcpy(s->scal + 2, &zero, 4, cudaMemcpyHostToDevice));
+  if (e == IBP_OK) s->h_scal[2] = 0;
   if (e != IBP_OK) {
+    cudaEventDestroy(s->props_ev);
+    cudaFreeHost(s->h_scal);
     cudaFree(s->base);
     delete s;
     return e;
-  }
-  // derive() sets the valid flag; a fresh store has no built Mask yet
-  uint32_t zero = 0;
-  if (cudaMemcpy(s->scal + 2, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess) {
-    cudaFree(s->base);
-    delete s;
-    return IBP_ECUDA;
   }
   *out = s;
   return IBP_OK;
@@ -191,6 +228,8 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
 ibp_status ibp_store_destroy(ibp_store* s) {
   if (!s) return IBP_OK;
   cudaDeviceSynchronize();
+  cudaEventDestroy(s->props_ev);
+  cudaFreeHost(s->h_scal);
   const cudaError_t e = cudaFree(s->base);
   delete s;
   return cu(e);

@@ -81,13 +81,32 @@ struct WarpSmem {
   uint32_t total_words; // per warp
 };
 
-// Shared-memory layout of the fast decoder (in words): descriptor table and
-// group table per CTA, then per warp P stream buffers and the chunk starts.
-struct FastLayout {
+// Store modes of the fast decoder: kModeRuntime reads the store's properties
+// from device memory; the others are specialised for a store whose
+// properties the host already knows (uniform: every word has the same ~Mask
+// and Bitval with <= 2 runs; run2: every word has <= 2 runs; net5: any Mask).
+enum { kModeRuntime = 0, kModeUniform = 1, kModeRun2 = 2, kModeNet5 = 3 };
+
+// Host-side copy of a store's derived properties (valid when `known`).
+struct HostProps {
+  bool known;
+  bool uniform;
+  uint32_t min_bits, max_runs;
+  uint32_t um0, um1, ush, ubv, ukeep;  // uniform word: run masks, s0 | s1 << 8, Bitval, keep
+};
+
+// Launch parameters of the fast decoder: shared-memory layout (in words:
+// descriptor table and group table per CTA, then per warp two stages of P
+// stream buffers and the chunk starts) and the store properties of the
+// specialised modes.
+struct FastParams {
   uint32_t table_words;
   uint32_t gtab_words;
   uint32_t sbuf_words;
   uint32_t warp_words;
+  uint32_t P;
+  uint32_t min_bits;
+  uint32_t um0, um1, ush, ubv, ukeep;
 };
 
 WarpSmem decode_smem(uint32_t W, uint32_t nch);
@@ -101,7 +120,8 @@ cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32
                           uint32_t* kr, uint32_t* mv, uint32_t* ckeep, uint32_t* scal,
                           uint4* t2, uint4* t5, uint32_t* gtab, uint32_t W, uint32_t wpc,
                           uint32_t nch, cudaStream_t st);
-cudaError_t launch_decode(const DecodeArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count,
+                          cudaStream_t st);
 cudaError_t launch_encode(const EncodeArgs& a, int sm_count, cudaStream_t st);
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,
                         const uint32_t* stored, uint64_t n, int sm_count, cudaStream_t st);

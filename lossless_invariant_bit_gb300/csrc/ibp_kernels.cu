@@ -451,40 +451,73 @@ __device__ __forceinline__ uint4 decode_group(const uint4* tab, const uint32_t* 
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-#ifndef IBP_FAST_MIN_BLOCKS
-#define IBP_FAST_MIN_BLOCKS 3  // 8-warp CTAs per SM the register budget allows
-#endif
+// 8-warp CTAs per SM the register budget is cut for: the uniform mode fits 64
+// registers without spilling (4 CTAs, 32 warps per SM), the others 80 (3 CTAs)
+#define IBP_FAST_MIN_BLOCKS(mode) ((mode) == kModeUniform ? 4 : 3)
 
-template <bool kIds, int P>
-__global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS) k_decode_fast(DecodeArgs a, FastLayout L) {
+// Decode of a word group under each store mode (FastMode): the uniform form
+// takes its run masks and shifts from the launch parameters.
+template <int kMode>
+__device__ __forceinline__ uint4 decode_packed_group(const uint4* tab, const uint32_t* sb,
+                                                     uint32_t g, uint32_t G, uint32_t nch,
+                                                     uint32_t delta, bool net5, bool uni,
+                                                     const FastParams& F, const uint32_t* up) {
+  if (kMode == kModeUniform || (kMode == kModeRuntime && uni)) {
+    uint32_t m0, m1, sh, bv, keep;
+    if (kMode == kModeUniform) {
+      m0 = F.um0; m1 = F.um1; sh = F.ush; bv = F.ubv; keep = F.ukeep;
+    } else {
+      m0 = up[0]; m1 = up[1]; sh = up[2]; bv = up[3]; keep = up[4];
+    }
+    uint32_t bit = nch + 4u * g * keep + delta;  // word w's kept bits at nch + w*keep
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t q = bit >> 5;
+      const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
+      o[e] = ((x << (sh & 31u)) & m0) | ((x << (sh >> 8)) & m1) | bv;
+      bit += keep;
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  return decode_group(tab, sb, g, G, delta, kMode == kModeNet5 || (kMode == kModeRuntime && net5));
+}
+
+template <bool kIds, int kMode>
+__global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast(DecodeArgs a, FastParams F) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
   const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
+  const uint32_t P = F.P;
   const uint32_t nvec = R >> 4;
   const uint32_t G = W >> 2;
-  const bool net5 = __ldg(a.m.scal + 1) > 2u;
-  const uint32_t min_words = (__ldg(a.m.scal) + 31u) >> 5;
+  const uint32_t min_bits = kMode == kModeRuntime ? __ldg(a.m.scal) : F.min_bits;
+  const bool net5 = kMode == kModeNet5 || (kMode == kModeRuntime && __ldg(a.m.scal + 1) > 2u);
+  const bool uni = kMode == kModeUniform || (kMode == kModeRuntime && __ldg(a.m.scal + 3) != 0u);
+  const uint32_t min_words = (min_bits + 31u) >> 5;
   const bool can_pack = 4u * min_words < R;
   const uint32_t min_vec = min((4u * min_words + 15u) >> 4, nvec);
-  const bool uni = __ldg(a.m.scal + 3) != 0u;
 
   uint4* tab = reinterpret_cast<uint4*>(smem);
-  uint32_t* gtab = smem + L.table_words;
-  uint32_t* uparm = gtab + L.gtab_words;  // uniform-store parameters
-  uint32_t* wbase = uparm + 8 + wid * L.warp_words;
-  uint32_t* cinfo = wbase + 2u * P * L.sbuf_words;
+  uint32_t* gtab = smem + F.table_words;
+  uint32_t* uparm = gtab + F.gtab_words;  // uniform-store parameters (runtime mode)
+  uint32_t* wbase = uparm + 8 + wid * F.warp_words;
+  uint32_t* cinfo = wbase + 2u * P * F.sbuf_words;
   {
-    const uint4* t = net5 ? a.t5 : a.t2;
-    const uint32_t nv = net5 ? 2u * W : W;
-    if (!uni)
+    if (F.table_words && !uni) {
+      const uint4* t = net5 ? a.t5 : a.t2;
+      const uint32_t nv = net5 ? 2u * W : W;
       for (uint32_t v = threadIdx.x; v < nv; v += blockDim.x) tab[v] = __ldg(t + v);
-    for (uint32_t g = threadIdx.x; g < L.gtab_words; g += blockDim.x) gtab[g] = __ldg(a.gtab + g);
-    if (threadIdx.x < 8) uparm[threadIdx.x] = __ldg(a.m.scal + 4 + threadIdx.x);
+    }
+    for (uint32_t g = threadIdx.x; g < F.gtab_words; g += blockDim.x) gtab[g] = __ldg(a.gtab + g);
+    if (kMode == kModeRuntime && threadIdx.x < 8) uparm[threadIdx.x] = __ldg(a.m.scal + 4 + threadIdx.x);
   }
   __syncthreads();
   const uint32_t* cstat = gtab + ((G + 3u) & ~3u);  // all-packed start of each chunk
   const uint32_t nhw = (nch + 31u) >> 5;             // header words
+  const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
+                                                                 : ((1u << (nch & 31u)) - 1u);
 
   const uint64_t nb = (a.n + P - 1) / P;
   const uint64_t wstride = (uint64_t)gridDim.x * (blockDim.x >> 5);
@@ -494,7 +527,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS) k_decode_fast(Decode
   auto resolve = [&](uint64_t bat, uint64_t& off, uint32_t& fl) {
     off = 0;
     fl = 0;
-    if (lane < (uint32_t)P && bat < nb) {
+    if (lane < P && bat < nb) {
       const uint64_t i = bat * P + lane;
       if (i < a.n) {
         const int64_t id = kIds ? __ldg(a.ids + i) : (int64_t)i;
@@ -512,14 +545,13 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS) k_decode_fast(Decode
   };
   // copy the stored bytes of a resolved batch into stage `stg` (one commit group)
   auto issue = [&](uint64_t off_l, uint32_t fl_l, uint32_t stg) {
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
+    for (uint32_t p = 0; p < P; ++p) {
       const uint32_t fl = __shfl_sync(kFull, fl_l, p);
       const uint64_t off = __shfl_sync(kFull, off_l, p);
       if ((fl & 13u) == 1u) {
         const uint32_t nv = (fl & 2u) ? nvec : min_vec;
         const uint4* src = reinterpret_cast<const uint4*>(a.src + off);
-        uint32_t* sb = wbase + (stg * P + (uint32_t)p) * L.sbuf_words;
+        uint32_t* sb = wbase + (stg * P + p) * F.sbuf_words;
         for (uint32_t v = lane; v < nv; v += 32) cp_async16(sb + 4u * v, src + v);
       }
     }
@@ -542,11 +574,11 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS) k_decode_fast(Decode
     cp_async_wait_prev();                 // batch b has landed
     __syncwarp();
 #pragma unroll 1
-    for (int p = 0; p < P; ++p) {
+    for (uint32_t p = 0; p < P; ++p) {
       const uint32_t fl = __shfl_sync(kFull, flC, p);
       if (!(fl & 1u)) continue;
-      uint4* drow = reinterpret_cast<uint4*>(a.dst + (b * P + (uint64_t)p) * a.dst_stride);
-      uint32_t* sb = wbase + (stg * P + (uint32_t)p) * L.sbuf_words;
+      uint4* drow = reinterpret_cast<uint4*>(a.dst + (b * P + p) * a.dst_stride);
+      uint32_t* sb = wbase + (stg * P + p) * F.sbuf_words;
       if (fl & 12u) {
         if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
         zero_row(drow, nvec, lane);
@@ -562,28 +594,10 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS) k_decode_fast(Decode
         zero_row(drow, nvec, lane);
         continue;
       }
-      const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
-                                                                     : ((1u << (nch & 31u)) - 1u);
       if (__all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp)) {
         // every chunk participates: static offsets, no scan
-        if (uni) {
-          const uint32_t um0 = uparm[0], um1 = uparm[1], ush = uparm[2], ubv = uparm[3];
-          const uint32_t ukeep = uparm[4];
-          for (uint32_t g = lane; g < G; g += 32) {
-            uint32_t bit = nch + 4u * g * ukeep;
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t q = bit >> 5;
-              const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
-              o[e] = ((x << (ush & 31u)) & um0) | ((x << (ush >> 8)) & um1) | ubv;
-              bit += ukeep;
-            }
-            drow[g] = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        } else {
-          for (uint32_t g = lane; g < G; g += 32) drow[g] = decode_group(tab, sb, g, G, 0u, net5);
-        }
+        for (uint32_t g = lane; g < G; g += 32)
+          drow[g] = decode_packed_group<kMode>(tab, sb, g, G, nch, 0u, net5, uni, F, uparm);
         continue;
       }
       // some chunks are raw: scan the chunk sizes
@@ -619,22 +633,8 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS) k_decode_fast(Decode
         const uint32_t ci = cinfo[k];
         const uint32_t start = ci & 0x7FFFFFFFu;
         if (ci >> 31) {
-          if (uni) {
-            const uint32_t um0 = uparm[0], um1 = uparm[1], ush = uparm[2], ubv = uparm[3];
-            const uint32_t ukeep = uparm[4];
-            uint32_t bit = nch + 4u * g * ukeep + (start - cstat[k]);
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t q = bit >> 5;
-              const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
-              o[e] = ((x << (ush & 31u)) & um0) | ((x << (ush >> 8)) & um1) | ubv;
-              bit += ukeep;
-            }
-            drow[g] = make_uint4(o[0], o[1], o[2], o[3]);
-          } else {
-            drow[g] = decode_group(tab, sb, g, G, start - cstat[k], net5);
-          }
+          drow[g] = decode_packed_group<kMode>(tab, sb, g, G, nch, start - cstat[k], net5, uni, F,
+                                               uparm);
         } else {
           const uint32_t bit = start + ((gd >> 16) << 5);
           const uint32_t q = bit >> 5;
@@ -647,7 +647,6 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS) k_decode_fast(Decode
     }
     __syncwarp();  // stage stg is refilled two steps from now
   }
-  cp_async_wait_prev();
   asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
@@ -897,46 +896,52 @@ cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32
 
 bool fast_geometry(uint32_t R, uint32_t C) { return R <= 2048u && (C % 16u) == 0u; }
 
-FastLayout fast_layout(uint32_t W, uint32_t nch, int P) {
-  FastLayout L;
-  L.table_words = 8u * W;
-  L.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
-  L.sbuf_words = ((W + 8u) + 3u) & ~3u;
-  L.warp_words = 2u * (uint32_t)P * L.sbuf_words + ((nch + 3u) & ~3u);
-  return L;
-}
-
-template <bool kIds, int P>
-cudaError_t launch_fast(const DecodeArgs& a, int sm_count, cudaStream_t st) {
-  const FastLayout L = fast_layout(a.m.W, a.m.nch, P);
+template <bool kIds, int kMode>
+cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, cudaStream_t st) {
+  FastParams F;
+  const uint32_t W = a.m.W, nch = a.m.nch;
+  // rows per warp batch: about 2 KB of stored bytes per stage
+  F.P = a.m.R <= 512u ? 4u : (a.m.R <= 1024u ? 2u : 1u);
+  F.table_words = kMode == kModeUniform ? 0u : 8u * W;
+  F.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
+  F.sbuf_words = ((W + 8u) + 3u) & ~3u;
+  F.warp_words = 2u * F.P * F.sbuf_words + ((nch + 3u) & ~3u);
+  F.min_bits = hp.min_bits;
+  F.um0 = hp.um0;
+  F.um1 = hp.um1;
+  F.ush = hp.ush;
+  F.ubv = hp.ubv;
+  F.ukeep = hp.ukeep;
   const int warps = 8;
-  const size_t smem =
-      4ull * (L.table_words + L.gtab_words + 8 + (uint64_t)warps * L.warp_words);
-  auto kern = k_decode_fast<kIds, P>;
+  const size_t smem = 4ull * (F.table_words + F.gtab_words + 8 + (uint64_t)warps * F.warp_words);
+  auto kern = k_decode_fast<kIds, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = ((a.n + P - 1) / P + warps - 1) / warps;
+  const uint64_t need = ((a.n + F.P - 1) / F.P + warps - 1) / warps;
   if (blocks > need) blocks = need;
-  kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, L);
+  kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, F);
   return cudaGetLastError();
 }
 
-// rows per warp batch: about 2 KB of stored bytes per stage
 template <bool kIds>
-cudaError_t launch_fast_v(const DecodeArgs& a, int sm_count, cudaStream_t st) {
-  if (a.m.R <= 512u) return launch_fast<kIds, 4>(a, sm_count, st);
-  if (a.m.R <= 1024u) return launch_fast<kIds, 2>(a, sm_count, st);
-  return launch_fast<kIds, 1>(a, sm_count, st);
+cudaError_t launch_fast_mode(const DecodeArgs& a, const HostProps& hp, int sm_count,
+                             cudaStream_t st) {
+  if (!hp.known) return launch_fast<kIds, kModeRuntime>(a, hp, sm_count, st);
+  if (hp.uniform) return launch_fast<kIds, kModeUniform>(a, hp, sm_count, st);
+  if (hp.max_runs <= 2u) return launch_fast<kIds, kModeRun2>(a, hp, sm_count, st);
+  return launch_fast<kIds, kModeNet5>(a, hp, sm_count, st);
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, int sm_count, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count,
+                          cudaStream_t st) {
   if (a.n == 0) return cudaSuccess;
   // cp.async staging pays off from HBM; reads of host memory over the link go
   // faster as plain 16-byte register loads (measured), so they take k_decode
   if (a.src_on_device && a.t2 && fast_geometry(a.m.R, a.m.wpc * 4u))
-    return a.ids ? launch_fast_v<true>(a, sm_count, st) : launch_fast_v<false>(a, sm_count, st);
+    return a.ids ? launch_fast_mode<true>(a, hp, sm_count, st)
+                 : launch_fast_mode<false>(a, hp, sm_count, st);
   const WarpSmem L = decode_smem(a.m.W, a.m.nch);
   const uint32_t warps = warps_for(4u * L.total_words);
   const int threads = (int)(32u * warps);
