@@ -345,3 +345,70 @@ def test_link_copy_and_gather_copy():
     o = out.cpu()
     assert torch.equal(o[:4], store[[3, 999, 0, 3], :R])
     assert torch.all(o[4:] == 0)
+
+
+# ---------------------------------------------------------------- decoder modes
+def _two_run_meta(W, seed):
+    """Per-word Masks whose kept bits form at most two runs, all different."""
+    g = np.random.default_rng(seed)
+    mask = np.zeros(W, np.uint32)
+    for w in range(W):
+        a0, l0 = int(g.integers(0, 20)), int(g.integers(1, 8))
+        a1 = int(g.integers(a0 + l0 + 1, 32)) if a0 + l0 + 1 < 32 else 31
+        l1 = int(g.integers(0, 32 - a1)) if a1 < 31 else 0
+        keep = ((1 << l0) - 1) << a0 | (((1 << l1) - 1) << a1 if l1 else 0)
+        mask[w] = np.uint32(~keep & 0xFFFFFFFF)
+    bitval = g.integers(0, 1 << 32, size=W, dtype=np.uint64).astype(np.uint32) & mask
+    return mask, bitval
+
+
+@pytest.mark.parametrize("R,C", [(1024, 256), (512, 1024), (2048, 64)])
+def test_decoder_two_run_store(stores, R, C):
+    n = 3000
+    mask, bitval = _two_run_meta(R // 4, seed=R + C)
+    g = np.random.default_rng(C)
+    rows = (g.integers(0, 1 << 32, size=(n, R // 4), dtype=np.uint64).astype(np.uint32)
+            & ~mask) | bitval
+    flip = g.random(n) < 0.1  # some rows miss the Bitval in one word: a raw chunk
+    rows[flip, g.integers(0, R // 4, size=int(flip.sum()))] ^= mask[0] | 1
+    b = rows.view(np.uint8)
+    st = stores(R, C, n)
+    st.set_meta(mask, bitval)
+    assert ibp.ibp_store_get_info(st.h).max_runs <= 2
+    ref_sl, ref_bm, ref_st = oracle_slots(b, C, mask, bitval, st.slot)
+    slots, stored = gpu_compress(st, to_dev(b), n)
+    assert np.array_equal(stored, ref_st)
+    assert_streams_equal(slots.cpu().numpy(), ref_sl, ref_st)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, slots, None, n)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
+
+
+@pytest.mark.parametrize("kind", ["tiny", "fuzz"])
+def test_decoder_before_store_properties_reach_host(stores, kind):
+    """A decode enqueued right behind the builder, while the GPU is still busy,
+    cannot know the store's mode on the host yet: it runs the kernel that reads
+    the mode on the device.  Same bytes either way."""
+    if kind == "tiny":
+        rows, _ = wl.tiny_rows(seed=3)
+        b = rows_u8(rows)
+        R, C = 1024, 256
+    else:
+        R, C = 512, 64
+        b = wl.fuzz_rows(2000, R, seed=31)
+    n = len(b)
+    st = stores(R, C, n)
+    d = to_dev(b)
+    slots = torch.zeros((n, st.slot), dtype=torch.uint8, device=DEV)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)  # keep the stream busy (about 0.1 s)
+    ibp.ibp_build_meta(st.h, d, R, None, n, 9, 10)
+    ibp.ibp_compress(st.h, slots, d, R, None, n, None)
+    ibp.ibp_decompress(st.h, out, slots, None, n)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
+    m, bv = st.meta()
+    mr, br = ref_c.build_meta(b, 9, 10)
+    assert np.array_equal(m, mr) and np.array_equal(bv, br)
