@@ -84,8 +84,9 @@ struct WarpSmem {
 // Store modes of the fast decoder: kModeRuntime reads the store's properties
 // from device memory; the others are specialised for a store whose
 // properties the host already knows (uniform: every word has the same ~Mask
-// and Bitval with <= 2 runs; run2: every word has <= 2 runs; net5: any Mask).
-enum { kModeRuntime = 0, kModeUniform = 1, kModeRun2 = 2, kModeNet5 = 3 };
+// and Bitval with <= 2 runs; uniform1: the same with one run; run2: every
+// word has <= 2 runs; net5: any Mask).
+enum { kModeRuntime = 0, kModeUniform = 1, kModeRun2 = 2, kModeNet5 = 3, kModeUniform1 = 4 };
 
 // Host-side copy of a store's derived properties (valid when `known`).
 struct HostProps {
@@ -96,15 +97,15 @@ struct HostProps {
 };
 
 // Launch parameters of the fast decoder: shared-memory layout (in words:
-// descriptor table and group table per CTA, then per warp two stages of P
-// stream buffers and the chunk starts) and the store properties of the
-// specialised modes.
+// descriptor table and group table per CTA, then per warp a ring of S
+// single-row stream buffers and the chunk starts) and the store properties of
+// the specialised modes.
 struct FastParams {
   uint32_t table_words;
   uint32_t gtab_words;
   uint32_t sbuf_words;
   uint32_t warp_words;
-  uint32_t P;
+  uint32_t S;
   uint32_t min_bits;
   uint32_t um0, um1, ush, ubv, ukeep;
 };

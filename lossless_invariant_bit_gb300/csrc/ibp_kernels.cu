@@ -391,13 +391,14 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
 
 // ------------------------------------------------------------------------
 // Fast decompression for rows of at most 2 KB whose chunks hold whole groups
-// of 4 words (C % 16 == 0): the common geometries (512 B - 2 KB rows, chunks
-// of 256 B / 1 KB / 4 KB).  Differences from k_decode:
-//   - a warp takes P rows per batch and keeps the next batch in flight while
-//     it decodes the current one: cp.async copies land each batch in one of
-//     two shared-memory stages, so the bytes in flight cost no registers; the
-//     batch after that is resolved (id -> offset, raw bit) one step ahead, so
-//     the dependent id -> slot -> data loads overlap too;
+// of 4 words (C % 16 == 0), from HBM: the common geometries (512 B - 2 KB
+// rows, chunks of 256 B / 1 KB / 4 KB).  Differences from k_decode:
+//   - a warp resolves 32 rows at a time, one per lane (id -> offset -> raw
+//     bit, coalesced), the next 32 one chunk ahead, and then walks them one
+//     by one; each row's (offset, flags) reach the warp by one shuffle;
+//   - the stored bytes travel by cp.async into a ring of S single-row stages
+//     in shared memory, S-1 rows ahead of the row being decoded, so the bytes
+//     in flight cost no registers;
 //   - a row whose chunks all participate (the usual case) needs no scan: word
 //     w's kept bits sit at a static offset (for a uniform store, one whose
 //     words all share the same ~Mask and Bitval, nch + w*keep);
@@ -413,8 +414,18 @@ __device__ __forceinline__ void cp_async16(uint32_t* sdst, const void* gsrc) {
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_prev() {  // all but the newest group done
-  asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait_n() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// wait until at most `pending` of this thread's newest commit groups are in flight
+__device__ __forceinline__ void cp_async_wait_keep(uint32_t pending) {
+  switch (pending) {
+    case 1: cp_async_wait_n<1>(); break;
+    case 3: cp_async_wait_n<3>(); break;
+    case 7: cp_async_wait_n<7>(); break;
+    default: cp_async_wait_n<0>(); break;
+  }
 }
 
 // Four output words 4g..4g+3 of a row whose chunk participates: their kept
@@ -453,7 +464,7 @@ __device__ __forceinline__ uint4 decode_group(const uint4* tab, const uint32_t* 
 
 // 8-warp CTAs per SM the register budget is cut for: the uniform mode fits 64
 // registers without spilling (4 CTAs, 32 warps per SM), the others 80 (3 CTAs)
-#define IBP_FAST_MIN_BLOCKS(mode) ((mode) == kModeUniform ? 4 : 3)
+#define IBP_FAST_MIN_BLOCKS(mode) ((mode) == kModeUniform || (mode) == kModeUniform1 ? 4 : 3)
 
 // Decode of a word group under each store mode (FastMode): the uniform form
 // takes its run masks and shifts from the launch parameters.
@@ -462,6 +473,18 @@ __device__ __forceinline__ uint4 decode_packed_group(const uint4* tab, const uin
                                                      uint32_t g, uint32_t G, uint32_t nch,
                                                      uint32_t delta, bool net5, bool uni,
                                                      const FastParams& F, const uint32_t* up) {
+  if (kMode == kModeUniform1) {  // one run: a shift and a mask per word
+    uint32_t bit = nch + 4u * g * F.ukeep + delta;
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t q = bit >> 5;
+      const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
+      o[e] = ((x << (F.ush & 31u)) & F.um0) | F.ubv;
+      bit += F.ukeep;
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
   if (kMode == kModeUniform || (kMode == kModeRuntime && uni)) {
     uint32_t m0, m1, sh, bv, keep;
     if (kMode == kModeUniform) {
@@ -489,12 +512,13 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
   const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
-  const uint32_t P = F.P;
+  const uint32_t S = F.S;  // ring stages per warp: 2, 4 or 8
   const uint32_t nvec = R >> 4;
   const uint32_t G = W >> 2;
   const uint32_t min_bits = kMode == kModeRuntime ? __ldg(a.m.scal) : F.min_bits;
   const bool net5 = kMode == kModeNet5 || (kMode == kModeRuntime && __ldg(a.m.scal + 1) > 2u);
-  const bool uni = kMode == kModeUniform || (kMode == kModeRuntime && __ldg(a.m.scal + 3) != 0u);
+  const bool uni = kMode == kModeUniform || kMode == kModeUniform1 ||
+                   (kMode == kModeRuntime && __ldg(a.m.scal + 3) != 0u);
   const uint32_t min_words = (min_bits + 31u) >> 5;
   const bool can_pack = 4u * min_words < R;
   const uint32_t min_vec = min((4u * min_words + 15u) >> 4, nvec);
@@ -502,8 +526,8 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   uint4* tab = reinterpret_cast<uint4*>(smem);
   uint32_t* gtab = smem + F.table_words;
   uint32_t* uparm = gtab + F.gtab_words;  // uniform-store parameters (runtime mode)
-  uint32_t* wbase = uparm + 8 + wid * F.warp_words;
-  uint32_t* cinfo = wbase + 2u * P * F.sbuf_words;
+  uint32_t* ring = uparm + 8 + wid * F.warp_words;
+  uint32_t* cinfo = ring + S * F.sbuf_words;
   {
     if (F.table_words && !uni) {
       const uint4* t = net5 ? a.t5 : a.t2;
@@ -519,66 +543,59 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
                                                                  : ((1u << (nch & 31u)) - 1u);
 
-  const uint64_t nb = (a.n + P - 1) / P;
+  const uint64_t nchunk = (a.n + 31) >> 5;  // 32 rows per chunk, one per lane
   const uint64_t wstride = (uint64_t)gridDim.x * (blockDim.x >> 5);
-  uint64_t b = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
+  uint64_t cC = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
+  if (cC >= nchunk) return;
 
-  // lane p < P resolves row bat*P + p.  flags: 1 present, 2 raw, 4 bad id, 8 misaligned
-  auto resolve = [&](uint64_t bat, uint64_t& off, uint32_t& fl) {
+  // lane l resolves row 32c + l.  flags: 1 present, 2 raw, 4 bad id, 8 misaligned
+  auto resolve = [&](uint64_t c, uint64_t& off, uint32_t& fl) {
     off = 0;
     fl = 0;
-    if (lane < P && bat < nb) {
-      const uint64_t i = bat * P + lane;
-      if (i < a.n) {
-        const int64_t id = kIds ? __ldg(a.ids + i) : (int64_t)i;
-        if (id < 0 || (uint64_t)id >= a.n_rows) {
-          fl = 1u | 4u;
-        } else {
-          off = a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
-          if (off & 15u)
-            fl = 1u | 8u;
-          else
-            fl = 1u | (((__ldg(a.bitmap + (id >> 5)) >> (id & 31)) & 1u) << 1);
-        }
+    const uint64_t i = (c << 5) + lane;
+    if (c < nchunk && i < a.n) {
+      const int64_t id = kIds ? __ldg(a.ids + i) : (int64_t)i;
+      if (id < 0 || (uint64_t)id >= a.n_rows) {
+        fl = 1u | 4u;
+      } else {
+        off = a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
+        if (off & 15u)
+          fl = 1u | 8u;
+        else
+          fl = 1u | (((__ldg(a.bitmap + (id >> 5)) >> (id & 31)) & 1u) << 1);
       }
     }
   };
-  // copy the stored bytes of a resolved batch into stage `stg` (one commit group)
-  auto issue = [&](uint64_t off_l, uint32_t fl_l, uint32_t stg) {
-    for (uint32_t p = 0; p < P; ++p) {
-      const uint32_t fl = __shfl_sync(kFull, fl_l, p);
-      const uint64_t off = __shfl_sync(kFull, off_l, p);
-      if ((fl & 13u) == 1u) {
-        const uint32_t nv = (fl & 2u) ? nvec : min_vec;
-        const uint4* src = reinterpret_cast<const uint4*>(a.src + off);
-        uint32_t* sb = wbase + (stg * P + p) * F.sbuf_words;
-        for (uint32_t v = lane; v < nv; v += 32) cp_async16(sb + 4u * v, src + v);
-      }
+  uint64_t offC, offN;
+  uint32_t flC, flN;
+  resolve(cC, offC, flC);
+  resolve(cC + wstride, offN, flN);
+
+  // copy row jj (jj < 32: current chunk, else the next) into ring stage jj % S
+  auto issue = [&](uint32_t jj) {
+    const bool nx = jj >= 32u;
+    const uint32_t fl = __shfl_sync(kFull, nx ? flN : flC, jj & 31u);
+    const uint64_t off = __shfl_sync(kFull, nx ? offN : offC, jj & 31u);
+    if ((fl & 13u) == 1u) {
+      const uint32_t nv = (fl & 2u) ? nvec : min_vec;
+      const uint4* src = reinterpret_cast<const uint4*>(a.src + off);
+      uint32_t* sb = ring + (jj & (S - 1u)) * F.sbuf_words;
+      for (uint32_t v = lane; v < nv; v += 32) cp_async16(sb + 4u * v, src + v);
     }
     cp_async_commit();
   };
 
-  uint64_t offA, offB;
-  uint32_t flA, flB;
-  resolve(b, offA, flA);
-  issue(offA, flA, 0);
-  resolve(b + wstride, offB, flB);
-  uint32_t stg = 0;
-  for (; b < nb; b += wstride, stg ^= 1u) {
-    const uint64_t offC = offA;
-    const uint32_t flC = flA;
-    offA = offB;
-    flA = flB;
-    issue(offA, flA, stg ^ 1u);           // next batch in flight
-    resolve(b + 2 * wstride, offB, flB);  // the one after: addresses
-    cp_async_wait_prev();                 // batch b has landed
-    __syncwarp();
+  for (uint32_t j = 0; j + 1u < S; ++j) issue(j);
+  for (;;) {
 #pragma unroll 1
-    for (uint32_t p = 0; p < P; ++p) {
-      const uint32_t fl = __shfl_sync(kFull, flC, p);
+    for (uint32_t j = 0; j < 32u; ++j) {
+      issue(j + S - 1u);         // S-1 rows stay in flight
+      cp_async_wait_keep(S - 1u);  // row j has landed
+      __syncwarp();
+      const uint32_t fl = __shfl_sync(kFull, flC, j);
       if (!(fl & 1u)) continue;
-      uint4* drow = reinterpret_cast<uint4*>(a.dst + (b * P + p) * a.dst_stride);
-      uint32_t* sb = wbase + (stg * P + p) * F.sbuf_words;
+      uint4* drow = reinterpret_cast<uint4*>(a.dst + ((cC << 5) + j) * a.dst_stride);
+      uint32_t* sb = ring + (j & (S - 1u)) * F.sbuf_words;
       if (fl & 12u) {
         if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
         zero_row(drow, nvec, lane);
@@ -587,6 +604,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       if (fl & 2u) {  // raw row
         for (uint32_t v = lane; v < nvec; v += 32)
           drow[v] = *reinterpret_cast<const uint4*>(sb + 4u * v);
+        __syncwarp();
         continue;
       }
       if (!can_pack) {
@@ -594,10 +612,13 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         zero_row(drow, nvec, lane);
         continue;
       }
-      if (__all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp)) {
+      const bool all_packed = nhw == 1u ? (sb[0] & hexp) == hexp
+                                        : __all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp);
+      if (all_packed) {
         // every chunk participates: static offsets, no scan
         for (uint32_t g = lane; g < G; g += 32)
           drow[g] = decode_packed_group<kMode>(tab, sb, g, G, nch, 0u, net5, uni, F, uparm);
+        __syncwarp();
         continue;
       }
       // some chunks are raw: scan the chunk sizes
@@ -622,7 +643,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       }
       const uint32_t need_vec = (4u * words + 15u) >> 4;
       if (need_vec > min_vec) {  // the raw chunks made the stream longer: second fetch
-        const uint64_t off = __shfl_sync(kFull, offC, p);
+        const uint64_t off = __shfl_sync(kFull, offC, j);
         const uint4* src = reinterpret_cast<const uint4*>(a.src + off);
         for (uint32_t v = min_vec + lane; v < need_vec; v += 32) st_smem_v4(sb + 4u * v, ld_nc_v4(src + v));
       }
@@ -644,10 +665,15 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
                                __funnelshift_r(sb[q + 3], sb[q + 4], bit));
         }
       }
+      __syncwarp();
     }
-    __syncwarp();  // stage stg is refilled two steps from now
+    cC += wstride;
+    if (cC >= nchunk) break;
+    offC = offN;
+    flC = flN;
+    resolve(cC + wstride, offN, flN);
   }
-  asm volatile("cp.async.wait_all;\n" ::: "memory");
+  cp_async_wait_n<0>();
 }
 
 // ------------------------------------------------------------------------
@@ -900,12 +926,12 @@ template <bool kIds, int kMode>
 cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, cudaStream_t st) {
   FastParams F;
   const uint32_t W = a.m.W, nch = a.m.nch;
-  // rows per warp batch: about 2 KB of stored bytes per stage
-  F.P = a.m.R <= 512u ? 4u : (a.m.R <= 1024u ? 2u : 1u);
-  F.table_words = kMode == kModeUniform ? 0u : 8u * W;
+  // ring stages per warp: about 4 KB of row buffers
+  F.S = a.m.R <= 512u ? 8u : (a.m.R <= 1024u ? 4u : 2u);
+  F.table_words = (kMode == kModeUniform || kMode == kModeUniform1) ? 0u : 8u * W;
   F.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
   F.sbuf_words = ((W + 8u) + 3u) & ~3u;
-  F.warp_words = 2u * F.P * F.sbuf_words + ((nch + 3u) & ~3u);
+  F.warp_words = F.S * F.sbuf_words + ((nch + 3u) & ~3u);
   F.min_bits = hp.min_bits;
   F.um0 = hp.um0;
   F.um1 = hp.um1;
@@ -919,7 +945,7 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   if (e != cudaSuccess) return e;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = ((a.n + F.P - 1) / F.P + warps - 1) / warps;
+  const uint64_t need = ((a.n + 31) / 32 + warps - 1) / warps;  // 32-row chunks per warp
   if (blocks > need) blocks = need;
   kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, F);
   return cudaGetLastError();
@@ -929,6 +955,7 @@ template <bool kIds>
 cudaError_t launch_fast_mode(const DecodeArgs& a, const HostProps& hp, int sm_count,
                              cudaStream_t st) {
   if (!hp.known) return launch_fast<kIds, kModeRuntime>(a, hp, sm_count, st);
+  if (hp.uniform && hp.um1 == 0u) return launch_fast<kIds, kModeUniform1>(a, hp, sm_count, st);
   if (hp.uniform) return launch_fast<kIds, kModeUniform>(a, hp, sm_count, st);
   if (hp.max_runs <= 2u) return launch_fast<kIds, kModeRun2>(a, hp, sm_count, st);
   return launch_fast<kIds, kModeNet5>(a, hp, sm_count, st);
