@@ -49,8 +49,16 @@ def test_dense_gnn_two_hop(C):
         ratio = stored.sum() / (n_rows * 512)
         assert 0.80 < ratio < 0.95  # modest saving, as the pages report for dense GNN
         ids = wl.two_hop_ids(n_rows, seed=1)
+        d_ids = torch.from_numpy(ids).to(DEV)
         out = torch.empty((len(ids), 512), dtype=torch.uint8, device=DEV)
-        ibp.ibp_gather_decompress(st.h, out, slots, None, torch.from_numpy(ids).to(DEV), len(ids))
+        ibp.ibp_gather_decompress(st.h, out, slots, None, d_ids, len(ids))
+        assert st.status() == ibp.IBP_OK
+        assert np.array_equal(out.cpu().numpy(), rb[ids])
+        # the same store as an HBM cache (slot layout): the fast decoder's path
+        info = ibp.ibp_store_get_info(st.h)
+        assert info.max_runs <= 2
+        out.zero_()
+        ibp.ibp_gather_decompress(st.h, out, slots.to(DEV), None, d_ids, len(ids))
         assert st.status() == ibp.IBP_OK
         assert np.array_equal(out.cpu().numpy(), rb[ids])
     finally:
@@ -97,7 +105,8 @@ def test_dlrm_26_tables_strided(dim):
                 assert np.array_equal(stored[:3000], ref_st)
                 assert_streams_equal(slots.numpy()[:3000], ref_sl, ref_st)
             ids = wl.zipf_ids(B, n_rows, table=t, seed=0)
-            ibp.ibp_gather_decompress_strided(st.h, out[:, t], T * R, slots, None,
+            src = slots if t % 2 == 0 else slots.to(DEV)  # host link or HBM cache
+            ibp.ibp_gather_decompress_strided(st.h, out[:, t], T * R, src, None,
                                               torch.from_numpy(ids).to(DEV), B)
             assert st.status() == ibp.IBP_OK
             want[:, t] = rb[ids]
