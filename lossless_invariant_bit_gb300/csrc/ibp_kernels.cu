@@ -527,7 +527,10 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   uint32_t* gtab = smem + F.table_words;
   uint32_t* uparm = gtab + F.gtab_words;  // uniform-store parameters (runtime mode)
   uint32_t* ring = uparm + 8 + wid * F.warp_words;
-  uint32_t* cinfo = ring + S * F.sbuf_words;
+  // row info ring, two 32-row chunks: {offset | flags (lo, hi), output offset (lo, hi)}
+  // flags (low 4 bits, offsets are 16-byte aligned): 1 present, 2 raw, 4 bad id, 8 misaligned
+  uint4* rinfo = reinterpret_cast<uint4*>(ring + S * F.sbuf_words);
+  uint32_t* cinfo = ring + S * F.sbuf_words + 256;
   {
     if (F.table_words && !uni) {
       const uint4* t = net5 ? a.t5 : a.t2;
@@ -543,74 +546,98 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
                                                                  : ((1u << (nch & 31u)) - 1u);
 
-  const uint64_t nchunk = (a.n + 31) >> 5;  // 32 rows per chunk, one per lane
-  const uint64_t wstride = (uint64_t)gridDim.x * (blockDim.x >> 5);
-  uint64_t cC = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
-  if (cC >= nchunk) return;
+  // this warp's rows: a contiguous, balanced share [r0, r0 + cnt) of [0, n)
+  const uint64_t nw = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  const uint64_t gw = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
+  const uint64_t r0 = a.n * gw / nw;
+  const uint32_t cnt = (uint32_t)(a.n * (gw + 1) / nw - r0);
+  if (cnt == 0) return;
 
-  // lane l resolves row 32c + l.  flags: 1 present, 2 raw, 4 bad id, 8 misaligned
-  auto resolve = [&](uint64_t c, uint64_t& off, uint32_t& fl) {
-    off = 0;
-    fl = 0;
-    const uint64_t i = (c << 5) + lane;
-    if (c < nchunk && i < a.n) {
-      const int64_t id = kIds ? __ldg(a.ids + i) : (int64_t)i;
-      if (id < 0 || (uint64_t)id >= a.n_rows) {
-        fl = 1u | 4u;
-      } else {
-        off = a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
-        if (off & 15u)
-          fl = 1u | 8u;
-        else
-          fl = 1u | (((__ldg(a.bitmap + (id >> 5)) >> (id & 31)) & 1u) << 1);
-      }
+  // Resolving chunk q (rows r0 + 32q + lane) is a chain of dependent loads
+  // (id -> offset, raw bit); it runs in three steps spread over the chunk two
+  // ahead, so the loads complete while other rows are decoded.
+  int64_t pid = 0;
+  uint64_t poff = 0;
+  uint32_t pbm = 0;
+  bool pin = false;
+  auto step_ids = [&](uint32_t q) {
+    const uint32_t t = 32u * q + lane;
+    pin = q < (cnt + 31u) / 32u && t < cnt;
+    if (pin) pid = kIds ? __ldg(a.ids + r0 + t) : (int64_t)(r0 + t);
+  };
+  auto step_loads = [&]() {
+    if (pin && pid >= 0 && (uint64_t)pid < a.n_rows) {
+      poff = a.offsets ? __ldg(a.offsets + pid) : (uint64_t)pid * a.slot;
+      pbm = __ldg(a.bitmap + (pid >> 5));
     }
   };
-  uint64_t offC, offN;
-  uint32_t flC, flN;
-  resolve(cC, offC, flC);
-  resolve(cC + wstride, offN, flN);
-
-  // copy row jj (jj < 32: current chunk, else the next) into ring stage jj % S
-  auto issue = [&](uint32_t jj) {
-    const bool nx = jj >= 32u;
-    const uint32_t fl = __shfl_sync(kFull, nx ? flN : flC, jj & 31u);
-    const uint64_t off = __shfl_sync(kFull, nx ? offN : offC, jj & 31u);
-    if ((fl & 13u) == 1u) {
-      const uint32_t nv = (fl & 2u) ? nvec : min_vec;
-      const uint4* src = reinterpret_cast<const uint4*>(a.src + off);
-      uint32_t* sb = ring + (jj & (S - 1u)) * F.sbuf_words;
-      for (uint32_t v = lane; v < nv; v += 32) cp_async16(sb + 4u * v, src + v);
+  auto step_store = [&](uint32_t q) {
+    uint32_t fl = 0;
+    uint64_t off = 0;
+    if (pin) {
+      if (pid < 0 || (uint64_t)pid >= a.n_rows) {
+        fl = 1u | 4u;
+      } else if (poff & 15u) {
+        fl = 1u | 8u;
+      } else {
+        fl = 1u | (((pbm >> (pid & 31)) & 1u) << 1);
+        off = poff;
+      }
+    }
+    const uint64_t dsto = (r0 + 32ull * q + lane) * a.dst_stride;
+    rinfo[((q & 1u) << 5) + lane] = make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32),
+                                               (uint32_t)dsto, (uint32_t)(dsto >> 32));
+  };
+  // copy row tt into ring stage tt % S (one commit group, empty past the end)
+  auto issue = [&](uint32_t tt) {
+    if (tt < cnt) {
+      const uint4 e = rinfo[tt & 63u];
+      const uint32_t fl = e.x & 15u;
+      if ((fl & 13u) == 1u) {
+        const uint32_t nv = (fl & 2u) ? nvec : min_vec;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.src + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u)));
+        uint32_t* sb = ring + (tt & (S - 1u)) * F.sbuf_words;
+        for (uint32_t v = lane; v < nv; v += 32) cp_async16(sb + 4u * v, src + v);
+      }
     }
     cp_async_commit();
   };
 
-  for (uint32_t j = 0; j + 1u < S; ++j) issue(j);
-  for (;;) {
+  for (uint32_t q = 0; q < 2u; ++q) {
+    step_ids(q);
+    step_loads();
+    step_store(q);
+  }
+  __syncwarp();
+  for (uint32_t t = 0; t + 1u < S; ++t) issue(t);
 #pragma unroll 1
-    for (uint32_t j = 0; j < 32u; ++j) {
-      issue(j + S - 1u);         // S-1 rows stay in flight
-      cp_async_wait_keep(S - 1u);  // row j has landed
-      __syncwarp();
-      const uint32_t fl = __shfl_sync(kFull, flC, j);
-      if (!(fl & 1u)) continue;
-      uint4* drow = reinterpret_cast<uint4*>(a.dst + ((cC << 5) + j) * a.dst_stride);
-      uint32_t* sb = ring + (j & (S - 1u)) * F.sbuf_words;
+  for (uint32_t t = 0; t < cnt; ++t) {
+    const uint32_t l = t & 31u;
+    if (l == 0u) step_ids((t >> 5) + 2u);
+    if (l == 16u) step_loads();
+    issue(t + S - 1u);           // S-1 rows stay in flight
+    cp_async_wait_keep(S - 1u);  // row t has landed
+    __syncwarp();
+    do {
+      const uint4 e = rinfo[t & 63u];
+      const uint32_t fl = e.x & 15u;
+      uint4* drow = reinterpret_cast<uint4*>(a.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
+      uint32_t* sb = ring + (t & (S - 1u)) * F.sbuf_words;
       if (fl & 12u) {
         if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
         zero_row(drow, nvec, lane);
-        continue;
+        break;
       }
       if (fl & 2u) {  // raw row
         for (uint32_t v = lane; v < nvec; v += 32)
           drow[v] = *reinterpret_cast<const uint4*>(sb + 4u * v);
-        __syncwarp();
-        continue;
+        break;
       }
       if (!can_pack) {
         if (lane == 0) set_status(a.status, IBP_ECORRUPT);
         zero_row(drow, nvec, lane);
-        continue;
+        break;
       }
       const bool all_packed = nhw == 1u ? (sb[0] & hexp) == hexp
                                         : __all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp);
@@ -618,8 +645,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         // every chunk participates: static offsets, no scan
         for (uint32_t g = lane; g < G; g += 32)
           drow[g] = decode_packed_group<kMode>(tab, sb, g, G, nch, 0u, net5, uni, F, uparm);
-        __syncwarp();
-        continue;
+        break;
       }
       // some chunks are raw: scan the chunk sizes
       uint32_t run = nch;
@@ -639,12 +665,12 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         if (lane == 0) set_status(a.status, IBP_ECORRUPT);
         __syncwarp();
         zero_row(drow, nvec, lane);
-        continue;
+        break;
       }
       const uint32_t need_vec = (4u * words + 15u) >> 4;
       if (need_vec > min_vec) {  // the raw chunks made the stream longer: second fetch
-        const uint64_t off = __shfl_sync(kFull, offC, j);
-        const uint4* src = reinterpret_cast<const uint4*>(a.src + off);
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.src + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u)));
         for (uint32_t v = min_vec + lane; v < need_vec; v += 32) st_smem_v4(sb + 4u * v, ld_nc_v4(src + v));
       }
       __syncwarp();
@@ -665,13 +691,12 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
                                __funnelshift_r(sb[q + 3], sb[q + 4], bit));
         }
       }
+    } while (false);
+    __syncwarp();  // stage t % S and row info slot t % 64 are refilled later
+    if (l == 31u) {
+      step_store((t >> 5) + 2u);  // chunk t/32 + 2 takes the slots of chunk t/32
       __syncwarp();
     }
-    cC += wstride;
-    if (cC >= nchunk) break;
-    offC = offN;
-    flC = flN;
-    resolve(cC + wstride, offN, flN);
   }
   cp_async_wait_n<0>();
 }
@@ -931,7 +956,7 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   F.table_words = (kMode == kModeUniform || kMode == kModeUniform1) ? 0u : 8u * W;
   F.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
   F.sbuf_words = ((W + 8u) + 3u) & ~3u;
-  F.warp_words = F.S * F.sbuf_words + ((nch + 3u) & ~3u);
+  F.warp_words = F.S * F.sbuf_words + 256u + ((nch + 3u) & ~3u);
   F.min_bits = hp.min_bits;
   F.um0 = hp.um0;
   F.um1 = hp.um1;
@@ -945,7 +970,7 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   if (e != cudaSuccess) return e;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = ((a.n + 31) / 32 + warps - 1) / warps;  // 32-row chunks per warp
+  const uint64_t need = (a.n + 32ull * warps - 1) / (32ull * warps);  // >= 32 rows per warp
   if (blocks > need) blocks = need;
   kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, F);
   return cudaGetLastError();
