@@ -407,10 +407,6 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
 //     bits (fp32 sign/exponent masks), the scatter is two shift-and-mask
 //     steps instead of the 5-stage network.
 // ------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(uint32_t* sdst, const void* gsrc) {
-  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(sdst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gsrc) : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -418,15 +414,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait_n() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
-// wait until at most `pending` of this thread's newest commit groups are in flight
-__device__ __forceinline__ void cp_async_wait_keep(uint32_t pending) {
-  switch (pending) {
-    case 1: cp_async_wait_n<1>(); break;
-    case 3: cp_async_wait_n<3>(); break;
-    case 7: cp_async_wait_n<7>(); break;
-    default: cp_async_wait_n<0>(); break;
-  }
-}
+
 
 // Four output words 4g..4g+3 of a row whose chunk participates: their kept
 // bits start at the static offsets plus `delta` (the extra bits of raw chunks
@@ -506,13 +494,15 @@ __device__ __forceinline__ uint4 decode_packed_group(const uint4* tab, const uin
   return decode_group(tab, sb, g, G, delta, kMode == kModeNet5 || (kMode == kModeRuntime && net5));
 }
 
+constexpr uint32_t kRingStages = 4;  // rows per warp ring: 3 in flight while one decodes
+
 template <bool kIds, int kMode>
 __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast(DecodeArgs a, FastParams F) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
   const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
-  const uint32_t S = F.S;  // ring stages per warp: 2, 4 or 8
+  constexpr uint32_t S = kRingStages;
   const uint32_t nvec = R >> 4;
   const uint32_t G = W >> 2;
   const uint32_t min_bits = kMode == kModeRuntime ? __ldg(a.m.scal) : F.min_bits;
@@ -588,17 +578,23 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
     rinfo[((q & 1u) << 5) + lane] = make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32),
                                                (uint32_t)dsto, (uint32_t)(dsto >> 32));
   };
-  // copy row tt into ring stage tt % S (one commit group, empty past the end)
+  // copy row tt into ring stage tt % S (one commit group, empty past the end);
+  // a row is at most 2 KB: four predicated 16-byte copies per lane
+  const uint32_t ring_sa = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + 16u * lane;
+  const uint8_t* src_lane = a.src + 16u * lane;
   auto issue = [&](uint32_t tt) {
     if (tt < cnt) {
       const uint4 e = rinfo[tt & 63u];
       const uint32_t fl = e.x & 15u;
       if ((fl & 13u) == 1u) {
         const uint32_t nv = (fl & 2u) ? nvec : min_vec;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.src + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u)));
-        uint32_t* sb = ring + (tt & (S - 1u)) * F.sbuf_words;
-        for (uint32_t v = lane; v < nv; v += 32) cp_async16(sb + 4u * v, src + v);
+        const uint8_t* src = src_lane + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u));
+        const uint32_t sa = ring_sa + 4u * (tt & (S - 1u)) * F.sbuf_words;
+#pragma unroll
+        for (uint32_t j = 0; j < 4u; ++j)
+          if (lane + 32u * j < nv)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * j),
+                         "l"(src + 512u * j));
       }
     }
     cp_async_commit();
@@ -617,7 +613,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
     if (l == 0u) step_ids((t >> 5) + 2u);
     if (l == 16u) step_loads();
     issue(t + S - 1u);           // S-1 rows stay in flight
-    cp_async_wait_keep(S - 1u);  // row t has landed
+    cp_async_wait_n<S - 1>();    // row t has landed
     __syncwarp();
     do {
       const uint4 e = rinfo[t & 63u];
@@ -630,8 +626,9 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         break;
       }
       if (fl & 2u) {  // raw row
-        for (uint32_t v = lane; v < nvec; v += 32)
-          drow[v] = *reinterpret_cast<const uint4*>(sb + 4u * v);
+        uint4* dp = drow + lane;
+        for (uint32_t v = lane; v < nvec; v += 32, dp += 32)
+          *dp = *reinterpret_cast<const uint4*>(sb + 4u * v);
         break;
       }
       if (!can_pack) {
@@ -643,8 +640,9 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
                                         : __all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp);
       if (all_packed) {
         // every chunk participates: static offsets, no scan
-        for (uint32_t g = lane; g < G; g += 32)
-          drow[g] = decode_packed_group<kMode>(tab, sb, g, G, nch, 0u, net5, uni, F, uparm);
+        uint4* dp = drow + lane;
+        for (uint32_t g = lane; g < G; g += 32, dp += 32)
+          *dp = decode_packed_group<kMode>(tab, sb, g, G, nch, 0u, net5, uni, F, uparm);
         break;
       }
       // some chunks are raw: scan the chunk sizes
@@ -951,12 +949,11 @@ template <bool kIds, int kMode>
 cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, cudaStream_t st) {
   FastParams F;
   const uint32_t W = a.m.W, nch = a.m.nch;
-  // ring stages per warp: about 4 KB of row buffers
-  F.S = a.m.R <= 512u ? 8u : (a.m.R <= 1024u ? 4u : 2u);
+  F.S = kRingStages;
   F.table_words = (kMode == kModeUniform || kMode == kModeUniform1) ? 0u : 8u * W;
   F.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
   F.sbuf_words = ((W + 8u) + 3u) & ~3u;
-  F.warp_words = F.S * F.sbuf_words + 256u + ((nch + 3u) & ~3u);
+  F.warp_words = kRingStages * F.sbuf_words + 256u + ((nch + 3u) & ~3u);
   F.min_bits = hp.min_bits;
   F.um0 = hp.um0;
   F.um1 = hp.um1;
