@@ -139,13 +139,39 @@ class SparseStore:
         torch.cuda.synchronize()
         t_meta = ev[0].elapsed_time(ev[1]) / 1e3
         t_comp = ev[2].elapsed_time(ev[3]) / 1e3
+        # the companions on HBM-resident data: builder over all 2M rows (1 GB),
+        # compressor into HBM slots (bound by HBM, not the host link)
+        st2 = ibp.ibp_store_create(self.R, chunk, n_rows, 0)
+        slots_dev = torch.empty((n_rows, self.slot), dtype=torch.uint8, device=dev)
+        ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ibp.ibp_build_meta(st2, d_rows, self.R, None, n_rows, num, den)
+        ev2[0].record()
+        ibp.ibp_build_meta(st2, d_rows, self.R, None, n_rows, num, den)
+        ev2[1].record()
+        ibp.ibp_compress(st2, slots_dev, d_rows, self.R, None, n_rows, None)
+        ev2[2].record()
+        ibp.ibp_compress(st2, slots_dev, d_rows, self.R, None, n_rows, None)
+        ev2[3].record()
+        torch.cuda.synchronize()
+        assert ibp.ibp_stream_status(st2, reset=True) == ibp.IBP_OK
+        t_meta_all = ev2[0].elapsed_time(ev2[1]) / 1e3
+        t_comp_hbm = ev2[2].elapsed_time(ev2[3]) / 1e3
+        ibp.ibp_store_destroy(st2)
+        del slots_dev
         self.companions = {
             "build_meta": {"rows": len(sample), "seconds": round(t_meta, 6),
                            "gbs": round(len(sample) * self.R / t_meta / 1e9, 2),
                            "note": "1% sample of rows in HBM, ones count + threshold + tables"},
             "compress": {"rows": n_rows, "seconds": round(t_comp, 6),
                          "gbs": round(n_rows * self.R / t_comp / 1e9, 2),
-                         "note": "raw rows in HBM -> pinned host slots over the link"}}
+                         "note": "raw rows in HBM -> pinned host slots over the link"},
+            "build_meta_all_rows_hbm": {"rows": n_rows, "seconds": round(t_meta_all, 6),
+                                        "gbs": round(n_rows * self.R / t_meta_all / 1e9, 2),
+                                        "note": "all 2M rows (1 GB) analysed, in HBM"},
+            "compress_hbm": {"rows": n_rows, "seconds": round(t_comp_hbm, 6),
+                             "gbs": round(n_rows * self.R / t_comp_hbm / 1e9, 2),
+                             "note": "raw rows in HBM -> HBM slots (ratio 0.726: R read + "
+                                     "stored written per row)"}}
         assert ibp.ibp_stream_status(self.st, reset=True) == ibp.IBP_OK
         self.raw_host = None
         if keep_raw:  # uncompressed host copy: the raw-gather baseline
@@ -456,6 +482,126 @@ def run_tiny(args, rank, world, torch, dist):
     return res
 
 
+def run_kv(args, rank, world, torch, dist):
+    """LLM KV-cache fetch, OPT-6.7B shape: 32 layers x {K, V}, batch 20, 2048
+    token slots, 32 heads x 128 fp16 = 8 KB rows (21.5 GB of pinned host
+    slots).  K/V ~ N(0,1) x per-channel log-normal scale, 2 % outlier channels
+    x20, generated on the GPU (seeded torch generator per layer and K|V).
+    Mask/Bitval per (layer, K|V) from its 20 x 1920 prompt rows, chunk 256 B
+    (one head).  A step is one decode step's re-fetch: for each of the 64
+    (layer, K|V) stores, gather the 20 x (1920 + s) rows of the history into
+    HBM (s = 0)."""
+    from lossless_invariant_bit_gb300 import dist as ibpdist
+    from lossless_invariant_bit_gb300 import ibp
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    # one step moves ~20 GB over the host link (~0.1 s): at most 20 timed steps
+    args = argparse.Namespace(**vars(args))
+    args.steps, args.warmup = min(args.steps, 20), min(args.warmup, 3)
+    L, B, T, P, CH = args.kv_layers, 20, 2048, 1920, 4096
+    R, C = CH * 2, 256
+    rows_per = B * T
+    t0 = time.time()
+    stores, slots = [], []
+    g = torch.Generator(device=dev)
+    ratio_num = 0
+    prompt_ids = torch.from_numpy(
+        (np.arange(B)[:, None] * T + np.arange(P)[None, :]).reshape(-1).astype(np.int64)).to(dev)
+    check = None
+    for layer in range(L):
+        for kv in range(2):
+            g.manual_seed(args.seed * 1000003 + layer * 2 + kv)
+            z = torch.randn(CH, generator=g, device=dev)
+            scale = torch.exp(0.5 * z)
+            out_ch = torch.randperm(CH, generator=g, device=dev)[:int(round(0.02 * CH))]
+            scale[out_ch] *= 20.0
+            x = (torch.randn((rows_per, CH), generator=g, device=dev) * scale).to(torch.float16)
+            xb = x.view(torch.uint8)
+            st = ibp.ibp_store_create(R, C, rows_per, R)
+            ibp.ibp_build_meta(st, xb, R, prompt_ids, len(prompt_ids), 95, 100)
+            sl = torch.empty((rows_per, R), dtype=torch.uint8, pin_memory=True)
+            stored = torch.empty(rows_per, dtype=torch.int32, device=dev)
+            ibp.ibp_compress(st, sl, xb, R, None, rows_per, stored)
+            ratio_num += int(stored[:].view(B, T)[:, :P].sum().item())
+            if layer == 0 and kv == 0:
+                check = xb.view(B, T, R)[:, :P].clone()
+            stores.append(st)
+            slots.append(sl)
+            del x, xb
+    torch.cuda.synchronize()
+    log("KV store ready in %.1fs" % (time.time() - t0))
+    ratio = ratio_num / (2 * L * B * P * R)
+    ids = prompt_ids  # history at decode step 0: the 1920 prompt tokens
+    n = len(ids)
+    out = torch.empty((B, P, R), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def step(_):
+        for st, sl in zip(stores, slots):
+            ibp.ibp_gather_decompress(st, out, sl, None, ids, n, sp)
+
+    for b in range(args.warmup):
+        step(b)
+    torch.cuda.synchronize()
+    ibp.ibp_gather_decompress(stores[0], out, slots[0], None, ids, n, sp)
+    torch.cuda.synchronize()
+    parity_ok = bool(torch.equal(out, check))
+    evs = []
+    with ClockSampler(dev.index) as clk:
+        for b in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(b)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+    for st in stores:
+        assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    times = [a.elapsed_time(c) / 1e3 for a, c in evs]
+    t_total = ibpdist.max_over_ranks(sum(times), dist, dev)
+    raw_bytes = 2 * L * n * R
+    value = raw_bytes * args.steps * world / t_total / 1e9
+    pbytes = (slots[0].numel() // 16) * 16  # one store's slots, 335 MB
+    probe = torch.empty(pbytes, dtype=torch.uint8, device=dev)
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ibp.ibp_link_copy(probe, slots[0], pbytes, sp)
+        e1.record(stream)
+        e1.synchronize()
+        tt = e0.elapsed_time(e1) / 1e3
+        best = tt if best is None else min(best, tt)
+    link = pbytes / best / 1e9
+    del probe
+    roof = min(measured_peaks()["hbm_gbs"], link / ratio)
+    res = {
+        "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
+        "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_total / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (seeded torch generator on the GPU: OPT-6.7B-shaped K/V)",
+        "config": {"workload": "KV-cache fetch: %d layers x {K,V}, batch 20, 1920 prompt "
+                               "tokens of 2048 slots, 8 KB fp16 rows in pinned host slots, "
+                               "chunk 256 B, T=0.95; one step = 64 per-layer gathers" % L,
+                   "rows_per_store": rows_per, "row_bytes": R, "chunk_bytes": C,
+                   "l2": "flushed between steps (256 MB write, outside the timed events)"},
+        "ratio": round(ratio, 5), "link_gbs": round(link, 2), "parity_layer0_ok": parity_ok,
+        "roofline": {"bound": "link", "achieved": round(value / world, 2), "peak": round(roof, 2),
+                     "unit": "GB/s", "frac": round(value / world / roof, 4), "traffic": None,
+                     "kernel": "k_decode<true> (ibp_gather_decompress, 8 KB rows)"},
+        "gpu_launches": 2 * L * args.steps,
+        "clocks": clk.summary(),
+    }
+    for st in stores:
+        ibp.ibp_store_destroy(st)
+    return res
+
+
 def cpu_baseline(store, batches, ibp, seconds=1.5):
     """The oracle's decoder on the host cores over whole batches of this workload,
     until about `seconds` of wall time (x cores of CPU work) have been spent."""
@@ -539,7 +685,8 @@ def main():
     ap.add_argument("--batch", type=int, default=200_000)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--workload", default="sparse", choices=["sparse", "tiny"])
+    ap.add_argument("--workload", default="sparse", choices=["sparse", "tiny", "kv"])
+    ap.add_argument("--kv-layers", type=int, default=32)
     ap.add_argument("--replicas", type=int, default=128)
     ap.add_argument("--no-cache-path", action="store_true",
                     help="skip the HBM cache-path sub-result of the default workload")
@@ -566,7 +713,7 @@ def main():
         libbuild.build()
     if dist:
         dist.barrier()
-    run = run_tiny if args.workload == "tiny" else run_ours
+    run = {"tiny": run_tiny, "kv": run_kv}.get(args.workload, run_ours)
     res = run(args, rank, world, torch, dist)
     if args.workload == "sparse" and not args.no_cache_path:
         # the HBM cache path of the same metric, reported beside the host path
