@@ -102,19 +102,20 @@ __global__ void __launch_bounds__(128) k_count_ones(CountArgs a) {
   uint32_t inplanes = 0;
   const uint64_t step = gridDim.x;
   uint64_t r = blockIdx.x;
-  // four rows per trip: their loads are independent and overlap
-  for (; r + 3 * step < a.n; r += 4 * step) {
-    uint32_t x[4];
+  // eight rows per trip: their loads are independent and in flight together
+  constexpr int U = 8;
+  for (; r + (U - 1) * step < a.n; r += U * step) {
+    uint32_t x[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const uint64_t i = r + (uint64_t)u * step;
       const uint64_t row = a.ids ? (uint64_t)__ldg(a.ids + i) : i;
       x[u] = __ldg(reinterpret_cast<const uint32_t*>(a.rows + row * a.row_stride) + w);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) vadd(c, x[u]);
-    inplanes += 4;
-    if (inplanes > 255 - 4) {
+    for (int u = 0; u < U; ++u) vadd(c, x[u]);
+    inplanes += U;
+    if (inplanes > 255 - U) {
       vspill(c, ones);
       inplanes = 0;
     }
@@ -916,8 +917,9 @@ WarpSmem encode_smem(uint32_t W, uint32_t nch) {
 cudaError_t launch_count_ones(const CountArgs& a, int sm_count, cudaStream_t st) {
   const uint32_t tpb = 128;
   const uint32_t gy = (a.W + tpb - 1) / tpb;
-  // enough CTAs for ~4 per SM over the word tiles; each covers n/gx rows
-  uint64_t gx = ((uint64_t)sm_count * 4 + gy - 1) / gy;
+  // ~8 CTAs of 4 warps per SM over the word tiles (with 8 rows in flight per
+  // thread that keeps several MB of loads outstanding); each CTA covers n/gx rows
+  uint64_t gx = ((uint64_t)sm_count * 8 + gy - 1) / gy;
   const uint64_t max_gx = (a.n + 63) / 64;  // at least 64 rows per CTA
   if (gx > max_gx) gx = max_gx;
   if (gx < 1) gx = 1;
