@@ -67,9 +67,14 @@ __device__ __forceinline__ uint32_t gather_bits(uint32_t x, const uint32_t* mv, 
 // ------------------------------------------------------------------------
 // Builder (Core Algorithm > Preprocessing): ones count per row bit position.
 // Thread = one word position; block.x tiles words, grid.x splits the rows.
-// Each thread adds its words into 8 bit-plane counters (a vertical
-// ripple-carry adder: 16 logic ops per word per row) and spills them into 32
-// per-bit counts every 255 rows, then adds those into the global counts.
+// Eight rows at a time go through a carry-save adder tree (the Harley-Seal
+// positional popcount: W. Muła, N. Kurz, D. Lemire, "Faster Population
+// Counts Using AVX2 Instructions", 2018): running bit vectors of weight 1, 2
+// and 4 absorb the rows, and the weight-8 carries feed 8 bit-plane counters
+// (a vertical ripple-carry adder).  A carry-save step is two 3-input logic
+// ops, so eight rows cost ~30 logic ops instead of 8 x 16.  The planes spill
+// into 32 per-bit counts every 255 blocks of 8 rows; the per-thread totals go
+// to the global counts with one atomic per bit.
 // ------------------------------------------------------------------------
 __device__ __forceinline__ void vadd(uint32_t (&c)[8], uint32_t x) {
 #pragma unroll
@@ -92,46 +97,66 @@ __device__ __forceinline__ void vspill(uint32_t (&c)[8], uint32_t (&ones)[32]) {
   for (int p = 0; p < 8; ++p) c[p] = 0;
 }
 
+// carry-save add of three bit vectors: sum bits (weight 1), carry bits (weight 2)
+__device__ __forceinline__ void csa(uint32_t& hi, uint32_t& lo, uint32_t a, uint32_t b,
+                                    uint32_t c) {
+  const uint32_t u = a ^ b;
+  hi = (a & b) | (u & c);
+  lo = u ^ c;
+}
+
 __global__ void __launch_bounds__(128) k_count_ones(CountArgs a) {
   const uint32_t w = blockIdx.y * blockDim.x + threadIdx.x;
   if (w >= a.W) return;
-  uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  uint32_t ones[32];
+  uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // planes counting weight-8 carries
+  uint32_t n8[32];                            // spilled plane counts (units of 8 rows)
 #pragma unroll
-  for (int b = 0; b < 32; ++b) ones[b] = 0;
-  uint32_t inplanes = 0;
+  for (int b = 0; b < 32; ++b) n8[b] = 0;
+  uint32_t o1 = 0, o2 = 0, o4 = 0;  // running bit vectors of weight 1, 2, 4
+  uint32_t blocks = 0;
   const uint64_t step = gridDim.x;
   uint64_t r = blockIdx.x;
-  // eight rows per trip: their loads are independent and in flight together
-  constexpr int U = 8;
-  for (; r + (U - 1) * step < a.n; r += U * step) {
-    uint32_t x[U];
+  for (; r + 7 * step < a.n; r += 8 * step) {
+    uint32_t x[8];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const uint64_t i = r + (uint64_t)u * step;
       const uint64_t row = a.ids ? (uint64_t)__ldg(a.ids + i) : i;
       x[u] = __ldg(reinterpret_cast<const uint32_t*>(a.rows + row * a.row_stride) + w);
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) vadd(c, x[u]);
-    inplanes += U;
-    if (inplanes > 255 - U) {
-      vspill(c, ones);
-      inplanes = 0;
+    uint32_t t2a, t2b, t4a, t4b, t8;
+    csa(t2a, o1, o1, x[0], x[1]);
+    csa(t2b, o1, o1, x[2], x[3]);
+    csa(t4a, o2, o2, t2a, t2b);
+    csa(t2a, o1, o1, x[4], x[5]);
+    csa(t2b, o1, o1, x[6], x[7]);
+    csa(t4b, o2, o2, t2a, t2b);
+    csa(t8, o4, o4, t4a, t4b);
+    vadd(c, t8);
+    if (++blocks == 255u) {
+      vspill(c, n8);
+      blocks = 0;
     }
   }
-  for (; r < a.n; r += step) {
+  vspill(c, n8);  // room for the tail's carries in the 8-bit planes
+  for (; r < a.n; r += step) {  // the last < 8 rows: half adders down the chain
     const uint64_t row = a.ids ? (uint64_t)__ldg(a.ids + r) : r;
-    vadd(c, __ldg(reinterpret_cast<const uint32_t*>(a.rows + row * a.row_stride) + w));
-    if (++inplanes == 255) {
-      vspill(c, ones);
-      inplanes = 0;
-    }
+    const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(a.rows + row * a.row_stride) + w);
+    const uint32_t k1 = o1 & x;
+    o1 ^= x;
+    const uint32_t k2 = o2 & k1;
+    o2 ^= k1;
+    const uint32_t k4 = o4 & k2;
+    o4 ^= k2;
+    vadd(c, k4);
   }
-  vspill(c, ones);
+  vspill(c, n8);
 #pragma unroll
-  for (int b = 0; b < 32; ++b)
-    if (ones[b]) atomicAdd(a.counts + 32u * w + b, ones[b]);
+  for (int b = 0; b < 32; ++b) {
+    const uint32_t tot = 8u * n8[b] + 4u * ((o4 >> b) & 1u) + 2u * ((o2 >> b) & 1u) +
+                         ((o1 >> b) & 1u);
+    if (tot) atomicAdd(a.counts + 32u * w + b, tot);
+  }
 }
 
 // Threshold: bit j is invariant when ones*den >= num*n (value 1) or
