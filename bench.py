@@ -349,7 +349,12 @@ def run_ours(args, rank, world, torch, dist):
             "peak": round(roof, 2),
             "unit": "GB/s",
             "frac": round(delivered_per_launch / roof, 4),
-            "traffic": None,
+            # host-link read bytes of one 200,000-id launch: ncu capture of this kernel
+            # (profiles/k_decode_gather_sparse_gnn.md), 18.93 MB per 50,000 ids x 4;
+            # its DRAM bytes are ~0 there (the output is still in L2 at kernel end)
+            "traffic": 75.7e6,
+            "traffic_is": "host-link (sysmem) read bytes per launch from ncu, scaled "
+                          "from a 50,000-id capture",
             "peak_is": "min(HBM %s %.0f GB/s, link %.1f GB/s measured in this run / ratio %.4f)"
                        % (peaks["source"], hbm, link_gbs, ratio),
             "kernel": "k_decode<true> (ibp_gather_decompress)",
@@ -469,7 +474,13 @@ def run_tiny(args, rank, world, torch, dist):
         "ratio": round(ratio, 5),
         "parity_all_rows_ok": parity_ok,
         "roofline": {"bound": "hbm", "achieved": round(moved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(moved / hbm, 4), "traffic": None,
+                     "frac": round(moved / hbm, 4),
+                     # dram read + write of a 48-replica launch (profiles/
+                     # k_decode_fast_tiny_cache.md) scaled to this launch's rows
+                     "traffic": round(211.7e6 * n / (48 * 4096)),
+                     "traffic_is": "dram__bytes_read.sum + dram__bytes_write.sum from ncu, "
+                                   "scaled from a 196,608-row capture (part of the output is "
+                                   "still in L2 when the kernel ends)",
                      "peak_is": "HBM copy bandwidth, %s" % peaks["source"],
                      "kernel": "k_decode<false> (ibp_decompress, packed offsets)",
                      "algorithmic_bytes_per_launch": int(stored_sum + n * R + 8 * n)},
