@@ -55,6 +55,7 @@ extern "C" {
 #define IBP_MAX_ROW_BYTES 32768u
 #define IBP_MAX_CHUNKS 256u
 #define IBP_NOALLOC_MAX_ROW_BYTES 8192u
+#define IBP_MAX_TUNE_CANDIDATES 8u
 
 typedef enum {
   IBP_OK = 0,
@@ -116,6 +117,26 @@ IBP_API ibp_status ibp_store_get_info(const ibp_store* store, ibp_store_info* in
 IBP_API ibp_status ibp_build_meta(ibp_store* store, const void* rows, uint64_t row_stride,
                           const int64_t* sample_ids, uint64_t n, uint32_t thr_num,
                           uint32_t thr_den, ibp_stream_t stream);
+
+/* Chunk-aware preprocessing.  Core Algorithm > Preprocessing leaves the
+ * threshold T a free parameter; this builder picks it from the sample itself:
+ * for each candidate T_c = thr_num[c]/thr_den[c] (host arrays, n_thr <=
+ * IBP_MAX_TUNE_CANDIDATES, each 1/2 < T_c <= 1) it builds the Mask/Bitval
+ * exactly as ibp_build_meta would, then prices it by the bytes the sampled
+ * rows would be stored in (participation per chunk, stream bits, raw
+ * fallback), and installs the cheapest (the first on ties).  A Mask bit that
+ * makes chunks fall back to raw costs more than it saves, so this drops such
+ * bits -- e.g. at T = 0.95 a sparse feature matrix keeps its rare non-zero
+ * bits in the Mask and most rows go raw, while T = 0.999 packs every row.
+ * Everything runs on the device, asynchronously on `stream`.
+ *   chosen_out  optional device uint32: index of the installed candidate
+ *   sizes_out   optional device uint64[n_thr]: the sample's stored bytes per candidate
+ * Other arguments and errors as ibp_build_meta. */
+IBP_API ibp_status ibp_build_meta_tuned(ibp_store* store, const void* rows, uint64_t row_stride,
+                                        const int64_t* sample_ids, uint64_t n,
+                                        const uint32_t* thr_num, const uint32_t* thr_den,
+                                        uint32_t n_thr, uint32_t* chosen_out, uint64_t* sizes_out,
+                                        ibp_stream_t stream);
 
 /* Allocation-free builder.  The paper has no counterpart: this entry point
  * exists for callers that cannot allocate device memory when they build a

@@ -16,6 +16,8 @@ struct ibp_store {
   int sm_count;
   void* base;  // one device allocation, carved below
   uint32_t *mask, *bitval, *nm, *pre, *kr, *mv, *ckeep, *scal, *counts, *bitmap, *status;
+  uint32_t* cand;             // tuned builder: a Mask/Bitval per candidate threshold
+  unsigned long long* sizes;  // tuned builder: the sample's stored size per candidate
   uint4 *t2, *t5;  // fast-decoder descriptors
   uint32_t* gtab;
   uint32_t* h_scal;       // pinned host mirror of scal, filled after each derive
@@ -172,7 +174,8 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
   //        each piece 16-byte aligned
   auto r4 = [](uint64_t x) { return (x + 3u) & ~(uint64_t)3u; };
   const uint64_t words = 10ull * r4(W) + r4(nch) + 16 + 32ull * W + 4 + 12ull * W +
-                         r4(W / 4) + r4(nch) + r4(s->bitmap_words);
+                         r4(W / 4) + r4(nch) + 2ull * IBP_MAX_TUNE_CANDIDATES * r4(W) +
+                         2ull * IBP_MAX_TUNE_CANDIDATES + r4(s->bitmap_words);
   if (cudaMalloc(&s->base, words * 4) != cudaSuccess) {
     cudaGetLastError();
     delete s;
@@ -206,6 +209,8 @@ ibp_status ibp_store_create(ibp_store** out, uint32_t row_bytes, uint32_t chunk_
   s->t2 = reinterpret_cast<uint4*>(take(4ull * W));
   s->t5 = reinterpret_cast<uint4*>(take(8ull * W));
   s->gtab = take(r4(W / 4) + r4(nch));
+  s->cand = take(2ull * IBP_MAX_TUNE_CANDIDATES * r4(W));
+  s->sizes = reinterpret_cast<unsigned long long*>(take(2ull * IBP_MAX_TUNE_CANDIDATES));
   s->bitmap = take(s->bitmap_words);
   ibp_status e = cu(cudaMemset(s->base, 0, words * 4));
   if (e == IBP_OK) e = derive(s, 0);  // all-zero Mask: tables for "everything raw"
@@ -273,6 +278,37 @@ ibp_status ibp_build_meta(ibp_store* s, const void* rows, uint64_t row_stride,
   e = cu(ibp::launch_count_ones(a, s->sm_count, st));
   if (e != IBP_OK) return e;
   e = cu(ibp::launch_finish_meta(s->counts, s->W, n, thr_num, thr_den, s->mask, s->bitval, st));
+  if (e != IBP_OK) return e;
+  return derive(s, st);
+}
+
+ibp_status ibp_build_meta_tuned(ibp_store* s, const void* rows, uint64_t row_stride,
+                                const int64_t* sample_ids, uint64_t n, const uint32_t* thr_num,
+                                const uint32_t* thr_den, uint32_t n_thr, uint32_t* chosen_out,
+                                uint64_t* sizes_out, ibp_stream_t stream) {
+  if (!s || !rows || !thr_num || !thr_den) return IBP_EINVAL;
+  if (n_thr == 0 || n_thr > IBP_MAX_TUNE_CANDIDATES) return IBP_EINVAL;
+  for (uint32_t c = 0; c < n_thr; ++c)
+    if (thr_den[c] == 0 || thr_num[c] > thr_den[c] || 2ull * thr_num[c] <= thr_den[c])
+      return IBP_EINVAL;
+  if (n == 0 || n >= (1ull << 32)) return IBP_EINVAL;
+  if (!aligned16(rows) || (row_stride & 15u) || row_stride < s->R) return IBP_EALIGN;
+  ibp_status e = on_device(s);
+  if (e != IBP_OK) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  e = cu(cudaMemsetAsync(s->counts, 0, 32ull * s->W * 4, st));
+  if (e != IBP_OK) return e;
+  ibp::CountArgs a;
+  a.rows = static_cast<const uint8_t*>(rows);
+  a.row_stride = row_stride;
+  a.ids = sample_ids;
+  a.n = n;
+  a.W = s->W;
+  a.counts = s->counts;
+  e = cu(ibp::launch_count_ones(a, s->sm_count, st));
+  if (e != IBP_OK) return e;
+  e = cu(ibp::launch_tune(a, s->counts, thr_num, thr_den, n_thr, s->wpc, s->nch, s->cand,
+                          s->sizes, s->mask, s->bitval, chosen_out, sizes_out, s->sm_count, st));
   if (e != IBP_OK) return e;
   return derive(s, st);
 }

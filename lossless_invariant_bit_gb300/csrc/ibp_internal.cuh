@@ -115,6 +115,14 @@ WarpSmem encode_smem(uint32_t W, uint32_t nch);
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_count_ones(const CountArgs& a, int sm_count, cudaStream_t st);
+// Candidate thresholds num[c]/den[c] (host arrays): a Mask per candidate into
+// cand, the sample's stored size under each into sizes, the cheapest into
+// mask/bitval (counts must already hold the sample's ones counts).
+cudaError_t launch_tune(const CountArgs& a, const uint32_t* counts, const uint32_t* num,
+                        const uint32_t* den, uint32_t n_c, uint32_t wpc, uint32_t nch,
+                        uint32_t* cand, unsigned long long* sizes, uint32_t* mask,
+                        uint32_t* bitval, uint32_t* chosen_out, uint64_t* sizes_out,
+                        int sm_count, cudaStream_t st);
 cudaError_t launch_finish_meta(const uint32_t* counts, uint32_t W, uint64_t n, uint32_t num,
                                uint32_t den, uint32_t* mask, uint32_t* bitval, cudaStream_t st);
 cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32_t* pre,

@@ -178,6 +178,76 @@ __global__ void k_finish_meta(const uint32_t* counts, uint32_t W, uint64_t n, ui
   bitval[w] = bv;
 }
 
+// Chunk-aware choice among candidate thresholds (the review's sampling
+// experiment uses the sample for the Mask; here the same sample also prices
+// each candidate Mask): for candidate c (blockIdx.y), the stored size every
+// sampled row would take -- participation per chunk, stream bits, raw
+// fallback -- summed into sizes[c].  cand holds, per candidate, W Mask words
+// then W Bitval words.
+__global__ void __launch_bounds__(256) k_size_estimate(const uint8_t* rows, uint64_t row_stride,
+                                                       const int64_t* ids, uint64_t n,
+                                                       const uint32_t* cand, uint32_t W,
+                                                       uint32_t wpc, uint32_t nch,
+                                                       unsigned long long* sizes) {
+  extern __shared__ uint32_t sm[];
+  const uint32_t c = blockIdx.y;
+  const uint32_t* M = cand + 2ull * W * c;
+  const uint32_t* B = M + W;
+  const uint32_t nr = (nch + 3u) & ~3u;
+  uint32_t* ck = sm;  // kept bits per chunk under this candidate
+  const uint32_t lane = threadIdx.x & 31u, wid = threadIdx.x >> 5;
+  uint32_t* mism = sm + nr * (1u + wid);
+  for (uint32_t k = threadIdx.x; k < nch; k += blockDim.x) ck[k] = 0;
+  __syncthreads();
+  for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) atomicAdd(&ck[w / wpc], (uint32_t)__popc(~M[w]));
+  __syncthreads();
+  const uint32_t R = 4u * W;
+  unsigned long long local = 0;
+  const uint64_t wstride = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  for (uint64_t i = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid; i < n; i += wstride) {
+    const uint64_t row = ids ? (uint64_t)__ldg(ids + i) : i;
+    const uint32_t* x = reinterpret_cast<const uint32_t*>(rows + row * row_stride);
+    for (uint32_t k = lane; k < nch; k += 32) mism[k] = 0;
+    __syncwarp();
+    for (uint32_t w = lane; w < W; w += 32)
+      if ((__ldg(x + w) & __ldg(M + w)) != __ldg(B + w)) mism[w / wpc] = 1u;
+    __syncwarp();
+    uint32_t part = 0;
+    for (uint32_t k = lane; k < nch; k += 32) {
+      const uint32_t full = 32u * min(wpc, W - k * wpc);
+      part += (mism[k] == 0u && ck[k] < full) ? ck[k] : full;
+    }
+    const uint32_t bits = nch + __reduce_add_sync(0xFFFFFFFFu, part);
+    const uint32_t stored = 4u * ((bits + 31u) >> 5);
+    local += stored >= R ? R : stored;
+    __syncwarp();
+  }
+  if (lane == 0 && local) atomicAdd(sizes + c, local);
+}
+
+// The cheapest candidate (the first on ties) becomes the store's Mask/Bitval.
+__global__ void __launch_bounds__(256) k_pick_meta(const uint32_t* cand,
+                                                   const unsigned long long* sizes, uint32_t n_c,
+                                                   uint32_t W, uint32_t* mask, uint32_t* bitval,
+                                                   uint32_t* chosen_out, uint64_t* sizes_out) {
+  __shared__ uint32_t best;
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+    for (uint32_t c = 1; c < n_c; ++c)
+      if (sizes[c] < sizes[b]) b = c;
+    best = b;
+    if (chosen_out) *chosen_out = b;
+  }
+  if (sizes_out)
+    for (uint32_t c = threadIdx.x; c < n_c; c += blockDim.x) sizes_out[c] = sizes[c];
+  __syncthreads();
+  const uint32_t* M = cand + 2ull * W * best;
+  for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
+    mask[w] = M[w];
+    bitval[w] = M[W + w];
+  }
+}
+
 // Decode tables from the Mask (one block).  The move masks are those of the
 // classic 5-stage bit gather (H. S. Warren, Hacker's Delight, sec. 7-4 and
 // 7-5): at stage i, the bits of the current mask with an odd number of
@@ -956,6 +1026,34 @@ cudaError_t launch_count_ones(const CountArgs& a, int sm_count, cudaStream_t st)
 cudaError_t launch_finish_meta(const uint32_t* counts, uint32_t W, uint64_t n, uint32_t num,
                                uint32_t den, uint32_t* mask, uint32_t* bitval, cudaStream_t st) {
   k_finish_meta<<<(W + 127) / 128, 128, 0, st>>>(counts, W, n, num, den, mask, bitval);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tune(const CountArgs& a, const uint32_t* counts, const uint32_t* num,
+                        const uint32_t* den, uint32_t n_c, uint32_t wpc, uint32_t nch,
+                        uint32_t* cand, unsigned long long* sizes, uint32_t* mask,
+                        uint32_t* bitval, uint32_t* chosen_out, uint64_t* sizes_out,
+                        int sm_count, cudaStream_t st) {
+  const uint32_t W = a.W;
+  for (uint32_t c = 0; c < n_c; ++c) {
+    k_finish_meta<<<(W + 127) / 128, 128, 0, st>>>(counts, W, a.n, num[c], den[c],
+                                                    cand + 2ull * W * c, cand + 2ull * W * c + W);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(sizes, 0, sizeof(unsigned long long) * n_c, st);
+  if (e != cudaSuccess) return e;
+  const uint32_t nr = (nch + 3u) & ~3u;
+  const size_t smem = 4ull * nr * 9u;
+  uint64_t gx = ((uint64_t)sm_count * 4 + n_c - 1) / n_c;
+  const uint64_t need = (a.n + 7) / 8;
+  if (gx > need) gx = need;
+  if (gx < 1) gx = 1;
+  k_size_estimate<<<dim3((uint32_t)gx, n_c), 256, smem, st>>>(a.rows, a.row_stride, a.ids, a.n,
+                                                              cand, W, wpc, nch, sizes);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_pick_meta<<<1, 256, 0, st>>>(cand, sizes, n_c, W, mask, bitval, chosen_out, sizes_out);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,7 @@ _SIGS = {
     "ibp_store_destroy": [_P],
     "ibp_store_get_info": [_P, ctypes.POINTER(ibp_store_info)],
     "ibp_build_meta": [_P, _P, _U64, _P, _U64, _U32, _U32, _P],
+    "ibp_build_meta_tuned": [_P, _P, _U64, _P, _U64, _P, _P, _U32, _P, _P, _P],
     "ibp_build_meta_noalloc": [_P, _U64, _U32, _P, _U64, _U32, _U32, _P, _P, _P],
     "ibp_compress": [_P, _P, _P, _U64, _P, _U64, _P, _P],
     "ibp_decompress": [_P, _P, _P, _P, _U64, _P],
@@ -139,6 +140,19 @@ def ibp_build_meta(store: int, rows, row_stride: int, sample_ids, n: int, thr_nu
                    thr_den: int, stream=None) -> None:
     _check(_lib_handle().ibp_build_meta(store, _ptr(rows), row_stride, _ptr(sample_ids), n,
                                         thr_num, thr_den, _stream(stream)), "ibp_build_meta")
+
+
+def ibp_build_meta_tuned(store: int, rows, row_stride: int, sample_ids, n: int, thr_num,
+                         thr_den, chosen_out=None, sizes_out=None, stream=None) -> None:
+    """thr_num / thr_den: sequences of candidate thresholds (host)."""
+    k = len(thr_num)
+    num = (ctypes.c_uint32 * k)(*[int(v) for v in thr_num])
+    den = (ctypes.c_uint32 * k)(*[int(v) for v in thr_den])
+    _check(_lib_handle().ibp_build_meta_tuned(store, _ptr(rows), row_stride, _ptr(sample_ids), n,
+                                              ctypes.cast(num, ctypes.c_void_p),
+                                              ctypes.cast(den, ctypes.c_void_p), k,
+                                              _ptr(chosen_out), _ptr(sizes_out), _stream(stream)),
+           "ibp_build_meta_tuned")
 
 
 def ibp_build_meta_noalloc(rows, row_stride: int, row_bytes: int, sample_ids, n: int,

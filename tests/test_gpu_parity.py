@@ -412,3 +412,70 @@ def test_decoder_before_store_properties_reach_host(stores, kind):
     m, bv = st.meta()
     mr, br = ref_c.build_meta(b, 9, 10)
     assert np.array_equal(m, mr) and np.array_equal(bv, br)
+
+
+# ---------------------------------------------------------------- chunk-aware builder
+CANDS = [(9, 10), (95, 100), (99, 100), (999, 1000), (1, 1)]
+
+
+@pytest.mark.parametrize("kind", ["sparse", "dense", "fuzz", "kv"])
+def test_tuned_builder_matches_oracle(stores, kind):
+    """The installed Mask is the candidate whose sample would be stored in the
+    fewest bytes (first on ties); sizes and choice match the oracle's."""
+    if kind == "sparse":
+        n, R, C = 60_000, 512, 1024
+        b = rows_u8(wl.sparse_gnn_rows(n, seed=5))
+        sample = wl.sample_ids(n, 50, seed=5)
+    elif kind == "dense":
+        n, R, C = 20_000, 512, 256
+        b = rows_u8(wl.dense_gnn_rows(n, seed=6))
+        sample = wl.sample_ids(n, 100, seed=6)
+    elif kind == "kv":
+        R, C = 8192, 256
+        b = wl.kv_rows(0, 1, 2, range(200)).view(np.uint8).reshape(-1, R)
+        n = len(b)
+        sample = None
+    else:
+        n, R, C = 5000, 256, 64
+        b = wl.fuzz_rows(n, R, seed=9)
+        sample = wl.sample_ids(n, 200, seed=9)
+    st = stores(R, C, n)
+    d = to_dev(b)
+    d_s = None if sample is None else to_dev(sample)
+    m_n = n if sample is None else len(sample)
+    chosen = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sizes = torch.zeros(len(CANDS), dtype=torch.int64, device=DEV)
+    ibp.ibp_build_meta_tuned(st.h, d, R, d_s, m_n, [c[0] for c in CANDS], [c[1] for c in CANDS],
+                             chosen, sizes)
+    assert st.status() == ibp.IBP_OK
+    m, bv = st.meta()
+    ref_sizes = []
+    metas = []
+    rows_s = b if sample is None else b[sample]
+    for num, den in CANDS:
+        mr, br = ref_c.build_meta(b, num, den, sample_ids=sample)
+        slots = np.zeros((len(rows_s), R), np.uint8)
+        bm = np.zeros((len(rows_s) + 31) // 32, np.uint32)
+        stored = ref_c.compress_batch(rows_s, C, mr, br, slots, bm, nthreads=8)
+        ref_sizes.append(int(stored.astype(np.int64).sum()))
+        metas.append((mr, br))
+    best = int(np.argmin(ref_sizes))
+    assert sizes.cpu().tolist() == ref_sizes
+    assert int(chosen.item()) == best
+    assert np.array_equal(m, metas[best][0]) and np.array_equal(bv, metas[best][1])
+    if kind == "sparse":  # the rare 1.0 bits leave the Mask: every row packs
+        assert CANDS[best] in [(999, 1000), (1, 1)]
+    # and the store decodes what it compresses under the chosen Mask
+    slots_g, stored_g = gpu_compress(st, d, n)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, slots_g, None, n)
+    assert st.status() == ibp.IBP_OK and np.array_equal(out.cpu().numpy(), b)
+
+
+def test_tuned_builder_rejects_bad_candidates(stores):
+    st = stores(64, 16, 4)
+    d = torch.zeros((4, 64), dtype=torch.uint8, device=DEV)
+    for nums, dens in [([], []), ([1] * 9, [1] * 9), ([1, 1], [2, 1])]:
+        with pytest.raises(ibp.IbpError) as e:
+            ibp.ibp_build_meta_tuned(st.h, d, 64, None, 4, nums, dens)
+        assert e.value.status == ibp.IBP_EINVAL
