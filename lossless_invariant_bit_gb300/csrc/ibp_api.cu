@@ -113,12 +113,6 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.n_rows = s->n_rows;
   a.dst = static_cast<uint8_t*>(dst);
   a.dst_stride = dst_stride;
-  cudaPointerAttributes attr;
-  if (cudaPointerGetAttributes(&attr, src) != cudaSuccess) {
-    cudaGetLastError();
-    return IBP_EINVAL;
-  }
-  a.src_on_device = attr.type == cudaMemoryTypeDevice;
   return cu(ibp::launch_decode(a, host_props(s), s->sm_count, st));
 }
 

@@ -47,7 +47,6 @@ struct DecodeArgs {
   uint64_t n_rows;
   uint8_t* dst;
   uint64_t dst_stride;
-  bool src_on_device;       // src is device (HBM) memory, not host-mapped memory
 };
 
 struct EncodeArgs {

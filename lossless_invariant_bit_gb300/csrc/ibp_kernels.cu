@@ -487,14 +487,15 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
 
 // ------------------------------------------------------------------------
 // Fast decompression for rows of at most 2 KB whose chunks hold whole groups
-// of 4 words (C % 16 == 0), from HBM: the common geometries (512 B - 2 KB
+// of 4 words (C % 16 == 0): the common geometries (512 B - 2 KB
 // rows, chunks of 256 B / 1 KB / 4 KB).  Differences from k_decode:
 //   - a warp resolves 32 rows at a time, one per lane (id -> offset -> raw
 //     bit, coalesced), the next 32 one chunk ahead, and then walks them one
 //     by one; each row's (offset, flags) reach the warp by one shuffle;
-//   - the stored bytes travel by cp.async into a ring of S single-row stages
-//     in shared memory, S-1 rows ahead of the row being decoded, so the bytes
-//     in flight cost no registers;
+//   - the stored bytes travel by cp.async (.ca) into a ring of S single-row
+//     stages in shared memory, S-1 rows ahead of the row being decoded, so the
+//     bytes in flight cost no registers; this holds for HBM sources and for
+//     pinned host memory read over the link;
 //   - a row whose chunks all participate (the usual case) needs no scan: word
 //     w's kept bits sit at a static offset (for a uniform store, one whose
 //     words all share the same ~Mask and Bitval, nch + w*keep);
@@ -689,7 +690,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
 #pragma unroll
         for (uint32_t j = 0; j < 4u; ++j)
           if (lane + 32u * j < nv)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * j),
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * j),
                          "l"(src + 512u * j));
       }
     }
@@ -1111,9 +1112,10 @@ cudaError_t launch_fast_mode(const DecodeArgs& a, const HostProps& hp, int sm_co
 cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count,
                           cudaStream_t st) {
   if (a.n == 0) return cudaSuccess;
-  // cp.async staging pays off from HBM; reads of host memory over the link go
-  // faster as plain 16-byte register loads (measured), so they take k_decode
-  if (a.src_on_device && a.t2 && fast_geometry(a.m.R, a.m.wpc * 4u))
+  // rows up to 2 KB take the fast decoder from HBM and from host memory alike
+  // (its cp.async copies use the .ca form: measured, the L2-only .cg form
+  // reads host memory over the link at 60 % of the rate)
+  if (a.t2 && fast_geometry(a.m.R, a.m.wpc * 4u))
     return a.ids ? launch_fast_mode<true>(a, hp, sm_count, st)
                  : launch_fast_mode<false>(a, hp, sm_count, st);
   const WarpSmem L = decode_smem(a.m.W, a.m.nch);
