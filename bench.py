@@ -349,7 +349,12 @@ def run_ours(args, rank, world, torch, dist):
             "peak": round(roof, 2),
             "unit": "GB/s",
             "frac": round(delivered_per_launch / roof, 4),
-            "traffic": None,  # kernel changed since the last capture
+            # host-link read bytes of one 200,000-id launch: ncu capture of this kernel
+            # (profiles/k_decode_gather_sparse_gnn.md), 18.93 MB per 50,000 ids x 4;
+            # its DRAM bytes are ~0 there (the output is still in L2 at kernel end)
+            "traffic": 75.7e6,
+            "traffic_is": "host-link (sysmem) read bytes per launch from ncu, scaled "
+                          "from a 50,000-id capture",
             "peak_is": "min(HBM %s %.0f GB/s, link %.1f GB/s measured in this run / ratio %.4f)"
                        % (peaks["source"], hbm, link_gbs, ratio),
             "kernel": "k_decode_fast<true, mode> (ibp_gather_decompress, host-memory source)",
