@@ -649,6 +649,119 @@ def run_kv(args, rank, world, torch, dist):
     return res
 
 
+def run_dlrm(args, rank, world, torch, dist):
+    """DLRM embedding lookup: 26 tables x 1,000,000 rows of fp32 ~ N(0, 0.01^2)
+    (dim 128/256/512: 512 B - 2 KB rows) compressed into pinned host slots
+    (13.3 GB at dim 128), one Mask/Bitval per table from a 1 % sample, T = 0.95,
+    chunk 1 KB.  A step is one batch of 8192 lookups, one Zipf(1.05) index per
+    table (through a seeded permutation), gather-decompressed into a dense
+    [8192, 26, dim] HBM tensor."""
+    from lossless_invariant_bit_gb300 import dist as ibpdist
+    from lossless_invariant_bit_gb300 import ibp
+    from lossless_invariant_bit_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    Tn, N, dim, B, C = 26, args.dlrm_rows, args.dlrm_dim, 8192, 1024
+    R = dim * 4
+    t0 = time.time()
+    stores, slots, tables_ok = [], [], []
+    g = torch.Generator(device=dev)
+    stored_sum = []
+    check_rows = []
+    batches = [np.stack([wl.zipf_ids(B, N, table=t, seed=args.seed * 1000 + bb)
+                         for t in range(Tn)], axis=1) for bb in range(min(args.pool, 4))]
+    for t in range(Tn):
+        g.manual_seed(args.seed * 7919 + t)
+        x = (torch.randn((N, dim), generator=g, device=dev) * 0.01).view(torch.uint8)
+        st = ibp.ibp_store_create(R, C, N, R)
+        sample = torch.from_numpy(wl.sample_ids(N, 10, seed=args.seed + t)).to(dev)
+        ibp.ibp_build_meta(st, x, R, sample, sample.numel(), 95, 100)
+        sl = torch.empty((N, R), dtype=torch.uint8, pin_memory=True)
+        stored = torch.empty(N, dtype=torch.int32, device=dev)
+        ibp.ibp_compress(st, sl, x, R, None, N, stored)
+        stored_sum.append(stored.to(torch.int64).cpu().numpy())
+        # the rows the last batch looks up in this table, for the parity check
+        check_rows.append(x[torch.from_numpy(batches[-1][:, t]).to(dev)].cpu())
+        stores.append(st)
+        slots.append(sl)
+        del x
+    torch.cuda.synchronize()
+    log("DLRM store ready in %.1fs" % (time.time() - t0))
+    ids_dev = [[torch.from_numpy(np.ascontiguousarray(bt[:, t])).to(dev) for t in range(Tn)]
+               for bt in batches]
+    out = torch.empty((B, Tn, R), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    pool = len(batches)
+
+    def step(b):
+        ids = ids_dev[b % pool]
+        for t in range(Tn):
+            ibp.ibp_gather_decompress_strided(stores[t], out[:, t], Tn * R, slots[t], None,
+                                              ids[t], B, sp)
+
+    for b in range(args.warmup):
+        step(b)
+    step(pool - 1)
+    torch.cuda.synchronize()
+    parity_ok = all(torch.equal(out[:, t].cpu(), check_rows[t]) for t in range(Tn))
+    evs = []
+    with ClockSampler(dev.index) as clk:
+        for b in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(b)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+    for st in stores:
+        assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    times = [a.elapsed_time(c) / 1e3 for a, c in evs]
+    t_total = ibpdist.max_over_ranks(sum(times), dist, dev)
+    value = B * Tn * R * args.steps * world / t_total / 1e9
+    ratio = statistics.mean(
+        sum(float(stored_sum[t][batches[b % pool][:, t]].sum()) for t in range(Tn)) / (B * Tn * R)
+        for b in range(args.steps))
+    pbytes = (slots[0].numel() // 16) * 16
+    probe = torch.empty(pbytes, dtype=torch.uint8, device=dev)
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ibp.ibp_link_copy(probe, slots[0], pbytes, sp)
+        e1.record(stream)
+        e1.synchronize()
+        tt = e0.elapsed_time(e1) / 1e3
+        best = tt if best is None else min(best, tt)
+    link = pbytes / best / 1e9
+    del probe
+    roof = min(measured_peaks()["hbm_gbs"], link / ratio)
+    res = {
+        "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
+        "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_total / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (seeded torch generator on the GPU: N(0, 0.01^2) embedding tables)",
+        "config": {"workload": "DLRM lookup: 26 tables x %d rows x dim %d fp32 in pinned host "
+                               "slots, chunk 1 KB, 1%% sample, T=0.95; batch 8192 Zipf(1.05) ids "
+                               "per table -> [8192, 26, %d]" % (N, dim, dim),
+                   "row_bytes": R, "launches_per_step": Tn,
+                   "l2": "flushed between steps (256 MB write, outside the timed events)"},
+        "ratio": round(ratio, 5), "link_gbs": round(link, 2), "parity_all_lookups_ok": parity_ok,
+        "roofline": {"bound": "link", "achieved": round(value / world, 2), "peak": round(roof, 2),
+                     "unit": "GB/s", "frac": round(value / world / roof, 4), "traffic": None,
+                     "kernel": "k_decode_fast<true, mode> (ibp_gather_decompress_strided)"},
+        "gpu_launches": Tn * args.steps,
+        "clocks": clk.summary(),
+    }
+    for st in stores:
+        ibp.ibp_store_destroy(st)
+    return res
+
+
 def cpu_baseline(store, batches, ibp, seconds=1.5):
     """The oracle's decoder on the host cores over whole batches of this workload,
     until about `seconds` of wall time (x cores of CPU work) have been spent."""
@@ -732,7 +845,9 @@ def main():
     ap.add_argument("--batch", type=int, default=200_000)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--workload", default="sparse", choices=["sparse", "tiny", "kv"])
+    ap.add_argument("--workload", default="sparse", choices=["sparse", "tiny", "kv", "dlrm"])
+    ap.add_argument("--dlrm-dim", type=int, default=128, choices=[128, 256, 512])
+    ap.add_argument("--dlrm-rows", type=int, default=1_000_000)
     ap.add_argument("--kv-layers", type=int, default=32)
     ap.add_argument("--replicas", type=int, default=128)
     ap.add_argument("--no-tuned", action="store_true",
@@ -762,7 +877,7 @@ def main():
         libbuild.build()
     if dist:
         dist.barrier()
-    run = {"tiny": run_tiny, "kv": run_kv}.get(args.workload, run_ours)
+    run = {"tiny": run_tiny, "kv": run_kv, "dlrm": run_dlrm}.get(args.workload, run_ours)
     res = run(args, rank, world, torch, dist)
     if args.workload == "sparse" and not args.no_cache_path:
         # the HBM cache path of the same metric, reported beside the host path
