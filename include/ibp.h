@@ -56,6 +56,7 @@ extern "C" {
 #define IBP_MAX_CHUNKS 256u
 #define IBP_NOALLOC_MAX_ROW_BYTES 8192u
 #define IBP_MAX_TUNE_CANDIDATES 8u
+#define IBP_MAX_GROUP_STORES 64u
 
 typedef enum {
   IBP_OK = 0,
@@ -71,6 +72,10 @@ typedef enum {
 /* Opaque store: geometry, Mask/Bitval, tables derived from them, the raw
  * bitmap of its n_rows slots and a device status word, all in HBM. */
 typedef struct ibp_store ibp_store;
+
+/* Opaque group of stores of one geometry, decoded together (see
+ * ibp_group_gather_decompress). */
+typedef struct ibp_group ibp_group;
 
 /* A cudaStream_t. */
 typedef struct CUstream_st* ibp_stream_t;
@@ -202,6 +207,31 @@ IBP_API ibp_status ibp_gather_decompress_strided(const ibp_store* store, void* d
                                          uint64_t dst_stride_bytes,
                                          const void* host_or_dev_src, const uint64_t* offsets,
                                          const int64_t* ids, uint64_t n, ibp_stream_t stream);
+
+/* A group of n stores (1 <= n <= IBP_MAX_GROUP_STORES) that share row and
+ * chunk size, with the slot storage srcs[t] of each (host-mapped or device,
+ * 16-byte aligned), for fused gathers: one launch serves a batch of lookups
+ * into every store, e.g. the per-table lookups of a DLRM batch (the review's
+ * DLRM embedding-lookup integration).  Rows must be <= 2 KB with chunks a
+ * multiple of 16 bytes, slots <= 64 KB.  Waits for the stores' pending
+ * Mask/Bitval builds; a store whose Mask/Bitval changes later needs a new
+ * group.  Allocates device memory.  Errors: IBP_EINVAL, IBP_EALIGN,
+ * IBP_ENOMEM, IBP_ECUDA. */
+IBP_API ibp_status ibp_group_create(ibp_group** out, ibp_store* const* stores,
+                                    const void* const* srcs, uint32_t n);
+
+/* Free a group (synchronises the device; the stores are not touched). */
+IBP_API ibp_status ibp_group_destroy(ibp_group* group);
+
+/* Fused gather-decompression over a group of T stores: ids is a device int64
+ * [batch, T] array; item (b, t) is the decompressed row ids[b*T + t] of store
+ * t and lands at dst + b*dst_row_stride + t*R (dst_row_stride >= T*R,
+ * multiple of 16), e.g. a dense [batch, T, dim] embedding output.  Data
+ * errors set the status word of the store concerned.  Errors: IBP_EINVAL,
+ * IBP_EALIGN, IBP_ECUDA. */
+IBP_API ibp_status ibp_group_gather_decompress(const ibp_group* group, void* dst,
+                                               uint64_t dst_row_stride, const int64_t* ids,
+                                               uint64_t batch, ibp_stream_t stream);
 
 /* Build a packed HBM cache (System Integration: compressed GPU software
  * cache) from compressed slots: row i's stored_bytes[i] bytes at

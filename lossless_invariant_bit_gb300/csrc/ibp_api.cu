@@ -25,6 +25,12 @@ struct ibp_store {
   uint64_t bitmap_words;
 };
 
+struct ibp_group {
+  uint32_t T, R, C, W, wpc, nch;
+  int device, sm_count;
+  ibp::GroupEntry* entries;  // device copy, one per store
+};
+
 namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -366,6 +372,123 @@ ibp_status ibp_pack(const ibp_store* s, void* dst_packed, uint64_t* offsets_out,
   return cu(ibp::launch_pack(static_cast<uint8_t*>(dst_packed), offsets_out,
                              static_cast<const uint8_t*>(src_slots), s->slot, stored_bytes, n,
                              s->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ibp_status ibp_group_create(ibp_group** out, ibp_store* const* stores, const void* const* srcs,
+                            uint32_t n) {
+  if (!out || !stores || !srcs || n == 0 || n > IBP_MAX_GROUP_STORES) return IBP_EINVAL;
+  *out = nullptr;
+  const ibp_store* s0 = stores[0];
+  if (!s0) return IBP_EINVAL;
+  if (!ibp::fast_geometry(s0->R, s0->C)) return IBP_EINVAL;
+  ibp::GroupEntry* h = new (std::nothrow) ibp::GroupEntry[n];
+  if (!h) return IBP_ENOMEM;
+  ibp_status e = on_device(s0);
+  for (uint32_t t = 0; t < n && e == IBP_OK; ++t) {
+    const ibp_store* s = stores[t];
+    if (!s || !srcs[t] || s->R != s0->R || s->C != s0->C || s->device != s0->device) {
+      e = IBP_EINVAL;
+      break;
+    }
+    if (!aligned16(srcs[t])) {
+      e = IBP_EALIGN;
+      break;
+    }
+    if (s->n_rows > (1ull << 40) || s->slot > (1ull << 16)) {  // item offsets fit 56 bits
+      e = IBP_EINVAL;
+      break;
+    }
+    if (cudaEventSynchronize(s->props_ev) != cudaSuccess) {
+      e = IBP_ECUDA;
+      break;
+    }
+    const ibp::HostProps hp = host_props(s);
+    ibp::GroupEntry& g = h[t];
+    g.src = static_cast<const uint8_t*>(srcs[t]);
+    g.bitmap = s->bitmap;
+    g.status = s->status;
+    g.gtab = s->gtab;
+    g.ckeep = s->ckeep;
+    g.slot = s->slot;
+    g.n_rows = s->n_rows;
+    g.mode = hp.uniform ? (hp.um1 == 0 ? ibp::kModeUniform1 : ibp::kModeUniform)
+                        : (hp.max_runs <= 2 ? ibp::kModeRun2 : ibp::kModeNet5);
+    g.tab = g.mode == ibp::kModeNet5 ? s->t5 : s->t2;
+    const uint32_t min_words = (hp.min_bits + 31u) / 32u;
+    const uint32_t nvec = s->R / 16u;
+    const uint32_t mv = (4u * min_words + 15u) / 16u;
+    g.min_vec = mv < nvec ? mv : nvec;
+    g.can_pack = 4u * min_words < s->R ? 1u : 0u;
+    g.um0 = hp.um0;
+    g.um1 = hp.um1;
+    g.ush = hp.ush;
+    g.ubv = hp.ubv;
+    g.ukeep = hp.ukeep;
+  }
+  ibp_group* grp = nullptr;
+  if (e == IBP_OK) {
+    grp = new (std::nothrow) ibp_group();
+    if (!grp) e = IBP_ENOMEM;
+  }
+  if (e == IBP_OK) {
+    grp->T = n;
+    grp->R = s0->R;
+    grp->C = s0->C;
+    grp->W = s0->W;
+    grp->wpc = s0->wpc;
+    grp->nch = s0->nch;
+    grp->device = s0->device;
+    grp->sm_count = s0->sm_count;
+    if (cudaMalloc(&grp->entries, sizeof(ibp::GroupEntry) * n) != cudaSuccess) {
+      cudaGetLastError();
+      e = IBP_ENOMEM;
+    } else if (cudaMemcpy(grp->entries, h, sizeof(ibp::GroupEntry) * n, cudaMemcpyHostToDevice) !=
+               cudaSuccess) {
+      cudaFree(grp->entries);
+      e = IBP_ECUDA;
+    }
+    if (e != IBP_OK) {
+      delete grp;
+      grp = nullptr;
+    }
+  }
+  delete[] h;
+  if (e == IBP_OK) *out = grp;
+  return e;
+}
+
+ibp_status ibp_group_destroy(ibp_group* g) {
+  if (!g) return IBP_OK;
+  cudaDeviceSynchronize();
+  const cudaError_t e = cudaFree(g->entries);
+  delete g;
+  return cu(e);
+}
+
+ibp_status ibp_group_gather_decompress(const ibp_group* g, void* dst, uint64_t dst_row_stride,
+                                       const int64_t* ids, uint64_t batch, ibp_stream_t stream) {
+  if (!g) return IBP_EINVAL;
+  if (batch == 0) return IBP_OK;
+  if (!dst || !ids) return IBP_EINVAL;
+  if (!aligned16(dst) || (dst_row_stride & 15u) || dst_row_stride < (uint64_t)g->T * g->R)
+    return IBP_EALIGN;
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) return IBP_ECUDA;
+  if (d != g->device) return IBP_EINVAL;
+  ibp::GroupArgs a;
+  a.entries = g->entries;
+  a.T = g->T;
+  a.R = g->R;
+  a.W = g->W;
+  a.wpc = g->wpc;
+  a.nch = g->nch;
+  a.ids = ids;
+  a.n_items = batch * g->T;
+  a.dst = static_cast<uint8_t*>(dst);
+  a.dst_row_stride = dst_row_stride;
+  a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
+  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u);
+  return cu(ibp::launch_group(a, g->sm_count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ibp_status ibp_meta_get(const ibp_store* s, uint32_t* mask_host, uint32_t* bitval_host) {

@@ -109,6 +109,37 @@ struct FastParams {
   uint32_t um0, um1, ush, ubv, ukeep;
 };
 
+// One store of a fused multi-store gather (all stores share R and C).
+struct GroupEntry {
+  const uint8_t* src;      // the store's slots (host-mapped or HBM)
+  const uint32_t* bitmap;  // raw bitmap
+  uint32_t* status;        // device status word
+  const uint4* tab;        // two-run (t2) or network (t5) descriptors, global memory
+  const uint32_t* gtab;    // group table, then the all-packed chunk starts
+  const uint32_t* ckeep;   // kept bits per chunk
+  uint64_t slot;
+  uint64_t n_rows;
+  uint32_t mode;           // kModeUniform / kModeUniform1 / kModeRun2 / kModeNet5
+  uint32_t min_vec;        // 16-byte vectors of the shortest compressed stream
+  uint32_t can_pack;       // some compressed row can exist
+  uint32_t um0, um1, ush, ubv, ukeep;  // uniform stores
+};
+
+struct GroupArgs {
+  const GroupEntry* entries;
+  uint32_t T;               // stores in the group
+  uint32_t R, W, wpc, nch;  // shared geometry
+  const int64_t* ids;       // [batch, T]: item b*T + t looks up ids[b*T + t] in store t
+  uint64_t n_items;         // batch * T
+  uint8_t* dst;             // item (b, t) at dst + b*dst_row_stride + t*R
+  uint64_t dst_row_stride;
+  uint32_t sbuf_words;
+  uint32_t warp_words;
+};
+
+cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st);
+bool fast_geometry(uint32_t R, uint32_t C);
+
 WarpSmem decode_smem(uint32_t W, uint32_t nch);
 WarpSmem encode_smem(uint32_t W, uint32_t nch);
 

@@ -797,6 +797,215 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
 }
 
 // ------------------------------------------------------------------------
+// Fused multi-store gather (a batch of lookups into several stores of one
+// geometry -- the 26 embedding tables of a DLRM batch -- in one launch, so
+// small per-table batches still fill the GPU).  Item i = b*T + t looks up
+// ids[i] in store t and lands at dst + b*dst_row_stride + t*R.  The pipeline
+// is k_decode_fast's; each row takes its store's parameters from a per-store
+// entry staged in shared memory, and stores that are not uniform read their
+// decode descriptors from global memory (L1/L2 resident: a few KB each).
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
+  extern __shared__ __align__(16) uint32_t smem[];
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t wid = threadIdx.x >> 5;
+  const uint32_t R = g.R, W = g.W, wpc = g.wpc, nch = g.nch, T = g.T;
+  const uint32_t nvec = R >> 4;
+  const uint32_t G = W >> 2;
+  const uint32_t G4 = (G + 3u) & ~3u;
+  constexpr uint32_t S = kRingStages;
+  GroupEntry* ent = reinterpret_cast<GroupEntry*>(smem);
+  const uint32_t ent_words = T * (uint32_t)(sizeof(GroupEntry) / 4);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(g.entries);
+    uint4* dstv = reinterpret_cast<uint4*>(smem);
+    for (uint32_t v = threadIdx.x; v < ent_words / 4u; v += blockDim.x) dstv[v] = __ldg(src + v);
+  }
+  uint32_t* ring = smem + ent_words + wid * g.warp_words;
+  uint4* rinfo = reinterpret_cast<uint4*>(ring + S * g.sbuf_words);
+  uint32_t* cinfo = ring + S * g.sbuf_words + 256;
+  __syncthreads();
+  const uint32_t nhw = (nch + 31u) >> 5;
+  const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
+                                                                 : ((1u << (nch & 31u)) - 1u);
+  const uint64_t nw = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  const uint64_t gw = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
+  const uint64_t r0 = g.n_items * gw / nw;
+  const uint32_t cnt = (uint32_t)(g.n_items * (gw + 1) / nw - r0);
+  if (cnt == 0) return;
+
+  int64_t pid = 0;
+  uint64_t poff = 0;
+  uint32_t pbm = 0, pt = 0;
+  bool pin = false;
+  auto step_ids = [&](uint32_t q) {
+    const uint32_t t = 32u * q + lane;
+    pin = q < (cnt + 31u) / 32u && t < cnt;
+    if (pin) {
+      pid = __ldg(g.ids + r0 + t);
+      pt = (uint32_t)((r0 + t) % T);
+    }
+  };
+  auto step_loads = [&]() {
+    if (pin && pid >= 0 && (uint64_t)pid < ent[pt].n_rows) {
+      poff = (uint64_t)pid * ent[pt].slot;
+      pbm = __ldg(ent[pt].bitmap + (pid >> 5));
+    }
+  };
+  auto step_store = [&](uint32_t q) {
+    uint32_t fl = 0;
+    uint64_t off = 0;
+    if (pin) {
+      if (pid < 0 || (uint64_t)pid >= ent[pt].n_rows) {
+        fl = 1u | 4u;
+      } else {
+        fl = 1u | (((pbm >> (pid & 31)) & 1u) << 1);
+        off = poff;
+      }
+    }
+    const uint64_t i = r0 + 32ull * q + lane;
+    const uint64_t dsto = (i / T) * g.dst_row_stride + (uint64_t)pt * R;
+    rinfo[((q & 1u) << 5) + lane] = make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32) | (pt << 24),
+                                               (uint32_t)dsto, (uint32_t)(dsto >> 32));
+  };
+  const uint32_t ring_sa = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + 16u * lane;
+  auto issue = [&](uint32_t tt) {
+    if (tt < cnt) {
+      const uint4 e = rinfo[tt & 63u];
+      const uint32_t fl = e.x & 15u;
+      if ((fl & 13u) == 1u) {
+        const GroupEntry& en = ent[e.y >> 24];
+        const uint32_t nv = (fl & 2u) ? nvec : en.min_vec;
+        const uint8_t* src = en.src + 16u * lane +
+                             ((((uint64_t)(e.y & 0xFFFFFFu)) << 32) | (uint64_t)(e.x & ~15u));
+        const uint32_t sa = ring_sa + 4u * (tt & (S - 1u)) * g.sbuf_words;
+#pragma unroll
+        for (uint32_t j = 0; j < 4u; ++j)
+          if (lane + 32u * j < nv)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * j),
+                         "l"(src + 512u * j));
+      }
+    }
+    cp_async_commit();
+  };
+
+  for (uint32_t q = 0; q < 2u; ++q) {
+    step_ids(q);
+    step_loads();
+    step_store(q);
+  }
+  __syncwarp();
+  for (uint32_t t = 0; t + 1u < S; ++t) issue(t);
+#pragma unroll 1
+  for (uint32_t t = 0; t < cnt; ++t) {
+    const uint32_t l = t & 31u;
+    if (l == 0u) step_ids((t >> 5) + 2u);
+    if (l == 16u) step_loads();
+    issue(t + S - 1u);
+    cp_async_wait_n<S - 1>();
+    __syncwarp();
+    do {
+      const uint4 e = rinfo[t & 63u];
+      const uint32_t fl = e.x & 15u;
+      const GroupEntry& en = ent[e.y >> 24];
+      uint4* drow = reinterpret_cast<uint4*>(g.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
+      uint32_t* sb = ring + (t & (S - 1u)) * g.sbuf_words;
+      if (fl & 12u) {
+        if (lane == 0) set_status(en.status, IBP_ERANGE);
+        zero_row(drow, nvec, lane);
+        break;
+      }
+      if (fl & 2u) {
+        uint4* dp = drow + lane;
+        for (uint32_t v = lane; v < nvec; v += 32, dp += 32)
+          *dp = *reinterpret_cast<const uint4*>(sb + 4u * v);
+        break;
+      }
+      if (!en.can_pack) {
+        if (lane == 0) set_status(en.status, IBP_ECORRUPT);
+        zero_row(drow, nvec, lane);
+        break;
+      }
+      const uint32_t mode = en.mode;
+      const bool uni = mode == (uint32_t)kModeUniform || mode == (uint32_t)kModeUniform1;
+      const bool net5 = mode == (uint32_t)kModeNet5;
+      const bool all_packed = nhw == 1u ? (sb[0] & hexp) == hexp
+                                        : __all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp);
+      uint32_t words = 0;
+      if (!all_packed) {
+        uint32_t run = nch;
+        for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
+          const uint32_t k = k0 + lane;
+          uint32_t size = 0, pk = 0;
+          if (k < nch) {
+            pk = (sb[k >> 5] >> (k & 31u)) & 1u;
+            size = pk ? __ldg(en.ckeep + k) : 32u * min(wpc, W - k * wpc);
+          }
+          const uint32_t incl = warp_inclusive_scan(size, lane);
+          if (k < nch) cinfo[k] = (run + incl - size) | (pk << 31);
+          run += __shfl_sync(kFull, incl, 31);
+        }
+        words = (run + 31u) >> 5;
+        if (4u * words >= R || 4ull * words > en.slot) {
+          if (lane == 0) set_status(en.status, IBP_ECORRUPT);
+          __syncwarp();
+          zero_row(drow, nvec, lane);
+          break;
+        }
+        const uint32_t need_vec = (4u * words + 15u) >> 4;
+        if (need_vec > en.min_vec) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              en.src + ((((uint64_t)(e.y & 0xFFFFFFu)) << 32) | (uint64_t)(e.x & ~15u)));
+          for (uint32_t v = en.min_vec + lane; v < need_vec; v += 32)
+            st_smem_v4(sb + 4u * v, ld_nc_v4(src + v));
+        }
+        __syncwarp();
+      }
+      const uint32_t* cstat = en.gtab + G4;
+      uint4* dp = drow + lane;
+      for (uint32_t gi = lane; gi < G; gi += 32, dp += 32) {
+        uint32_t delta = 0;
+        bool packed = true;
+        uint32_t start = 0, gd = 0;
+        if (!all_packed) {
+          gd = __ldg(en.gtab + gi);
+          const uint32_t k = gd & 0xFFFFu;
+          const uint32_t ci = cinfo[k];
+          start = ci & 0x7FFFFFFFu;
+          packed = (ci >> 31) != 0u;
+          delta = start - __ldg(cstat + k);
+        }
+        if (!packed) {
+          const uint32_t bit = start + ((gd >> 16) << 5);
+          const uint32_t q = bit >> 5;
+          *dp = make_uint4(__funnelshift_r(sb[q], sb[q + 1], bit), __funnelshift_r(sb[q + 1], sb[q + 2], bit),
+                           __funnelshift_r(sb[q + 2], sb[q + 3], bit), __funnelshift_r(sb[q + 3], sb[q + 4], bit));
+        } else if (uni) {
+          uint32_t bit = nch + 4u * gi * en.ukeep + delta;
+          uint32_t o[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const uint32_t q = bit >> 5;
+            const uint32_t v = __funnelshift_r(sb[q], sb[q + 1], bit);
+            o[x] = ((v << (en.ush & 31u)) & en.um0) | ((v << (en.ush >> 8)) & en.um1) | en.ubv;
+            bit += en.ukeep;
+          }
+          *dp = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          *dp = decode_group(en.tab, sb, gi, G, delta, net5);
+        }
+      }
+    } while (false);
+    __syncwarp();
+    if (l == 31u) {
+      step_store((t >> 5) + 2u);
+      __syncwarp();
+    }
+  }
+  cp_async_wait_n<0>();
+}
+
+// ------------------------------------------------------------------------
 // Compression (Core Algorithm > Compression).  One warp per row: stage the
 // row in shared memory, flag chunks with a Mask mismatch, decide the
 // participation bits, scan the chunk sizes, then every lane gathers the kept
@@ -1093,7 +1302,7 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   if (e != cudaSuccess) return e;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = (a.n + 32ull * warps - 1) / (32ull * warps);  // >= 32 rows per warp
+  const uint64_t need = (a.n + 8ull * warps - 1) / (8ull * warps);  // >= 8 rows per warp
   if (blocks > need) blocks = need;
   kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, F);
   return cudaGetLastError();
@@ -1164,6 +1373,21 @@ cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uin
   const uint64_t need = (n + 7) / 8;
   if (blocks > need) blocks = need;
   k_pack_copy<<<(uint32_t)blocks, 256, 0, st>>>(dst, offsets, src, slot, stored, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st) {
+  if (g.n_items == 0) return cudaSuccess;
+  const int warps = 8;
+  const size_t smem = 4ull * (g.T * (sizeof(GroupEntry) / 4) + (uint64_t)warps * g.warp_words);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_gather_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int bps = blocks_per_sm(k_gather_group, 32 * warps, smem);
+  uint64_t blocks = (uint64_t)sm_count * bps;
+  const uint64_t need = (g.n_items + 8ull * warps - 1) / (8ull * warps);
+  if (blocks > need) blocks = need;
+  k_gather_group<<<(uint32_t)blocks, 32 * warps, smem, st>>>(g);
   return cudaGetLastError();
 }
 

@@ -54,6 +54,9 @@ _SIGS = {
     "ibp_gather_decompress": [_P, _P, _P, _P, _P, _U64, _P],
     "ibp_gather_decompress_strided": [_P, _P, _U64, _P, _P, _P, _U64, _P],
     "ibp_pack": [_P, _P, _P, _P, _P, _U64, _P],
+    "ibp_group_create": [ctypes.POINTER(ctypes.c_void_p), _P, _P, _U32],
+    "ibp_group_destroy": [_P],
+    "ibp_group_gather_decompress": [_P, _P, _U64, _P, _U64, _P],
     "ibp_meta_get": [_P, _P, _P],
     "ibp_meta_set": [_P, _P, _P],
     "ibp_bitmap_get": [_P, _P],
@@ -195,6 +198,29 @@ def ibp_pack(store: int, dst_packed, offsets_out, src_slots, stored_bytes, n: in
              stream=None) -> None:
     _check(_lib_handle().ibp_pack(store, _ptr(dst_packed), _ptr(offsets_out), _ptr(src_slots),
                                   _ptr(stored_bytes), n, _stream(stream)), "ibp_pack")
+
+
+def ibp_group_create(stores, srcs) -> int:
+    """stores: sequence of store handles; srcs: their slot buffers (tensors or addresses)."""
+    n = len(stores)
+    st_arr = (ctypes.c_void_p * n)(*stores)
+    src_arr = (ctypes.c_void_p * n)(*[_ptr(x) for x in srcs])
+    h = ctypes.c_void_p()
+    _check(_lib_handle().ibp_group_create(ctypes.byref(h), ctypes.cast(st_arr, ctypes.c_void_p),
+                                          ctypes.cast(src_arr, ctypes.c_void_p), n),
+           "ibp_group_create")
+    return h.value
+
+
+def ibp_group_destroy(group: int) -> None:
+    _check(_lib_handle().ibp_group_destroy(group), "ibp_group_destroy")
+
+
+def ibp_group_gather_decompress(group: int, dst, dst_row_stride: int, ids, batch: int,
+                                stream=None) -> None:
+    _check(_lib_handle().ibp_group_gather_decompress(group, _ptr(dst), dst_row_stride, _ptr(ids),
+                                                     batch, _stream(stream)),
+           "ibp_group_gather_decompress")
 
 
 def ibp_meta_get(store: int, mask_host, bitval_host) -> None:

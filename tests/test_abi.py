@@ -58,6 +58,15 @@ def test_host_side_argument_checks(lib):
     st = ctypes.c_int()
     assert lib.ibp_stream_status(None, None, ctypes.byref(st), 0) == ibp.IBP_EINVAL
     assert lib.ibp_store_destroy(None) == ibp.IBP_OK
+    grp = ctypes.c_void_p()
+    assert lib.ibp_group_create(ctypes.byref(grp), None, None, 1) == ibp.IBP_EINVAL
+    assert lib.ibp_group_create(None, 16, 16, 1) == ibp.IBP_EINVAL
+    assert lib.ibp_group_gather_decompress(None, 16, 512, 16, 1, None) == ibp.IBP_EINVAL
+    assert lib.ibp_group_destroy(None) == ibp.IBP_OK
+    num = (ctypes.c_uint32 * 1)(95)
+    den = (ctypes.c_uint32 * 1)(100)
+    assert lib.ibp_build_meta_tuned(None, 16, 16, None, 1, num, den, 1, None, None,
+                                    None) == ibp.IBP_EINVAL
     # copies: alignment and size checked on the host
     assert lib.ibp_link_copy(16, 16, 0, None) == ibp.IBP_OK
     assert lib.ibp_link_copy(None, 16, 16, None) == ibp.IBP_EINVAL

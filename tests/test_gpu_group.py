@@ -1,0 +1,153 @@
+"""Fused multi-store gather (ibp_group_*) against the rows and the per-store path.
+
+A DLRM-shaped group (26 tables, Zipf lookups, [batch, tables, dim] output)
+and a mixed group whose stores cover every decode mode (uniform, two-run,
+network, all-raw), host and HBM sources, raw chunks and an out-of-range id.
+"""
+import numpy as np
+import pytest
+import torch
+
+from lossless_invariant_bit_gb300 import ibp
+from lossless_invariant_bit_gb300 import workloads as wl
+from oracle import ref_c
+from tests.gpu_util import DEV, Store, oracle_slots, rows_u8, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _host_store(R, C, rows_b, sample=None, num=95, den=100, host=True):
+    n = rows_b.shape[0]
+    st = Store(R, C, n)
+    d = torch.from_numpy(rows_b).to(DEV)
+    ids = None if sample is None else torch.from_numpy(sample).to(DEV)
+    ibp.ibp_build_meta(st.h, d, R, ids, n if sample is None else len(sample), num, den)
+    slots = (torch.empty((n, st.slot), dtype=torch.uint8, pin_memory=True) if host
+             else torch.empty((n, st.slot), dtype=torch.uint8, device=DEV))
+    ibp.ibp_compress(st.h, slots, d, R, None, n, None)
+    torch.cuda.synchronize()
+    return st, slots
+
+
+@pytest.mark.parametrize("dim", [128, 512])
+def test_group_dlrm_matches_per_store(dim):
+    T, N, B, R, C = 26, 5000, 2049, dim * 4, 1024
+    stores, slots, tables = [], [], []
+    try:
+        for t in range(T):
+            rb = rows_u8(wl.dlrm_rows(N, dim, table=t, seed=1))
+            st, sl = _host_store(R, C, rb, wl.sample_ids(N, 50, seed=t), host=(t % 3 != 0))
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+        ids = np.stack([wl.zipf_ids(B, N, table=t, seed=2) for t in range(T)], axis=1)
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            out = torch.full((B, T, R), 0xCC, dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress(grp, out, T * R, to_dev(ids), B)
+            for s in stores:
+                assert s.status() == ibp.IBP_OK
+            o = out.cpu().numpy()
+            for t in range(T):
+                assert np.array_equal(o[:, t], tables[t][ids[:, t]]), t
+            # the per-store strided gathers give the same bytes
+            ref = torch.zeros((B, T, R), dtype=torch.uint8, device=DEV)
+            for t in range(T):
+                ibp.ibp_gather_decompress_strided(stores[t].h, ref[:, t], T * R, slots[t], None,
+                                                  to_dev(np.ascontiguousarray(ids[:, t])), B)
+            assert torch.equal(out, ref)
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()
+
+
+def test_group_mixed_modes_errors_and_raw_chunks():
+    R, C, N, B = 512, 64, 3000, 777
+    stores, slots, tables = [], [], []
+    specs = []
+    try:
+        # uniform two-run (dense fp32), uniform with empty ~Mask (sparse), network (fuzz),
+        # two-run non-uniform (set), all raw (fresh store), uniform one run (1 + k/1024)
+        dense = rows_u8(wl.dense_gnn_rows(N, seed=3))
+        sparse = rows_u8(wl.sparse_gnn_rows(N, seed=3))
+        fuzz = wl.fuzz_rows(N, R, seed=4)
+        tiny = rows_u8(wl.tiny_rows(seed=5, n_rows=N, dim=R // 4, raw_frac=0.02)[0])
+        for rb, host in [(dense, True), (sparse, False), (fuzz, True), (tiny, False)]:
+            st, sl = _host_store(R, C, rb, host=host)
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+        # two-run, non-uniform Masks, set on the host; a tenth of the rows miss one word
+        g = np.random.default_rng(6)
+        mask = np.zeros(R // 4, np.uint32)
+        for w in range(R // 4):
+            a0 = int(g.integers(0, 16))
+            keep = ((1 << int(g.integers(1, 9))) - 1) << a0 | (1 << 31)
+            mask[w] = ~np.uint32(keep & 0xFFFFFFFF)
+        bitval = g.integers(0, 1 << 32, size=R // 4, dtype=np.uint64).astype(np.uint32) & mask
+        rows = (g.integers(0, 1 << 32, size=(N, R // 4), dtype=np.uint64).astype(np.uint32)
+                & ~mask) | bitval
+        miss = g.random(N) < 0.1
+        rows[miss, 3] ^= mask[3] & 0x00FF0000
+        rb = rows.view(np.uint8)
+        st = Store(R, C, N)
+        st.set_meta(mask, bitval)
+        assert ibp.ibp_store_get_info(st.h).max_runs <= 2
+        sl = torch.empty((N, st.slot), dtype=torch.uint8, pin_memory=True)
+        ibp.ibp_compress(st.h, sl, torch.from_numpy(rb).to(DEV), R, None, N, None)
+        stores.append(st)
+        slots.append(sl)
+        tables.append(rb)
+        # all raw: a store whose Mask was never built
+        st = Store(R, C, N)
+        sl = torch.empty((N, st.slot), dtype=torch.uint8, device=DEV)
+        ibp.ibp_compress(st.h, sl, torch.from_numpy(fuzz).to(DEV), R, None, N, None)
+        stores.append(st)
+        slots.append(sl)
+        tables.append(fuzz)
+        torch.cuda.synchronize()
+        T = len(stores)
+        ids = np.stack([g.integers(0, N, size=B) for _ in range(T)], axis=1).astype(np.int64)
+        ids[5, 2] = N + 7  # out of range in store 2
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            stride = T * R + 64
+            out = torch.full((B, stride), 0xCC, dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress(grp, out, stride, to_dev(ids), B)
+            st_codes = [s.status() for s in stores]
+            assert st_codes[2] == ibp.IBP_ERANGE
+            assert all(c == ibp.IBP_OK for i, c in enumerate(st_codes) if i != 2)
+            o = out.cpu().numpy()
+            for t in range(T):
+                got = o[:, t * R:(t + 1) * R]
+                want = tables[t][np.clip(ids[:, t], 0, N - 1)]
+                if t == 2:
+                    assert np.all(got[5] == 0)
+                    got = np.delete(got, 5, axis=0)
+                    want = np.delete(want, 5, axis=0)
+                assert np.array_equal(got, want), t
+            assert np.all(o[:, T * R:] == 0xCC)  # bytes past the last table untouched
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()
+
+
+def test_group_rejects_mixed_geometry():
+    a = Store(512, 256, 10)
+    b = Store(1024, 256, 10)
+    c = Store(4096, 256, 10)
+    try:
+        buf = torch.empty(10 * 4096, dtype=torch.uint8, device=DEV)
+        with pytest.raises(ibp.IbpError) as e:
+            ibp.ibp_group_create([a.h, b.h], [buf, buf])
+        assert e.value.status == ibp.IBP_EINVAL
+        with pytest.raises(ibp.IbpError) as e:  # rows above 2 KB are not fused
+            ibp.ibp_group_create([c.h], [buf])
+        assert e.value.status == ibp.IBP_EINVAL
+    finally:
+        for s in (a, b, c):
+            s.close()
