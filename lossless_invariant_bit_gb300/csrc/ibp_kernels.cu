@@ -12,6 +12,9 @@
 // decoder is bound by the host link (zero-copy source) or by HBM (cache
 // source), the builder by the bandwidth of the rows it reads, and the bit
 // work runs on the integer pipes.
+#include <mutex>
+#include <vector>
+
 #include "ibp_internal.cuh"
 
 namespace ibp {
@@ -1184,12 +1187,42 @@ __global__ void __launch_bounds__(256) k_pack_copy(uint8_t* dst, const uint64_t*
   }
 }
 
+// Resident blocks per SM of a kernel at a launch shape, with its dynamic
+// shared-memory limit raised as needed.  Both runtime queries cost more host
+// time than a small launch takes on the GPU, so the answers are kept per
+// (device, kernel, threads, shared memory).
+struct LaunchCfg {
+  int dev;
+  const void* fn;
+  int threads;
+  size_t smem;
+  int bps;
+};
+std::mutex g_cfg_mu;
+std::vector<LaunchCfg> g_cfg;
+
 template <typename K>
 int blocks_per_sm(K kernel, int threads, size_t smem) {
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_cfg_mu);
+  size_t max_smem = 0;
+  for (const LaunchCfg& c : g_cfg) {
+    if (c.dev != dev || c.fn != fn) continue;
+    if (c.threads == threads && c.smem == smem) return c.bps;
+    if (c.smem > max_smem) max_smem = c.smem;
+  }
+  if (smem > max_smem && smem > 48u * 1024u)
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int b = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, smem) != cudaSuccess)
-    return 1;
-  return b > 0 ? b : 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    b = 1;
+  }
+  if (b < 1) b = 1;
+  g_cfg.push_back({dev, fn, threads, smem, b});
+  return b;
 }
 
 uint32_t warps_for(uint32_t per_warp_bytes) {
@@ -1298,11 +1331,9 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   const int warps = 8;
   const size_t smem = 4ull * (F.table_words + F.gtab_words + 8 + (uint64_t)warps * F.warp_words);
   auto kern = k_decode_fast<kIds, kMode>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = (a.n + 8ull * warps - 1) / (8ull * warps);  // >= 8 rows per warp
+  const uint64_t need = (a.n + 32ull * warps - 1) / (32ull * warps);  // >= 32 rows per warp
   if (blocks > need) blocks = need;
   kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, F);
   return cudaGetLastError();
@@ -1332,13 +1363,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count
   const int threads = (int)(32u * warps);
   const size_t smem = (size_t)4u * L.total_words * warps;
   int bps;
-  if (a.ids) {
-    cudaFuncSetAttribute(k_decode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (a.ids)
     bps = blocks_per_sm(k_decode<true>, threads, smem);
-  } else {
-    cudaFuncSetAttribute(k_decode<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  else
     bps = blocks_per_sm(k_decode<false>, threads, smem);
-  }
   uint64_t blocks = (uint64_t)sm_count * bps;
   const uint64_t need = (a.n + warps - 1) / warps;
   if (blocks > need) blocks = need;
@@ -1355,7 +1383,6 @@ cudaError_t launch_encode(const EncodeArgs& a, int sm_count, cudaStream_t st) {
   const uint32_t warps = warps_for(4u * L.total_words);
   const int threads = (int)(32u * warps);
   const size_t smem = (size_t)4u * L.total_words * warps;
-  cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const int bps = blocks_per_sm(k_encode, threads, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
   const uint64_t need = (a.n + warps - 1) / warps;
@@ -1380,9 +1407,6 @@ cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st) {
   if (g.n_items == 0) return cudaSuccess;
   const int warps = 8;
   const size_t smem = 4ull * (g.T * (sizeof(GroupEntry) / 4) + (uint64_t)warps * g.warp_words);
-  cudaError_t e =
-      cudaFuncSetAttribute(k_gather_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   const int bps = blocks_per_sm(k_gather_group, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
   const uint64_t need = (g.n_items + 8ull * warps - 1) / (8ull * warps);
