@@ -795,6 +795,93 @@ def run_dlrm(args, rank, world, torch, dist):
     return res
 
 
+def run_transfers(args, rank, world, torch, dist):
+    """The review's Figure 5 on this machine: moving randomly chosen rows (tensors)
+    from pinned host memory into HBM, by method and row size.  Rows are
+    uncompressed; GB/s of rows delivered.  GPU aligned = ibp_gather_copy on
+    128-byte aligned slots; GPU unaligned = the same kernel on a source shifted
+    64 bytes off the line boundaries; CPU fine-grained = one cudaMemcpyAsync
+    per row; CPU bulk = gather into a pinned staging buffer, then one copy.
+    Timed with host wall clock to the stream's completion (the CPU methods do
+    their work on the host)."""
+    from lossless_invariant_bit_gb300 import ibp
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    total = 1 << 30
+    res_sizes = {}
+    for R in (128, 512, 2048, 8192):
+        slot = ((R + 127) // 128) * 128
+        N = total // slot
+        host = torch.empty(N * slot + 128, dtype=torch.uint8, pin_memory=True)
+        host.random_(0, 256)
+        g = np.random.default_rng(R)
+        n = min(100_000, N // 4)
+        ids_np = g.integers(0, N - 1, size=n).astype(np.int64)
+        ids_host = torch.from_numpy(ids_np).pin_memory()
+        ids_dev = ids_host.to(dev)
+        out = torch.empty((n, R), dtype=torch.uint8, device=dev)
+        staging = torch.empty(n * R, dtype=torch.uint8, pin_memory=True)
+
+        def wall(fn, reps):
+            fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                fn()
+            torch.cuda.synchronize()
+            return (time.perf_counter() - t0) / reps
+
+        m = {}
+        t = wall(lambda: ibp.ibp_gather_copy(out, host, slot, R, ids_dev, n, N, sp), 20)
+        m["gpu_aligned"] = n * R / t / 1e9
+        shifted = host.data_ptr() + 64
+        t = wall(lambda: ibp.ibp_gather_copy(out, shifted, slot, R, ids_dev, n, N - 1, sp), 20)
+        m["gpu_unaligned"] = n * R / t / 1e9
+        nb = min(n, 20_000)
+        t = wall(lambda: ibp.ibp_gather_copy_staged(out, host, slot, R, ids_host, nb, N, staging,
+                                                     sp), 3)
+        m["cpu_bulk"] = nb * R / t / 1e9
+        nd = min(n, 5_000)
+        t = wall(lambda: ibp.ibp_gather_copy_dma(out, host, slot, R, ids_host, nd, N, sp), 3)
+        m["cpu_fine_grained"] = nd * R / t / 1e9
+        # the aligned gather's output is checked against the host rows
+        ibp.ibp_gather_copy(out, host, slot, R, ids_dev, n, N, sp)
+        torch.cuda.synchronize()
+        hv = host[:N * slot].view(N, slot)
+        pick = torch.from_numpy(g.choice(n, 500, replace=False))
+        ok = torch.equal(out.cpu()[pick], hv[torch.from_numpy(ids_np)[pick], :R])
+        res_sizes[str(R)] = {k: round(v, 2) for k, v in m.items()}
+        res_sizes[str(R)]["aligned_over_unaligned"] = round(m["gpu_aligned"] / m["gpu_unaligned"], 3)
+        res_sizes[str(R)]["parity_ok"] = bool(ok)
+        del host, staging, out
+        torch.cuda.empty_cache()
+    probe_src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    probe_dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    best = None
+    for _ in range(5):
+        ev[0].record(stream)
+        ibp.ibp_link_copy(probe_dst, probe_src, 1 << 30, sp)
+        ev[1].record(stream)
+        ev[1].synchronize()
+        tt = ev[0].elapsed_time(ev[1]) / 1e3
+        best = tt if best is None else min(best, tt)
+    head = res_sizes["512"]["gpu_aligned"]
+    return {
+        "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
+        "value": head, "unit": "GB/s", "n_gpus": 1, "steps": 20, "warmup": 1,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8", "data": "synthetic random bytes",
+        "config": {"workload": "transfer methods (Figure 5 of the review): random rows of "
+                               "128 B - 8 KB from 1 GB of pinned host memory into HBM"},
+        "link_limit_gbs": round((1 << 30) / best / 1e9, 2),
+        "by_row_bytes": res_sizes,
+    }
+
+
 def cpu_baseline(store, batches, ibp, seconds=1.5):
     """The oracle's decoder on the host cores over whole batches of this workload,
     until about `seconds` of wall time (x cores of CPU work) have been spent."""
@@ -878,7 +965,8 @@ def main():
     ap.add_argument("--batch", type=int, default=200_000)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--workload", default="sparse", choices=["sparse", "tiny", "kv", "dlrm"])
+    ap.add_argument("--workload", default="sparse",
+                    choices=["sparse", "tiny", "kv", "dlrm", "transfers"])
     ap.add_argument("--dlrm-dim", type=int, default=128, choices=[128, 256, 512])
     ap.add_argument("--dlrm-rows", type=int, default=1_000_000)
     ap.add_argument("--kv-layers", type=int, default=32)
@@ -910,7 +998,8 @@ def main():
         libbuild.build()
     if dist:
         dist.barrier()
-    run = {"tiny": run_tiny, "kv": run_kv, "dlrm": run_dlrm}.get(args.workload, run_ours)
+    run = {"tiny": run_tiny, "kv": run_kv, "dlrm": run_dlrm,
+           "transfers": run_transfers}.get(args.workload, run_ours)
     res = run(args, rank, world, torch, dist)
     if args.workload == "sparse" and not args.no_cache_path:
         # the HBM cache path of the same metric, reported beside the host path

@@ -278,6 +278,25 @@ IBP_API ibp_status ibp_gather_copy(void* dst, const void* src, uint64_t slot_byt
                            const int64_t* ids, uint64_t n, uint64_t n_rows,
                            ibp_stream_t stream);
 
+/* CPU-initiated baselines of the review's Figure 5 (transfer methods for
+ * small random tensors), for comparison with the GPU-initiated gathers above.
+ * Both gather rows ids_host[i] (a HOST int64 array, ids in [0, n_rows)) of
+ * row_bytes from src + id*slot_bytes (host memory) into dst (device, row i at
+ * dst + i*row_bytes).
+ * ibp_gather_copy_dma: "CPU fine-grained" -- one cudaMemcpyAsync per row.
+ * ibp_gather_copy_staged: "CPU bulk" -- the host copies the rows into
+ * staging_host (pinned, n*row_bytes, 16-byte aligned) and issues one
+ * cudaMemcpyAsync; it first synchronises `stream` (the staging buffer may
+ * still feed an earlier copy).
+ * Errors: IBP_EINVAL, IBP_EALIGN, IBP_ERANGE (checked on the host), IBP_ECUDA. */
+IBP_API ibp_status ibp_gather_copy_dma(void* dst, const void* src, uint64_t slot_bytes,
+                                       uint32_t row_bytes, const int64_t* ids_host, uint64_t n,
+                                       uint64_t n_rows, ibp_stream_t stream);
+IBP_API ibp_status ibp_gather_copy_staged(void* dst, const void* src, uint64_t slot_bytes,
+                                          uint32_t row_bytes, const int64_t* ids_host, uint64_t n,
+                                          uint64_t n_rows, void* staging_host,
+                                          ibp_stream_t stream);
+
 /* Static text of a status code. */
 IBP_API const char* ibp_status_str(ibp_status s);
 

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libibp.so")
-SOURCES = ["ibp_kernels.cu", "ibp_api.cu", "ibp_noalloc.cu"]
+SOURCES = ["ibp_kernels.cu", "ibp_api.cu", "ibp_noalloc.cu", "ibp_transfer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

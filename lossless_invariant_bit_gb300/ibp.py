@@ -64,6 +64,8 @@ _SIGS = {
     "ibp_stream_status": [_P, _P, ctypes.POINTER(ctypes.c_int), ctypes.c_int],
     "ibp_link_copy": [_P, _P, _U64, _P],
     "ibp_gather_copy": [_P, _P, _U64, _U32, _P, _U64, _U64, _P],
+    "ibp_gather_copy_dma": [_P, _P, _U64, _U32, _P, _U64, _U64, _P],
+    "ibp_gather_copy_staged": [_P, _P, _U64, _U32, _P, _U64, _U64, _P, _P],
 }
 
 
@@ -255,6 +257,20 @@ def ibp_gather_copy(dst, src, slot_bytes: int, row_bytes: int, ids, n: int, n_ro
                     stream=None) -> None:
     _check(_lib_handle().ibp_gather_copy(_ptr(dst), _ptr(src), slot_bytes, row_bytes, _ptr(ids),
                                          n, n_rows, _stream(stream)), "ibp_gather_copy")
+
+
+def ibp_gather_copy_dma(dst, src, slot_bytes: int, row_bytes: int, ids_host, n: int, n_rows: int,
+                        stream=None) -> None:
+    _check(_lib_handle().ibp_gather_copy_dma(_ptr(dst), _ptr(src), slot_bytes, row_bytes,
+                                             _ptr(ids_host), n, n_rows, _stream(stream)),
+           "ibp_gather_copy_dma")
+
+
+def ibp_gather_copy_staged(dst, src, slot_bytes: int, row_bytes: int, ids_host, n: int,
+                           n_rows: int, staging_host, stream=None) -> None:
+    _check(_lib_handle().ibp_gather_copy_staged(_ptr(dst), _ptr(src), slot_bytes, row_bytes,
+                                                _ptr(ids_host), n, n_rows, _ptr(staging_host),
+                                                _stream(stream)), "ibp_gather_copy_staged")
 
 
 def ibp_status_str(status: int) -> str:

@@ -345,6 +345,21 @@ def test_link_copy_and_gather_copy():
     o = out.cpu()
     assert torch.equal(o[:4], store[[3, 999, 0, 3], :R])
     assert torch.all(o[4:] == 0)
+    # the CPU-initiated baselines: one copy per row, and gather-then-copy
+    ids_h = torch.tensor([5, 0, 999, 5, 17], dtype=torch.int64).pin_memory()
+    out = torch.zeros((5, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_copy_dma(out, store, S, R, ids_h, 5, N)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), store[[5, 0, 999, 5, 17], :R])
+    staging = torch.empty(5 * R, dtype=torch.uint8, pin_memory=True)
+    out.zero_()
+    ibp.ibp_gather_copy_staged(out, store, S, R, ids_h, 5, N, staging)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), store[[5, 0, 999, 5, 17], :R])
+    bad = torch.tensor([1, N], dtype=torch.int64).pin_memory()
+    with pytest.raises(ibp.IbpError) as e:
+        ibp.ibp_gather_copy_dma(out, store, S, R, bad, 2, N)
+    assert e.value.status == ibp.IBP_ERANGE
 
 
 # ---------------------------------------------------------------- decoder modes
