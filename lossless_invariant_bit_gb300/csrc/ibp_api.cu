@@ -336,7 +336,8 @@ ibp_status ibp_compress(ibp_store* s, void* dst_slots, const void* src_rows, uin
   a.dst = static_cast<uint8_t*>(dst_slots);
   a.slot = s->slot;
   a.stored_out = stored_bytes_out;
-  return cu(ibp::launch_encode(a, s->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+  return cu(ibp::launch_encode(a, host_props(s), s->sm_count,
+                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ibp_status ibp_decompress(const ibp_store* s, void* dst, const void* src, const uint64_t* offsets,

@@ -61,6 +61,7 @@ struct EncodeArgs {
   uint8_t* dst;
   uint64_t slot;
   uint32_t* stored_out;
+  uint32_t um0, um1, ush, ubv, ukeep;  // uniform store (the k_encode<true> form)
 };
 
 struct CountArgs {
@@ -161,7 +162,8 @@ cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32
                           uint32_t nch, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count,
                           cudaStream_t st);
-cudaError_t launch_encode(const EncodeArgs& a, int sm_count, cudaStream_t st);
+cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count,
+                          cudaStream_t st);
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,
                         const uint32_t* stored, uint64_t n, int sm_count, cudaStream_t st);
 cudaError_t launch_link_copy(uint4* dst, const uint4* src, uint64_t nvec, int sm_count,

@@ -1016,6 +1016,10 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
 // into the packed buffer at their stream offset with shared-memory atomics.
 // A row that would not shrink is written raw and flagged in the bitmap.
 // ------------------------------------------------------------------------
+// kUni: a uniform store (every word has the same ~Mask, at most two runs,
+// and the same Bitval, known on the host): the match test and the bit gather
+// take their masks and shifts from the launch parameters.
+template <bool kUni>
 __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
@@ -1039,9 +1043,15 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
     for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
     for (uint32_t k = lane; k < nch; k += 32) cinfo[k] = 0;
     __syncwarp();
-    for (uint32_t w = lane; w < W; w += 32)
-      if ((xbuf[w] & __ldg(a.m.mask + w)) != __ldg(a.m.bitval + w))
-        cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
+    if (kUni) {
+      const uint32_t msk = ~(a.um0 | a.um1);
+      for (uint32_t w = lane; w < W; w += 32)
+        if ((xbuf[w] & msk) != a.ubv) cinfo[w / wpc] = 1u;  // mismatch flag
+    } else {
+      for (uint32_t w = lane; w < W; w += 32)
+        if ((xbuf[w] & __ldg(a.m.mask + w)) != __ldg(a.m.bitval + w))
+          cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
+    }
     __syncwarp();
     uint32_t run = nch;
     for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
@@ -1071,16 +1081,31 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
       for (uint32_t k = lane; k < nch; k += 32)
         if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
       for (uint32_t w = lane; w < W; w += 32) {
-        const uint32_t krw = __ldg(a.m.kr + w);
+        uint32_t krw;
+        if (kUni) {
+          const uint32_t k = w / wpc;
+          krw = k | ((w - k * wpc) << 16);
+        } else {
+          krw = __ldg(a.m.kr + w);
+        }
         const uint32_t ci = cinfo[krw & 0xFFFFu];
         const bool packed = (ci >> 31) != 0u;
-        const uint32_t bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
         uint32_t v = xbuf[w];
         uint32_t nbits = 32;
-        if (packed) {
-          const uint32_t keepm = __ldg(a.m.nm + w);
-          v = gather_bits(v & keepm, a.m.mv, W, w);
-          nbits = __popc(keepm);
+        uint32_t bit;
+        if (kUni) {
+          bit = (ci & 0x7FFFFFFFu) + (krw >> 16) * (packed ? a.ukeep : 32u);
+          if (packed) {
+            v = ((v & a.um0) >> (a.ush & 31u)) | ((v & a.um1) >> (a.ush >> 8));
+            nbits = a.ukeep;
+          }
+        } else {
+          bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
+          if (packed) {
+            const uint32_t keepm = __ldg(a.m.nm + w);
+            v = gather_bits(v & keepm, a.m.mv, W, w);
+            nbits = __popc(keepm);
+          }
         }
         if (nbits) {
           const uint32_t q = bit >> 5, sh = bit & 31u;
@@ -1377,18 +1402,33 @@ cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count
   return cudaGetLastError();
 }
 
-cudaError_t launch_encode(const EncodeArgs& a, int sm_count, cudaStream_t st) {
-  if (a.n == 0) return cudaSuccess;
+template <bool kUni>
+cudaError_t launch_encode_t(const EncodeArgs& a, int sm_count, cudaStream_t st) {
   const WarpSmem L = encode_smem(a.m.W, a.m.nch);
   const uint32_t warps = warps_for(4u * L.total_words);
   const int threads = (int)(32u * warps);
   const size_t smem = (size_t)4u * L.total_words * warps;
-  const int bps = blocks_per_sm(k_encode, threads, smem);
+  const int bps = blocks_per_sm(k_encode<kUni>, threads, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
   const uint64_t need = (a.n + warps - 1) / warps;
   if (blocks > need) blocks = need;
-  k_encode<<<(uint32_t)blocks, threads, smem, st>>>(a, L);
+  k_encode<kUni><<<(uint32_t)blocks, threads, smem, st>>>(a, L);
   return cudaGetLastError();
+}
+
+cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count,
+                          cudaStream_t st) {
+  if (a.n == 0) return cudaSuccess;
+  if (hp.known && hp.uniform) {
+    EncodeArgs u = a;
+    u.um0 = hp.um0;
+    u.um1 = hp.um1;
+    u.ush = hp.ush;
+    u.ubv = hp.ubv;
+    u.ukeep = hp.ukeep;
+    return launch_encode_t<true>(u, sm_count, st);
+  }
+  return launch_encode_t<false>(a, sm_count, st);
 }
 
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,

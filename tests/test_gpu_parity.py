@@ -494,3 +494,33 @@ def test_tuned_builder_rejects_bad_candidates(stores):
         with pytest.raises(ibp.IbpError) as e:
             ibp.ibp_build_meta_tuned(st.h, d, 64, None, 4, nums, dens)
         assert e.value.status == ibp.IBP_EINVAL
+
+
+@pytest.mark.parametrize("kind", ["dense", "sparse999", "tiny"])
+def test_compress_uniform_store_matches_oracle(stores, kind):
+    """Once the store's properties have reached the host, a uniform store is
+    packed by the compressor's uniform form (masks and shifts as launch
+    parameters): its bytes must equal the oracle's."""
+    if kind == "dense":
+        b = rows_u8(wl.dense_gnn_rows(30_000, seed=8))
+        R, C, num, den = 512, 256, 95, 100
+    elif kind == "sparse999":
+        b = rows_u8(wl.sparse_gnn_rows(30_000, seed=8))
+        R, C, num, den = 512, 1024, 999, 1000
+    else:
+        b = rows_u8(wl.tiny_rows(seed=8)[0])
+        R, C, num, den = 1024, 256, 95, 100
+    n = len(b)
+    st = stores(R, C, n)
+    d = to_dev(b)
+    ibp.ibp_build_meta(st.h, d, R, None, n, num, den)
+    torch.cuda.synchronize()
+    info = ibp.ibp_store_get_info(st.h)
+    assert info.max_runs <= 2
+    slots, stored = gpu_compress(st, d, n)
+    m, bv = st.meta()
+    assert len(set(m.tolist())) == 1 and len(set(bv.tolist())) == 1  # uniform
+    ref_sl, ref_bm, ref_st = oracle_slots(b, C, m, bv, st.slot)
+    assert np.array_equal(stored, ref_st)
+    assert np.array_equal(st.bitmap(), ref_bm)
+    assert_streams_equal(slots.cpu().numpy(), ref_sl, ref_st)
