@@ -148,6 +148,7 @@ class SparseStore:
         ev2[0].record()
         ibp.ibp_build_meta(st2, d_rows, self.R, None, n_rows, num, den)
         ev2[1].record()
+        torch.cuda.synchronize()  # the store's properties reach the host: specialised forms
         ibp.ibp_compress(st2, slots_dev, d_rows, self.R, None, n_rows, None)
         ev2[2].record()
         ibp.ibp_compress(st2, slots_dev, d_rows, self.R, None, n_rows, None)

@@ -1032,15 +1032,38 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
   const uint64_t wpb = blockDim.x >> 5;
   const uint64_t stride = (uint64_t)gridDim.x * wpb;
 
+  // rows up to 2 KB: the warp's next row is loaded into registers while it
+  // packs the current one
+  const bool prefetch = nvec <= 128u;
+  uint4 pf[4];
+  auto load_row = [&](uint64_t r) {
+    if (r < a.n) {
+      const uint4* srow = reinterpret_cast<const uint4*>(a.src + r * a.src_stride);
+#pragma unroll
+      for (uint32_t j = 0; j < 4u; ++j)
+        if (lane + 32u * j < nvec) pf[j] = ld_nc_v4(srow + lane + 32u * j);
+    }
+  };
+  if (prefetch) load_row((uint64_t)blockIdx.x * wpb + wid);
+
   for (uint64_t i = (uint64_t)blockIdx.x * wpb + wid; i < a.n; i += stride) {
+    if (prefetch) {
+#pragma unroll
+      for (uint32_t j = 0; j < 4u; ++j)
+        if (lane + 32u * j < nvec) st_smem_v4(xbuf + 4u * (lane + 32u * j), pf[j]);
+      load_row(i + stride);
+    }
     const int64_t slot = a.slot_ids ? __ldg(a.slot_ids + i) : (int64_t)i;
     if (slot < 0 || (uint64_t)slot >= a.n_rows) {
       if (lane == 0) set_status(a.status, IBP_ERANGE);
       if (a.stored_out && lane == 0) a.stored_out[i] = 0;
+      __syncwarp();
       continue;
     }
-    const uint4* srow = reinterpret_cast<const uint4*>(a.src + i * a.src_stride);
-    for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
+    if (!prefetch) {
+      const uint4* srow = reinterpret_cast<const uint4*>(a.src + i * a.src_stride);
+      for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
+    }
     for (uint32_t k = lane; k < nch; k += 32) cinfo[k] = 0;
     __syncwarp();
     if (kUni) {
