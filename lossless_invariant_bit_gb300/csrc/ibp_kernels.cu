@@ -1009,12 +1009,13 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
 }
 
 // ------------------------------------------------------------------------
-// Compression (Core Algorithm > Compression).  One warp per row: stage the
-// row in shared memory, flag chunks with a Mask mismatch, decide the
-// participation bits, scan the chunk sizes, then every lane gathers the kept
-// bits of its words (or takes the whole word of a raw chunk) and ORs them
-// into the packed buffer at their stream offset with shared-memory atomics.
-// A row that would not shrink is written raw and flagged in the bitmap.
+// Compression (Core Algorithm > Compression).  One warp per row (a warp
+// takes 32 consecutive rows at a time): stage the row in shared memory, flag
+// chunks with a Mask mismatch, decide the participation bits, scan the chunk
+// sizes, then every lane gathers the kept bits of its words (or takes the
+// whole word of a raw chunk) and ORs them into the packed buffer at their
+// stream offset with shared-memory atomics.  A row that would not shrink is
+// written raw and flagged in the bitmap.
 // ------------------------------------------------------------------------
 // kUni: a uniform store (every word has the same ~Mask, at most two runs,
 // and the same Bitval, known on the host): the match test and the bit gather
@@ -1032,9 +1033,12 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
   const uint64_t wpb = blockDim.x >> 5;
   const uint64_t stride = (uint64_t)gridDim.x * wpb;
 
-  // rows up to 2 KB: the warp's next row is loaded into registers while it
-  // packs the current one
+  // A warp takes 32 consecutive rows at a time (so with identity slots it owns
+  // one raw-bitmap word and writes it once, instead of 32 warps contending on
+  // it with atomics); rows up to 2 KB load the warp's next row into
+  // registers while the current one is packed.
   const bool prefetch = nvec <= 128u;
+  const uint64_t nchunk = (a.n + 31) >> 5;
   uint4 pf[4];
   auto load_row = [&](uint64_t r) {
     if (r < a.n) {
@@ -1044,111 +1048,130 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
         if (lane + 32u * j < nvec) pf[j] = ld_nc_v4(srow + lane + 32u * j);
     }
   };
-  if (prefetch) load_row((uint64_t)blockIdx.x * wpb + wid);
+  if (prefetch) load_row(((uint64_t)blockIdx.x * wpb + wid) << 5);
 
-  for (uint64_t i = (uint64_t)blockIdx.x * wpb + wid; i < a.n; i += stride) {
-    if (prefetch) {
+  for (uint64_t c = (uint64_t)blockIdx.x * wpb + wid; c < nchunk; c += stride) {
+    uint32_t rawmask = 0, donemask = 0;
+#pragma unroll 1
+    for (uint32_t j = 0; j < 32u; ++j) {
+      const uint64_t i = (c << 5) + j;
+      if (i >= a.n) break;
+      if (prefetch) {
 #pragma unroll
-      for (uint32_t j = 0; j < 4u; ++j)
-        if (lane + 32u * j < nvec) st_smem_v4(xbuf + 4u * (lane + 32u * j), pf[j]);
-      load_row(i + stride);
-    }
-    const int64_t slot = a.slot_ids ? __ldg(a.slot_ids + i) : (int64_t)i;
-    if (slot < 0 || (uint64_t)slot >= a.n_rows) {
-      if (lane == 0) set_status(a.status, IBP_ERANGE);
-      if (a.stored_out && lane == 0) a.stored_out[i] = 0;
-      __syncwarp();
-      continue;
-    }
-    if (!prefetch) {
-      const uint4* srow = reinterpret_cast<const uint4*>(a.src + i * a.src_stride);
-      for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
-    }
-    for (uint32_t k = lane; k < nch; k += 32) cinfo[k] = 0;
-    __syncwarp();
-    if (kUni) {
-      const uint32_t msk = ~(a.um0 | a.um1);
-      for (uint32_t w = lane; w < W; w += 32)
-        if ((xbuf[w] & msk) != a.ubv) cinfo[w / wpc] = 1u;  // mismatch flag
-    } else {
-      for (uint32_t w = lane; w < W; w += 32)
-        if ((xbuf[w] & __ldg(a.m.mask + w)) != __ldg(a.m.bitval + w))
-          cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
-    }
-    __syncwarp();
-    uint32_t run = nch;
-    for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
-      const uint32_t k = k0 + lane;
-      uint32_t size = 0, p = 0;
-      if (k < nch) {
-        const uint32_t full = 32u * min(wpc, W - k * wpc);
-        const uint32_t keep = __ldg(a.m.ckeep + k);
-        p = (cinfo[k] == 0u && keep < full) ? 1u : 0u;
-        size = p ? keep : full;
+        for (uint32_t q = 0; q < 4u; ++q)
+          if (lane + 32u * q < nvec) st_smem_v4(xbuf + 4u * (lane + 32u * q), pf[q]);
+        load_row(j < 31u ? i + 1 : (c + stride) << 5);
       }
-      const uint32_t incl = warp_inclusive_scan(size, lane);
+      const int64_t slot = a.slot_ids ? __ldg(a.slot_ids + i) : (int64_t)i;
+      if (slot < 0 || (uint64_t)slot >= a.n_rows) {
+        if (lane == 0) set_status(a.status, IBP_ERANGE);
+        if (a.stored_out && lane == 0) a.stored_out[i] = 0;
+        __syncwarp();
+        continue;
+      }
+      if (!prefetch) {
+        const uint4* srow = reinterpret_cast<const uint4*>(a.src + i * a.src_stride);
+        for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
+      }
+      for (uint32_t k = lane; k < nch; k += 32) cinfo[k] = 0;
       __syncwarp();
-      if (k < nch) cinfo[k] = (run + incl - size) | (p << 31);
-      run += __shfl_sync(kFull, incl, 31);
-    }
-    const uint32_t words = (run + 31u) >> 5;
-    const bool raw = 4u * words >= R;
-    uint4* dslot = reinterpret_cast<uint4*>(a.dst + (uint64_t)slot * a.slot);
-    if (raw) {
-      for (uint32_t v = lane; v < nvec; v += 32)
-        dslot[v] = *reinterpret_cast<const uint4*>(xbuf + 4u * v);
-    } else {
-      const uint32_t padded = (words + 3u) & ~3u;
-      for (uint32_t j = lane; j < padded + 4u; j += 32) obuf[j] = 0;
-      __syncwarp();
-      for (uint32_t k = lane; k < nch; k += 32)
-        if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
-      for (uint32_t w = lane; w < W; w += 32) {
-        uint32_t krw;
-        if (kUni) {
-          const uint32_t k = w / wpc;
-          krw = k | ((w - k * wpc) << 16);
-        } else {
-          krw = __ldg(a.m.kr + w);
-        }
-        const uint32_t ci = cinfo[krw & 0xFFFFu];
-        const bool packed = (ci >> 31) != 0u;
-        uint32_t v = xbuf[w];
-        uint32_t nbits = 32;
-        uint32_t bit;
-        if (kUni) {
-          bit = (ci & 0x7FFFFFFFu) + (krw >> 16) * (packed ? a.ukeep : 32u);
-          if (packed) {
-            v = ((v & a.um0) >> (a.ush & 31u)) | ((v & a.um1) >> (a.ush >> 8));
-            nbits = a.ukeep;
-          }
-        } else {
-          bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
-          if (packed) {
-            const uint32_t keepm = __ldg(a.m.nm + w);
-            v = gather_bits(v & keepm, a.m.mv, W, w);
-            nbits = __popc(keepm);
-          }
-        }
-        if (nbits) {
-          const uint32_t q = bit >> 5, sh = bit & 31u;
-          atomicOr(obuf + q, v << sh);
-          if (sh != 0u && sh + nbits > 32u) atomicOr(obuf + q + 1, v >> (32u - sh));
-        }
+      if (kUni) {
+        const uint32_t msk = ~(a.um0 | a.um1);
+        for (uint32_t w = lane; w < W; w += 32)
+          if ((xbuf[w] & msk) != a.ubv) cinfo[w / wpc] = 1u;  // mismatch flag
+      } else {
+        for (uint32_t w = lane; w < W; w += 32)
+          if ((xbuf[w] & __ldg(a.m.mask + w)) != __ldg(a.m.bitval + w))
+            cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
       }
       __syncwarp();
-      for (uint32_t v = lane; 4u * v < padded; v += 32)
-        dslot[v] = *reinterpret_cast<const uint4*>(obuf + 4u * v);
+      uint32_t run = nch;
+      for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
+        const uint32_t k = k0 + lane;
+        uint32_t size = 0, p = 0;
+        if (k < nch) {
+          const uint32_t full = 32u * min(wpc, W - k * wpc);
+          const uint32_t keep = __ldg(a.m.ckeep + k);
+          p = (cinfo[k] == 0u && keep < full) ? 1u : 0u;
+          size = p ? keep : full;
+        }
+        const uint32_t incl = warp_inclusive_scan(size, lane);
+        __syncwarp();
+        if (k < nch) cinfo[k] = (run + incl - size) | (p << 31);
+        run += __shfl_sync(kFull, incl, 31);
+      }
+      const uint32_t words = (run + 31u) >> 5;
+      const bool raw = 4u * words >= R;
+      uint4* dslot = reinterpret_cast<uint4*>(a.dst + (uint64_t)slot * a.slot);
+      if (raw) {
+        for (uint32_t v = lane; v < nvec; v += 32)
+          dslot[v] = *reinterpret_cast<const uint4*>(xbuf + 4u * v);
+      } else {
+        const uint32_t padded = (words + 3u) & ~3u;
+        for (uint32_t z = lane; z < padded + 4u; z += 32) obuf[z] = 0;
+        __syncwarp();
+        for (uint32_t k = lane; k < nch; k += 32)
+          if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
+        for (uint32_t w = lane; w < W; w += 32) {
+          uint32_t krw;
+          if (kUni) {
+            const uint32_t k = w / wpc;
+            krw = k | ((w - k * wpc) << 16);
+          } else {
+            krw = __ldg(a.m.kr + w);
+          }
+          const uint32_t ci = cinfo[krw & 0xFFFFu];
+          const bool packed = (ci >> 31) != 0u;
+          uint32_t v = xbuf[w];
+          uint32_t nbits = 32;
+          uint32_t bit;
+          if (kUni) {
+            bit = (ci & 0x7FFFFFFFu) + (krw >> 16) * (packed ? a.ukeep : 32u);
+            if (packed) {
+              v = ((v & a.um0) >> (a.ush & 31u)) | ((v & a.um1) >> (a.ush >> 8));
+              nbits = a.ukeep;
+            }
+          } else {
+            bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
+            if (packed) {
+              const uint32_t keepm = __ldg(a.m.nm + w);
+              v = gather_bits(v & keepm, a.m.mv, W, w);
+              nbits = __popc(keepm);
+            }
+          }
+          if (nbits) {
+            const uint32_t q = bit >> 5, sh = bit & 31u;
+            atomicOr(obuf + q, v << sh);
+            if (sh != 0u && sh + nbits > 32u) atomicOr(obuf + q + 1, v >> (32u - sh));
+          }
+        }
+        __syncwarp();
+        for (uint32_t v = lane; 4u * v < padded; v += 32)
+          dslot[v] = *reinterpret_cast<const uint4*>(obuf + 4u * v);
+      }
+      if (a.slot_ids) {
+        if (lane == 0) {
+          const uint32_t bitm = 1u << ((uint64_t)slot & 31u);
+          if (raw)
+            atomicOr(a.bitmap + ((uint64_t)slot >> 5), bitm);
+          else
+            atomicAnd(a.bitmap + ((uint64_t)slot >> 5), ~bitm);
+        }
+      } else {
+        rawmask |= (uint32_t)raw << j;
+        donemask |= 1u << j;
+      }
+      if (lane == 0 && a.stored_out) a.stored_out[i] = raw ? R : 4u * words;
+      __syncwarp();
     }
-    if (lane == 0) {
-      const uint32_t bitm = 1u << ((uint64_t)slot & 31u);
-      if (raw)
-        atomicOr(a.bitmap + ((uint64_t)slot >> 5), bitm);
-      else
-        atomicAnd(a.bitmap + ((uint64_t)slot >> 5), ~bitm);
-      if (a.stored_out) a.stored_out[i] = raw ? R : 4u * words;
+    if (!a.slot_ids && lane == 0 && donemask) {
+      if (donemask == 0xFFFFFFFFu) {
+        a.bitmap[c] = rawmask;  // this warp wrote every row of the word
+      } else {
+        atomicOr(a.bitmap + c, rawmask);
+        atomicAnd(a.bitmap + c, rawmask | ~donemask);
+      }
     }
-    __syncwarp();
   }
 }
 
@@ -1433,7 +1456,7 @@ cudaError_t launch_encode_t(const EncodeArgs& a, int sm_count, cudaStream_t st) 
   const size_t smem = (size_t)4u * L.total_words * warps;
   const int bps = blocks_per_sm(k_encode<kUni>, threads, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = (a.n + warps - 1) / warps;
+  const uint64_t need = ((a.n + 31) / 32 + warps - 1) / warps;  // 32-row chunks per warp
   if (blocks > need) blocks = need;
   k_encode<kUni><<<(uint32_t)blocks, threads, smem, st>>>(a, L);
   return cudaGetLastError();
