@@ -1078,7 +1078,7 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
       if (kUni) {
         const uint32_t msk = ~(a.um0 | a.um1);
         for (uint32_t w = lane; w < W; w += 32)
-          if ((xbuf[w] & msk) != a.ubv) cinfo[w / wpc] = 1u;  // mismatch flag
+          if ((xbuf[w] & msk) != a.ubv) cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
       } else {
         for (uint32_t w = lane; w < W; w += 32)
           if ((xbuf[w] & __ldg(a.m.mask + w)) != __ldg(a.m.bitval + w))
@@ -1113,13 +1113,7 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
         for (uint32_t k = lane; k < nch; k += 32)
           if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
         for (uint32_t w = lane; w < W; w += 32) {
-          uint32_t krw;
-          if (kUni) {
-            const uint32_t k = w / wpc;
-            krw = k | ((w - k * wpc) << 16);
-          } else {
-            krw = __ldg(a.m.kr + w);
-          }
+          const uint32_t krw = __ldg(a.m.kr + w);  // chunk | word in chunk << 16
           const uint32_t ci = cinfo[krw & 0xFFFFu];
           const bool packed = (ci >> 31) != 0u;
           uint32_t v = xbuf[w];
