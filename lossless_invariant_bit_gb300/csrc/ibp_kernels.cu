@@ -720,43 +720,6 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       const uint32_t fl = e.x & 15u;
       uint4* drow = reinterpret_cast<uint4*>(a.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
       uint32_t* sb = ring + (t & (S - 1u)) * F.sbuf_words;
-      if (kMode == kModeUniform || kMode == kModeUniform1) {
-        // Raw rows and rows with a bad id or offset go through the packed-row
-        // loop with their own parameters -- a raw row keeps all 32 bits of
-        // each word from bit 32w, a bad row keeps none and no Bitval (zeros) --
-        // so the usual rows take no branch; only rows with raw chunks leave.
-        const bool err = (fl & 12u) != 0u;
-        const bool raw = (fl & 2u) != 0u;
-        const bool hdr_ok = nhw == 1u ? (sb[0] & hexp) == hexp
-                                      : __all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp);
-        if (err || raw || (can_pack && hdr_ok)) {
-          if (err && lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
-          const bool plain = raw || err;
-          const uint32_t keep = raw ? 32u : (err ? 0u : F.ukeep);
-          const uint32_t base = plain ? 0u : nch;
-          const uint32_t m0 = raw ? 0xFFFFFFFFu : (err ? 0u : F.um0);
-          const uint32_t m1 = (plain || kMode == kModeUniform1) ? 0u : F.um1;
-          const uint32_t s0 = plain ? 0u : (F.ush & 31u);
-          const uint32_t s1 = plain ? 0u : (F.ush >> 8);
-          const uint32_t bv = plain ? 0u : F.ubv;
-          uint4* dp = drow + lane;
-          for (uint32_t g = lane; g < G; g += 32, dp += 32) {
-            uint32_t bit = base + 4u * g * keep;
-            uint32_t o[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const uint32_t q = bit >> 5;
-              const uint32_t v = __funnelshift_r(sb[q], sb[q + 1], bit);
-              o[x] = (kMode == kModeUniform1)
-                         ? (((v << s0) & m0) | bv)
-                         : (((v << s0) & m0) | ((v << s1) & m1) | bv);
-              bit += keep;
-            }
-            *dp = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-          break;
-        }
-      }
       if (fl & 12u) {
         if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
         zero_row(drow, nvec, lane);
