@@ -185,8 +185,14 @@ IBP_API ibp_status ibp_compress(ibp_store* store, void* dst_slots, const void* s
  * row i's stored bytes start at src + offsets[i] (a packed HBM cache; offsets
  * device uint64[n], multiples of 16) or, with offsets NULL, at
  * src + i*slot_bytes (a slot store).  dst receives n rows of R bytes,
- * contiguous.  Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA; corrupt streams and
- * misaligned offsets set the status word. */
+ * contiguous.  A valid stream is read only within its own stored bytes
+ * (rounded up to 16); a corrupt one is detected after reading at most R bytes
+ * from its start (slot stores: within the slot), so a packed cache that may
+ * hold corrupt data should keep R readable bytes after its last row.
+ * Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA; corrupt streams and misaligned
+ * offsets set the status word.  Calls on one store from several host threads
+ * are safe for decompression; building or setting the Mask/Bitval or the
+ * bitmap while other calls use the store is not. */
 IBP_API ibp_status ibp_decompress(const ibp_store* store, void* dst, const void* src,
                           const uint64_t* offsets, uint64_t n, ibp_stream_t stream);
 
