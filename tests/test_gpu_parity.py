@@ -524,3 +524,31 @@ def test_compress_uniform_store_matches_oracle(stores, kind):
     assert np.array_equal(stored, ref_st)
     assert np.array_equal(st.bitmap(), ref_bm)
     assert_streams_equal(slots.cpu().numpy(), ref_sl, ref_st)
+
+
+def test_store_state_save_and_restore(stores):
+    """A store's whole state is its Mask/Bitval and raw bitmap: copied out to
+    the host and installed into a fresh store, the slots decode the same."""
+    R, C, n = 1024, 256, 3000
+    rows, _ = wl.tiny_rows(seed=12, n_rows=n)
+    b = rows_u8(rows)
+    a = stores(R, C, n)
+    d = to_dev(b)
+    ibp.ibp_build_meta(a.h, d, R, None, n, 95, 100)
+    slots, stored = gpu_compress(a, d, n)
+    m, bv = a.meta()
+    bm = a.bitmap()
+    # a new store, the saved state installed from host arrays
+    c = stores(R, C, n)
+    c.set_meta(m, bv)
+    c.set_bitmap(bm)
+    info_a, info_c = ibp.ibp_store_get_info(a.h), ibp.ibp_store_get_info(c.h)
+    assert (info_a.min_bits, info_a.max_runs) == (info_c.min_bits, info_c.max_runs)
+    host_slots = slots.cpu().pin_memory()
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(c.h, out, host_slots, None, n)
+    assert c.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
+    with pytest.raises(ibp.IbpError) as e:  # a Bitval bit outside the Mask is refused
+        c.set_meta(np.zeros_like(m), np.ones_like(bv))
+    assert e.value.status == ibp.IBP_EINVAL
