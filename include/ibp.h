@@ -239,6 +239,21 @@ IBP_API ibp_status ibp_group_gather_decompress(const ibp_group* group, void* dst
                                                uint64_t dst_row_stride, const int64_t* ids,
                                                uint64_t batch, ibp_stream_t stream);
 
+/* Gather-decompression through a compressed HBM cache in front of the host
+ * store (System Integration: cache compression and PCIe-transfer compression
+ * together): row i of dst (at dst + i*dst_stride_bytes) is the decompressed
+ * row ids[i]; if cache_map[id] >= 0 its stored bytes are read from the HBM
+ * cache slot cache_src + cache_map[id]*slot_bytes, otherwise from
+ * host_src + id*slot_bytes over the host link -- in one launch.  The cache
+ * holds copies of the store's slots (same stride, same raw bitmap).
+ *   cache_map  device int64[n_rows]: cache slot of each row, -1 if not cached
+ * Errors: as ibp_gather_decompress_strided. */
+IBP_API ibp_status ibp_gather_decompress_cached(const ibp_store* store, void* dst,
+                                                uint64_t dst_stride_bytes, const void* host_src,
+                                                const void* cache_src, const int64_t* cache_map,
+                                                const int64_t* ids, uint64_t n,
+                                                ibp_stream_t stream);
+
 /* Build a packed HBM cache (System Integration: compressed GPU software
  * cache) from compressed slots: row i's stored_bytes[i] bytes at
  * src_slots + i*slot_bytes are copied to dst_packed + offsets_out[i], where

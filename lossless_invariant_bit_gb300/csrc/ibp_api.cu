@@ -94,7 +94,8 @@ ibp::HostProps host_props(const ibp_store* s) {
 }
 
 ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void* src,
-                  const uint64_t* offsets, const int64_t* ids, uint64_t n, cudaStream_t st) {
+                  const uint64_t* offsets, const int64_t* ids, uint64_t n, cudaStream_t st,
+                  const int64_t* cache_map = nullptr, const void* cache_src = nullptr) {
   if (!s) return IBP_EINVAL;
   if (n == 0) return IBP_OK;
   if (!dst || !src) return IBP_EINVAL;
@@ -119,6 +120,8 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.n_rows = s->n_rows;
   a.dst = static_cast<uint8_t*>(dst);
   a.dst_stride = dst_stride;
+  a.cache_map = cache_map;
+  a.cache_src = static_cast<const uint8_t*>(cache_src);
   return cu(ibp::launch_decode(a, host_props(s), s->sm_count, st));
 }
 
@@ -359,6 +362,17 @@ ibp_status ibp_gather_decompress_strided(const ibp_store* s, void* dst, uint64_t
                                          const int64_t* ids, uint64_t n, ibp_stream_t stream) {
   if (!ids && n) return IBP_EINVAL;
   return decode(s, dst, dst_stride, src, offsets, ids, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ibp_status ibp_gather_decompress_cached(const ibp_store* s, void* dst, uint64_t dst_stride,
+                                        const void* host_src, const void* cache_src,
+                                        const int64_t* cache_map, const int64_t* ids, uint64_t n,
+                                        ibp_stream_t stream) {
+  if (!ids && n) return IBP_EINVAL;
+  if (n && (!cache_map || !cache_src)) return IBP_EINVAL;
+  if (cache_src && !aligned16(cache_src)) return IBP_EALIGN;
+  return decode(s, dst, dst_stride, host_src, nullptr, ids, n,
+                reinterpret_cast<cudaStream_t>(stream), cache_map, cache_src);
 }
 
 ibp_status ibp_pack(const ibp_store* s, void* dst_packed, uint64_t* offsets_out,

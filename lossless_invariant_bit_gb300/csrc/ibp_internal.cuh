@@ -47,6 +47,8 @@ struct DecodeArgs {
   uint64_t n_rows;
   uint8_t* dst;
   uint64_t dst_stride;
+  const int64_t* cache_map;  // NULL, or per row id: its slot in the HBM cache, -1 if none
+  const uint8_t* cache_src;  // the HBM cache's slots (stride `slot`)
 };
 
 struct EncodeArgs {

@@ -398,6 +398,19 @@ __global__ void __launch_bounds__(1024) k_derive_fast(const uint32_t* nm, const 
 //             coalesced 16-byte store.
 // A raw row is a straight 16-byte vector copy.
 // ------------------------------------------------------------------------
+// Where row `id`'s stored bytes start, relative to a.src: packed offsets,
+// a slot, or -- with a cache map -- the row's slot in the HBM cache when it
+// has one (the unsigned difference of the two bases wraps, so a.src + result
+// addresses the cache).
+__device__ __forceinline__ uint64_t source_offset(const DecodeArgs& a, int64_t id) {
+  if (a.cache_map) {
+    const int64_t cs = __ldg(a.cache_map + id);
+    if (cs >= 0)
+      return (uint64_t)((uintptr_t)a.cache_src - (uintptr_t)a.src) + (uint64_t)cs * a.slot;
+  }
+  return a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
+}
+
 __device__ __forceinline__ void zero_row(uint4* drow, uint32_t nvec, uint32_t lane) {
   for (uint32_t v = lane; v < nvec; v += 32) drow[v] = make_uint4(0, 0, 0, 0);
 }
@@ -424,7 +437,7 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
       zero_row(drow, nvec, lane);
       continue;
     }
-    const uint64_t off = a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
+    const uint64_t off = source_offset(a, id);
     if (off & 15u) {
       if (lane == 0) set_status(a.status, IBP_EALIGN);
       zero_row(drow, nvec, lane);
@@ -657,7 +670,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   };
   auto step_loads = [&]() {
     if (pin && pid >= 0 && (uint64_t)pid < a.n_rows) {
-      poff = a.offsets ? __ldg(a.offsets + pid) : (uint64_t)pid * a.slot;
+      poff = source_offset(a, pid);
       pbm = __ldg(a.bitmap + (pid >> 5));
     }
   };

@@ -552,3 +552,42 @@ def test_store_state_save_and_restore(stores):
     with pytest.raises(ibp.IbpError) as e:  # a Bitval bit outside the Mask is refused
         c.set_meta(np.zeros_like(m), np.ones_like(bv))
     assert e.value.status == ibp.IBP_EINVAL
+
+
+@pytest.mark.parametrize("R,C", [(512, 256), (8192, 256)])
+def test_gather_through_hbm_cache_front(stores, R, C):
+    """Rows cached in HBM are read from the cache, the rest over the host link,
+    in one launch: the output is every requested row either way."""
+    N = 4000 if R <= 2048 else 600
+    b = (rows_u8(wl.dense_gnn_rows(N, dim=R // 4, seed=13)) if R <= 2048
+         else wl.kv_rows(1, 0, 3, range(N // 3)).view(np.uint8).reshape(-1, R)[:N])
+    N = len(b)
+    st = stores(R, C, N)
+    d = to_dev(b)
+    ibp.ibp_build_meta(st.h, d, R, None, N, 95, 100)
+    host = torch.zeros((N, st.slot), dtype=torch.uint8, pin_memory=True)
+    ibp.ibp_compress(st.h, host, d, R, None, N, None)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(R)
+    cached = np.sort(g.choice(N, size=N // 3, replace=False))
+    cmap = np.full(N, -1, np.int64)
+    cmap[cached] = np.arange(len(cached))[::-1]  # cache slots in another order
+    cache = torch.zeros((len(cached), st.slot), dtype=torch.uint8, device=DEV)
+    cache[torch.from_numpy(cmap[cached])] = host[torch.from_numpy(cached)].to(DEV)
+    ids = g.integers(0, N, size=5 * N // 2).astype(np.int64)
+    stride = R + 32
+    out = torch.zeros((len(ids), stride), dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress_cached(st.h, out, stride, host, cache, to_dev(cmap), to_dev(ids),
+                                     len(ids))
+    assert st.status() == ibp.IBP_OK
+    o = out.cpu().numpy()
+    assert np.array_equal(o[:, :R], b[ids]) and np.all(o[:, R:] == 0)
+    # the cache really is read: poison the host copies of the cached rows
+    host[torch.from_numpy(cached)] = 0xEE
+    out.zero_()
+    ibp.ibp_gather_decompress_cached(st.h, out, stride, host, cache, to_dev(cmap), to_dev(ids),
+                                     len(ids))
+    assert st.status() == ibp.IBP_OK
+    o = out.cpu().numpy()
+    hit = np.isin(ids, cached)
+    assert np.array_equal(o[hit, :R], b[ids[hit]])
