@@ -850,6 +850,184 @@ def run_dlrm(args, rank, world, torch, dist):
     return res
 
 
+def _link_probe(torch, ibp, host, stream, sp, dev):
+    """Best of 5 aligned zero-copy copies of a pinned host buffer into HBM, GB/s."""
+    pbytes = (host.numel() // 16) * 16
+    probe = torch.empty(pbytes, dtype=torch.uint8, device=dev)
+    ibp.ibp_link_copy(probe, host, pbytes, sp)
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ibp.ibp_link_copy(probe, host, pbytes, sp)
+        e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3
+        best = t if best is None else min(best, t)
+    del probe
+    return pbytes / best / 1e9
+
+
+def run_sweep(args, rank, world, torch, dist):
+    """The pages' two sweeps, measured on this machine.
+
+    Space saving (the review's Figure 7): rows whose words have exactly k
+    invariant bits (k = 0, 4, ..., 28: space saving 0 to 87.5 %), either the k
+    high bits of every word with one value (a uniform store: fp32 rows of one
+    magnitude class) or k scattered positions per word with a per-word value
+    (the general scatter network); rows of 4 KB at chunks of 256 B, 1 KB and
+    4 KB, and rows of 1 KB at 256 B and 1 KB; 1 GB of pinned host slots, a step
+    is one gather-decompress of 65,536 uniform ids.  Throughput is reported as
+    a fraction of the ideal, link / ratio (decompression for free).
+
+    Sampling (the review's sampling paragraph): the compression ratio of the
+    sparse and dense GNN stores (2M x 128 fp32) with the Mask/Bitval built from
+    1 %, 5 %, 10 % and all rows, at T = 0.95 and with the chunk-aware builder,
+    and the builder's time."""
+    from lossless_invariant_bit_gb300 import ibp
+    from lossless_invariant_bit_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    hbm = measured_peaks()["hbm_gbs"]
+    steps, warm = max(3, min(args.steps, 30)), 3
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    total = 1 << 30
+    host = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    link = _link_probe(torch, ibp, host, stream, sp, dev)
+    log("link probe: %.1f GB/s host->HBM" % link)
+    n = 65536
+    points, launches = [], 0
+    gen = torch.Generator(device=dev)
+    with ClockSampler(dev.index) as clk:
+        for R, chunks in ((4096, (256, 1024, 4096)), (1024, (256, 1024))):
+            N, W = total // R, R // 4
+            slots = host.view(N, R)
+            gen.manual_seed(args.seed * 1000003 + R)
+            base = torch.randint(0, 256, (N, R), dtype=torch.uint8, device=dev,
+                                 generator=gen).view(torch.int32)
+            sample = torch.from_numpy(wl.sample_ids(N, 10, seed=args.seed)).to(dev)
+            ids = [torch.from_numpy(wl.uniform_ids(n, N, seed=args.seed, batch=b)).to(dev)
+                   for b in range(4)]
+            out = torch.empty((n, R), dtype=torch.uint8, device=dev)
+            stored = torch.empty(N, dtype=torch.int32, device=dev)
+            pick = torch.from_numpy(np.random.default_rng(R).choice(n, 1000, replace=False)).to(dev)
+            for scattered in (False, True):
+                for k in range(0, 32, 4):
+                    keep, const = wl.invariant_pattern(W, k, scattered, seed=args.seed)
+                    rows = ((base & torch.from_numpy(keep.view(np.int32)).to(dev))
+                            | torch.from_numpy(const.view(np.int32)).to(dev)).view(torch.uint8)
+                    for C in chunks:
+                        st = ibp.ibp_store_create(R, C, N, 0)
+                        assert ibp.ibp_store_get_info(st).slot_bytes == R
+                        ibp.ibp_build_meta(st, rows, R, sample, len(sample), 95, 100)
+                        ibp.ibp_compress(st, slots, rows, R, None, N, stored)
+                        torch.cuda.synchronize()
+                        assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+                        ratio = statistics.mean(
+                            float(stored[x].sum().item()) / (n * R) for x in ids)
+                        for b in range(warm):
+                            ibp.ibp_gather_decompress(st, out, slots, None, ids[b % 4], n, sp)
+                        evs = []
+                        for b in range(steps):
+                            flush.zero_()
+                            e0 = torch.cuda.Event(enable_timing=True)
+                            e1 = torch.cuda.Event(enable_timing=True)
+                            e0.record(stream)
+                            ibp.ibp_gather_decompress(st, out, slots, None, ids[b % 4], n, sp)
+                            e1.record(stream)
+                            evs.append((e0, e1))
+                        torch.cuda.synchronize()
+                        launches += steps
+                        assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+                        t = statistics.mean(a.elapsed_time(c) / 1e3 for a, c in evs)
+                        last = ids[(steps - 1) % 4]
+                        ok = bool(torch.equal(out[pick], rows.view(N, R)[last[pick]]))
+                        gbs = n * R / t / 1e9
+                        ideal = min(hbm, link / ratio)
+                        points.append({"row_bytes": R, "chunk_bytes": C,
+                                       "pattern": "scattered" if scattered else "high bits",
+                                       "k": k, "saving": round(1 - ratio, 4),
+                                       "ratio": round(ratio, 5), "gbs": round(gbs, 2),
+                                       "ideal_gbs": round(ideal, 2),
+                                       "frac": round(gbs / ideal, 4),
+                                       "parity_sampled_rows_ok": ok})
+                        log("R=%d C=%d %s k=%d: ratio %.3f  %.1f GB/s  %.3f of ideal" % (
+                            R, C, points[-1]["pattern"], k, ratio, gbs, gbs / ideal))
+                        ibp.ibp_store_destroy(st)
+                    del rows
+            del base, out, stored
+            torch.cuda.empty_cache()
+
+    # sampling sweep: ratio of the whole store against the share of rows analysed
+    sampling = []
+    cands = [(9, 10), (95, 100), (99, 100), (999, 1000), (1, 1)]
+    for name, gen_rows in (("sparse GNN", wl.sparse_gnn_rows), ("dense GNN", wl.dense_gnn_rows)):
+        NR, R, C = 2_000_000, 512, 1024
+        rows_np = np.empty((NR, 128), np.float32)
+        gen_rows(NR, 128, seed=args.seed, out=rows_np)
+        d_rows = torch.from_numpy(rows_np.view(np.uint8)).to(dev)
+        del rows_np
+        slots_dev = torch.empty((NR, R), dtype=torch.uint8, device=dev)
+        stored = torch.empty(NR, dtype=torch.int32, device=dev)
+        chosen = torch.zeros(1, dtype=torch.int32, device=dev)
+        for pm in (10, 50, 100, 1000):
+            smp = None if pm == 1000 else torch.from_numpy(
+                wl.sample_ids(NR, pm, seed=args.seed)).to(dev)
+            ns = NR if smp is None else len(smp)
+            st = ibp.ibp_store_create(R, C, NR, 0)
+            ibp.ibp_build_meta(st, d_rows, R, smp, ns, 95, 100)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ibp.ibp_build_meta(st, d_rows, R, smp, ns, 95, 100)
+            e1.record(stream)
+            ibp.ibp_compress(st, slots_dev, d_rows, R, None, NR, stored)
+            torch.cuda.synchronize()
+            r95 = float(stored.sum().item()) / (NR * R)
+            t_build = e0.elapsed_time(e1) / 1e3
+            ibp.ibp_build_meta_tuned(st, d_rows, R, smp, ns, [c[0] for c in cands],
+                                     [c[1] for c in cands], chosen, None, sp)
+            ibp.ibp_compress(st, slots_dev, d_rows, R, None, NR, stored)
+            torch.cuda.synchronize()
+            assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+            rt = float(stored.sum().item()) / (NR * R)
+            sampling.append({"workload": name, "sample_per_mille": pm, "sample_rows": ns,
+                             "ratio_T0.95": round(r95, 5), "build_seconds": round(t_build, 6),
+                             "ratio_tuned": round(rt, 5),
+                             "tuned_T": "%d/%d" % cands[int(chosen.item())]})
+            log("%s sample %d/1000: ratio %.4f (T=0.95), %.4f (tuned)" % (name, pm, r95, rt))
+            ibp.ibp_store_destroy(st)
+        del d_rows, slots_dev, stored
+        torch.cuda.empty_cache()
+
+    head = next(p for p in points if p["row_bytes"] == 4096 and p["chunk_bytes"] == 1024
+                and p["pattern"] == "high bits" and p["k"] == 16)
+    below = [p["frac"] for p in points if p["saving"] < 0.5]
+    return {
+        "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
+        "value": head["gbs"], "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": round(n * 4096 / head["gbs"] / 1e6, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (seeded torch generator on the GPU for the saving sweep; seeded "
+                "numpy GNN features for the sampling sweep)",
+        "config": {"workload": "space-saving sweep: value is the 4 KB row, 1 KB chunk, 50 %% "
+                               "saving point (high bits); gather of %d uniform ids from 1 GB "
+                               "of pinned host slots" % n,
+                   "l2": "flushed between steps (256 MB write, outside the timed events)"},
+        "link_gbs": round(link, 2),
+        "roofline": {"bound": "link", "achieved": head["gbs"], "peak": head["ideal_gbs"],
+                     "unit": "GB/s", "frac": head["frac"], "traffic": None,
+                     "kernel": "k_decode<true> (4 KB rows, ibp_gather_decompress)"},
+        "saving_sweep": points,
+        "min_frac_below_50pct_saving": min(below),
+        "sampling_sweep": sampling,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+
+
 def run_transfers(args, rank, world, torch, dist):
     """The review's Figure 5 on this machine: moving randomly chosen rows (tensors)
     from pinned host memory into HBM, by method and row size.  Rows are
@@ -1021,7 +1199,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--workload", default="sparse",
-                    choices=["sparse", "tiny", "kv", "dlrm", "transfers"])
+                    choices=["sparse", "tiny", "kv", "dlrm", "transfers", "sweep"])
     ap.add_argument("--dlrm-dim", type=int, default=128, choices=[128, 256, 512])
     ap.add_argument("--dlrm-rows", type=int, default=1_000_000)
     ap.add_argument("--kv-layers", type=int, default=32)
@@ -1055,8 +1233,8 @@ def main():
         libbuild.build()
     if dist:
         dist.barrier()
-    run = {"tiny": run_tiny, "kv": run_kv, "dlrm": run_dlrm,
-           "transfers": run_transfers}.get(args.workload, run_ours)
+    run = {"tiny": run_tiny, "kv": run_kv, "dlrm": run_dlrm, "transfers": run_transfers,
+           "sweep": run_sweep}.get(args.workload, run_ours)
     res = run(args, rank, world, torch, dist)
     if args.workload == "sparse" and not args.no_cache_path:
         # the HBM cache path of the same metric, reported beside the host path

@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(1024) k_derive_fast(const uint32_t* nm, const 
 // with fewer than 32 chunks still keeps all lanes busy.  Per row:
 //   resolve   id, raw bit, source address;
 //   fetch     the shortest stream any compressed row can have (min_bits) in
-//             16-byte vectors, staged in the warp's shared memory;
+//             16-byte cp.async copies, staged in the warp's shared memory;
 //   scan      participation bits -> chunk sizes -> exclusive warp scan;
 //   fetch     the rest of the stream when raw chunks made it longer;
 //   re-insert each lane builds 4 output words at a time: a funnel shift
@@ -411,6 +411,26 @@ __device__ __forceinline__ uint64_t source_offset(const DecodeArgs& a, int64_t i
   return a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
 }
 
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_n() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// 16-byte vectors [v0, v1) of a stored stream into the warp's buffer at
+// shared address `sa`, all issued before any is waited for: one round trip
+// to host memory per fetch instead of one per 512 bytes.
+__device__ __forceinline__ void fetch_vectors(uint32_t sa, const uint4* src, uint32_t v0,
+                                              uint32_t v1, uint32_t lane) {
+  for (uint32_t v = v0 + lane; v < v1; v += 32)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 16u * v),
+                 "l"(src + v));
+  cp_async_commit();
+  cp_async_wait_n<0>();
+  __syncwarp();
+}
+
 __device__ __forceinline__ void zero_row(uint4* drow, uint32_t nvec, uint32_t lane) {
   for (uint32_t v = lane; v < nvec; v += 32) drow[v] = make_uint4(0, 0, 0, 0);
 }
@@ -422,6 +442,7 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
   const uint32_t wid = threadIdx.x >> 5;
   uint32_t* sbuf = smem + wid * L.total_words;
   uint32_t* cinfo = sbuf + L.sbuf_words;
+  const uint32_t sbuf_sa = static_cast<uint32_t>(__cvta_generic_to_shared(sbuf));
   const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
   const uint32_t nvec = R >> 4;
   const uint32_t min_words = (__ldg(a.m.scal) + 31u) >> 5;
@@ -454,8 +475,7 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
       zero_row(drow, nvec, lane);
       continue;
     }
-    for (uint32_t v = lane; v < min_vec; v += 32) st_smem_v4(sbuf + 4u * v, ld_nc_v4(srow + v));
-    __syncwarp();
+    fetch_vectors(sbuf_sa, srow, 0u, min_vec, lane);
     // chunk starts: exclusive scan of the chunk sizes, 32 chunks per pass
     uint32_t run = nch;
     for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
@@ -477,9 +497,7 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
       continue;
     }
     const uint32_t need_vec = (4u * words + 15u) >> 4;
-    for (uint32_t v = min_vec + lane; v < need_vec; v += 32)
-      st_smem_v4(sbuf + 4u * v, ld_nc_v4(srow + v));
-    __syncwarp();
+    if (need_vec > min_vec) fetch_vectors(sbuf_sa, srow, min_vec, need_vec, lane);
     for (uint32_t v = lane; v < nvec; v += 32) {
       uint32_t o[4];
 #pragma unroll
@@ -520,13 +538,7 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
 //     bits (fp32 sign/exponent masks), the scatter is two shift-and-mask
 //     steps instead of the 5-stage network.
 // ------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait_n() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
+
 
 
 // Four output words 4g..4g+3 of a row whose chunk participates: their kept
@@ -609,7 +621,7 @@ __device__ __forceinline__ uint4 decode_packed_group(const uint4* tab, const uin
 
 constexpr uint32_t kRingStages = 4;  // rows per warp ring: 3 in flight while one decodes
 
-template <bool kIds, int kMode>
+template <bool kIds, int kMode, bool kBig>
 __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast(DecodeArgs a, FastParams F) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
@@ -692,7 +704,8 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
                                                (uint32_t)dsto, (uint32_t)(dsto >> 32));
   };
   // copy row tt into ring stage tt % S (one commit group, empty past the end);
-  // a row is at most 2 KB: four predicated 16-byte copies per lane
+  // rows of at most 2 KB: four predicated 16-byte copies per lane; larger
+  // rows (kBig, up to 8 KB): up to sixteen
   const uint32_t ring_sa = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + 16u * lane;
   const uint8_t* src_lane = a.src + 16u * lane;
   auto issue = [&](uint32_t tt) {
@@ -704,7 +717,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         const uint8_t* src = src_lane + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u));
         const uint32_t sa = ring_sa + 4u * (tt & (S - 1u)) * F.sbuf_words;
 #pragma unroll
-        for (uint32_t j = 0; j < 4u; ++j)
+        for (uint32_t j = 0; j < (kBig ? 16u : 4u); ++j)
           if (lane + 32u * j < nv)
             asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * j),
                          "l"(src + 512u * j));
@@ -1391,7 +1404,19 @@ cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32
 
 bool fast_geometry(uint32_t R, uint32_t C) { return R <= 2048u && (C % 16u) == 0u; }
 
-template <bool kIds, int kMode>
+namespace {
+int max_smem_optin() {
+  int dev = 0, v = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    cudaGetLastError();
+    v = 48 * 1024;
+  }
+  return v;
+}
+}  // namespace
+
+template <bool kIds, int kMode, bool kBig>
 cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, cudaStream_t st) {
   FastParams F;
   const uint32_t W = a.m.W, nch = a.m.nch;
@@ -1406,9 +1431,18 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   F.ush = hp.ush;
   F.ubv = hp.ubv;
   F.ukeep = hp.ukeep;
-  const int warps = 8;
-  const size_t smem = 4ull * (F.table_words + F.gtab_words + 8 + (uint64_t)warps * F.warp_words);
-  auto kern = k_decode_fast<kIds, kMode>;
+  // 8 warps per CTA; rows above 2 KB take fewer where the rings would not fit
+  int warps = 8;
+  size_t smem = 4ull * (F.table_words + F.gtab_words + 8 + (uint64_t)warps * F.warp_words);
+  if (kBig) {
+    const size_t cap = (size_t)max_smem_optin();
+    while (warps > 1 && smem > cap) {
+      warps >>= 1;
+      smem = 4ull * (F.table_words + F.gtab_words + 8 + (uint64_t)warps * F.warp_words);
+    }
+    if (smem > cap) return cudaErrorInvalidConfiguration;
+  }
+  auto kern = k_decode_fast<kIds, kMode, kBig>;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
   const uint64_t need = (a.n + 32ull * warps - 1) / (32ull * warps);  // >= 32 rows per warp
@@ -1417,14 +1451,15 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   return cudaGetLastError();
 }
 
-template <bool kIds>
+template <bool kIds, bool kBig>
 cudaError_t launch_fast_mode(const DecodeArgs& a, const HostProps& hp, int sm_count,
                              cudaStream_t st) {
-  if (!hp.known) return launch_fast<kIds, kModeRuntime>(a, hp, sm_count, st);
-  if (hp.uniform && hp.um1 == 0u) return launch_fast<kIds, kModeUniform1>(a, hp, sm_count, st);
-  if (hp.uniform) return launch_fast<kIds, kModeUniform>(a, hp, sm_count, st);
-  if (hp.max_runs <= 2u) return launch_fast<kIds, kModeRun2>(a, hp, sm_count, st);
-  return launch_fast<kIds, kModeNet5>(a, hp, sm_count, st);
+  if (!hp.known) return launch_fast<kIds, kModeRuntime, kBig>(a, hp, sm_count, st);
+  if (hp.uniform && hp.um1 == 0u)
+    return launch_fast<kIds, kModeUniform1, kBig>(a, hp, sm_count, st);
+  if (hp.uniform) return launch_fast<kIds, kModeUniform, kBig>(a, hp, sm_count, st);
+  if (hp.max_runs <= 2u) return launch_fast<kIds, kModeRun2, kBig>(a, hp, sm_count, st);
+  return launch_fast<kIds, kModeNet5, kBig>(a, hp, sm_count, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count,
@@ -1434,8 +1469,13 @@ cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count
   // (its cp.async copies use the .ca form: measured, the L2-only .cg form
   // reads host memory over the link at 60 % of the rate)
   if (a.t2 && fast_geometry(a.m.R, a.m.wpc * 4u))
-    return a.ids ? launch_fast_mode<true>(a, hp, sm_count, st)
-                 : launch_fast_mode<false>(a, hp, sm_count, st);
+    return a.ids ? launch_fast_mode<true, false>(a, hp, sm_count, st)
+                 : launch_fast_mode<false, false>(a, hp, sm_count, st);
+  // rows of 2-8 KB: the same pipeline with longer copies and, where the rings
+  // need it, fewer warps per CTA
+  if (a.t2 && a.m.R <= 8192u && (a.m.wpc & 3u) == 0u)
+    return a.ids ? launch_fast_mode<true, true>(a, hp, sm_count, st)
+                 : launch_fast_mode<false, true>(a, hp, sm_count, st);
   const WarpSmem L = decode_smem(a.m.W, a.m.nch);
   const uint32_t warps = warps_for(4u * L.total_words);
   const int threads = (int)(32u * warps);

@@ -14,6 +14,9 @@ stand-ins for their datasets):
   DLRM        tables of N x dim fp32 ~ N(0, 0.01^2), Zipf(1.05) lookups
   KV cache    fp16 K/V rows of 32 heads x 128, N(0,1) x per-channel log-normal
               scale, 2 % outlier channels x 20
+  saving      rows with exactly k invariant bits per 32-bit word (space-saving
+              sweep): the k high bits, equal in every word, or k scattered
+              positions per word with a per-word constant
 """
 from __future__ import annotations
 
@@ -23,7 +26,8 @@ import numpy as np
 
 BLOCK_ROWS = 65536
 
-_TAG = {"tiny": 1, "sparse": 2, "dense": 3, "dlrm": 4, "kv": 5, "ids": 6, "fuzz": 7}
+_TAG = {"tiny": 1, "sparse": 2, "dense": 3, "dlrm": 4, "kv": 5, "ids": 6, "fuzz": 7,
+        "saving": 8}
 
 
 def _rng(seed: int, tag: str, *more: int) -> np.random.Generator:
@@ -204,3 +208,35 @@ def fuzz_rows(n: int, R: int, seed: int, tag: int = 0) -> np.ndarray:
     wild = g.random(n) < 0.05
     rows[wild] = g.integers(0, 1 << 32, size=(int(wild.sum()), W), dtype=np.uint64).astype(np.uint32)
     return rows.view(np.uint8).reshape(n, R)
+
+
+def invariant_pattern(W: int, k: int, scattered: bool, seed: int = 0
+                      ) -> Tuple[np.ndarray, np.ndarray]:
+    """(keep, const), u32[W] each: keep marks the 32 - k bits of each word that vary,
+    const gives the value of the k others.
+
+    Not scattered: the k high bits of every word are invariant and take the same
+    value (fp32 rows of one magnitude class).  Scattered: k distinct random
+    positions per word, a random constant per word."""
+    assert 0 <= k <= 32
+    g = _rng(seed, "saving", k, int(scattered))
+    if not scattered:
+        inv = 0 if k == 0 else ((0xFFFFFFFF << (32 - k)) & 0xFFFFFFFF)
+        keep = np.full(W, (~inv) & 0xFFFFFFFF, np.uint32)
+        const = np.full(W, int(g.integers(0, 1 << 32, dtype=np.uint64)) & inv, np.uint32)
+        return keep, const
+    keep = np.full(W, 0xFFFFFFFF, np.uint32)
+    for w in range(W):
+        for b in g.choice(32, size=k, replace=False):
+            keep[w] &= np.uint32(~(1 << int(b)) & 0xFFFFFFFF)
+    const = g.integers(0, 1 << 32, size=W, dtype=np.uint64).astype(np.uint32) & ~keep
+    return keep, const
+
+
+def invariant_rows(n: int, R: int, k: int, scattered: bool, seed: int = 0) -> np.ndarray:
+    """Rows [n, R bytes]: random bits where keep is set, const elsewhere."""
+    W = R // 4
+    keep, const = invariant_pattern(W, k, scattered, seed)
+    noise = _rng(seed, "saving", k, int(scattered), 1).integers(
+        0, 1 << 32, size=(n, W), dtype=np.uint64).astype(np.uint32)
+    return ((noise & keep[None, :]) | const[None, :]).view(np.uint8).reshape(n, R)

@@ -158,3 +158,32 @@ def test_kv_cache_prefill_decode_flow():
                     assert np.array_equal(out.cpu().numpy(), want)
             finally:
                 st.close()
+
+
+@pytest.mark.parametrize("R,C", [(4096, 256), (4096, 1024), (4096, 4096), (1024, 256)])
+@pytest.mark.parametrize("k", [0, 4, 16, 28])
+@pytest.mark.parametrize("scattered", [False, True])
+def test_space_saving_sweep_rows(R, C, k, scattered):
+    """The space-saving sweep's input at reduced size: the GPU builder and
+    compressor agree with the oracle, and the gather from host slots returns
+    the rows, at every saving and chunk size of the sweep."""
+    n = 3000 if R == 4096 else 6000
+    rb = wl.invariant_rows(n, R, k, scattered, seed=2)
+    sample = wl.sample_ids(n, 100, seed=2)
+    st = Store(R, C, n)
+    try:
+        slots, stored = _host_store(st, rb, sample)
+        mr, br = ref_c.build_meta(rb, 95, 100, sample_ids=sample)
+        m, b = st.meta()
+        assert np.array_equal(m, mr) and np.array_equal(b, br)
+        ref_sl, ref_bm, ref_st = oracle_slots(rb, C, mr, br, st.slot)
+        assert np.array_equal(stored, ref_st)
+        assert np.array_equal(st.bitmap(), ref_bm)
+        assert_streams_equal(slots.numpy(), ref_sl, ref_st)
+        ids = wl.uniform_ids(2 * n, n, seed=3)
+        out = torch.empty((len(ids), R), dtype=torch.uint8, device=DEV)
+        ibp.ibp_gather_decompress(st.h, out, slots, None, torch.from_numpy(ids).to(DEV), len(ids))
+        assert st.status() == ibp.IBP_OK
+        assert np.array_equal(out.cpu().numpy(), rb[ids])
+    finally:
+        st.close()

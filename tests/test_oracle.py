@@ -142,6 +142,31 @@ def test_sparse_closed_form(num, den):
     assert bad == 0 and np.array_equal(out, rows.view(np.uint8))
 
 
+@pytest.mark.parametrize("R,C", [(4096, 256), (4096, 1024), (4096, 4096), (512, 256), (48, 8)])
+@pytest.mark.parametrize("k", [0, 1, 5, 16, 28, 32])
+@pytest.mark.parametrize("scattered", [False, True])
+def test_invariant_rows_closed_form(R, C, k, scattered):
+    """Rows with exactly k invariant bits per word (the space-saving sweep's input):
+    the builder finds Mask = those bits and Bitval = their values; with k > 0 every
+    chunk participates, so a row is nch + W*(32 - k) bits, rounded up to words, and
+    raw only if that reaches R; with k = 0 every row is raw."""
+    n, W = 400, R // 4
+    nch = (W + C // 4 - 1) // (C // 4)
+    rows = wl.invariant_rows(n, R, k, scattered, seed=5)
+    keep, const = wl.invariant_pattern(W, k, scattered, seed=5)
+    mask, bitval = ref_c.build_meta(rows, 95, 100)
+    assert np.array_equal(mask, ~keep) and np.array_equal(bitval, const)
+    slots = np.zeros((n, R), np.uint8)
+    bitmap = np.zeros((n + 31) // 32, np.uint32)
+    stored = ref_c.compress_batch(rows, C, mask, bitval, slots, bitmap, nthreads=4)
+    want = R if k == 0 else 4 * ((nch + W * (32 - k) + 31) // 32)
+    want = R if want >= R else want
+    assert np.all(stored == want)
+    out, bad = ref_c.decompress_batch(slots, bitmap, R, C, mask, bitval, n=n, slot_stride=R,
+                                      nthreads=4)
+    assert bad == 0 and np.array_equal(out, rows)
+
+
 # ------------------------------------------------------------ special cases
 def test_mask_zero_all_raw():
     rows = wl.fuzz_rows(64, 64, seed=1)
