@@ -402,7 +402,7 @@ def run_ours(args, rank, world, torch, dist):
                           "from a 50,000-id capture",
             "peak_is": "min(HBM %s %.0f GB/s, link %.1f GB/s measured in this run / ratio %.4f)"
                        % (peaks["source"], hbm, link_gbs, ratio),
-            "kernel": "k_decode_fast<true, mode> (ibp_gather_decompress, host-memory source)",
+            "kernel": "k_decode_fast<true, mode, small> (ibp_gather_decompress, host-memory source)",
             "algorithmic_bytes_per_launch": int(algo_bytes),
             "link_bytes_achieved_gbs": round(ratio * delivered_per_launch, 2),
         },
@@ -573,7 +573,7 @@ def run_tiny(args, rank, world, torch, dist):
                                    "scaled from a 196,608-row capture (part of the output is "
                                    "still in L2 when the kernel ends)",
                      "peak_is": "HBM copy bandwidth, %s" % peaks["source"],
-                     "kernel": "k_decode<false> (ibp_decompress, packed offsets)",
+                     "kernel": "k_decode_fast<false, uniform1, small> (ibp_decompress, packed offsets)",
                      "algorithmic_bytes_per_launch": int(stored_sum + n * R + 8 * n)},
         "e2e": {"value": round(n * R * e2e_steps / e2e_t / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": n * R},
@@ -695,7 +695,7 @@ def run_kv(args, rank, world, torch, dist):
         "ratio": round(ratio, 5), "link_gbs": round(link, 2), "parity_layer0_ok": parity_ok,
         "roofline": {"bound": "link", "achieved": round(value / world, 2), "peak": round(roof, 2),
                      "unit": "GB/s", "frac": round(value / world / roof, 4), "traffic": None,
-                     "kernel": "k_decode<true> (ibp_gather_decompress, 8 KB rows)"},
+                     "kernel": "k_decode_fast<true, mode, big> (ibp_gather_decompress, 8 KB rows)"},
         "gpu_launches": 2 * L * args.steps,
         "clocks": clk.summary(),
     }
@@ -1019,7 +1019,7 @@ def run_sweep(args, rank, world, torch, dist):
         "link_gbs": round(link, 2),
         "roofline": {"bound": "link", "achieved": head["gbs"], "peak": head["ideal_gbs"],
                      "unit": "GB/s", "frac": head["frac"], "traffic": None,
-                     "kernel": "k_decode<true> (4 KB rows, ibp_gather_decompress)"},
+                     "kernel": "k_decode_fast<true, uniform, big> (4 KB rows, ibp_gather_decompress)"},
         "saving_sweep": points,
         "min_frac_below_50pct_saving": min(below),
         "sampling_sweep": sampling,
@@ -1102,6 +1102,29 @@ def run_transfers(args, rank, world, torch, dist):
         ev[1].synchronize()
         tt = ev[0].elapsed_time(ev[1]) / 1e3
         best = tt if best is None else min(best, tt)
+    # read granularity of the link: X bytes from the start of random 256-byte
+    # slots (X = 16 .. 256); rows per microsecond show what each partly read
+    # 128-byte line costs
+    gran = []
+    slot, N = 256, (1 << 30) // 256
+    ng = 1 << 21
+    ids_g = torch.from_numpy(np.random.default_rng(7).integers(0, N, size=ng).astype(np.int64)
+                             ).to(dev)
+    out_g = torch.empty(ng * slot, dtype=torch.uint8, device=dev)
+    for X in range(16, 257, 16):
+        for _ in range(3):
+            ibp.ibp_gather_copy(out_g, probe_src, slot, X, ids_g, ng, N, sp)
+        ts = []
+        for _ in range(10):
+            ev[0].record(stream)
+            ibp.ibp_gather_copy(out_g, probe_src, slot, X, ids_g, ng, N, sp)
+            ev[1].record(stream)
+            ev[1].synchronize()
+            ts.append(ev[0].elapsed_time(ev[1]) / 1e3)
+        t = min(ts)
+        gran.append({"row_bytes": X, "rows_per_us": round(ng / t / 1e6, 1),
+                     "gbs": round(ng * X / t / 1e9, 2)})
+    del out_g
     head = res_sizes["512"]["gpu_aligned"]
     return {
         "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
@@ -1112,6 +1135,7 @@ def run_transfers(args, rank, world, torch, dist):
                                "128 B - 8 KB from 1 GB of pinned host memory into HBM"},
         "link_limit_gbs": round((1 << 30) / best / 1e9, 2),
         "by_row_bytes": res_sizes,
+        "read_granularity": gran,
     }
 
 
