@@ -681,6 +681,37 @@ def run_kv(args, rank, world, torch, dist):
     link = pbytes / best / 1e9
     del probe
     roof = min(measured_peaks()["hbm_gbs"], link / ratio)
+
+    # the same fetch decompressed straight into the attention layout
+    # [B, H, P, D] (ibp_gather_decompress_split: each 256-byte head to its own row)
+    H, D = 32, 128
+    att = torch.empty((B, H, P, D * 2), dtype=torch.uint8, device=dev)
+
+    def step_att(_):
+        for st, sl in zip(stores, slots):
+            ibp.ibp_gather_decompress_split(st, att, P, H * P * D * 2, D * 2, P * D * 2, sl, None,
+                                            ids, n, sp)
+
+    step_att(0)
+    ibp.ibp_gather_decompress_split(stores[0], att, P, H * P * D * 2, D * 2, P * D * 2, slots[0],
+                                    None, ids, n, sp)
+    torch.cuda.synchronize()
+    att_ok = bool(torch.equal(att, check.view(B, P, H, D * 2).permute(0, 2, 1, 3)))
+    asteps = min(args.steps, 10)
+    aev = []
+    for b in range(asteps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step_att(b)
+        e1.record(stream)
+        aev.append((e0, e1))
+    torch.cuda.synchronize()
+    for st in stores:
+        assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    t_att = sum(a.elapsed_time(c) / 1e3 for a, c in aev)
+    att_gbs = 2 * L * n * R * asteps / t_att / 1e9
+    del att
     res = {
         "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
         "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -698,6 +729,10 @@ def run_kv(args, rank, world, torch, dist):
                      "kernel": "k_decode_fast<true, mode, big> (ibp_gather_decompress, 8 KB rows)"},
         "gpu_launches": 2 * L * args.steps,
         "clocks": clk.summary(),
+        "attention_layout": {"value": round(att_gbs, 3), "unit": "GB/s", "steps": asteps,
+                             "frac": round(att_gbs / roof, 4), "parity_layer0_ok": att_ok,
+                             "note": "the same 64 gathers per step written as [20, 32, 1920, "
+                                     "128] fp16 per layer and K|V (ibp_gather_decompress_split)"},
     }
     for st in stores:
         ibp.ibp_store_destroy(st)

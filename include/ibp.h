@@ -239,6 +239,25 @@ IBP_API ibp_status ibp_group_gather_decompress(const ibp_group* group, void* dst
                                                uint64_t dst_row_stride, const int64_t* ids,
                                                uint64_t batch, ibp_stream_t stream);
 
+/* Gather-decompression into a layout that splits each row by chunks (the
+ * KV-cache fetch of System Integration, decompressed straight into the
+ * attention layout): output row i = g*group_rows + r puts its chunk k (C
+ * bytes; the last chunk of a row may be shorter) at
+ *   dst + g*group_stride + r*row_stride + k*chunk_stride.
+ * KV rows of one token (H heads x D fp16, chunk = one head), gathered for B
+ * sequences of T tokens each in order, land in a [B, H, T, D] tensor with
+ * group_rows = T, group_stride = H*T*D*2, row_stride = D*2,
+ * chunk_stride = T*D*2.  The caller keeps the placements disjoint.  Needs
+ * C % 16 == 0 and R <= 8192 (IBP_EINVAL otherwise); the three strides are
+ * multiples of 16 (IBP_EALIGN); chunk_stride and group_rows are nonzero.
+ * Other errors: as ibp_gather_decompress. */
+IBP_API ibp_status ibp_gather_decompress_split(const ibp_store* store, void* dst,
+                                               uint64_t group_rows, uint64_t group_stride,
+                                               uint64_t row_stride, uint64_t chunk_stride,
+                                               const void* host_or_dev_src,
+                                               const uint64_t* offsets, const int64_t* ids,
+                                               uint64_t n, ibp_stream_t stream);
+
 /* Gather-decompression through a compressed HBM cache in front of the host
  * store (System Integration: cache compression and PCIe-transfer compression
  * together): row i of dst (at dst + i*dst_stride_bytes) is the decompressed

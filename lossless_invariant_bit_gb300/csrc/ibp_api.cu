@@ -93,13 +93,20 @@ ibp::HostProps host_props(const ibp_store* s) {
   return hp;
 }
 
+// Where output rows go when each row is split by chunks (chunk_stride != 0).
+struct SplitOut {
+  uint64_t chunk_stride = 0, group_rows = 1, group_stride = 0;
+};
+
 ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void* src,
                   const uint64_t* offsets, const int64_t* ids, uint64_t n, cudaStream_t st,
-                  const int64_t* cache_map = nullptr, const void* cache_src = nullptr) {
+                  const int64_t* cache_map = nullptr, const void* cache_src = nullptr,
+                  SplitOut split = SplitOut()) {
   if (!s) return IBP_EINVAL;
   if (n == 0) return IBP_OK;
   if (!dst || !src) return IBP_EINVAL;
-  if (!aligned16(dst) || !aligned16(src) || (dst_stride & 15u) || dst_stride < s->R)
+  if (!aligned16(dst) || !aligned16(src) || (dst_stride & 15u) ||
+      (split.chunk_stride == 0 && dst_stride < s->R))
     return IBP_EALIGN;
   if (!ids && n > s->n_rows) return IBP_ERANGE;
   ibp_status e = on_device(s);
@@ -122,6 +129,9 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.dst_stride = dst_stride;
   a.cache_map = cache_map;
   a.cache_src = static_cast<const uint8_t*>(cache_src);
+  a.chunk_stride = split.chunk_stride;
+  a.group_rows = split.group_rows;
+  a.group_stride = split.group_stride;
   return cu(ibp::launch_decode(a, host_props(s), s->sm_count, st));
 }
 
@@ -362,6 +372,24 @@ ibp_status ibp_gather_decompress_strided(const ibp_store* s, void* dst, uint64_t
                                          const int64_t* ids, uint64_t n, ibp_stream_t stream) {
   if (!ids && n) return IBP_EINVAL;
   return decode(s, dst, dst_stride, src, offsets, ids, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ibp_status ibp_gather_decompress_split(const ibp_store* s, void* dst, uint64_t group_rows,
+                                       uint64_t group_stride, uint64_t row_stride,
+                                       uint64_t chunk_stride, const void* src,
+                                       const uint64_t* offsets, const int64_t* ids, uint64_t n,
+                                       ibp_stream_t stream) {
+  if (!s || group_rows == 0 || chunk_stride == 0) return IBP_EINVAL;
+  if (!ids && n) return IBP_EINVAL;
+  // the fast decoder's geometries: chunks of whole 16-byte groups, rows <= 8 KB
+  if (s->C % 16u != 0u || s->R > 8192u) return IBP_EINVAL;
+  if ((group_stride | row_stride | chunk_stride) & 15u) return IBP_EALIGN;
+  SplitOut sp;
+  sp.chunk_stride = chunk_stride;
+  sp.group_rows = group_rows;
+  sp.group_stride = group_stride;
+  return decode(s, dst, row_stride, src, offsets, ids, n, reinterpret_cast<cudaStream_t>(stream),
+                nullptr, nullptr, sp);
 }
 
 ibp_status ibp_gather_decompress_cached(const ibp_store* s, void* dst, uint64_t dst_stride,

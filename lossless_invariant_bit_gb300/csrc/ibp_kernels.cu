@@ -621,7 +621,16 @@ __device__ __forceinline__ uint4 decode_packed_group(const uint4* tab, const uin
 
 constexpr uint32_t kRingStages = 4;  // rows per warp ring: 3 in flight while one decodes
 
-template <bool kIds, int kMode, bool kBig>
+// Split output: where the 16-byte group g of a row lands, from the group
+// table entry (chunk k | word offset in the chunk << 16).
+__device__ __forceinline__ uint4* split_group(uint4* drow, const uint32_t* gtab, uint32_t g,
+                                              uint64_t chunk_stride) {
+  const uint32_t gd = gtab[g];
+  return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(drow) +
+                                  (uint64_t)(gd & 0xFFFFu) * chunk_stride + 4u * (gd >> 16));
+}
+
+template <bool kIds, int kMode, bool kBig, bool kSplit>
 __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast(DecodeArgs a, FastParams F) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
@@ -699,7 +708,10 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         off = poff;
       }
     }
-    const uint64_t dsto = (r0 + 32ull * q + lane) * a.dst_stride;
+    const uint64_t ri = r0 + 32ull * q + lane;
+    const uint64_t dsto = !kSplit ? ri * a.dst_stride
+                                  : (ri / a.group_rows) * a.group_stride +
+                                        (ri % a.group_rows) * a.dst_stride;
     rinfo[((q & 1u) << 5) + lane] = make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32),
                                                (uint32_t)dsto, (uint32_t)(dsto >> 32));
   };
@@ -746,12 +758,22 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       const uint32_t fl = e.x & 15u;
       uint4* drow = reinterpret_cast<uint4*>(a.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
       uint32_t* sb = ring + (t & (S - 1u)) * F.sbuf_words;
+      constexpr bool split = kSplit;
       if (fl & 12u) {
         if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
-        zero_row(drow, nvec, lane);
+        if (split)
+          for (uint32_t v = lane; v < nvec; v += 32)
+            *split_group(drow, gtab, v, a.chunk_stride) = make_uint4(0, 0, 0, 0);
+        else
+          zero_row(drow, nvec, lane);
         break;
       }
       if (fl & 2u) {  // raw row
+        if (split) {
+          for (uint32_t v = lane; v < nvec; v += 32)
+            *split_group(drow, gtab, v, a.chunk_stride) = *reinterpret_cast<const uint4*>(sb + 4u * v);
+          break;
+        }
         uint4* dp = drow + lane;
         for (uint32_t v = lane; v < nvec; v += 32, dp += 32)
           *dp = *reinterpret_cast<const uint4*>(sb + 4u * v);
@@ -759,13 +781,23 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       }
       if (!can_pack) {
         if (lane == 0) set_status(a.status, IBP_ECORRUPT);
-        zero_row(drow, nvec, lane);
+        if (split)
+          for (uint32_t v = lane; v < nvec; v += 32)
+            *split_group(drow, gtab, v, a.chunk_stride) = make_uint4(0, 0, 0, 0);
+        else
+          zero_row(drow, nvec, lane);
         break;
       }
       const bool all_packed = nhw == 1u ? (sb[0] & hexp) == hexp
                                         : __all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp);
       if (all_packed) {
         // every chunk participates: static offsets, no scan
+        if (split) {
+          for (uint32_t g = lane; g < G; g += 32)
+            *split_group(drow, gtab, g, a.chunk_stride) =
+                decode_packed_group<kMode>(tab, sb, g, G, nch, 0u, net5, uni, F, uparm);
+          break;
+        }
         uint4* dp = drow + lane;
         for (uint32_t g = lane; g < G; g += 32, dp += 32)
           *dp = decode_packed_group<kMode>(tab, sb, g, G, nch, 0u, net5, uni, F, uparm);
@@ -788,7 +820,11 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       if (4u * words >= R || 4ull * words > a.avail) {
         if (lane == 0) set_status(a.status, IBP_ECORRUPT);
         __syncwarp();
-        zero_row(drow, nvec, lane);
+        if (split)
+          for (uint32_t v = lane; v < nvec; v += 32)
+            *split_group(drow, gtab, v, a.chunk_stride) = make_uint4(0, 0, 0, 0);
+        else
+          zero_row(drow, nvec, lane);
         break;
       }
       const uint32_t need_vec = (4u * words + 15u) >> 4;
@@ -803,16 +839,19 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         const uint32_t k = gd & 0xFFFFu;
         const uint32_t ci = cinfo[k];
         const uint32_t start = ci & 0x7FFFFFFFu;
+        uint4* dp = split ? reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(drow) +
+                                                     (uint64_t)k * a.chunk_stride + 4u * (gd >> 16))
+                          : drow + g;
         if (ci >> 31) {
-          drow[g] = decode_packed_group<kMode>(tab, sb, g, G, nch, start - cstat[k], net5, uni, F,
-                                               uparm);
+          *dp = decode_packed_group<kMode>(tab, sb, g, G, nch, start - cstat[k], net5, uni, F,
+                                           uparm);
         } else {
           const uint32_t bit = start + ((gd >> 16) << 5);
           const uint32_t q = bit >> 5;
-          drow[g] = make_uint4(__funnelshift_r(sb[q], sb[q + 1], bit),
-                               __funnelshift_r(sb[q + 1], sb[q + 2], bit),
-                               __funnelshift_r(sb[q + 2], sb[q + 3], bit),
-                               __funnelshift_r(sb[q + 3], sb[q + 4], bit));
+          *dp = make_uint4(__funnelshift_r(sb[q], sb[q + 1], bit),
+                           __funnelshift_r(sb[q + 1], sb[q + 2], bit),
+                           __funnelshift_r(sb[q + 2], sb[q + 3], bit),
+                           __funnelshift_r(sb[q + 3], sb[q + 4], bit));
         }
       }
     } while (false);
@@ -1416,7 +1455,7 @@ int max_smem_optin() {
 }
 }  // namespace
 
-template <bool kIds, int kMode, bool kBig>
+template <bool kIds, int kMode, bool kBig, bool kSplit>
 cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, cudaStream_t st) {
   FastParams F;
   const uint32_t W = a.m.W, nch = a.m.nch;
@@ -1442,7 +1481,7 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
     }
     if (smem > cap) return cudaErrorInvalidConfiguration;
   }
-  auto kern = k_decode_fast<kIds, kMode, kBig>;
+  auto kern = k_decode_fast<kIds, kMode, kBig, kSplit>;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
   const uint64_t need = (a.n + 32ull * warps - 1) / (32ull * warps);  // >= 32 rows per warp
@@ -1451,20 +1490,26 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   return cudaGetLastError();
 }
 
-template <bool kIds, bool kBig>
+template <bool kIds, bool kBig, bool kSplit = false>
 cudaError_t launch_fast_mode(const DecodeArgs& a, const HostProps& hp, int sm_count,
                              cudaStream_t st) {
-  if (!hp.known) return launch_fast<kIds, kModeRuntime, kBig>(a, hp, sm_count, st);
+  if (!hp.known) return launch_fast<kIds, kModeRuntime, kBig, kSplit>(a, hp, sm_count, st);
   if (hp.uniform && hp.um1 == 0u)
-    return launch_fast<kIds, kModeUniform1, kBig>(a, hp, sm_count, st);
-  if (hp.uniform) return launch_fast<kIds, kModeUniform, kBig>(a, hp, sm_count, st);
-  if (hp.max_runs <= 2u) return launch_fast<kIds, kModeRun2, kBig>(a, hp, sm_count, st);
-  return launch_fast<kIds, kModeNet5, kBig>(a, hp, sm_count, st);
+    return launch_fast<kIds, kModeUniform1, kBig, kSplit>(a, hp, sm_count, st);
+  if (hp.uniform) return launch_fast<kIds, kModeUniform, kBig, kSplit>(a, hp, sm_count, st);
+  if (hp.max_runs <= 2u) return launch_fast<kIds, kModeRun2, kBig, kSplit>(a, hp, sm_count, st);
+  return launch_fast<kIds, kModeNet5, kBig, kSplit>(a, hp, sm_count, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count,
                           cudaStream_t st) {
   if (a.n == 0) return cudaSuccess;
+  if (a.chunk_stride) {  // split output: gathers on the fast decoder's geometries only
+    if (!a.ids || !a.t2 || a.m.R > 8192u || (a.m.wpc & 3u) != 0u || a.group_rows == 0)
+      return cudaErrorInvalidValue;
+    return a.m.R <= 2048u ? launch_fast_mode<true, false, true>(a, hp, sm_count, st)
+                          : launch_fast_mode<true, true, true>(a, hp, sm_count, st);
+  }
   // rows up to 2 KB take the fast decoder from HBM and from host memory alike
   // (its cp.async copies use the .ca form: measured, the L2-only .cg form
   // reads host memory over the link at 60 % of the rate)

@@ -55,6 +55,7 @@ _SIGS = {
     "ibp_gather_decompress_strided": [_P, _P, _U64, _P, _P, _P, _U64, _P],
     "ibp_pack": [_P, _P, _P, _P, _P, _U64, _P],
     "ibp_gather_decompress_cached": [_P, _P, _U64, _P, _P, _P, _P, _U64, _P],
+    "ibp_gather_decompress_split": [_P, _P, _U64, _U64, _U64, _U64, _P, _P, _P, _U64, _P],
     "ibp_group_create": [ctypes.POINTER(ctypes.c_void_p), _P, _P, _U32],
     "ibp_group_destroy": [_P],
     "ibp_group_gather_decompress": [_P, _P, _U64, _P, _U64, _P],
@@ -195,6 +196,16 @@ def ibp_gather_decompress_strided(store: int, dst, dst_stride_bytes: int, host_o
                                                        _ptr(host_or_dev_src), _ptr(offsets),
                                                        _ptr(ids), n, _stream(stream)),
            "ibp_gather_decompress_strided")
+
+
+def ibp_gather_decompress_split(store: int, dst, group_rows: int, group_stride: int,
+                                row_stride: int, chunk_stride: int, src, offsets, ids, n: int,
+                                stream=None) -> None:
+    _check(_lib_handle().ibp_gather_decompress_split(store, _ptr(dst), group_rows, group_stride,
+                                                     row_stride, chunk_stride, _ptr(src),
+                                                     _ptr(offsets), _ptr(ids), n,
+                                                     _stream(stream)),
+           "ibp_gather_decompress_split")
 
 
 def ibp_gather_decompress_cached(store: int, dst, dst_stride_bytes: int, host_src, cache_src,

@@ -187,3 +187,70 @@ def test_space_saving_sweep_rows(R, C, k, scattered):
         assert np.array_equal(out.cpu().numpy(), rb[ids])
     finally:
         st.close()
+
+
+@pytest.mark.parametrize("R,C,H", [(8192, 256, 32), (1024, 128, 8), (2048, 512, 4)])
+def test_kv_fetch_into_attention_layout(R, C, H):
+    """ibp_gather_decompress_split: K rows of B sequences (one token = H heads
+    of D fp16, chunk = one head) land in a [B, H, T, D] tensor; a raw row, an
+    out-of-range id (zeros) and the padding between sequences (untouched)."""
+    D = R // (2 * H)
+    assert C == 2 * D
+    B, T_store, T = 3, 64, 41
+    rows = wl.kv_rows(2, 0, B, range(T_store), channels=R // 2, seed=4)  # [B, T_store, R/2] fp16
+    rb = rows.view(np.uint8).reshape(B * T_store, R).copy()
+    rb[5] = np.random.default_rng(0).integers(0, 256, R, dtype=np.uint8)  # an incompressible row
+    st = Store(R, C, B * T_store)
+    try:
+        prompt = (np.arange(B)[:, None] * T_store + np.arange(32)[None, :]).reshape(-1)
+        slots, stored = _host_store(st, rb, prompt)
+        ids = (np.arange(B)[:, None] * T_store + np.arange(T)[None, :]).reshape(-1).astype(np.int64)
+        ids[7] = B * T_store + 3  # out of range: its pieces are zeroed
+        gpad = 4096  # bytes between sequences, left untouched
+        gstride = H * T * D * 2 + gpad
+        out = torch.full((B * gstride,), 0xCC, dtype=torch.uint8, device=DEV)
+        ibp.ibp_gather_decompress_split(st.h, out, T, gstride, D * 2, T * D * 2, slots, None,
+                                        torch.from_numpy(ids).to(DEV), len(ids))
+        assert st.status() == ibp.IBP_ERANGE
+        o = out.cpu().numpy().reshape(B, gstride)
+        got = o[:, :H * T * D * 2].reshape(B, H, T, D * 2)
+        want = rb[np.clip(ids, 0, B * T_store - 1)].reshape(B, T, H, D * 2).transpose(0, 2, 1, 3)
+        want = want.copy()
+        want[0, :, 7] = 0
+        assert np.array_equal(got, want)
+        assert np.all(o[:, H * T * D * 2:] == 0xCC)
+        # the same rows through the plain gather, transposed on the host
+        ids_ok = ids.copy()
+        ids_ok[7] = 0
+        flat = torch.empty((len(ids), R), dtype=torch.uint8, device=DEV)
+        ibp.ibp_gather_decompress(st.h, flat, slots, None, torch.from_numpy(ids_ok).to(DEV),
+                                  len(ids))
+        assert st.status() == ibp.IBP_OK
+        f = flat.cpu().numpy().reshape(B, T, H, D * 2).transpose(0, 2, 1, 3)
+        mask = np.ones((B, H, T), bool)
+        mask[0, :, 7] = False
+        assert np.array_equal(f[mask], got[mask])
+    finally:
+        st.close()
+
+
+def test_split_gather_rejects_other_geometries():
+    a = Store(1000 // 16 * 16, 100, 16)  # chunk of 100 B: not whole 16-byte groups
+    b = Store(16384, 1024, 16)           # rows above 8 KB
+    try:
+        ids = torch.zeros(4, dtype=torch.int64, device=DEV)
+        buf = torch.zeros(1 << 20, dtype=torch.uint8, device=DEV)
+        for s in (a, b):
+            with pytest.raises(ibp.IbpError) as e:
+                ibp.ibp_gather_decompress_split(s.h, buf, 4, 0, 16, 256, buf, None, ids, 4)
+            assert e.value.status == ibp.IBP_EINVAL
+        c = Store(1024, 256, 16)
+        try:
+            with pytest.raises(ibp.IbpError) as e:  # strides must be multiples of 16
+                ibp.ibp_gather_decompress_split(c.h, buf, 4, 0, 8, 256, buf, None, ids, 4)
+            assert e.value.status == ibp.IBP_EALIGN
+        finally:
+            c.close()
+    finally:
+        a.close()
+        b.close()
