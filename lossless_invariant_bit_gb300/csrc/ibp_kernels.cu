@@ -12,6 +12,7 @@
 // decoder is bound by the host link (zero-copy source) or by HBM (cache
 // source), the builder by the bandwidth of the rows it reads, and the bit
 // work runs on the integer pipes.
+#include <cooperative_groups.h>
 #include <mutex>
 #include <vector>
 
@@ -39,6 +40,14 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) { return __ldg(p); }
 
 __device__ __forceinline__ void st_smem_v4(uint32_t* s, const uint4& v) {
   *reinterpret_cast<uint4*>(s) = v;
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_n() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 // Scatter network of a kept-bit mask: the low popcount(nm) bits of v move to
@@ -108,58 +117,135 @@ __device__ __forceinline__ void csa(uint32_t& hi, uint32_t& lo, uint32_t a, uint
   lo = u ^ c;
 }
 
-__global__ void __launch_bounds__(128) k_count_ones(CountArgs a) {
-  const uint32_t w = blockIdx.y * blockDim.x + threadIdx.x;
-  if (w >= a.W) return;
+// Rows reach the counting threads through shared memory: a CTA copies the
+// slice of 16 rows it counts next with 16-byte cp.async copies (lane v of
+// warp q copies vector v of rows q, q+4, q+8, q+12) into a ring of 4 stages,
+// 3 of them in flight while one is counted, so many bytes are in flight
+// without costing registers; each thread then reads its word position of the
+// 16 rows from shared memory.
+constexpr uint32_t kCountRows = 16;   // rows per stage: two carry-save blocks
+constexpr uint32_t kCountStages = 4;  // ring stages
+constexpr uint32_t kCountTile = 128;  // word positions per CTA, one per thread (4 warps)
+constexpr uint32_t kCountCluster = 8; // CTAs (same word tile, other rows) that pool their totals
+
+__device__ __forceinline__ void count8(const uint32_t* sg, uint32_t& o1, uint32_t& o2,
+                                       uint32_t& o4, uint32_t (&c)[8]) {
+  uint32_t x[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) x[u] = sg[u * kCountTile];
+  uint32_t t2a, t2b, t4a, t4b, t8;
+  csa(t2a, o1, o1, x[0], x[1]);
+  csa(t2b, o1, o1, x[2], x[3]);
+  csa(t4a, o2, o2, t2a, t2b);
+  csa(t2a, o1, o1, x[4], x[5]);
+  csa(t2b, o1, o1, x[6], x[7]);
+  csa(t4b, o2, o2, t2a, t2b);
+  csa(t8, o4, o4, t4a, t4b);
+  vadd(c, t8);
+}
+
+// The CTAs of a cluster cover the same word positions: at the end they add
+// their totals through distributed shared memory (CTA r of the cluster sums
+// bits 4r..4r+3 of all eight), so the global counters take one atomic per
+// cluster instead of one per CTA.
+__global__ void __cluster_dims__(kCountCluster, 1, 1) __launch_bounds__(128)
+    k_count_ones(CountArgs a) {
+  extern __shared__ __align__(16) uint32_t cring[];  // [stage][row][word of the tile]
+  const uint32_t t = threadIdx.x;
+  const uint32_t w0 = blockIdx.y * kCountTile;
+  const uint32_t tw = min(kCountTile, a.W - w0);  // a multiple of 4 (rows are 16-byte multiples)
+  const uint32_t nvr = tw >> 2;                   // 16-byte vectors of a row's slice, <= 32
+  const uint32_t w = w0 + t;
+  const bool active = t < tw;
+  // this CTA's rows: a contiguous share [r0, r1) of [0, n)
+  const uint64_t r0 = a.n * blockIdx.x / gridDim.x;
+  const uint64_t r1 = a.n * (blockIdx.x + 1) / gridDim.x;
+  const uint64_t ngrp = (r1 - r0 + kCountRows - 1) / kCountRows;
+  const uint32_t cv = t & 31u, cq = t >> 5;  // the vector and first row this thread copies
+  const uint32_t ring_sa =
+      static_cast<uint32_t>(__cvta_generic_to_shared(cring)) + 16u * cv + 4u * cq * kCountTile;
+  const uint8_t* src_v = a.rows + 4ull * w0 + 16u * cv;
+  auto issue = [&](uint64_t j) {  // rows of group j into stage j % kCountStages
+    if (j < ngrp && cv < nvr) {
+      const uint32_t sb = ring_sa + 4u * (uint32_t)(j % kCountStages) * kCountRows * kCountTile;
+      const uint64_t ib = r0 + kCountRows * j + cq;
+#pragma unroll
+      for (uint32_t k = 0; k < kCountRows / 4u; ++k) {
+        const uint64_t i = ib + 4u * k;
+        if (i < r1) {
+          const uint64_t row = a.ids ? (uint64_t)__ldg(a.ids + i) : i;
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(
+                           sb + 16u * k * kCountTile),
+                       "l"(src_v + row * a.row_stride));
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
   uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // planes counting weight-8 carries
   uint32_t n8[32];                            // spilled plane counts (units of 8 rows)
 #pragma unroll
   for (int b = 0; b < 32; ++b) n8[b] = 0;
   uint32_t o1 = 0, o2 = 0, o4 = 0;  // running bit vectors of weight 1, 2, 4
   uint32_t blocks = 0;
-  const uint64_t step = gridDim.x;
-  uint64_t r = blockIdx.x;
-  for (; r + 7 * step < a.n; r += 8 * step) {
-    uint32_t x[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint64_t i = r + (uint64_t)u * step;
-      const uint64_t row = a.ids ? (uint64_t)__ldg(a.ids + i) : i;
-      x[u] = __ldg(reinterpret_cast<const uint32_t*>(a.rows + row * a.row_stride) + w);
+  for (uint32_t j = 0; j + 1 < kCountStages; ++j) issue(j);
+  for (uint64_t j = 0; j < ngrp; ++j) {
+    issue(j + kCountStages - 1);
+    cp_async_wait_n<kCountStages - 1>();  // this thread's copies of group j have landed
+    __syncthreads();                       // and everyone else's
+    const uint32_t* sg = cring + (uint32_t)(j % kCountStages) * kCountRows * kCountTile + t;
+    const uint64_t left = r1 - r0 - kCountRows * j;
+    if (active) {
+      if (left >= kCountRows) {
+        count8(sg, o1, o2, o4, c);
+        count8(sg + 8u * kCountTile, o1, o2, o4, c);
+        blocks += 2;
+        if (blocks >= 254u) {  // the 8-bit planes hold at most 255 carries
+          vspill(c, n8);
+          blocks = 0;
+        }
+      } else {  // the last < 16 rows
+        uint32_t u = 0;
+        if (left >= 8u) {
+          count8(sg, o1, o2, o4, c);
+          u = 8;
+        }
+        vspill(c, n8);  // room for the tail's carries in the 8-bit planes
+        for (; u < (uint32_t)left; ++u) {  // half adders down the chain
+          const uint32_t x = sg[u * kCountTile];
+          const uint32_t k1 = o1 & x;
+          o1 ^= x;
+          const uint32_t k2 = o2 & k1;
+          o2 ^= k1;
+          const uint32_t k4 = o4 & k2;
+          o4 ^= k2;
+          vadd(c, k4);
+        }
+      }
     }
-    uint32_t t2a, t2b, t4a, t4b, t8;
-    csa(t2a, o1, o1, x[0], x[1]);
-    csa(t2b, o1, o1, x[2], x[3]);
-    csa(t4a, o2, o2, t2a, t2b);
-    csa(t2a, o1, o1, x[4], x[5]);
-    csa(t2b, o1, o1, x[6], x[7]);
-    csa(t4b, o2, o2, t2a, t2b);
-    csa(t8, o4, o4, t4a, t4b);
-    vadd(c, t8);
-    if (++blocks == 255u) {
-      vspill(c, n8);
-      blocks = 0;
-    }
+    __syncthreads();  // stage j % kCountStages is refilled by the next issue
   }
-  vspill(c, n8);  // room for the tail's carries in the 8-bit planes
-  for (; r < a.n; r += step) {  // the last < 8 rows: half adders down the chain
-    const uint64_t row = a.ids ? (uint64_t)__ldg(a.ids + r) : r;
-    const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(a.rows + row * a.row_stride) + w);
-    const uint32_t k1 = o1 & x;
-    o1 ^= x;
-    const uint32_t k2 = o2 & k1;
-    o2 ^= k1;
-    const uint32_t k4 = o4 & k2;
-    o4 ^= k2;
-    vadd(c, k4);
-  }
+  cp_async_wait_n<0>();
+  __syncthreads();  // the ring is free: it takes this CTA's totals, [bit][word of the tile]
   vspill(c, n8);
 #pragma unroll
-  for (int b = 0; b < 32; ++b) {
-    const uint32_t tot = 8u * n8[b] + 4u * ((o4 >> b) & 1u) + 2u * ((o2 >> b) & 1u) +
-                         ((o1 >> b) & 1u);
-    if (tot) atomicAdd(a.counts + 32u * w + b, tot);
+  for (int b = 0; b < 32; ++b)
+    cring[(uint32_t)b * kCountTile + t] = 8u * n8[b] + 4u * ((o4 >> b) & 1u) +
+                                          2u * ((o2 >> b) & 1u) + ((o1 >> b) & 1u);
+  cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
+  cl.sync();
+  constexpr uint32_t kBitsPer = 32u / kCountCluster;
+  const uint32_t b0 = cl.block_rank() * kBitsPer;
+#pragma unroll
+  for (uint32_t bb = 0; bb < kBitsPer; ++bb) {
+    uint32_t sum = 0;
+#pragma unroll
+    for (uint32_t r = 0; r < kCountCluster; ++r)
+      sum += cl.map_shared_rank(cring, r)[(b0 + bb) * kCountTile + t];
+    if (active && sum) atomicAdd(a.counts + 32u * w + b0 + bb, sum);
   }
+  cl.sync();  // no CTA leaves while the others read its totals
 }
 
 // Threshold: bit j is invariant when ones*den >= num*n (value 1) or
@@ -411,13 +497,6 @@ __device__ __forceinline__ uint64_t source_offset(const DecodeArgs& a, int64_t i
   return a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
 }
 
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait_n() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 // 16-byte vectors [v0, v1) of a stored stream into the warp's buffer at
 // shared address `sa`, all issued before any is waited for: one round trip
 // to host memory per fetch instead of one per 512 bytes.
@@ -1355,6 +1434,29 @@ int blocks_per_sm(K kernel, int threads, size_t smem) {
   return b;
 }
 
+// Clusters of a kernel with compile-time cluster dimensions that fit on the
+// GPU at once (0 if the runtime cannot tell).
+template <typename K>
+int max_active_clusters(K kernel, int threads, size_t smem) {
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_cfg_mu);
+  for (const LaunchCfg& c : g_cfg)
+    if (c.dev == dev && c.fn == fn && c.threads == -threads && c.smem == smem) return c.bps;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCountCluster * 1024u, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  g_cfg.push_back({dev, fn, -threads, smem, n});  // cached under a negative thread count
+  return n;
+}
+
 uint32_t warps_for(uint32_t per_warp_bytes) {
   uint32_t w = (96u * 1024u) / per_warp_bytes;
   if (w > 8u) w = 8u;
@@ -1383,16 +1485,21 @@ WarpSmem encode_smem(uint32_t W, uint32_t nch) {
 }
 
 cudaError_t launch_count_ones(const CountArgs& a, int sm_count, cudaStream_t st) {
-  const uint32_t tpb = 128;
+  const uint32_t tpb = kCountTile;
   const uint32_t gy = (a.W + tpb - 1) / tpb;
-  // ~8 CTAs of 4 warps per SM over the word tiles (with 8 rows in flight per
-  // thread that keeps several MB of loads outstanding); each CTA covers n/gx rows
-  uint64_t gx = ((uint64_t)sm_count * 8 + gy - 1) / gy;
+  const size_t smem = 4ull * kCountStages * kCountRows * kCountTile;  // 32 KB
+  // one wave: as many CTAs as fit on the GPU at once, split over the word
+  // tiles; each CTA covers n/gx rows
+  const int clusters = max_active_clusters(k_count_ones, (int)tpb, smem);
+  uint64_t gx = clusters > 0
+                    ? ((uint64_t)clusters / gy) * kCountCluster
+                    : ((uint64_t)sm_count * blocks_per_sm(k_count_ones, (int)tpb, smem) / 2) / gy;
+  if (gx < kCountCluster) gx = kCountCluster;
   const uint64_t max_gx = (a.n + 63) / 64;  // at least 64 rows per CTA
   if (gx > max_gx) gx = max_gx;
-  if (gx < 1) gx = 1;
-  if (gx > 65535) gx = 65535;
-  k_count_ones<<<dim3((uint32_t)gx, gy), tpb, 0, st>>>(a);
+  if (gx > 65528) gx = 65528;
+  gx = (gx + kCountCluster - 1) / kCountCluster * kCountCluster;  // whole clusters
+  k_count_ones<<<dim3((uint32_t)gx, gy), tpb, smem, st>>>(a);
   return cudaGetLastError();
 }
 
