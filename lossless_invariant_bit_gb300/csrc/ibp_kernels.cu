@@ -1164,14 +1164,16 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
 // kUni: a uniform store (every word has the same ~Mask, at most two runs,
 // and the same Bitval, known on the host): the match test and the bit gather
 // take their masks and shifts from the launch parameters.
+constexpr uint32_t kEncodeStages = 4;  // rows per warp ring (rows up to 2 KB)
+
 template <bool kUni>
-__global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
+__global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
   uint32_t* obuf = smem + wid * L.total_words;
-  uint32_t* xbuf = obuf + L.sbuf_words;
-  uint32_t* cinfo = xbuf + L.xbuf_words;
+  uint32_t* cinfo = obuf + L.sbuf_words;
+  uint32_t* rows = cinfo + L.cinfo_words;  // kEncodeStages rows (ring), or one row
   const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
   const uint32_t nvec = R >> 4;
   const uint64_t wpb = blockDim.x >> 5;
@@ -1179,33 +1181,42 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
 
   // A warp takes 32 consecutive rows at a time (so with identity slots it owns
   // one raw-bitmap word and writes it once, instead of 32 warps contending on
-  // it with atomics); rows up to 2 KB load the warp's next row into
-  // registers while the current one is packed.
-  const bool prefetch = nvec <= 128u;
+  // it with atomics).  Rows up to 2 KB travel by cp.async into a ring of 4
+  // single-row stages, 3 rows ahead of the row being packed; larger rows are
+  // loaded when their turn comes.
+  const bool use_ring = nvec <= 128u;
+  constexpr uint32_t S = kEncodeStages;
   const uint64_t nchunk = (a.n + 31) >> 5;
-  uint4 pf[4];
-  auto load_row = [&](uint64_t r) {
-    if (r < a.n) {
-      const uint4* srow = reinterpret_cast<const uint4*>(a.src + r * a.src_stride);
-#pragma unroll
-      for (uint32_t j = 0; j < 4u; ++j)
-        if (lane + 32u * j < nvec) pf[j] = ld_nc_v4(srow + lane + 32u * j);
-    }
-  };
-  if (prefetch) load_row(((uint64_t)blockIdx.x * wpb + wid) << 5);
-
-  for (uint64_t c = (uint64_t)blockIdx.x * wpb + wid; c < nchunk; c += stride) {
-    uint32_t rawmask = 0, donemask = 0;
-#pragma unroll 1
-    for (uint32_t j = 0; j < 32u; ++j) {
-      const uint64_t i = (c << 5) + j;
-      if (i >= a.n) break;
-      if (prefetch) {
+  const uint64_t c0 = (uint64_t)blockIdx.x * wpb + wid;
+  const uint32_t ring_sa = static_cast<uint32_t>(__cvta_generic_to_shared(rows)) + 16u * lane;
+  auto issue = [&](uint64_t t) {  // the warp's t-th row (32 per chunk) into stage t % S
+    if (use_ring) {
+      const uint64_t r = ((c0 + (t >> 5) * stride) << 5) + (t & 31u);
+      if (r < a.n) {
+        const uint8_t* src = a.src + r * a.src_stride + 16u * lane;
+        const uint32_t sa = ring_sa + 4u * (uint32_t)(t % S) * W;
 #pragma unroll
         for (uint32_t q = 0; q < 4u; ++q)
-          if (lane + 32u * q < nvec) st_smem_v4(xbuf + 4u * (lane + 32u * q), pf[q]);
-        load_row(j < 31u ? i + 1 : (c + stride) << 5);
+          if (lane + 32u * q < nvec)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * q),
+                         "l"(src + 512u * q));
       }
+    }
+    cp_async_commit();
+  };
+  for (uint32_t t = 0; t + 1 < S; ++t) issue(t);
+
+  uint64_t t = 0;  // the warp's row counter
+  for (uint64_t c = c0; c < nchunk; c += stride) {
+    uint32_t rawmask = 0, donemask = 0;
+#pragma unroll 1
+    for (uint32_t j = 0; j < 32u; ++j, ++t) {
+      const uint64_t i = (c << 5) + j;
+      if (i >= a.n) break;
+      issue(t + S - 1);
+      cp_async_wait_n<S - 1>();  // row t has landed
+      __syncwarp();
+      uint32_t* xbuf = use_ring ? rows + (uint32_t)(t % S) * W : rows;
       const int64_t slot = a.slot_ids ? __ldg(a.slot_ids + i) : (int64_t)i;
       if (slot < 0 || (uint64_t)slot >= a.n_rows) {
         if (lane == 0) set_status(a.status, IBP_ERANGE);
@@ -1213,79 +1224,140 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
         __syncwarp();
         continue;
       }
-      if (!prefetch) {
-        const uint4* srow = reinterpret_cast<const uint4*>(a.src + i * a.src_stride);
-        for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
-      }
-      for (uint32_t k = lane; k < nch; k += 32) cinfo[k] = 0;
-      __syncwarp();
-      if (kUni) {
-        const uint32_t msk = ~(a.um0 | a.um1);
-        for (uint32_t w = lane; w < W; w += 32)
-          if ((xbuf[w] & msk) != a.ubv) cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
-      } else {
-        for (uint32_t w = lane; w < W; w += 32)
-          if ((xbuf[w] & __ldg(a.m.mask + w)) != __ldg(a.m.bitval + w))
-            cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
-      }
-      __syncwarp();
-      uint32_t run = nch;
-      for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
-        const uint32_t k = k0 + lane;
-        uint32_t size = 0, p = 0;
-        if (k < nch) {
-          const uint32_t full = 32u * min(wpc, W - k * wpc);
-          const uint32_t keep = __ldg(a.m.ckeep + k);
-          p = (cinfo[k] == 0u && keep < full) ? 1u : 0u;
-          size = p ? keep : full;
-        }
-        const uint32_t incl = warp_inclusive_scan(size, lane);
-        __syncwarp();
-        if (k < nch) cinfo[k] = (run + incl - size) | (p << 31);
-        run += __shfl_sync(kFull, incl, 31);
-      }
-      const uint32_t words = (run + 31u) >> 5;
-      const bool raw = 4u * words >= R;
       uint4* dslot = reinterpret_cast<uint4*>(a.dst + (uint64_t)slot * a.slot);
-      if (raw) {
-        for (uint32_t v = lane; v < nvec; v += 32)
-          dslot[v] = *reinterpret_cast<const uint4*>(xbuf + 4u * v);
-      } else {
-        const uint32_t padded = (words + 3u) & ~3u;
-        for (uint32_t z = lane; z < padded + 4u; z += 32) obuf[z] = 0;
+      bool raw = false, done = false;
+      uint32_t words = 0;
+      if (kUni && use_ring) {
+        // Uniform store: when no word misses the Mask every chunk participates
+        // and word w's kept bits go to nch + w*keep; when the row is one chunk
+        // and some word misses, the row is raw.  Other rows take the general
+        // path below.
+        uint4 cur[4];
+#pragma unroll
+        for (uint32_t q = 0; q < 4u; ++q)
+          if (lane + 32u * q < nvec) cur[q] = *reinterpret_cast<const uint4*>(xbuf + 4u * (lane + 32u * q));
+        const uint32_t msk = ~(a.um0 | a.um1);
+        bool mis = false;
+#pragma unroll
+        for (uint32_t q = 0; q < 4u; ++q)
+          if (lane + 32u * q < nvec)
+            mis |= ((cur[q].x & msk) != a.ubv) | ((cur[q].y & msk) != a.ubv) |
+                   ((cur[q].z & msk) != a.ubv) | ((cur[q].w & msk) != a.ubv);
+        mis = __any_sync(kFull, mis);
+        if (a.ukeep >= 32u || (mis && nch == 1u)) {
+          raw = done = true;
+        } else if (!mis) {
+          words = (nch + W * a.ukeep + 31u) >> 5;
+          raw = 4u * words >= R;
+          done = true;
+        }
+        if (done && raw) {
+#pragma unroll
+          for (uint32_t q = 0; q < 4u; ++q)
+            if (lane + 32u * q < nvec) dslot[lane + 32u * q] = cur[q];
+        } else if (done) {
+          const uint32_t padded = (words + 3u) & ~3u;
+          const uint32_t hw = nch >> 5;  // header: nch one bits from bit 0
+          for (uint32_t z = lane; z < padded; z += 32)
+            obuf[z] = z < hw ? 0xFFFFFFFFu : (z == hw ? (1u << (nch & 31u)) - 1u : 0u);
+          __syncwarp();
+          if (a.ukeep) {
+#pragma unroll
+            for (uint32_t q = 0; q < 4u; ++q) {
+              if (lane + 32u * q < nvec) {
+                const uint32_t xs[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
+                uint32_t bit = nch + 4u * (lane + 32u * q) * a.ukeep;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const uint32_t v = ((xs[e] & a.um0) >> (a.ush & 31u)) |
+                                     ((xs[e] & a.um1) >> (a.ush >> 8));
+                  const uint32_t qw = bit >> 5, sh = bit & 31u;
+                  atomicOr(obuf + qw, v << sh);
+                  if (sh != 0u && sh + a.ukeep > 32u) atomicOr(obuf + qw + 1, v >> (32u - sh));
+                  bit += a.ukeep;
+                }
+              }
+            }
+          }
+          __syncwarp();
+          for (uint32_t v = lane; 4u * v < padded; v += 32)
+            dslot[v] = *reinterpret_cast<const uint4*>(obuf + 4u * v);
+        }
+      }
+      if (!done) {
+        if (!use_ring) {
+          const uint4* srow = reinterpret_cast<const uint4*>(a.src + i * a.src_stride);
+          for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
+        }
+        for (uint32_t k = lane; k < nch; k += 32) cinfo[k] = 0;
         __syncwarp();
-        for (uint32_t k = lane; k < nch; k += 32)
-          if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
-        for (uint32_t w = lane; w < W; w += 32) {
-          const uint32_t krw = __ldg(a.m.kr + w);  // chunk | word in chunk << 16
-          const uint32_t ci = cinfo[krw & 0xFFFFu];
-          const bool packed = (ci >> 31) != 0u;
-          uint32_t v = xbuf[w];
-          uint32_t nbits = 32;
-          uint32_t bit;
-          if (kUni) {
-            bit = (ci & 0x7FFFFFFFu) + (krw >> 16) * (packed ? a.ukeep : 32u);
-            if (packed) {
-              v = ((v & a.um0) >> (a.ush & 31u)) | ((v & a.um1) >> (a.ush >> 8));
-              nbits = a.ukeep;
-            }
-          } else {
-            bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
-            if (packed) {
-              const uint32_t keepm = __ldg(a.m.nm + w);
-              v = gather_bits(v & keepm, a.m.mv, W, w);
-              nbits = __popc(keepm);
-            }
-          }
-          if (nbits) {
-            const uint32_t q = bit >> 5, sh = bit & 31u;
-            atomicOr(obuf + q, v << sh);
-            if (sh != 0u && sh + nbits > 32u) atomicOr(obuf + q + 1, v >> (32u - sh));
-          }
+        if (kUni) {
+          const uint32_t msk = ~(a.um0 | a.um1);
+          for (uint32_t w = lane; w < W; w += 32)
+            if ((xbuf[w] & msk) != a.ubv) cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
+        } else {
+          for (uint32_t w = lane; w < W; w += 32)
+            if ((xbuf[w] & __ldg(a.m.mask + w)) != __ldg(a.m.bitval + w))
+              cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
         }
         __syncwarp();
-        for (uint32_t v = lane; 4u * v < padded; v += 32)
-          dslot[v] = *reinterpret_cast<const uint4*>(obuf + 4u * v);
+        uint32_t run = nch;
+        for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
+          const uint32_t k = k0 + lane;
+          uint32_t size = 0, p = 0;
+          if (k < nch) {
+            const uint32_t full = 32u * min(wpc, W - k * wpc);
+            const uint32_t keep = __ldg(a.m.ckeep + k);
+            p = (cinfo[k] == 0u && keep < full) ? 1u : 0u;
+            size = p ? keep : full;
+          }
+          const uint32_t incl = warp_inclusive_scan(size, lane);
+          __syncwarp();
+          if (k < nch) cinfo[k] = (run + incl - size) | (p << 31);
+          run += __shfl_sync(kFull, incl, 31);
+        }
+        words = (run + 31u) >> 5;
+        raw = 4u * words >= R;
+        if (raw) {
+          for (uint32_t v = lane; v < nvec; v += 32)
+            dslot[v] = *reinterpret_cast<const uint4*>(xbuf + 4u * v);
+        } else {
+          const uint32_t padded = (words + 3u) & ~3u;
+          for (uint32_t z = lane; z < padded + 4u; z += 32) obuf[z] = 0;
+          __syncwarp();
+          for (uint32_t k = lane; k < nch; k += 32)
+            if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
+          for (uint32_t w = lane; w < W; w += 32) {
+            const uint32_t krw = __ldg(a.m.kr + w);  // chunk | word in chunk << 16
+            const uint32_t ci = cinfo[krw & 0xFFFFu];
+            const bool packed = (ci >> 31) != 0u;
+            uint32_t v = xbuf[w];
+            uint32_t nbits = 32;
+            uint32_t bit;
+            if (kUni) {
+              bit = (ci & 0x7FFFFFFFu) + (krw >> 16) * (packed ? a.ukeep : 32u);
+              if (packed) {
+                v = ((v & a.um0) >> (a.ush & 31u)) | ((v & a.um1) >> (a.ush >> 8));
+                nbits = a.ukeep;
+              }
+            } else {
+              bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
+              if (packed) {
+                const uint32_t keepm = __ldg(a.m.nm + w);
+                v = gather_bits(v & keepm, a.m.mv, W, w);
+                nbits = __popc(keepm);
+              }
+            }
+            if (nbits) {
+              const uint32_t q = bit >> 5, sh = bit & 31u;
+              atomicOr(obuf + q, v << sh);
+              if (sh != 0u && sh + nbits > 32u) atomicOr(obuf + q + 1, v >> (32u - sh));
+            }
+          }
+          __syncwarp();
+          for (uint32_t v = lane; 4u * v < padded; v += 32)
+            dslot[v] = *reinterpret_cast<const uint4*>(obuf + 4u * v);
+        }
       }
       if (a.slot_ids) {
         if (lane == 0) {
@@ -1311,6 +1383,7 @@ __global__ void __launch_bounds__(256) k_encode(EncodeArgs a, WarpSmem L) {
       }
     }
   }
+  cp_async_wait_n<0>();
 }
 
 // ------------------------------------------------------------------------
@@ -1478,8 +1551,9 @@ WarpSmem decode_smem(uint32_t W, uint32_t nch) {
 WarpSmem encode_smem(uint32_t W, uint32_t nch) {
   WarpSmem L;
   L.sbuf_words = ((W + 8u) + 3u) & ~3u;
-  L.xbuf_words = (W + 3u) & ~3u;
   L.cinfo_words = (nch + 3u) & ~3u;
+  // rows up to 2 KB: a ring of kEncodeStages rows; larger rows: one
+  L.xbuf_words = (W <= 512u ? kEncodeStages : 1u) * ((W + 3u) & ~3u);
   L.total_words = L.sbuf_words + L.xbuf_words + L.cinfo_words;
   return L;
 }
