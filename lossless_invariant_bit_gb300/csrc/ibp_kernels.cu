@@ -1166,7 +1166,9 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
 // take their masks and shifts from the launch parameters.
 constexpr uint32_t kEncodeStages = 4;  // rows per warp ring (rows up to 2 KB)
 
-template <bool kUni>
+// kVpl: 16-byte vectors per lane of a row staged in the ring (1, 2 or 4:
+// rows up to 512 B, 1 KB, 2 KB); 0: larger rows, loaded when their turn comes.
+template <bool kUni, int kVpl>
 __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
@@ -1184,27 +1186,24 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
   // it with atomics).  Rows up to 2 KB travel by cp.async into a ring of 4
   // single-row stages, 3 rows ahead of the row being packed; larger rows are
   // loaded when their turn comes.
-  const bool use_ring = nvec <= 128u;
+  constexpr bool use_ring = kVpl > 0;
   constexpr uint32_t S = kEncodeStages;
   const uint64_t nchunk = (a.n + 31) >> 5;
   const uint64_t c0 = (uint64_t)blockIdx.x * wpb + wid;
   const uint32_t ring_sa = static_cast<uint32_t>(__cvta_generic_to_shared(rows)) + 16u * lane;
-  auto issue = [&](uint64_t t) {  // the warp's t-th row (32 per chunk) into stage t % S
-    if (use_ring) {
-      const uint64_t r = ((c0 + (t >> 5) * stride) << 5) + (t & 31u);
-      if (r < a.n) {
-        const uint8_t* src = a.src + r * a.src_stride + 16u * lane;
-        const uint32_t sa = ring_sa + 4u * (uint32_t)(t % S) * W;
+  auto issue = [&](uint64_t r, uint32_t stage) {  // row r into ring stage `stage`
+    if (use_ring && r < a.n) {
+      const uint8_t* src = a.src + r * a.src_stride + 16u * lane;
+      const uint32_t sa = ring_sa + 4u * stage * W;
 #pragma unroll
-        for (uint32_t q = 0; q < 4u; ++q)
-          if (lane + 32u * q < nvec)
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * q),
-                         "l"(src + 512u * q));
-      }
+      for (uint32_t q = 0; q < (uint32_t)kVpl; ++q)
+        if (lane + 32u * q < nvec)
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * q),
+                       "l"(src + 512u * q));
     }
     cp_async_commit();
   };
-  for (uint32_t t = 0; t + 1 < S; ++t) issue(t);
+  for (uint32_t t = 0; t + 1 < S; ++t) issue((c0 << 5) + t, t);  // a chunk has 32 >= S rows
 
   uint64_t t = 0;  // the warp's row counter
   for (uint64_t c = c0; c < nchunk; c += stride) {
@@ -1213,7 +1212,9 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
     for (uint32_t j = 0; j < 32u; ++j, ++t) {
       const uint64_t i = (c << 5) + j;
       if (i >= a.n) break;
-      issue(t + S - 1);
+      // the row S-1 ahead: later in this chunk or early in the warp's next one
+      issue(j + S - 1u < 32u ? i + S - 1u : ((c + stride) << 5) + (j + S - 1u - 32u),
+            (uint32_t)((t + S - 1u) % S));
       cp_async_wait_n<S - 1>();  // row t has landed
       __syncwarp();
       uint32_t* xbuf = use_ring ? rows + (uint32_t)(t % S) * W : rows;
@@ -1232,18 +1233,18 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
         // and word w's kept bits go to nch + w*keep; when the row is one chunk
         // and some word misses, the row is raw.  Other rows take the general
         // path below.
-        uint4 cur[4];
-#pragma unroll
-        for (uint32_t q = 0; q < 4u; ++q)
-          if (lane + 32u * q < nvec) cur[q] = *reinterpret_cast<const uint4*>(xbuf + 4u * (lane + 32u * q));
+        uint4 cur[kVpl > 0 ? kVpl : 1];
         const uint32_t msk = ~(a.um0 | a.um1);
-        bool mis = false;
+        uint32_t diff = 0;
 #pragma unroll
-        for (uint32_t q = 0; q < 4u; ++q)
-          if (lane + 32u * q < nvec)
-            mis |= ((cur[q].x & msk) != a.ubv) | ((cur[q].y & msk) != a.ubv) |
-                   ((cur[q].z & msk) != a.ubv) | ((cur[q].w & msk) != a.ubv);
-        mis = __any_sync(kFull, mis);
+        for (uint32_t q = 0; q < (uint32_t)kVpl; ++q) {
+          if (lane + 32u * q < nvec) {
+            cur[q] = *reinterpret_cast<const uint4*>(xbuf + 4u * (lane + 32u * q));
+            diff |= ((cur[q].x & msk) ^ a.ubv) | ((cur[q].y & msk) ^ a.ubv) |
+                    ((cur[q].z & msk) ^ a.ubv) | ((cur[q].w & msk) ^ a.ubv);
+          }
+        }
+        const bool mis = __any_sync(kFull, diff != 0u);
         if (a.ukeep >= 32u || (mis && nch == 1u)) {
           raw = done = true;
         } else if (!mis) {
@@ -1253,7 +1254,7 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
         }
         if (done && raw) {
 #pragma unroll
-          for (uint32_t q = 0; q < 4u; ++q)
+          for (uint32_t q = 0; q < (uint32_t)kVpl; ++q)
             if (lane + 32u * q < nvec) dslot[lane + 32u * q] = cur[q];
         } else if (done) {
           const uint32_t padded = (words + 3u) & ~3u;
@@ -1263,7 +1264,7 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
           __syncwarp();
           if (a.ukeep) {
 #pragma unroll
-            for (uint32_t q = 0; q < 4u; ++q) {
+            for (uint32_t q = 0; q < (uint32_t)kVpl; ++q) {
               if (lane + 32u * q < nvec) {
                 const uint32_t xs[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
                 uint32_t bit = nch + 4u * (lane + 32u * q) * a.ukeep;
@@ -1721,18 +1722,27 @@ cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count
   return cudaGetLastError();
 }
 
-template <bool kUni>
-cudaError_t launch_encode_t(const EncodeArgs& a, int sm_count, cudaStream_t st) {
+template <bool kUni, int kVpl>
+cudaError_t launch_encode_v(const EncodeArgs& a, int sm_count, cudaStream_t st) {
   const WarpSmem L = encode_smem(a.m.W, a.m.nch);
   const uint32_t warps = warps_for(4u * L.total_words);
   const int threads = (int)(32u * warps);
   const size_t smem = (size_t)4u * L.total_words * warps;
-  const int bps = blocks_per_sm(k_encode<kUni>, threads, smem);
+  const int bps = blocks_per_sm(k_encode<kUni, kVpl>, threads, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
   const uint64_t need = ((a.n + 31) / 32 + warps - 1) / warps;  // 32-row chunks per warp
   if (blocks > need) blocks = need;
-  k_encode<kUni><<<(uint32_t)blocks, threads, smem, st>>>(a, L);
+  k_encode<kUni, kVpl><<<(uint32_t)blocks, threads, smem, st>>>(a, L);
   return cudaGetLastError();
+}
+
+template <bool kUni>
+cudaError_t launch_encode_t(const EncodeArgs& a, int sm_count, cudaStream_t st) {
+  const uint32_t nvec = a.m.R >> 4;
+  if (nvec <= 32u) return launch_encode_v<kUni, 1>(a, sm_count, st);
+  if (nvec <= 64u) return launch_encode_v<kUni, 2>(a, sm_count, st);
+  if (nvec <= 128u) return launch_encode_v<kUni, 4>(a, sm_count, st);
+  return launch_encode_v<kUni, 0>(a, sm_count, st);
 }
 
 cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count,
