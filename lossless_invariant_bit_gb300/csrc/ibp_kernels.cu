@@ -1429,33 +1429,90 @@ __global__ void __launch_bounds__(256) k_gather_copy(uint8_t* dst, const uint8_t
   }
 }
 
-// Packed-cache offsets: exclusive scan of roundup(stored, 16) in one block.
-// Thread t owns a contiguous range; range sums are scanned in shared memory.
-__global__ void __launch_bounds__(1024) k_pack_offsets(const uint32_t* stored, uint64_t n,
-                                                       uint64_t* offsets) {
-  __shared__ uint64_t part[1024];
-  const uint64_t per = (n + blockDim.x - 1) / blockDim.x;
-  const uint64_t b = (uint64_t)threadIdx.x * per;
-  const uint64_t e = min(b + per, n);
-  uint64_t sum = 0;
-  for (uint64_t i = b; i < e; ++i) sum += (__ldg(stored + i) + 15u) & ~15u;
-  part[threadIdx.x] = sum;
-  __syncthreads();
-  for (uint32_t d = 1; d < blockDim.x; d <<= 1) {
-    const uint64_t t = threadIdx.x >= d ? part[threadIdx.x - d] : 0;
-    __syncthreads();
-    part[threadIdx.x] += t;
-    __syncthreads();
-  }
-  uint64_t run = part[threadIdx.x] - sum;
-  for (uint64_t i = b; i < e; ++i) {
-    offsets[i] = run;
-    run += (__ldg(stored + i) + 15u) & ~15u;
-  }
-  if (threadIdx.x == blockDim.x - 1) offsets[n] = part[threadIdx.x];
+// Packed-cache offsets: exclusive scan of roundup(stored, 16), in tiles of
+// 8192 rows.  (1) each tile's sum is parked in offsets[first row of the next
+// tile] (offsets[n] for the last tile); (2) one block turns those sums into
+// tile bases in place and writes the total to offsets[n]; (3) each tile scans
+// its rows from its base, one warp per 1024 rows, 32 at a time with a
+// shuffle scan (coalesced reads and writes).  The slots that (1) and (2) use
+// are rewritten by (3) with the same value, so the tiles never race.
+constexpr uint32_t kPackTile = 8192;
+
+__device__ __forceinline__ uint64_t pack_len(const uint32_t* stored, uint64_t i) {
+  return (__ldg(stored + i) + 15u) & ~15u;
 }
 
-// Copy each row's stored bytes (16-byte granules) from its slot to the cache.
+__global__ void __launch_bounds__(256) k_pack_tile_sums(const uint32_t* stored, uint64_t n,
+                                                        uint64_t* offsets) {
+  __shared__ uint64_t wsum[8];
+  const uint64_t t0 = (uint64_t)blockIdx.x * kPackTile;
+  const uint64_t t1 = min(t0 + kPackTile, n);
+  uint64_t sum = 0;
+  for (uint64_t i = t0 + threadIdx.x; i < t1; i += blockDim.x) sum += pack_len(stored, i);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) sum += __shfl_down_sync(0xFFFFFFFFu, sum, d);
+  if ((threadIdx.x & 31u) == 0) wsum[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint64_t tot = 0;
+    for (uint32_t w = 0; w < (blockDim.x >> 5); ++w) tot += wsum[w];
+    offsets[t1] = tot;  // the next tile's first slot, or offsets[n]
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_pack_tile_bases(uint64_t n, uint64_t* offsets) {
+  __shared__ uint64_t part[1024];
+  const uint64_t T = (n + kPackTile - 1) / kPackTile;
+  uint64_t carry = 0;
+  for (uint64_t b0 = 0; b0 < T; b0 += blockDim.x) {
+    const uint64_t t = b0 + threadIdx.x;
+    const uint64_t v = t < T ? offsets[min((t + 1) * kPackTile, n)] : 0;
+    part[threadIdx.x] = v;
+    __syncthreads();
+    for (uint32_t d = 1; d < blockDim.x; d <<= 1) {
+      const uint64_t x = threadIdx.x >= d ? part[threadIdx.x - d] : 0;
+      __syncthreads();
+      part[threadIdx.x] += x;
+      __syncthreads();
+    }
+    // tile t + 1 starts where tiles 0..t end; the last one's end is the total
+    if (t < T) offsets[min((t + 1) * kPackTile, n)] = carry + part[threadIdx.x];
+    carry += part[blockDim.x - 1];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) offsets[0] = 0;
+}
+
+__global__ void __launch_bounds__(256) k_pack_tile_scan(const uint32_t* stored, uint64_t n,
+                                                        uint64_t* offsets) {
+  __shared__ uint64_t wsum[8];
+  const uint32_t lane = threadIdx.x & 31u, wid = threadIdx.x >> 5;
+  const uint64_t t0 = (uint64_t)blockIdx.x * kPackTile;
+  const uint64_t w0 = t0 + (uint64_t)wid * (kPackTile / 8u);
+  const uint64_t w1 = min(w0 + kPackTile / 8u, n);
+  const uint64_t base = offsets[t0];  // written by k_pack_tile_bases
+  uint64_t sum = 0;
+  for (uint64_t i = w0 + lane; i < w1; i += 32) sum += pack_len(stored, i);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, d);
+  if (lane == 0) wsum[wid] = sum;
+  __syncthreads();
+  uint64_t run = base;
+  for (uint32_t w = 0; w < wid; ++w) run += wsum[w];
+  for (uint64_t i0 = w0; i0 < w1; i0 += 32) {
+    const uint64_t i = i0 + lane;
+    const uint64_t v = i < w1 ? pack_len(stored, i) : 0;
+    uint64_t incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint64_t x = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= (uint32_t)d) incl += x;
+    }
+    if (i < w1) offsets[i] = run + incl - v;
+    run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+}
+
 __global__ void __launch_bounds__(256) k_pack_copy(uint8_t* dst, const uint64_t* offsets,
                                                    const uint8_t* src, uint64_t slot,
                                                    const uint32_t* stored, uint64_t n) {
@@ -1762,9 +1819,17 @@ cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count
 
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,
                         const uint32_t* stored, uint64_t n, int sm_count, cudaStream_t st) {
-  k_pack_offsets<<<1, 1024, 0, st>>>(stored, n, offsets);
+  const uint64_t T = (n + kPackTile - 1) / kPackTile;
+  if (n == 0) {
+    k_pack_tile_bases<<<1, 1024, 0, st>>>(0, offsets);  // offsets[0] = 0
+    return cudaGetLastError();
+  }
+  if (T > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+  k_pack_tile_sums<<<(uint32_t)T, 256, 0, st>>>(stored, n, offsets);
+  k_pack_tile_bases<<<1, 1024, 0, st>>>(n, offsets);
+  k_pack_tile_scan<<<(uint32_t)T, 256, 0, st>>>(stored, n, offsets);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || dst == nullptr || n == 0) return e;
+  if (e != cudaSuccess || dst == nullptr) return e;
   uint64_t blocks = (uint64_t)sm_count * blocks_per_sm(k_pack_copy, 256, 0);
   const uint64_t need = (n + 7) / 8;
   if (blocks > need) blocks = need;
