@@ -143,20 +143,24 @@ class SparseStore:
         # compressor into HBM slots (bound by HBM, not the host link)
         st2 = ibp.ibp_store_create(self.R, chunk, n_rows, 0)
         slots_dev = torch.empty((n_rows, self.slot), dtype=torch.uint8, device=dev)
-        ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        ibp.ibp_build_meta(st2, d_rows, self.R, None, n_rows, num, den)
-        ev2[0].record()
-        ibp.ibp_build_meta(st2, d_rows, self.R, None, n_rows, num, den)
-        ev2[1].record()
+        def med_time(fn, reps=5):  # median of `reps` timed calls after one warm-up
+            fn()
+            ts = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) / 1e3)
+            return statistics.median(ts)
+
+        t_meta_all = med_time(lambda: ibp.ibp_build_meta(st2, d_rows, self.R, None, n_rows, num,
+                                                         den))
         torch.cuda.synchronize()  # the store's properties reach the host: specialised forms
-        ibp.ibp_compress(st2, slots_dev, d_rows, self.R, None, n_rows, None)
-        ev2[2].record()
-        ibp.ibp_compress(st2, slots_dev, d_rows, self.R, None, n_rows, None)
-        ev2[3].record()
-        torch.cuda.synchronize()
+        t_comp_hbm = med_time(lambda: ibp.ibp_compress(st2, slots_dev, d_rows, self.R, None,
+                                                       n_rows, None))
         assert ibp.ibp_stream_status(st2, reset=True) == ibp.IBP_OK
-        t_meta_all = ev2[0].elapsed_time(ev2[1]) / 1e3
-        t_comp_hbm = ev2[2].elapsed_time(ev2[3]) / 1e3
         ibp.ibp_store_destroy(st2)
         del slots_dev
         self.companions = {
@@ -167,9 +171,10 @@ class SparseStore:
                          "gbs": round(n_rows * self.R / t_comp / 1e9, 2),
                          "note": "raw rows in HBM -> pinned host slots over the link"},
             "build_meta_all_rows_hbm": {"rows": n_rows, "seconds": round(t_meta_all, 6),
+                                        "reps": "median of 5",
                                         "gbs": round(n_rows * self.R / t_meta_all / 1e9, 2),
                                         "note": "all 2M rows (1 GB) analysed, in HBM"},
-            "compress_hbm": {"rows": n_rows, "seconds": round(t_comp_hbm, 6),
+            "compress_hbm": {"rows": n_rows, "seconds": round(t_comp_hbm, 6), "reps": "median of 5",
                              "gbs": round(n_rows * self.R / t_comp_hbm / 1e9, 2),
                              "note": "raw rows in HBM -> HBM slots (ratio 0.726: R read + "
                                      "stored written per row)"}}
@@ -369,6 +374,8 @@ def run_ours(args, rank, world, torch, dist):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(t_total / args.steps * 1e3, 4),
+        "ms_per_step_median": round(statistics.median(times) * 1e3, 4),
+        "ms_per_step_min": round(min(times) * 1e3, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -463,11 +470,11 @@ def run_ours(args, rank, world, torch, dist):
     return result
 
 def run_tiny(args, rank, world, torch, dist):
-    from lossless_invariant_bit_gb300 import dist as ibpdist
     """Cache path: full decompression of a packed HBM cache.  128 distinct
     replicas of the tiny workload (4096 x 256 fp32 each, 524,288 rows, 512 MB
     raw) so that one launch moves far more than the 129 MB L2; Mask/Bitval from
     replica 0 at T = 0.95, chunk 256 B."""
+    from lossless_invariant_bit_gb300 import dist as ibpdist
     from lossless_invariant_bit_gb300 import ibp
     from lossless_invariant_bit_gb300 import workloads as wl
 
@@ -538,6 +545,17 @@ def run_tiny(args, rank, world, torch, dist):
     hbm = peaks["hbm_gbs"]
     moved = (stored_sum + n * R) / t_launch / 1e9  # read stored + write rows
 
+    # single-batch latency: one replica (4096 rows, 4 MB: L2-resident, launch-bound)
+    lat = []
+    for b in range(23):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ibp.ibp_decompress(st, out, cache, offs, per, sp)
+        e1.record(stream)
+        e1.synchronize()
+        if b >= 3:
+            lat.append(e0.elapsed_time(e1) * 1e3)
+
     # e2e: packed cache in HBM, output read back to pinned host each step
     out_host = torch.empty((n, R), dtype=torch.uint8, pin_memory=True)
 
@@ -564,6 +582,8 @@ def run_tiny(args, rank, world, torch, dist):
                    "parallelism": "dp%d (replicas, no collective)" % world},
         "ratio": round(ratio, 5),
         "parity_all_rows_ok": parity_ok,
+        "single_batch_us": {"median": round(statistics.median(lat), 2), "min": round(min(lat), 2),
+                            "rows": per},
         "roofline": {"bound": "hbm", "achieved": round(moved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(moved / hbm, 4),
                      # dram read + write of a 48-replica launch (profiles/
@@ -611,6 +631,7 @@ def run_kv(args, rank, world, torch, dist):
     prompt_ids = torch.from_numpy(
         (np.arange(B)[:, None] * T + np.arange(P)[None, :]).reshape(-1).astype(np.int64)).to(dev)
     check = None
+    newrows = []  # rows of the decode tokens 1920..2047, kept on the GPU for the decode steps
     for layer in range(L):
         for kv in range(2):
             g.manual_seed(args.seed * 1000003 + layer * 2 + kv)
@@ -628,6 +649,7 @@ def run_kv(args, rank, world, torch, dist):
             ratio_num += int(stored[:].view(B, T)[:, :P].sum().item())
             if layer == 0 and kv == 0:
                 check = xb.view(B, T, R)[:, :P].clone()
+            newrows.append(xb.view(B, T, R)[:, P:].clone())
             stores.append(st)
             slots.append(sl)
             del x, xb
@@ -712,6 +734,53 @@ def run_kv(args, rank, world, torch, dist):
     t_att = sum(a.elapsed_time(c) / 1e3 for a, c in aev)
     att_gbs = 2 * L * n * R * asteps / t_att / 1e9
     del att
+
+    # decode steps: each compresses the 20 new rows of every (layer, K|V) into
+    # their host slots (1280 rows), then re-fetches the whole history
+    decode = []
+    stored1 = torch.empty(B, dtype=torch.int32, device=dev)
+    for s_ in (0, 63, 127):
+        tok = P + s_
+        sids = torch.from_numpy((np.arange(B) * T + tok).astype(np.int64)).to(dev)
+        hist = torch.from_numpy((np.arange(B)[:, None] * T + np.arange(tok + 1)[None, :])
+                                .reshape(-1).astype(np.int64)).to(dev)
+        nh = len(hist)
+        outh = torch.empty((nh, R), dtype=torch.uint8, device=dev)
+
+        def comp():
+            for st, sl, nr in zip(stores, slots, newrows):
+                ibp.ibp_compress(st, sl, nr[:, s_], (T - P) * R, sids, B, stored1, sp)
+
+        def fetch():
+            for st, sl in zip(stores, slots):
+                ibp.ibp_gather_decompress(st, outh, sl, None, hist, nh, sp)
+
+        tc, tf = [], []
+        for rep_ in range(4):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            comp()
+            e[1].record(stream)
+            fetch()
+            e[2].record(stream)
+            torch.cuda.synchronize()
+            if rep_:  # the first is a warm-up
+                tc.append(e[0].elapsed_time(e[1]) / 1e3)
+                tf.append(e[1].elapsed_time(e[2]) / 1e3)
+        for st in stores:
+            assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+        ibp.ibp_gather_decompress(stores[0], outh, slots[0], None, hist, nh, sp)
+        torch.cuda.synchronize()
+        got = outh.view(B, tok + 1, R)
+        ok = bool(torch.equal(got[:, :P], check) and torch.equal(got[:, P:], newrows[0][:, :s_ + 1]))
+        decode.append({"step": s_, "history_rows_per_store": nh,
+                       "compress_us": round(statistics.median(tc) * 1e6, 1),
+                       "compress_gbs": round(2 * L * B * R / statistics.median(tc) / 1e9, 2),
+                       "fetch_gbs": round(2 * L * nh * R / statistics.median(tf) / 1e9, 2),
+                       "parity_layer0_ok": ok})
+        del outh
+    del newrows
     res = {
         "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
         "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -729,6 +798,7 @@ def run_kv(args, rank, world, torch, dist):
                      "kernel": "k_decode_fast<true, mode, big> (ibp_gather_decompress, 8 KB rows)"},
         "gpu_launches": 2 * L * args.steps,
         "clocks": clk.summary(),
+        "decode_steps": decode,
         "attention_layout": {"value": round(att_gbs, 3), "unit": "GB/s", "steps": asteps,
                              "frac": round(att_gbs / roof, 4), "parity_layer0_ok": att_ok,
                              "note": "the same 64 gathers per step written as [20, 32, 1920, "
@@ -1192,7 +1262,12 @@ def cpu_baseline(store, batches, ibp, seconds=1.5):
         assert bad == 0
         rows += len(batches[k])
         k += 1
+    # the same decoder on one core, over the first batch's first 20,000 ids
+    t0 = time.perf_counter()
+    cpu_oracle_decode(store, batches[0][:20000], mask, bitval, bitmap, 1)
+    single = 20000 * store.R / (time.perf_counter() - t0) / 1e9
     return {"value": round(rows * store.R / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "single_core_gbs": round(single, 4),
             "kind": "oracle",
             "sample": "%d batches of %d ids of the same workload (%.1f s wall), oracle C "
                       "decoder, OpenMP over rows" % (k, len(batches[0]), dt)}
@@ -1301,7 +1376,8 @@ def main():
         sub.steps, sub.warmup = min(args.steps, 200), max(3, min(args.warmup, 5))
         t = run_tiny(sub, rank, world, torch, dist)
         res["cache_path"] = {k: t[k] for k in ("value", "unit", "steps", "ms_per_step", "ratio",
-                                               "parity_all_rows_ok", "roofline", "e2e", "clocks")}
+                                               "parity_all_rows_ok", "single_batch_us", "roofline", "e2e",
+                                               "clocks")}
         res["cache_path"]["config"] = t["config"]["workload"]
     if rank == 0:
         print(json.dumps(res), flush=True)

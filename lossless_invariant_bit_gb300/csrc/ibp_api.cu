@@ -339,6 +339,8 @@ ibp_status ibp_compress(ibp_store* s, void* dst_slots, const void* src_rows, uin
   if (e != IBP_OK) return e;
   ibp::EncodeArgs a;
   a.m = view(s);
+  a.t5 = s->t5;
+  a.gtab = s->gtab;
   a.bitmap = s->bitmap;
   a.status = s->status;
   a.src = static_cast<const uint8_t*>(src_rows);

@@ -58,6 +58,8 @@ struct DecodeArgs {
 
 struct EncodeArgs {
   MetaView m;
+  const uint4* t5;        // per-word network descriptors (k_derive_fast), 2W entries
+  const uint32_t* gtab;   // group table: chunk | word in chunk << 16, then chunk starts
   uint32_t* bitmap;
   uint32_t* status;
   const uint8_t* src;
@@ -69,6 +71,8 @@ struct EncodeArgs {
   uint64_t slot;
   uint32_t* stored_out;
   uint32_t um0, um1, ush, ubv, ukeep;  // uniform store (the k_encode<true> form)
+  uint32_t chunk_lg;  // log2 of the rows a warp takes at a time: 5 (32 rows, one
+                      // raw-bitmap word) or 0 (one row; bitmap bits set by atomics)
 };
 
 struct CountArgs {

@@ -1181,14 +1181,17 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
   const uint64_t wpb = blockDim.x >> 5;
   const uint64_t stride = (uint64_t)gridDim.x * wpb;
 
-  // A warp takes 32 consecutive rows at a time (so with identity slots it owns
-  // one raw-bitmap word and writes it once, instead of 32 warps contending on
-  // it with atomics).  Rows up to 2 KB travel by cp.async into a ring of 4
-  // single-row stages, 3 rows ahead of the row being packed; larger rows are
-  // loaded when their turn comes.
+  // A warp takes rpc consecutive rows at a time: 32 for large batches with
+  // identity slots (the warp owns one raw-bitmap word and writes it once,
+  // instead of 32 warps contending on it with atomics), else 1 (small batches
+  // spread over many warps).  Rows up to 2 KB travel by cp.async into a ring
+  // of 4 single-row stages, 3 rows ahead of the row being packed; larger rows
+  // are fetched when their turn comes, every copy issued before any is awaited.
   constexpr bool use_ring = kVpl > 0;
   constexpr uint32_t S = kEncodeStages;
-  const uint64_t nchunk = (a.n + 31) >> 5;
+  const uint32_t lg = a.chunk_lg, rpc = 1u << lg;
+  const bool word_owner = lg == 5u && a.slot_ids == nullptr;
+  const uint64_t nchunk = (a.n + rpc - 1) >> lg;
   const uint64_t c0 = (uint64_t)blockIdx.x * wpb + wid;
   const uint32_t ring_sa = static_cast<uint32_t>(__cvta_generic_to_shared(rows)) + 16u * lane;
   auto issue = [&](uint64_t r, uint32_t stage) {  // row r into ring stage `stage`
@@ -1203,18 +1206,21 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
     }
     cp_async_commit();
   };
-  for (uint32_t t = 0; t + 1 < S; ++t) issue((c0 << 5) + t, t);  // a chunk has 32 >= S rows
+  // the warp's rows in order: chunk c0, c0 + stride, ... of rpc rows each
+  auto row_at = [&](uint64_t c, uint32_t p) {  // p rows after the start of chunk c
+    return ((c + (uint64_t)(p >> lg) * stride) << lg) + (p & (rpc - 1u));
+  };
+  for (uint32_t t = 0; t + 1 < S; ++t) issue(row_at(c0, t), t);
 
   uint64_t t = 0;  // the warp's row counter
   for (uint64_t c = c0; c < nchunk; c += stride) {
     uint32_t rawmask = 0, donemask = 0;
 #pragma unroll 1
-    for (uint32_t j = 0; j < 32u; ++j, ++t) {
-      const uint64_t i = (c << 5) + j;
+    for (uint32_t j = 0; j < rpc; ++j, ++t) {
+      const uint64_t i = (c << lg) + j;
       if (i >= a.n) break;
-      // the row S-1 ahead: later in this chunk or early in the warp's next one
-      issue(j + S - 1u < 32u ? i + S - 1u : ((c + stride) << 5) + (j + S - 1u - 32u),
-            (uint32_t)((t + S - 1u) % S));
+      // the row S-1 ahead: later in this chunk or in one of the warp's next ones
+      issue(j + S - 1u < rpc ? i + S - 1u : row_at(c, j + S - 1u), (uint32_t)((t + S - 1u) % S));
       cp_async_wait_n<S - 1>();  // row t has landed
       __syncwarp();
       uint32_t* xbuf = use_ring ? rows + (uint32_t)(t % S) * W : rows;
@@ -1286,13 +1292,32 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
         }
       }
       if (!done) {
-        if (!use_ring) {
-          const uint4* srow = reinterpret_cast<const uint4*>(a.src + i * a.src_stride);
-          for (uint32_t v = lane; v < nvec; v += 32) st_smem_v4(xbuf + 4u * v, ld_nc_v4(srow + v));
-        }
+        if (!use_ring)
+          fetch_vectors(static_cast<uint32_t>(__cvta_generic_to_shared(xbuf)),
+                        reinterpret_cast<const uint4*>(a.src + i * a.src_stride), 0u, nvec, lane);
         for (uint32_t k = lane; k < nch; k += 32) cinfo[k] = 0;
         __syncwarp();
-        if (kUni) {
+        // chunks of whole 4-word groups: the work goes by 16-byte groups (one
+        // table entry per group, 4 words' loads in flight together)
+        const bool by_group = (wpc & 3u) == 0u;
+        const uint32_t G = W >> 2;
+        if (by_group) {
+          const uint32_t msk = ~(a.um0 | a.um1);
+          for (uint32_t g = lane; g < G; g += 32) {
+            const uint4 x4 = *reinterpret_cast<const uint4*>(xbuf + 4u * g);
+            uint32_t d;
+            if (kUni) {
+              d = ((x4.x & msk) ^ a.ubv) | ((x4.y & msk) ^ a.ubv) | ((x4.z & msk) ^ a.ubv) |
+                  ((x4.w & msk) ^ a.ubv);
+            } else {
+              const uint4 m4 = __ldg(reinterpret_cast<const uint4*>(a.m.mask) + g);
+              const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(a.m.bitval) + g);
+              d = ((x4.x & m4.x) ^ b4.x) | ((x4.y & m4.y) ^ b4.y) | ((x4.z & m4.z) ^ b4.z) |
+                  ((x4.w & m4.w) ^ b4.w);
+            }
+            if (d) cinfo[__ldg(a.gtab + g) & 0xFFFFu] = 1u;  // mismatch flag
+          }
+        } else if (kUni) {
           const uint32_t msk = ~(a.um0 | a.um1);
           for (uint32_t w = lane; w < W; w += 32)
             if ((xbuf[w] & msk) != a.ubv) cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;  // mismatch flag
@@ -1328,7 +1353,60 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
           __syncwarp();
           for (uint32_t k = lane; k < nch; k += 32)
             if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
-          for (uint32_t w = lane; w < W; w += 32) {
+          auto put = [&](uint32_t v, uint32_t bit, uint32_t nbits) {
+            const uint32_t q = bit >> 5, sh = bit & 31u;
+            atomicOr(obuf + q, v << sh);
+            if (sh != 0u && sh + nbits > 32u) atomicOr(obuf + q + 1, v >> (32u - sh));
+          };
+          const uint32_t G4 = (G + 3u) & ~3u;
+          for (uint32_t g = lane; by_group && g < G; g += 32) {
+            const uint32_t gd = __ldg(a.gtab + g);
+            const uint32_t k = gd & 0xFFFFu;
+            const uint32_t ci = cinfo[k];
+            const uint32_t start = ci & 0x7FFFFFFFu;
+            const uint4 x4 = *reinterpret_cast<const uint4*>(xbuf + 4u * g);
+            const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+            if (ci >> 31) {  // packed chunk: word w's kept bits at its all-packed offset + delta
+              const uint32_t delta = start - __ldg(a.gtab + G4 + k);
+              if (kUni) {
+                uint32_t bit = start + (gd >> 16) * a.ukeep;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const uint32_t v = ((xs[e] & a.um0) >> (a.ush & 31u)) |
+                                     ((xs[e] & a.um1) >> (a.ush >> 8));
+                  if (a.ukeep) put(v, bit, a.ukeep);
+                  bit += a.ukeep;
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const uint4 t0 = __ldg(a.t5 + (2u * (uint32_t)e) * G + g);
+                  const uint4 t1 = __ldg(a.t5 + (2u * (uint32_t)e + 1u) * G + g);
+                  uint32_t x = xs[e] & t1.y;  // the kept bits, gathered to the low end
+                  uint32_t t = x & t0.x;
+                  x = (x ^ t) | (t >> 1);
+                  t = x & t0.y;
+                  x = (x ^ t) | (t >> 2);
+                  t = x & t0.z;
+                  x = (x ^ t) | (t >> 4);
+                  t = x & t0.w;
+                  x = (x ^ t) | (t >> 8);
+                  t = x & t1.x;
+                  x = (x ^ t) | (t >> 16);
+                  const uint32_t nb = __popc(t1.y);
+                  if (nb) put(x, t1.w + delta, nb);
+                }
+              }
+            } else {  // raw chunk: the 4 words verbatim
+              uint32_t bit = start + ((gd >> 16) << 5);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                put(xs[e], bit, 32u);
+                bit += 32u;
+              }
+            }
+          }
+          for (uint32_t w = lane; !by_group && w < W; w += 32) {
             const uint32_t krw = __ldg(a.m.kr + w);  // chunk | word in chunk << 16
             const uint32_t ci = cinfo[krw & 0xFFFFu];
             const bool packed = (ci >> 31) != 0u;
@@ -1360,7 +1438,7 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
             dslot[v] = *reinterpret_cast<const uint4*>(obuf + 4u * v);
         }
       }
-      if (a.slot_ids) {
+      if (!word_owner) {
         if (lane == 0) {
           const uint32_t bitm = 1u << ((uint64_t)slot & 31u);
           if (raw)
@@ -1375,7 +1453,7 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
       if (lane == 0 && a.stored_out) a.stored_out[i] = raw ? R : 4u * words;
       __syncwarp();
     }
-    if (!a.slot_ids && lane == 0 && donemask) {
+    if (word_owner && lane == 0 && donemask) {
       if (donemask == 0xFFFFFFFFu) {
         a.bitmap[c] = rawmask;  // this warp wrote every row of the word
       } else {
@@ -1787,9 +1865,12 @@ cudaError_t launch_encode_v(const EncodeArgs& a, int sm_count, cudaStream_t st) 
   const size_t smem = (size_t)4u * L.total_words * warps;
   const int bps = blocks_per_sm(k_encode<kUni, kVpl>, threads, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = ((a.n + 31) / 32 + warps - 1) / warps;  // 32-row chunks per warp
+  // 32-row chunks only when there are enough of them to fill every warp
+  EncodeArgs b = a;
+  b.chunk_lg = (a.slot_ids == nullptr && a.n >= 32ull * warps * blocks) ? 5u : 0u;
+  const uint64_t need = (((a.n + (1ull << b.chunk_lg) - 1) >> b.chunk_lg) + warps - 1) / warps;
   if (blocks > need) blocks = need;
-  k_encode<kUni, kVpl><<<(uint32_t)blocks, threads, smem, st>>>(a, L);
+  k_encode<kUni, kVpl><<<(uint32_t)blocks, threads, smem, st>>>(b, L);
   return cudaGetLastError();
 }
 
