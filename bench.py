@@ -809,6 +809,113 @@ def run_kv(args, rank, world, torch, dist):
     return res
 
 
+def run_weights(args, rank, world, torch, dist):
+    """bf16 weight offloading (the pages' LLM weight-offload stream): the
+    weights of L transformer layers of OPT-6.7B shape (q, k, v, o: 4096 x 4096;
+    fc1: 16384 x 4096; fc2: 4096 x 16384, all as rows of 4096 bf16 = 8 KB),
+    N(0, 0.02^2), compressed into pinned host slots, one store per matrix,
+    Mask/Bitval from a 1 % sample, chunk 256 B.  A step streams one layer's
+    six matrices back to HBM (six ibp_decompress launches, 384 MB of weights),
+    layers in turn."""
+    from lossless_invariant_bit_gb300 import dist as ibpdist
+    from lossless_invariant_bit_gb300 import ibp
+    from lossless_invariant_bit_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    args = argparse.Namespace(**vars(args))
+    args.steps = min(args.steps, 64)
+    L, R, C = args.weight_layers, 8192, 256
+    mats = [4096, 4096, 4096, 4096, 16384, 16384]  # rows per matrix
+    layer_rows = sum(mats)
+    t0 = time.time()
+    g = torch.Generator(device=dev)
+    stores, slots, stored_tot = [], [], 0
+    check = []
+    for layer in range(L):
+        for m, nr in enumerate(mats):
+            g.manual_seed(args.seed * 1000003 + layer * 8 + m)
+            w = (torch.randn((nr, 4096), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            wb = w.view(torch.uint8)
+            st = ibp.ibp_store_create(R, C, nr, 0)
+            sample = torch.from_numpy(wl.sample_ids(nr, 10, seed=layer * 8 + m)).to(dev)
+            ibp.ibp_build_meta(st, wb, R, sample, len(sample), 95, 100)
+            sl = torch.empty((nr, R), dtype=torch.uint8, pin_memory=True)
+            stored = torch.empty(nr, dtype=torch.int32, device=dev)
+            ibp.ibp_compress(st, sl, wb, R, None, nr, stored)
+            stored_tot += int(stored.sum().item())
+            if layer == 0:
+                check.append(wb.clone())
+            stores.append(st)
+            slots.append(sl)
+            del w, wb
+    torch.cuda.synchronize()
+    log("weight store ready in %.1fs" % (time.time() - t0))
+    ratio = stored_tot / (L * layer_rows * R)
+    out = torch.empty((layer_rows, R), dtype=torch.uint8, device=dev)
+    offs = np.cumsum([0] + mats)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def step(b):
+        layer = b % L
+        for m, nr in enumerate(mats):
+            k = layer * len(mats) + m
+            ibp.ibp_decompress(stores[k], out[offs[m]:offs[m + 1]], slots[k], None, nr, sp)
+
+    for b in range(args.warmup):
+        step(b)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    evs = []
+    with ClockSampler(dev.index) as clk:
+        for b in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(args.warmup + b)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    for st in stores:
+        assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    times = [a.elapsed_time(c) / 1e3 for a, c in evs]
+    t_total = ibpdist.max_over_ranks(sum(times), dist, dev)
+    value = layer_rows * R * args.steps * world / t_total / 1e9
+    step(0)
+    torch.cuda.synchronize()
+    parity_ok = all(bool(torch.equal(out[offs[m]:offs[m + 1]], check[m])) for m in range(len(mats)))
+    link = _link_probe(torch, ibp, slots[4], stream, sp, dev)
+    roof = min(measured_peaks()["hbm_gbs"], link / ratio)
+    res = {
+        "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
+        "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_total / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (seeded torch generator on the GPU: bf16 N(0, 0.02^2) weights)",
+        "config": {"workload": "bf16 weight offload: %d layers of OPT-6.7B shape (q, k, v, o, "
+                               "fc1, fc2; 384 MB per layer) in pinned host slots, chunk 256 B, "
+                               "1%% sample, T=0.95; one step = one layer's 6 matrices "
+                               "decompressed into HBM" % L,
+                   "row_bytes": R, "chunk_bytes": C, "launches_per_step": len(mats),
+                   "l2": "flushed between steps (256 MB write, outside the timed events)"},
+        "ratio": round(ratio, 5), "space_saving": round(1 - ratio, 4), "link_gbs": round(link, 2),
+        "parity_layer0_ok": parity_ok,
+        "roofline": {"bound": "link", "achieved": round(value / world, 2), "peak": round(roof, 2),
+                     "unit": "GB/s", "frac": round(value / world / roof, 4), "traffic": None,
+                     "kernel": "k_decode_fast<false, mode, big> (ibp_decompress, 8 KB rows)"},
+        "gpu_launches": len(mats) * args.steps,
+        "clocks": clk.summary(),
+    }
+    for st in stores:
+        ibp.ibp_store_destroy(st)
+    return res
+
+
 def run_dlrm(args, rank, world, torch, dist):
     """DLRM embedding lookup: 26 tables x 1,000,000 rows of fp32 ~ N(0, 0.01^2)
     (dim 128/256/512: 512 B - 2 KB rows) compressed into pinned host slots
@@ -1333,10 +1440,11 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--workload", default="sparse",
-                    choices=["sparse", "tiny", "kv", "dlrm", "transfers", "sweep"])
+                    choices=["sparse", "tiny", "kv", "dlrm", "transfers", "sweep", "weights"])
     ap.add_argument("--dlrm-dim", type=int, default=128, choices=[128, 256, 512])
     ap.add_argument("--dlrm-rows", type=int, default=1_000_000)
     ap.add_argument("--kv-layers", type=int, default=32)
+    ap.add_argument("--weight-layers", type=int, default=16)
     ap.add_argument("--replicas", type=int, default=128)
     ap.add_argument("--no-tuned", action="store_true",
                     help="skip the chunk-aware builder sub-result of the default workload")
@@ -1368,7 +1476,7 @@ def main():
     if dist:
         dist.barrier()
     run = {"tiny": run_tiny, "kv": run_kv, "dlrm": run_dlrm, "transfers": run_transfers,
-           "sweep": run_sweep}.get(args.workload, run_ours)
+           "sweep": run_sweep, "weights": run_weights}.get(args.workload, run_ours)
     res = run(args, rank, world, torch, dist)
     if args.workload == "sparse" and not args.no_cache_path:
         # the HBM cache path of the same metric, reported beside the host path

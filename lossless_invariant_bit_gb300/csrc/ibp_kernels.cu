@@ -908,9 +908,11 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       }
       const uint32_t need_vec = (4u * words + 15u) >> 4;
       if (need_vec > min_vec) {  // the raw chunks made the stream longer: second fetch
+        // (every copy issued before any is awaited: one round trip, not one per 512 bytes)
         const uint4* src = reinterpret_cast<const uint4*>(
             a.src + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u)));
-        for (uint32_t v = min_vec + lane; v < need_vec; v += 32) st_smem_v4(sb + 4u * v, ld_nc_v4(src + v));
+        fetch_vectors(static_cast<uint32_t>(__cvta_generic_to_shared(sb)), src, min_vec,
+                      need_vec, lane);
       }
       __syncwarp();
       for (uint32_t g = lane; g < G; g += 32) {
@@ -1103,8 +1105,8 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
         if (need_vec > en.min_vec) {
           const uint4* src = reinterpret_cast<const uint4*>(
               en.src + ((((uint64_t)(e.y & 0xFFFFFFu)) << 32) | (uint64_t)(e.x & ~15u)));
-          for (uint32_t v = en.min_vec + lane; v < need_vec; v += 32)
-            st_smem_v4(sb + 4u * v, ld_nc_v4(src + v));
+          fetch_vectors(static_cast<uint32_t>(__cvta_generic_to_shared(sb)), src, en.min_vec,
+                        need_vec, lane);
         }
         __syncwarp();
       }
@@ -1780,7 +1782,7 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   F.table_words = (kMode == kModeUniform || kMode == kModeUniform1) ? 0u : 8u * W;
   F.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
   F.sbuf_words = ((W + 8u) + 3u) & ~3u;
-  F.warp_words = kRingStages * F.sbuf_words + 256u + ((nch + 3u) & ~3u);
+  F.warp_words = F.S * F.sbuf_words + 256u + ((nch + 3u) & ~3u);
   F.min_bits = hp.min_bits;
   F.um0 = hp.um0;
   F.um1 = hp.um1;

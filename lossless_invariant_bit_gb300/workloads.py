@@ -17,6 +17,8 @@ stand-ins for their datasets):
   saving      rows with exactly k invariant bits per 32-bit word (space-saving
               sweep): the k high bits, equal in every word, or k scattered
               positions per word with a per-word constant
+  weights     bf16 weight matrices ~ N(0, 0.02^2) (rounded to nearest even),
+              rows of 4096 values (weight-offload stream)
 """
 from __future__ import annotations
 
@@ -27,7 +29,7 @@ import numpy as np
 BLOCK_ROWS = 65536
 
 _TAG = {"tiny": 1, "sparse": 2, "dense": 3, "dlrm": 4, "kv": 5, "ids": 6, "fuzz": 7,
-        "saving": 8}
+        "saving": 8, "weights": 9}
 
 
 def _rng(seed: int, tag: str, *more: int) -> np.random.Generator:
@@ -240,3 +242,17 @@ def invariant_rows(n: int, R: int, k: int, scattered: bool, seed: int = 0) -> np
     noise = _rng(seed, "saving", k, int(scattered), 1).integers(
         0, 1 << 32, size=(n, W), dtype=np.uint64).astype(np.uint32)
     return ((noise & keep[None, :]) | const[None, :]).view(np.uint8).reshape(n, R)
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns (uint16), round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def bf16_weight_rows(n_rows: int, cols: int = 4096, sigma: float = 0.02, seed: int = 0,
+                     matrix: int = 0) -> np.ndarray:
+    """Rows [n_rows, cols] of bf16 bit patterns of one weight matrix ~ N(0, sigma^2)."""
+    z = _rng(seed, "weights", matrix).standard_normal((n_rows, cols), dtype=np.float32)
+    return to_bf16_bits(z * np.float32(sigma))

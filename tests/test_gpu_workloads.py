@@ -254,3 +254,32 @@ def test_split_gather_rejects_other_geometries():
     finally:
         a.close()
         b.close()
+
+
+def test_bf16_weight_offload_stream():
+    """bf16 weight matrices (the weight-offload stream): the GPU builder and
+    compressor match the oracle, the dense decompression from host slots
+    returns the weights, and the saving is of the order the pages report."""
+    R, C, n = 8192, 256, 700
+    try_stores = []
+    try:
+        for m in range(2):
+            rb = wl.bf16_weight_rows(n, 4096, seed=5, matrix=m).view(np.uint8).reshape(n, R)
+            sample = wl.sample_ids(n, 100, seed=m)
+            st = Store(R, C, n)
+            try_stores.append(st)
+            slots, stored = _host_store(st, rb, sample)
+            mr, br = ref_c.build_meta(rb, 95, 100, sample_ids=sample)
+            mm, bb = st.meta()
+            assert np.array_equal(mm, mr) and np.array_equal(bb, br)
+            ref_sl, ref_bm, ref_st = oracle_slots(rb, C, mr, br, st.slot)
+            assert np.array_equal(stored, ref_st)
+            assert_streams_equal(slots.numpy(), ref_sl, ref_st)
+            assert 0.70 < stored.sum() / rb.size < 0.90
+            out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+            ibp.ibp_decompress(st.h, out, slots, None, n)
+            assert st.status() == ibp.IBP_OK
+            assert np.array_equal(out.cpu().numpy(), rb)
+    finally:
+        for st in try_stores:
+            st.close()
