@@ -698,7 +698,8 @@ __device__ __forceinline__ uint4 decode_packed_group(const uint4* tab, const uin
   return decode_group(tab, sb, g, G, delta, kMode == kModeNet5 || (kMode == kModeRuntime && net5));
 }
 
-constexpr uint32_t kRingStages = 4;  // rows per warp ring: 3 in flight while one decodes
+constexpr uint32_t kRingStages = 4;     // rows per warp ring: 3 in flight while one decodes
+constexpr uint32_t kRingStagesBig = 3;  // rows above 2 KB: 2 in flight, more warps per SM
 
 // Split output: where the 16-byte group g of a row lands, from the group
 // table entry (chunk k | word offset in the chunk << 16).
@@ -715,7 +716,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
   const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
-  constexpr uint32_t S = kRingStages;
+  constexpr uint32_t S = kBig ? kRingStagesBig : kRingStages;
   const uint32_t nvec = R >> 4;
   const uint32_t G = W >> 2;
   const uint32_t min_bits = kMode == kModeRuntime ? __ldg(a.m.scal) : F.min_bits;
@@ -806,7 +807,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       if ((fl & 13u) == 1u) {
         const uint32_t nv = (fl & 2u) ? nvec : min_vec;
         const uint8_t* src = src_lane + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u));
-        const uint32_t sa = ring_sa + 4u * (tt & (S - 1u)) * F.sbuf_words;
+        const uint32_t sa = ring_sa + 4u * (tt % S) * F.sbuf_words;
 #pragma unroll
         for (uint32_t j = 0; j < (kBig ? 16u : 4u); ++j)
           if (lane + 32u * j < nv)
@@ -836,7 +837,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       const uint4 e = rinfo[t & 63u];
       const uint32_t fl = e.x & 15u;
       uint4* drow = reinterpret_cast<uint4*>(a.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
-      uint32_t* sb = ring + (t & (S - 1u)) * F.sbuf_words;
+      uint32_t* sb = ring + (t % S) * F.sbuf_words;
       constexpr bool split = kSplit;
       if (fl & 12u) {
         if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
@@ -1778,7 +1779,7 @@ template <bool kIds, int kMode, bool kBig, bool kSplit>
 cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, cudaStream_t st) {
   FastParams F;
   const uint32_t W = a.m.W, nch = a.m.nch;
-  F.S = kRingStages;
+  F.S = kBig ? kRingStagesBig : kRingStages;
   F.table_words = (kMode == kModeUniform || kMode == kModeUniform1) ? 0u : 8u * W;
   F.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
   F.sbuf_words = ((W + 8u) + 3u) & ~3u;
@@ -1789,13 +1790,13 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   F.ush = hp.ush;
   F.ubv = hp.ubv;
   F.ukeep = hp.ukeep;
-  // 8 warps per CTA; rows above 2 KB take fewer where the rings would not fit
+  // 8 warps per CTA; rows above 2 KB take as many as their rings leave room for
   int warps = 8;
   size_t smem = 4ull * (F.table_words + F.gtab_words + 8 + (uint64_t)warps * F.warp_words);
   if (kBig) {
     const size_t cap = (size_t)max_smem_optin();
     while (warps > 1 && smem > cap) {
-      warps >>= 1;
+      --warps;
       smem = 4ull * (F.table_words + F.gtab_words + 8 + (uint64_t)warps * F.warp_words);
     }
     if (smem > cap) return cudaErrorInvalidConfiguration;
@@ -1803,7 +1804,9 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   auto kern = k_decode_fast<kIds, kMode, kBig, kSplit>;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = (a.n + 32ull * warps - 1) / (32ull * warps);  // >= 32 rows per warp
+  // at least 8 rows per warp (the ring's depth twice over), else as many CTAs
+  // as fit: a batch of a few thousand rows still spreads over every SM
+  const uint64_t need = (a.n + 8ull * warps - 1) / (8ull * warps);
   if (blocks > need) blocks = need;
   kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, F);
   return cudaGetLastError();
