@@ -38,9 +38,6 @@ __device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v, uint32_t lan
 
 __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) { return __ldg(p); }
 
-__device__ __forceinline__ void st_smem_v4(uint32_t* s, const uint4& v) {
-  *reinterpret_cast<uint4*>(s) = v;
-}
 
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -599,16 +596,17 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
 }
 
 // ------------------------------------------------------------------------
-// Fast decompression for rows of at most 2 KB whose chunks hold whole groups
-// of 4 words (C % 16 == 0): the common geometries (512 B - 2 KB
-// rows, chunks of 256 B / 1 KB / 4 KB).  Differences from k_decode:
+// Fast decompression for rows of at most 8 KB whose chunks hold whole groups
+// of 4 words (C % 16 == 0): the common geometries (512 B - 8 KB rows, chunks
+// of 256 B / 1 KB / 4 KB).  Differences from k_decode:
 //   - a warp resolves 32 rows at a time, one per lane (id -> offset -> raw
 //     bit, coalesced), the next 32 one chunk ahead, and then walks them one
-//     by one; each row's (offset, flags) reach the warp by one shuffle;
+//     by one; each row's (offset, flags) sit in a shared-memory ring;
 //   - the stored bytes travel by cp.async (.ca) into a ring of S single-row
 //     stages in shared memory, S-1 rows ahead of the row being decoded, so the
 //     bytes in flight cost no registers; this holds for HBM sources and for
-//     pinned host memory read over the link;
+//     pinned host memory read over the link (rows above 2 KB: the kBig
+//     instances, with a 3-row ring and up to 16 copies per lane);
 //   - a row whose chunks all participate (the usual case) needs no scan: word
 //     w's kept bits sit at a static offset (for a uniform store, one whose
 //     words all share the same ~Mask and Bitval, nch + w*keep);
@@ -1202,7 +1200,7 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
       const uint8_t* src = a.src + r * a.src_stride + 16u * lane;
       const uint32_t sa = ring_sa + 4u * stage * W;
 #pragma unroll
-      for (uint32_t q = 0; q < (uint32_t)kVpl; ++q)
+      for (int q = 0; q < kVpl; ++q)
         if (lane + 32u * q < nvec)
           asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * q),
                        "l"(src + 512u * q));
@@ -1246,7 +1244,7 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
         const uint32_t msk = ~(a.um0 | a.um1);
         uint32_t diff = 0;
 #pragma unroll
-        for (uint32_t q = 0; q < (uint32_t)kVpl; ++q) {
+        for (int q = 0; q < kVpl; ++q) {
           if (lane + 32u * q < nvec) {
             cur[q] = *reinterpret_cast<const uint4*>(xbuf + 4u * (lane + 32u * q));
             diff |= ((cur[q].x & msk) ^ a.ubv) | ((cur[q].y & msk) ^ a.ubv) |
@@ -1263,7 +1261,7 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
         }
         if (done && raw) {
 #pragma unroll
-          for (uint32_t q = 0; q < (uint32_t)kVpl; ++q)
+          for (int q = 0; q < kVpl; ++q)
             if (lane + 32u * q < nvec) dslot[lane + 32u * q] = cur[q];
         } else if (done) {
           const uint32_t padded = (words + 3u) & ~3u;
@@ -1273,7 +1271,7 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
           __syncwarp();
           if (a.ukeep) {
 #pragma unroll
-            for (uint32_t q = 0; q < (uint32_t)kVpl; ++q) {
+            for (int q = 0; q < kVpl; ++q) {
               if (lane + 32u * q < nvec) {
                 const uint32_t xs[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
                 uint32_t bit = nch + 4u * (lane + 32u * q) * a.ukeep;
@@ -1804,9 +1802,11 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   auto kern = k_decode_fast<kIds, kMode, kBig, kSplit>;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  // at least 8 rows per warp (the ring's depth twice over), else as many CTAs
-  // as fit: a batch of a few thousand rows still spreads over every SM
-  const uint64_t need = (a.n + 8ull * warps - 1) / (8ull * warps);
+  // rows per warp at least 32 (one resolve chunk; measured best for batches of
+  // a few thousand rows up to 2 KB) or, above 2 KB, 8 (a few thousand such
+  // rows still spread over every SM); else as many CTAs as fit
+  const uint64_t rpw = kBig ? 8ull : 32ull;
+  const uint64_t need = (a.n + rpw * warps - 1) / (rpw * warps);
   if (blocks > need) blocks = need;
   kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, F);
   return cudaGetLastError();
