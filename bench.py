@@ -747,9 +747,9 @@ def run_kv(args, rank, world, torch, dist):
         nh = len(hist)
         outh = torch.empty((nh, R), dtype=torch.uint8, device=dev)
 
-        def comp():
+        def comp(stream_handle=sp):
             for st, sl, nr in zip(stores, slots, newrows):
-                ibp.ibp_compress(st, sl, nr[:, s_], (T - P) * R, sids, B, stored1, sp)
+                ibp.ibp_compress(st, sl, nr[:, s_], (T - P) * R, sids, B, stored1, stream_handle)
 
         def fetch():
             for st, sl in zip(stores, slots):
@@ -768,6 +768,20 @@ def run_kv(args, rank, world, torch, dist):
             if rep_:  # the first is a warm-up
                 tc.append(e[0].elapsed_time(e[1]) / 1e3)
                 tf.append(e[1].elapsed_time(e[2]) / 1e3)
+        # the same 64 compress calls replayed from one CUDA graph
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph):
+            comp(torch.cuda.current_stream().cuda_stream)
+        tgr = []
+        for rep_ in range(4):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record(stream)
+            gph.replay()
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            if rep_:
+                tgr.append(e[0].elapsed_time(e[1]) / 1e3)
+        del gph
         for st in stores:
             assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
         ibp.ibp_gather_decompress(stores[0], outh, slots[0], None, hist, nh, sp)
@@ -776,6 +790,7 @@ def run_kv(args, rank, world, torch, dist):
         ok = bool(torch.equal(got[:, :P], check) and torch.equal(got[:, P:], newrows[0][:, :s_ + 1]))
         decode.append({"step": s_, "history_rows_per_store": nh,
                        "compress_us": round(statistics.median(tc) * 1e6, 1),
+                       "compress_us_cuda_graph": round(statistics.median(tgr) * 1e6, 1),
                        "compress_gbs": round(2 * L * B * R / statistics.median(tc) / 1e9, 2),
                        "fetch_gbs": round(2 * L * nh * R / statistics.median(tf) / 1e9, 2),
                        "parity_layer0_ok": ok})

@@ -192,7 +192,12 @@ IBP_API ibp_status ibp_compress(ibp_store* store, void* dst_slots, const void* s
  * Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA; corrupt streams and misaligned
  * offsets set the status word.  Calls on one store from several host threads
  * are safe for decompression; building or setting the Mask/Bitval or the
- * bitmap while other calls use the store is not. */
+ * bitmap while other calls use the store is not.  The decompression and
+ * compression calls may be captured into a CUDA graph once the store's
+ * properties have reached the host (after any such call that follows the
+ * Mask/Bitval build and a synchronisation of its stream; earlier captures
+ * run the slower forms that read them on the device); the builder calls may
+ * not be captured. */
 IBP_API ibp_status ibp_decompress(const ibp_store* store, void* dst, const void* src,
                           const uint64_t* offsets, uint64_t n, ibp_stream_t stream);
 

@@ -3,6 +3,7 @@
 // Lossless Compression for ML -- Extended" (gist.science explainer, Technical
 // Summary, Methodology > Core Algorithm and System Integration); see ibp.h
 // for the contract of each entry point.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -22,6 +23,7 @@ struct ibp_store {
   uint32_t* gtab;
   uint32_t* h_scal;       // pinned host mirror of scal, filled after each derive
   cudaEvent_t props_ev;   // completes when h_scal is current
+  std::atomic<int> props_ready{0};  // 1 once props_ev was seen complete (reset by derive)
   uint64_t bitmap_words;
 };
 
@@ -69,16 +71,29 @@ ibp_status derive(ibp_store* s, cudaStream_t st) {
                                        s->ckeep, s->scal, s->t2, s->t5, s->gtab, s->W, s->wpc,
                                        s->nch, st));
   if (e != IBP_OK) return e;
+  s->props_ready.store(0);
   e = cu(cudaMemcpyAsync(s->h_scal, s->scal, 16 * sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
   if (e != IBP_OK) return e;
   return cu(cudaEventRecord(s->props_ev, st));
 }
 
-ibp::HostProps host_props(const ibp_store* s) {
+// The store's properties as the host knows them.  Once the mirror has been
+// seen current no query is made, so calls captured into a CUDA graph (where
+// querying an event is not allowed) use it; a capture before that runs the
+// decoders' runtime forms.
+ibp::HostProps host_props(const ibp_store* s, cudaStream_t st) {
   ibp::HostProps hp = {};
-  if (cudaEventQuery(s->props_ev) != cudaSuccess) {
-    cudaGetLastError();  // cudaErrorNotReady: not known yet
-    return hp;
+  if (s->props_ready.load() != 1) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return hp;
+    }
+    if (cudaEventQuery(s->props_ev) != cudaSuccess) {
+      cudaGetLastError();  // cudaErrorNotReady: not known yet
+      return hp;
+    }
+    const_cast<ibp_store*>(s)->props_ready.store(1);
   }
   const volatile uint32_t* h = s->h_scal;
   hp.known = true;
@@ -132,7 +147,7 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.chunk_stride = split.chunk_stride;
   a.group_rows = split.group_rows;
   a.group_stride = split.group_stride;
-  return cu(ibp::launch_decode(a, host_props(s), s->sm_count, st));
+  return cu(ibp::launch_decode(a, host_props(s, st), s->sm_count, st));
 }
 
 }  // namespace
@@ -351,8 +366,8 @@ ibp_status ibp_compress(ibp_store* s, void* dst_slots, const void* src_rows, uin
   a.dst = static_cast<uint8_t*>(dst_slots);
   a.slot = s->slot;
   a.stored_out = stored_bytes_out;
-  return cu(ibp::launch_encode(a, host_props(s), s->sm_count,
-                               reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cu(ibp::launch_encode(a, host_props(s, st), s->sm_count, st));
 }
 
 ibp_status ibp_decompress(const ibp_store* s, void* dst, const void* src, const uint64_t* offsets,
@@ -447,7 +462,7 @@ ibp_status ibp_group_create(ibp_group** out, ibp_store* const* stores, const voi
       e = IBP_ECUDA;
       break;
     }
-    const ibp::HostProps hp = host_props(s);
+    const ibp::HostProps hp = host_props(s, 0);
     ibp::GroupEntry& g = h[t];
     g.src = static_cast<const uint8_t*>(srcs[t]);
     g.bitmap = s->bitmap;

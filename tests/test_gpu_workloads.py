@@ -283,3 +283,51 @@ def test_bf16_weight_offload_stream():
     finally:
         for st in try_stores:
             st.close()
+
+
+def test_decode_step_captured_in_a_cuda_graph():
+    """A KV decode step (compress the step's new rows into their slots, then
+    gather the history) captured once in a CUDA graph and replayed with new
+    rows: every replay's gather returns the rows it just compressed."""
+    R, C, B, T = 8192, 256, 4, 96
+    N = B * T
+    rows = wl.kv_rows(1, 1, B, range(T), seed=9).view(np.uint8).reshape(N, R)
+    st = Store(R, C, N)
+    try:
+        prompt = (np.arange(B)[:, None] * T + np.arange(64)[None, :]).reshape(-1)
+        slots, _ = _host_store(st, rows, prompt)
+        new = torch.zeros((B, R), dtype=torch.uint8, device=DEV)
+        sids = torch.zeros(B, dtype=torch.int64, device=DEV)
+        ids = torch.from_numpy(np.arange(N, dtype=np.int64)).to(DEV)
+        out = torch.zeros((N, R), dtype=torch.uint8, device=DEV)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # warm-up: store properties and launch shapes known
+            ibp.ibp_compress(st.h, slots, new, R, sids, B, None, side)
+            ibp.ibp_gather_decompress(st.h, out, slots, None, ids, N, side)
+        torch.cuda.synchronize()
+        ibp.ibp_compress(st.h, slots, torch.from_numpy(rows[:B]).to(DEV), R,
+                         torch.arange(B, dtype=torch.int64, device=DEV), B, None)
+        torch.cuda.synchronize()
+        assert st.status() == ibp.IBP_OK
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            sp = torch.cuda.current_stream()
+            ibp.ibp_compress(st.h, slots, new, R, sids, B, None, sp)
+            ibp.ibp_gather_decompress(st.h, out, slots, None, ids, N, sp)
+        expect = rows.copy()
+        gen = np.random.default_rng(11)
+        for step in range(3):
+            t = 64 + step
+            tok = (np.arange(B) * T + t).astype(np.int64)
+            fresh = wl.kv_rows(1, 1, B, [T + 100 + step], seed=9).view(np.uint8).reshape(B, R).copy()
+            fresh[gen.integers(0, B)] = gen.integers(0, 256, R, dtype=np.uint8)  # one raw row
+            new.copy_(torch.from_numpy(fresh))
+            sids.copy_(torch.from_numpy(tok))
+            g.replay()
+            torch.cuda.synchronize()
+            assert st.status() == ibp.IBP_OK
+            expect[tok] = fresh
+            assert np.array_equal(out.cpu().numpy(), expect), step
+    finally:
+        st.close()
