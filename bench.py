@@ -1352,6 +1352,24 @@ def run_transfers(args, rank, world, torch, dist):
         gran.append({"row_bytes": X, "rows_per_us": round(ng / t / 1e6, 1),
                      "gbs": round(ng * X / t / 1e9, 2)})
     del out_g
+    # the link's other directions, by the same copy kernel: HBM -> pinned host
+    # (GPU stores over the link) and pinned host -> pinned host through the GPU
+    # (reads and writes at once: the ceiling of an end-to-end call whose
+    # inputs and outputs both live in host memory)
+    host_dst = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dirs = {}
+    for name, dst_, src_ in (("hbm_to_host", host_dst, probe_dst),
+                             ("host_to_host_via_gpu", host_dst, probe_src)):
+        bestd = None
+        for _ in range(5):
+            ev[0].record(stream)
+            ibp.ibp_link_copy(dst_, src_, 1 << 30, sp)
+            ev[1].record(stream)
+            ev[1].synchronize()
+            tt = ev[0].elapsed_time(ev[1]) / 1e3
+            bestd = tt if bestd is None else min(bestd, tt)
+        dirs[name + "_gbs"] = round((1 << 30) / bestd / 1e9, 2)
+    del host_dst
     head = res_sizes["512"]["gpu_aligned"]
     return {
         "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
@@ -1363,6 +1381,7 @@ def run_transfers(args, rank, world, torch, dist):
         "link_limit_gbs": round((1 << 30) / best / 1e9, 2),
         "by_row_bytes": res_sizes,
         "read_granularity": gran,
+        "link_directions": dirs,
     }
 
 
