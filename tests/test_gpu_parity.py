@@ -591,3 +591,30 @@ def test_gather_through_hbm_cache_front(stores, R, C):
     o = out.cpu().numpy()
     hit = np.isin(ids, cached)
     assert np.array_equal(o[hit, :R], b[ids[hit]])
+
+
+@pytest.mark.parametrize("n", [8192, 8193, 20_000, 3 * 8192 - 1])
+def test_pack_offsets_across_tiles(stores, n):
+    """The packed-cache offset scan runs in tiles of 8192 rows: offsets over
+    several tiles and a ragged last tile equal the oracle's packing, and the
+    packed cache decodes to the rows."""
+    R, C = 64, 16
+    b = wl.fuzz_rows(n, R, seed=n)
+    st = stores(R, C, n, R)
+    d = to_dev(b)
+    ibp.ibp_build_meta(st.h, d, R, None, n, 9, 10)
+    slots, stored = gpu_compress(st, d, n)
+    mr, br = st.meta()
+    ref_sl, _, ref_st = oracle_slots(b, C, mr, br, R)
+    assert np.array_equal(stored, ref_st)
+    _, offs_ref = ref_c.pack_slots(ref_sl, ref_st)
+    offs = torch.zeros(n + 1, dtype=torch.int64, device=DEV)
+    ibp.ibp_pack(st.h, None, offs, slots, to_dev(stored.astype(np.int32)), n)
+    total = int(offs[-1].item())
+    assert np.array_equal(offs.cpu().numpy().astype(np.uint64), offs_ref)
+    packed = torch.zeros(total + R, dtype=torch.uint8, device=DEV)
+    ibp.ibp_pack(st.h, packed, offs, slots, to_dev(stored.astype(np.int32)), n)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, packed, offs, n)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
