@@ -347,3 +347,28 @@ def test_corrupt_stream_detected():
     bad = w2b([0x0, 0x0, 0x0, 0x0, 0x0])
     assert ref_c.decompress_row(bad, False, 16, 4, mask, bitval) is None
     assert py.decompress(bad, False, 16, 4, list(mask), list(bitval)) is None
+
+
+def test_pack_slots_layout():
+    """The packed cache: every row starts on a 16-byte boundary right after the
+    previous row's bytes rounded up, the last offset is the total, and the
+    stored bytes (not the rest of the slot) are what is copied; a packed
+    cache decodes to the rows."""
+    n, R, C = 300, 96, 32
+    rows = wl.fuzz_rows(n, R, seed=8)
+    mask, bitval = ref_c.build_meta(rows, 9, 10)
+    slots = np.full((n, R), 0xAB, np.uint8)
+    bitmap = np.zeros((n + 31) // 32, np.uint32)
+    stored = ref_c.compress_batch(rows, C, mask, bitval, slots, bitmap, nthreads=2)
+    packed, offs = ref_c.pack_slots(slots, stored)
+    assert offs[0] == 0 and len(offs) == n + 1
+    for i in range(n):
+        assert offs[i] % 16 == 0
+        assert offs[i + 1] - offs[i] == -(-int(stored[i]) // 16) * 16
+        assert np.array_equal(packed[offs[i]:offs[i] + stored[i]], slots[i, :stored[i]])
+    assert offs[-1] == len(packed)
+    for i in (0, 1, n // 2, n - 1):
+        raw = bool((bitmap[i >> 5] >> (i & 31)) & 1)
+        got = py.decompress(bytes(packed[offs[i]:offs[i] + stored[i]]), raw, R, C, list(mask),
+                            list(bitval))
+        assert got == rows[i].tobytes()
