@@ -308,8 +308,8 @@ def run_ours(args, rank, world, torch, dist):
         cmap_dev = torch.from_numpy(cmap_np).to(dev)
 
         def step_front(b):
-            ibp.ibp_gather_decompress_cached(store.st, out, R, store.slots, cache, cmap_dev,
-                                             ids_dev[b % pool], n, sp)
+            ibp.ibp_gather_decompress_cached(store.st, out, R, store.slots, cache, n_cache,
+                                             cmap_dev, ids_dev[b % pool], n, sp)
 
         fsteps = min(args.steps, 200)
         for b in range(args.warmup):

@@ -270,11 +270,14 @@ IBP_API ibp_status ibp_gather_decompress_split(const ibp_store* store, void* dst
  * cache slot cache_src + cache_map[id]*slot_bytes, otherwise from
  * host_src + id*slot_bytes over the host link -- in one launch.  The cache
  * holds copies of the store's slots (same stride, same raw bitmap).
+ *   cache_slots  slots in the cache; a map entry >= cache_slots sets IBP_ERANGE
+ *                and zeroes the row instead of reading past the cache
  *   cache_map  device int64[n_rows]: cache slot of each row, -1 if not cached
  * Errors: as ibp_gather_decompress_strided. */
 IBP_API ibp_status ibp_gather_decompress_cached(const ibp_store* store, void* dst,
                                                 uint64_t dst_stride_bytes, const void* host_src,
-                                                const void* cache_src, const int64_t* cache_map,
+                                                const void* cache_src, uint64_t cache_slots,
+                                                const int64_t* cache_map,
                                                 const int64_t* ids, uint64_t n,
                                                 ibp_stream_t stream);
 

@@ -116,6 +116,7 @@ struct SplitOut {
 ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void* src,
                   const uint64_t* offsets, const int64_t* ids, uint64_t n, cudaStream_t st,
                   const int64_t* cache_map = nullptr, const void* cache_src = nullptr,
+                  uint64_t cache_slots = 0,
                   SplitOut split = SplitOut()) {
   if (!s) return IBP_EINVAL;
   if (n == 0) return IBP_OK;
@@ -144,6 +145,7 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.dst_stride = dst_stride;
   a.cache_map = cache_map;
   a.cache_src = static_cast<const uint8_t*>(cache_src);
+  a.cache_slots = cache_slots;
   a.chunk_stride = split.chunk_stride;
   a.group_rows = split.group_rows;
   a.group_stride = split.group_stride;
@@ -406,18 +408,18 @@ ibp_status ibp_gather_decompress_split(const ibp_store* s, void* dst, uint64_t g
   sp.group_rows = group_rows;
   sp.group_stride = group_stride;
   return decode(s, dst, row_stride, src, offsets, ids, n, reinterpret_cast<cudaStream_t>(stream),
-                nullptr, nullptr, sp);
+                nullptr, nullptr, 0, sp);
 }
 
 ibp_status ibp_gather_decompress_cached(const ibp_store* s, void* dst, uint64_t dst_stride,
                                         const void* host_src, const void* cache_src,
-                                        const int64_t* cache_map, const int64_t* ids, uint64_t n,
-                                        ibp_stream_t stream) {
+                                        uint64_t cache_slots, const int64_t* cache_map,
+                                        const int64_t* ids, uint64_t n, ibp_stream_t stream) {
   if (!ids && n) return IBP_EINVAL;
   if (n && (!cache_map || !cache_src)) return IBP_EINVAL;
   if (cache_src && !aligned16(cache_src)) return IBP_EALIGN;
   return decode(s, dst, dst_stride, host_src, nullptr, ids, n,
-                reinterpret_cast<cudaStream_t>(stream), cache_map, cache_src);
+                reinterpret_cast<cudaStream_t>(stream), cache_map, cache_src, cache_slots);
 }
 
 ibp_status ibp_pack(const ibp_store* s, void* dst_packed, uint64_t* offsets_out,

@@ -49,6 +49,7 @@ struct DecodeArgs {
   uint64_t dst_stride;
   const int64_t* cache_map;  // NULL, or per row id: its slot in the HBM cache, -1 if none
   const uint8_t* cache_src;  // the HBM cache's slots (stride `slot`)
+  uint64_t cache_slots;      // slots in the HBM cache; a map entry beyond it is an error
   // split output (chunk_stride != 0): output row i = g*group_rows + r puts its
   // chunk k at dst + g*group_stride + r*dst_stride + k*chunk_stride
   uint64_t chunk_stride;

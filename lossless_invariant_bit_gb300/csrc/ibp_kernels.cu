@@ -485,11 +485,15 @@ __global__ void __launch_bounds__(1024) k_derive_fast(const uint32_t* nm, const 
 // a slot, or -- with a cache map -- the row's slot in the HBM cache when it
 // has one (the unsigned difference of the two bases wraps, so a.src + result
 // addresses the cache).
+constexpr uint64_t kBadSource = ~0ull;  // a cache map entry past the cache's slots
+
 __device__ __forceinline__ uint64_t source_offset(const DecodeArgs& a, int64_t id) {
   if (a.cache_map) {
     const int64_t cs = __ldg(a.cache_map + id);
-    if (cs >= 0)
+    if (cs >= 0) {
+      if ((uint64_t)cs >= a.cache_slots) return kBadSource;
       return (uint64_t)((uintptr_t)a.cache_src - (uintptr_t)a.src) + (uint64_t)cs * a.slot;
+    }
   }
   return a.offsets ? __ldg(a.offsets + id) : (uint64_t)id * a.slot;
 }
@@ -535,6 +539,11 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
       continue;
     }
     const uint64_t off = source_offset(a, id);
+    if (off == kBadSource) {
+      if (lane == 0) set_status(a.status, IBP_ERANGE);
+      zero_row(drow, nvec, lane);
+      continue;
+    }
     if (off & 15u) {
       if (lane == 0) set_status(a.status, IBP_EALIGN);
       zero_row(drow, nvec, lane);
@@ -777,7 +786,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
     uint32_t fl = 0;
     uint64_t off = 0;
     if (pin) {
-      if (pid < 0 || (uint64_t)pid >= a.n_rows) {
+      if (pid < 0 || (uint64_t)pid >= a.n_rows || poff == kBadSource) {
         fl = 1u | 4u;
       } else if (poff & 15u) {
         fl = 1u | 8u;

@@ -54,7 +54,7 @@ _SIGS = {
     "ibp_gather_decompress": [_P, _P, _P, _P, _P, _U64, _P],
     "ibp_gather_decompress_strided": [_P, _P, _U64, _P, _P, _P, _U64, _P],
     "ibp_pack": [_P, _P, _P, _P, _P, _U64, _P],
-    "ibp_gather_decompress_cached": [_P, _P, _U64, _P, _P, _P, _P, _U64, _P],
+    "ibp_gather_decompress_cached": [_P, _P, _U64, _P, _P, _U64, _P, _P, _U64, _P],
     "ibp_gather_decompress_split": [_P, _P, _U64, _U64, _U64, _U64, _P, _P, _P, _U64, _P],
     "ibp_group_create": [ctypes.POINTER(ctypes.c_void_p), _P, _P, _U32],
     "ibp_group_destroy": [_P],
@@ -209,9 +209,9 @@ def ibp_gather_decompress_split(store: int, dst, group_rows: int, group_stride: 
 
 
 def ibp_gather_decompress_cached(store: int, dst, dst_stride_bytes: int, host_src, cache_src,
-                                 cache_map, ids, n: int, stream=None) -> None:
+                                 cache_slots: int, cache_map, ids, n: int, stream=None) -> None:
     _check(_lib_handle().ibp_gather_decompress_cached(store, _ptr(dst), dst_stride_bytes,
-                                                      _ptr(host_src), _ptr(cache_src),
+                                                      _ptr(host_src), _ptr(cache_src), cache_slots,
                                                       _ptr(cache_map), _ptr(ids), n,
                                                       _stream(stream)),
            "ibp_gather_decompress_cached")

@@ -49,13 +49,13 @@ def test_host_side_argument_checks(lib):
     assert lib.ibp_decompress(None, 16, 16, None, 1, None) == ibp.IBP_EINVAL
     assert lib.ibp_gather_decompress(None, 16, 16, None, 16, 1, None) == ibp.IBP_EINVAL
     assert lib.ibp_gather_decompress_strided(None, 16, 16, 16, None, 16, 1, None) == ibp.IBP_EINVAL
-    assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, 16, 16, 16, 1, None) == ibp.IBP_EINVAL
+    assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, 16, 1, 16, 16, 1, None) == ibp.IBP_EINVAL
     assert lib.ibp_gather_decompress_split(None, 16, 1, 0, 16, 256, 16, None, 16, 1,
                                            None) == ibp.IBP_EINVAL
     # a cache front needs both its map and its cache, the cache 16-byte aligned
-    assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, 16, None, 16, 1, None) == ibp.IBP_EINVAL
-    assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, None, 16, 16, 1, None) == ibp.IBP_EINVAL
-    assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, 17, 16, 16, 1, None) == ibp.IBP_EALIGN
+    assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, 16, 1, None, 16, 1, None) == ibp.IBP_EINVAL
+    assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, None, 1, 16, 16, 1, None) == ibp.IBP_EINVAL
+    assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, 17, 1, 16, 16, 1, None) == ibp.IBP_EALIGN
     assert lib.ibp_pack(None, None, 16, None, None, 0, None) == ibp.IBP_EINVAL
     assert lib.ibp_meta_get(None, 16, 16) == ibp.IBP_EINVAL
     assert lib.ibp_meta_set(None, 16, 16) == ibp.IBP_EINVAL

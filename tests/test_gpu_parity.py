@@ -577,19 +577,32 @@ def test_gather_through_hbm_cache_front(stores, R, C):
     ids = g.integers(0, N, size=5 * N // 2).astype(np.int64)
     stride = R + 32
     out = torch.zeros((len(ids), stride), dtype=torch.uint8, device=DEV)
-    ibp.ibp_gather_decompress_cached(st.h, out, stride, host, cache, to_dev(cmap), to_dev(ids),
-                                     len(ids))
+    ibp.ibp_gather_decompress_cached(st.h, out, stride, host, cache, len(cached), to_dev(cmap),
+                                     to_dev(ids), len(ids))
     assert st.status() == ibp.IBP_OK
     o = out.cpu().numpy()
     assert np.array_equal(o[:, :R], b[ids]) and np.all(o[:, R:] == 0)
     # the cache really is read: poison the host copies of the cached rows
     host[torch.from_numpy(cached)] = 0xEE
     out.zero_()
-    ibp.ibp_gather_decompress_cached(st.h, out, stride, host, cache, to_dev(cmap), to_dev(ids),
-                                     len(ids))
+    ibp.ibp_gather_decompress_cached(st.h, out, stride, host, cache, len(cached), to_dev(cmap),
+                                     to_dev(ids), len(ids))
     assert st.status() == ibp.IBP_OK
     o = out.cpu().numpy()
     hit = np.isin(ids, cached)
+    assert np.array_equal(o[hit, :R], b[ids[hit]])
+    # a map entry past the cache's slots is an error, not a read past the cache
+    bad = int(cached[0])
+    ids[0] = bad
+    cmap[bad] = len(cached) + 5
+    out.fill_(0x77)
+    ibp.ibp_gather_decompress_cached(st.h, out, stride, host, cache, len(cached), to_dev(cmap),
+                                     to_dev(ids), len(ids))
+    assert st.status() == ibp.IBP_ERANGE
+    o = out.cpu().numpy()
+    isbad = ids == bad
+    assert np.all(o[isbad, :R] == 0)
+    hit = np.isin(ids, cached) & ~isbad
     assert np.array_equal(o[hit, :R], b[ids[hit]])
 
 
