@@ -1,6 +1,7 @@
 """Build libibp.so in-tree with nvcc for sm_103a (GB300).
 
-Two translation units (kernels, C-ABI) compile in parallel, then link into a
+The translation units (kernels, C-ABI, allocation-free builder, transfer
+baselines) compile in parallel, then link into a
 shared library beside this file.  The CUDA runtime is linked statically, so
 the library loads without any other CUDA library on the path.
 """

@@ -117,7 +117,7 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
                   const uint64_t* offsets, const int64_t* ids, uint64_t n, cudaStream_t st,
                   const int64_t* cache_map = nullptr, const void* cache_src = nullptr,
                   uint64_t cache_slots = 0,
-                  SplitOut split = SplitOut()) {
+                  SplitOut split = SplitOut(), const int64_t* out_pos = nullptr) {
   if (!s) return IBP_EINVAL;
   if (n == 0) return IBP_OK;
   if (!dst || !src) return IBP_EINVAL;
@@ -149,6 +149,7 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.chunk_stride = split.chunk_stride;
   a.group_rows = split.group_rows;
   a.group_stride = split.group_stride;
+  a.out_pos = out_pos;
   return cu(ibp::launch_decode(a, host_props(s, st), s->sm_count, st));
 }
 
@@ -409,6 +410,28 @@ ibp_status ibp_gather_decompress_split(const ibp_store* s, void* dst, uint64_t g
   sp.group_stride = group_stride;
   return decode(s, dst, row_stride, src, offsets, ids, n, reinterpret_cast<cudaStream_t>(stream),
                 nullptr, nullptr, 0, sp);
+}
+
+ibp_status ibp_gather_decompress_ordered(const ibp_store* s, void* dst, uint64_t dst_stride,
+                                         const void* src, const uint64_t* offsets,
+                                         const int64_t* ids, uint64_t n, void* workspace,
+                                         uint64_t workspace_bytes, ibp_stream_t stream) {
+  if (!s) return IBP_EINVAL;
+  if (n == 0) return IBP_OK;
+  if (!ids || !workspace || workspace_bytes < IBP_ORDER_WORKSPACE_BYTES(n)) return IBP_EINVAL;
+  if (!aligned16(workspace)) return IBP_EALIGN;
+  ibp_status e = on_device(s);
+  if (e != IBP_OK) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int64_t* ids_out = static_cast<int64_t*>(workspace);
+  int64_t* pos_out = ids_out + n;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(pos_out + n);
+  e = cu(cudaMemsetAsync(hist, 0, 4ull * ibp::kOrderBuckets, st));
+  if (e != IBP_OK) return e;
+  e = cu(ibp::launch_order_ids(ids, n, s->n_rows, ids_out, pos_out, hist, s->sm_count, st));
+  if (e != IBP_OK) return e;
+  return decode(s, dst, dst_stride, src, offsets, ids_out, n, st, nullptr, nullptr, 0, SplitOut(),
+                pos_out);
 }
 
 ibp_status ibp_gather_decompress_cached(const ibp_store* s, void* dst, uint64_t dst_stride,

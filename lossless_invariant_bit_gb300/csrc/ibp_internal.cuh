@@ -55,6 +55,10 @@ struct DecodeArgs {
   uint64_t chunk_stride;
   uint64_t group_rows;
   uint64_t group_stride;
+  // ordered gather (out_pos != NULL): ids come sorted by address region and
+  // row i lands at dst + out_pos[i]*dst_stride; warps take 32-row chunks in
+  // turn, so all of them sweep the sorted ids together
+  const int64_t* out_pos;
 };
 
 struct EncodeArgs {
@@ -174,6 +178,12 @@ cudaError_t launch_derive(uint32_t* mask, uint32_t* bitval, uint32_t* nm, uint32
                           uint32_t nch, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count,
                           cudaStream_t st);
+// Bucket the ids by address region (a counting sort on id * kOrderBuckets /
+// n_rows): ids_out, in bucket order, and pos_out, each id's index in ids.
+// hist: kOrderBuckets zeroed counters.
+constexpr uint32_t kOrderBuckets = 1024;
+cudaError_t launch_order_ids(const int64_t* ids, uint64_t n, uint64_t n_rows, int64_t* ids_out,
+                             int64_t* pos_out, uint32_t* hist, int sm_count, cudaStream_t st);
 cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count,
                           cudaStream_t st);
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,

@@ -531,7 +531,8 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
   const uint64_t stride = (uint64_t)gridDim.x * wpb;
 
   for (uint64_t i = (uint64_t)blockIdx.x * wpb + wid; i < a.n; i += stride) {
-    uint4* drow = reinterpret_cast<uint4*>(a.dst + i * a.dst_stride);
+    const uint64_t orow = (kIds && a.out_pos) ? (uint64_t)__ldg(a.out_pos + i) : i;
+    uint4* drow = reinterpret_cast<uint4*>(a.dst + orow * a.dst_stride);
     const int64_t id = kIds ? __ldg(a.ids + i) : (int64_t)i;
     if (id < 0 || (uint64_t)id >= a.n_rows) {
       if (lane == 0) set_status(a.status, IBP_ERANGE);
@@ -757,24 +758,36 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
                                                                  : ((1u << (nch & 31u)) - 1u);
 
-  // this warp's rows: a contiguous, balanced share [r0, r0 + cnt) of [0, n)
+  // this warp's rows: a contiguous, balanced share [r0, r0 + cnt) of [0, n);
+  // ordered gathers: 32-row chunks gw, gw + nw, ... (cnt counts whole chunks,
+  // rows past n are absent)
   const uint64_t nw = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t gw = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
-  const uint64_t r0 = a.n * gw / nw;
-  const uint32_t cnt = (uint32_t)(a.n * (gw + 1) / nw - r0);
+  const bool ordered = kIds && a.out_pos != nullptr;
+  const uint64_t nq_all = (a.n + 31) >> 5;
+  const uint64_t r0 = ordered ? 0 : a.n * gw / nw;
+  const uint32_t cnt = ordered ? (gw < nq_all ? 32u * (uint32_t)((nq_all - 1 - gw) / nw + 1) : 0u)
+                               : (uint32_t)(a.n * (gw + 1) / nw - r0);
   if (cnt == 0) return;
+  auto row_base = [&](uint32_t q) -> uint64_t {
+    return ordered ? (gw + (uint64_t)q * nw) * 32u : r0 + 32ull * q;
+  };
 
   // Resolving chunk q (rows r0 + 32q + lane) is a chain of dependent loads
   // (id -> offset, raw bit); it runs in three steps spread over the chunk two
   // ahead, so the loads complete while other rows are decoded.
-  int64_t pid = 0;
+  int64_t pid = 0, ppos = 0;
   uint64_t poff = 0;
   uint32_t pbm = 0;
   bool pin = false;
   auto step_ids = [&](uint32_t q) {
     const uint32_t t = 32u * q + lane;
-    pin = q < (cnt + 31u) / 32u && t < cnt;
-    if (pin) pid = kIds ? __ldg(a.ids + r0 + t) : (int64_t)(r0 + t);
+    const uint64_t ri = row_base(q) + lane;
+    pin = q < (cnt + 31u) / 32u && t < cnt && ri < a.n;
+    if (pin) {
+      pid = kIds ? __ldg(a.ids + ri) : (int64_t)ri;
+      if (ordered) ppos = __ldg(a.out_pos + ri);
+    }
   };
   auto step_loads = [&]() {
     if (pin && pid >= 0 && (uint64_t)pid < a.n_rows) {
@@ -795,10 +808,11 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         off = poff;
       }
     }
-    const uint64_t ri = r0 + 32ull * q + lane;
-    const uint64_t dsto = !kSplit ? ri * a.dst_stride
-                                  : (ri / a.group_rows) * a.group_stride +
-                                        (ri % a.group_rows) * a.dst_stride;
+    const uint64_t ri = row_base(q) + lane;
+    const uint64_t dsto = ordered ? (uint64_t)ppos * a.dst_stride
+                          : !kSplit ? ri * a.dst_stride
+                                    : (ri / a.group_rows) * a.group_stride +
+                                          (ri % a.group_rows) * a.dst_stride;
     rinfo[((q & 1u) << 5) + lane] = make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32),
                                                (uint32_t)dsto, (uint32_t)(dsto >> 32));
   };
@@ -843,6 +857,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
     do {
       const uint4 e = rinfo[t & 63u];
       const uint32_t fl = e.x & 15u;
+      if (!(fl & 1u)) break;  // past the end of an ordered gather's last chunk
       uint4* drow = reinterpret_cast<uint4*>(a.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
       uint32_t* sb = ring + (t % S) * F.sbuf_words;
       constexpr bool split = kSplit;
@@ -1702,6 +1717,78 @@ WarpSmem encode_smem(uint32_t W, uint32_t nch) {
   L.xbuf_words = (W <= 512u ? kEncodeStages : 1u) * ((W + 3u) & ~3u);
   L.total_words = L.sbuf_words + L.xbuf_words + L.cinfo_words;
   return L;
+}
+
+// ------------------------------------------------------------------------
+// Ordered gathers.  A GPU reads pinned host memory through address
+// translation whose reach is limited: random gathers over a store larger than
+// that reach (measured on GB300: beyond ~20 GB of host slots) fall to a
+// fraction of the link, while the same gathers in address order keep it
+// busy.  The ids are bucketed by region (a counting sort on
+// id * kOrderBuckets / n_rows, order within a bucket arbitrary) and the
+// decoder's warps sweep the bucketed list together, each row written back to
+// its original output position.
+// ------------------------------------------------------------------------
+namespace {
+
+__device__ __forceinline__ uint32_t order_bucket(int64_t id, uint64_t n_rows) {
+  if (id < 0 || (uint64_t)id >= n_rows) return 0;  // flagged by the decoder later
+  return (uint32_t)((uint64_t)id * kOrderBuckets / n_rows);
+}
+
+__global__ void __launch_bounds__(256) k_order_count(const int64_t* ids, uint64_t n,
+                                                     uint64_t n_rows, uint32_t* hist) {
+  __shared__ uint32_t h[kOrderBuckets];
+  for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) h[b] = 0;
+  __syncthreads();
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (uint64_t)gridDim.x * blockDim.x)
+    atomicAdd(&h[order_bucket(__ldg(ids + i), n_rows)], 1u);
+  __syncthreads();
+  for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x)
+    if (h[b]) atomicAdd(hist + b, h[b]);
+}
+
+// counts -> exclusive starts, in place (one block of kOrderBuckets threads)
+__global__ void __launch_bounds__(1024) k_order_scan(uint32_t* hist) {
+  __shared__ uint32_t part[kOrderBuckets];
+  const uint32_t t = threadIdx.x;
+  const uint32_t v = hist[t];
+  part[t] = v;
+  __syncthreads();
+  for (uint32_t d = 1; d < kOrderBuckets; d <<= 1) {
+    const uint32_t x = t >= d ? part[t - d] : 0u;
+    __syncthreads();
+    part[t] += x;
+    __syncthreads();
+  }
+  hist[t] = part[t] - v;
+}
+
+__global__ void __launch_bounds__(256) k_order_scatter(const int64_t* ids, uint64_t n,
+                                                       uint64_t n_rows, uint32_t* cursor,
+                                                       int64_t* ids_out, int64_t* pos_out) {
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    const int64_t id = __ldg(ids + i);
+    const uint32_t p = atomicAdd(cursor + order_bucket(id, n_rows), 1u);
+    ids_out[p] = id;
+    pos_out[p] = (int64_t)i;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_order_ids(const int64_t* ids, uint64_t n, uint64_t n_rows, int64_t* ids_out,
+                             int64_t* pos_out, uint32_t* hist, int sm_count, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  uint64_t blocks = (uint64_t)sm_count * 4;
+  const uint64_t need = (n + 255) / 256;
+  if (blocks > need) blocks = need;
+  k_order_count<<<(uint32_t)blocks, 256, 0, st>>>(ids, n, n_rows, hist);
+  k_order_scan<<<1, kOrderBuckets, 0, st>>>(hist);
+  k_order_scatter<<<(uint32_t)blocks, 256, 0, st>>>(ids, n, n_rows, hist, ids_out, pos_out);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_count_ones(const CountArgs& a, int sm_count, cudaStream_t st) {

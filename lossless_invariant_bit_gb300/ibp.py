@@ -55,6 +55,7 @@ _SIGS = {
     "ibp_gather_decompress_strided": [_P, _P, _U64, _P, _P, _P, _U64, _P],
     "ibp_pack": [_P, _P, _P, _P, _P, _U64, _P],
     "ibp_gather_decompress_cached": [_P, _P, _U64, _P, _P, _U64, _P, _P, _U64, _P],
+    "ibp_gather_decompress_ordered": [_P, _P, _U64, _P, _P, _P, _U64, _P, _U64, _P],
     "ibp_gather_decompress_split": [_P, _P, _U64, _U64, _U64, _U64, _P, _P, _P, _U64, _P],
     "ibp_group_create": [ctypes.POINTER(ctypes.c_void_p), _P, _P, _U32],
     "ibp_group_destroy": [_P],
@@ -206,6 +207,20 @@ def ibp_gather_decompress_split(store: int, dst, group_rows: int, group_stride: 
                                                      _ptr(offsets), _ptr(ids), n,
                                                      _stream(stream)),
            "ibp_gather_decompress_split")
+
+
+def order_workspace_bytes(n: int) -> int:
+    """Bytes of workspace ibp_gather_decompress_ordered needs for n ids."""
+    return 16 * int(n) + 4096
+
+
+def ibp_gather_decompress_ordered(store: int, dst, dst_stride_bytes: int, src, offsets, ids,
+                                  n: int, workspace, workspace_bytes: int, stream=None) -> None:
+    _check(_lib_handle().ibp_gather_decompress_ordered(store, _ptr(dst), dst_stride_bytes,
+                                                       _ptr(src), _ptr(offsets), _ptr(ids), n,
+                                                       _ptr(workspace), workspace_bytes,
+                                                       _stream(stream)),
+           "ibp_gather_decompress_ordered")
 
 
 def ibp_gather_decompress_cached(store: int, dst, dst_stride_bytes: int, host_src, cache_src,

@@ -631,3 +631,46 @@ def test_pack_offsets_across_tiles(stores, n):
     ibp.ibp_decompress(st.h, out, packed, offs, n)
     assert st.status() == ibp.IBP_OK
     assert np.array_equal(out.cpu().numpy(), b)
+
+
+@pytest.mark.parametrize("R,C,n", [(512, 1024, 5000), (512, 256, 33), (8192, 256, 700),
+                                   (400, 100, 1500), (512, 1024, 1)])
+def test_ordered_gather_matches_gather(stores, R, C, n):
+    """The ordered gather (ids bucketed by address, rows written back to their
+    own positions) gives the plain gather's bytes, duplicates, a strided output
+    and an out-of-range id included, on the fast and the generic decoders."""
+    N = 3000
+    b = wl.fuzz_rows(N, R, seed=R + n)
+    st = stores(R, C, N)
+    d = to_dev(b)
+    ibp.ibp_build_meta(st.h, d, R, None, N, 9, 10)
+    slots, _ = gpu_compress(st, d, N, host=True)
+    g = np.random.default_rng(n)
+    ids = g.integers(0, N, size=n).astype(np.int64)
+    ids[n // 2] = N + 3 if n > 2 else ids[n // 2]
+    stride = R + 48
+    ref = torch.full((n, stride), 0x5A, dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress_strided(st.h, ref, stride, slots, None, to_dev(ids), n)
+    s_ref = st.status()
+    out = torch.full((n, stride), 0x5A, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(ibp.order_workspace_bytes(n), dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress_ordered(st.h, out, stride, slots, None, to_dev(ids), n, ws,
+                                      ws.numel())
+    assert st.status() == s_ref
+    assert torch.equal(out, ref)
+    ok = (ids >= 0) & (ids < N)
+    assert np.array_equal(out.cpu().numpy()[ok, :R], b[ids[ok]])
+
+
+def test_ordered_gather_checks_its_workspace(stores):
+    st = stores(512, 1024, 100)
+    buf = torch.zeros(1 << 16, dtype=torch.uint8, device=DEV)
+    ids = torch.zeros(64, dtype=torch.int64, device=DEV)
+    with pytest.raises(ibp.IbpError) as e:
+        ibp.ibp_gather_decompress_ordered(st.h, buf, 512, buf, None, ids, 64, buf,
+                                          ibp.order_workspace_bytes(64) - 16)
+    assert e.value.status == ibp.IBP_EINVAL
+    with pytest.raises(ibp.IbpError) as e:
+        ibp.ibp_gather_decompress_ordered(st.h, buf, 512, buf, None, ids, 64,
+                                          buf.data_ptr() + 8, ibp.order_workspace_bytes(64))
+    assert e.value.status == ibp.IBP_EALIGN
