@@ -244,6 +244,21 @@ IBP_API ibp_status ibp_group_gather_decompress(const ibp_group* group, void* dst
                                                uint64_t dst_row_stride, const int64_t* ids,
                                                uint64_t batch, ibp_stream_t stream);
 
+/* As ibp_group_gather_decompress, in address order (see
+ * ibp_gather_decompress_ordered): the batch*T items are bucketed by store
+ * and by region within it, then decoded bucket by bucket, each to its own
+ * place in dst.  For groups whose slots together exceed the GPU's reach into
+ * host memory (DLRM tables of 1-2 KB rows: 26-53 GB).
+ *   workspace  device memory of IBP_ORDER_WORKSPACE_BYTES(batch*T) bytes,
+ *              16-byte aligned
+ * Errors: as ibp_group_gather_decompress; IBP_EINVAL for a missing or short
+ * workspace, IBP_EALIGN for a misaligned one. */
+IBP_API ibp_status ibp_group_gather_decompress_ordered(const ibp_group* group, void* dst,
+                                                       uint64_t dst_row_stride,
+                                                       const int64_t* ids, uint64_t batch,
+                                                       void* workspace, uint64_t workspace_bytes,
+                                                       ibp_stream_t stream);
+
 /* Gather-decompression into a layout that splits each row by chunks (the
  * KV-cache fetch of System Integration, decompressed straight into the
  * attention layout): output row i = g*group_rows + r puts its chunk k (C

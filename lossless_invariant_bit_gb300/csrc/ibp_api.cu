@@ -573,7 +573,47 @@ ibp_status ibp_group_gather_decompress(const ibp_group* g, void* dst, uint64_t d
   a.dst_row_stride = dst_row_stride;
   a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
   a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u);
+  a.order = nullptr;
   return cu(ibp::launch_group(a, g->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ibp_status ibp_group_gather_decompress_ordered(const ibp_group* g, void* dst,
+                                               uint64_t dst_row_stride, const int64_t* ids,
+                                               uint64_t batch, void* workspace,
+                                               uint64_t workspace_bytes, ibp_stream_t stream) {
+  if (!g) return IBP_EINVAL;
+  if (batch == 0) return IBP_OK;
+  if (!dst || !ids) return IBP_EINVAL;
+  if (!aligned16(dst) || (dst_row_stride & 15u) || dst_row_stride < (uint64_t)g->T * g->R)
+    return IBP_EALIGN;
+  const uint64_t n_items = batch * g->T;
+  if (!workspace || workspace_bytes < IBP_ORDER_WORKSPACE_BYTES(n_items)) return IBP_EINVAL;
+  if (!aligned16(workspace)) return IBP_EALIGN;
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) return IBP_ECUDA;
+  if (d != g->device) return IBP_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int64_t* order = static_cast<int64_t*>(workspace);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(order + 2 * n_items);
+  ibp_status e = cu(cudaMemsetAsync(hist, 0, 4ull * ibp::kOrderBuckets, st));
+  if (e != IBP_OK) return e;
+  e = cu(ibp::launch_order_items(g->entries, g->T, ids, n_items, order, hist, g->sm_count, st));
+  if (e != IBP_OK) return e;
+  ibp::GroupArgs a;
+  a.entries = g->entries;
+  a.T = g->T;
+  a.R = g->R;
+  a.W = g->W;
+  a.wpc = g->wpc;
+  a.nch = g->nch;
+  a.ids = ids;
+  a.n_items = n_items;
+  a.dst = static_cast<uint8_t*>(dst);
+  a.dst_row_stride = dst_row_stride;
+  a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
+  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u);
+  a.order = order;
+  return cu(ibp::launch_group(a, g->sm_count, st));
 }
 
 ibp_status ibp_meta_get(const ibp_store* s, uint32_t* mask_host, uint32_t* bitval_host) {

@@ -152,6 +152,7 @@ struct GroupArgs {
   uint64_t dst_row_stride;
   uint32_t sbuf_words;
   uint32_t warp_words;
+  const int64_t* order;     // NULL, or the items in address order (ordered gather)
 };
 
 cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st);
@@ -184,6 +185,11 @@ cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count
 constexpr uint32_t kOrderBuckets = 1024;
 cudaError_t launch_order_ids(const int64_t* ids, uint64_t n, uint64_t n_rows, int64_t* ids_out,
                              int64_t* pos_out, uint32_t* hist, int sm_count, cudaStream_t st);
+// The same for a group's items (b, t): bucket t * (kOrderBuckets / T) plus the
+// region of ids[b*T + t] in store t; order_out receives the item indices.
+cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int64_t* ids,
+                               uint64_t n_items, int64_t* order_out, uint32_t* hist,
+                               int sm_count, cudaStream_t st);
 cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count,
                           cudaStream_t st);
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,

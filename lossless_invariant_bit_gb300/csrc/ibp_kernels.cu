@@ -1000,22 +1000,31 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
   const uint32_t nhw = (nch + 31u) >> 5;
   const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
                                                                  : ((1u << (nch & 31u)) - 1u);
+  // contiguous item shares, or (ordered) 32-item chunks gw, gw + nw, ...
   const uint64_t nw = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t gw = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
-  const uint64_t r0 = g.n_items * gw / nw;
-  const uint32_t cnt = (uint32_t)(g.n_items * (gw + 1) / nw - r0);
+  const bool ordered = g.order != nullptr;
+  const uint64_t nq_all = (g.n_items + 31) >> 5;
+  const uint64_t r0 = ordered ? 0 : g.n_items * gw / nw;
+  const uint32_t cnt = ordered ? (gw < nq_all ? 32u * (uint32_t)((nq_all - 1 - gw) / nw + 1) : 0u)
+                               : (uint32_t)(g.n_items * (gw + 1) / nw - r0);
   if (cnt == 0) return;
+  auto row_base = [&](uint32_t q) -> uint64_t {
+    return ordered ? (gw + (uint64_t)q * nw) * 32u : r0 + 32ull * q;
+  };
 
   int64_t pid = 0;
-  uint64_t poff = 0;
+  uint64_t poff = 0, pitem = 0;
   uint32_t pbm = 0, pt = 0;
   bool pin = false;
   auto step_ids = [&](uint32_t q) {
     const uint32_t t = 32u * q + lane;
-    pin = q < (cnt + 31u) / 32u && t < cnt;
+    const uint64_t ri = row_base(q) + lane;
+    pin = q < (cnt + 31u) / 32u && t < cnt && ri < g.n_items;
     if (pin) {
-      pid = __ldg(g.ids + r0 + t);
-      pt = (uint32_t)((r0 + t) % T);
+      pitem = ordered ? (uint64_t)__ldg(g.order + ri) : ri;
+      pid = __ldg(g.ids + pitem);
+      pt = (uint32_t)(pitem % T);
     }
   };
   auto step_loads = [&]() {
@@ -1035,8 +1044,7 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
         off = poff;
       }
     }
-    const uint64_t i = r0 + 32ull * q + lane;
-    const uint64_t dsto = (i / T) * g.dst_row_stride + (uint64_t)pt * R;
+    const uint64_t dsto = (pitem / T) * g.dst_row_stride + (uint64_t)pt * R;
     rinfo[((q & 1u) << 5) + lane] = make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32) | (pt << 24),
                                                (uint32_t)dsto, (uint32_t)(dsto >> 32));
   };
@@ -1079,6 +1087,7 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
     do {
       const uint4 e = rinfo[t & 63u];
       const uint32_t fl = e.x & 15u;
+      if (!(fl & 1u)) break;  // past the end of an ordered gather's last chunk
       const GroupEntry& en = ent[e.y >> 24];
       uint4* drow = reinterpret_cast<uint4*>(g.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
       uint32_t* sb = ring + (t & (S - 1u)) * g.sbuf_words;
@@ -1788,6 +1797,58 @@ cudaError_t launch_order_ids(const int64_t* ids, uint64_t n, uint64_t n_rows, in
   k_order_count<<<(uint32_t)blocks, 256, 0, st>>>(ids, n, n_rows, hist);
   k_order_scan<<<1, kOrderBuckets, 0, st>>>(hist);
   k_order_scatter<<<(uint32_t)blocks, 256, 0, st>>>(ids, n, n_rows, hist, ids_out, pos_out);
+  return cudaGetLastError();
+}
+
+namespace {
+
+__device__ __forceinline__ uint32_t item_bucket(const GroupEntry* ent, uint32_t T, uint32_t bpt,
+                                                const int64_t* ids, uint64_t i) {
+  const uint32_t t = (uint32_t)(i % T);
+  const int64_t id = __ldg(ids + i);
+  const uint64_t nr = ent[t].n_rows;
+  const uint32_t r = (id < 0 || (uint64_t)id >= nr) ? 0u : (uint32_t)((uint64_t)id * bpt / nr);
+  return t * bpt + r;
+}
+
+__global__ void __launch_bounds__(256) k_order_items_count(const GroupEntry* ent, uint32_t T,
+                                                           const int64_t* ids, uint64_t n,
+                                                           uint32_t* hist) {
+  __shared__ uint32_t h[kOrderBuckets];
+  const uint32_t bpt = kOrderBuckets / T;
+  for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) h[b] = 0;
+  __syncthreads();
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (uint64_t)gridDim.x * blockDim.x)
+    atomicAdd(&h[item_bucket(ent, T, bpt, ids, i)], 1u);
+  __syncthreads();
+  for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x)
+    if (h[b]) atomicAdd(hist + b, h[b]);
+}
+
+__global__ void __launch_bounds__(256) k_order_items_scatter(const GroupEntry* ent, uint32_t T,
+                                                             const int64_t* ids, uint64_t n,
+                                                             uint32_t* cursor, int64_t* order) {
+  const uint32_t bpt = kOrderBuckets / T;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (uint64_t)gridDim.x * blockDim.x)
+    order[atomicAdd(cursor + item_bucket(ent, T, bpt, ids, i), 1u)] = (int64_t)i;
+}
+
+}  // namespace
+
+cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int64_t* ids,
+                               uint64_t n_items, int64_t* order_out, uint32_t* hist,
+                               int sm_count, cudaStream_t st) {
+  if (n_items == 0) return cudaSuccess;
+  if (T == 0 || T > kOrderBuckets) return cudaErrorInvalidValue;
+  uint64_t blocks = (uint64_t)sm_count * 4;
+  const uint64_t need = (n_items + 255) / 256;
+  if (blocks > need) blocks = need;
+  k_order_items_count<<<(uint32_t)blocks, 256, 0, st>>>(entries, T, ids, n_items, hist);
+  k_order_scan<<<1, kOrderBuckets, 0, st>>>(hist);
+  k_order_items_scatter<<<(uint32_t)blocks, 256, 0, st>>>(entries, T, ids, n_items, hist,
+                                                          order_out);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,7 @@ _SIGS = {
     "ibp_pack": [_P, _P, _P, _P, _P, _U64, _P],
     "ibp_gather_decompress_cached": [_P, _P, _U64, _P, _P, _U64, _P, _P, _U64, _P],
     "ibp_gather_decompress_ordered": [_P, _P, _U64, _P, _P, _P, _U64, _P, _U64, _P],
+    "ibp_group_gather_decompress_ordered": [_P, _P, _U64, _P, _U64, _P, _U64, _P],
     "ibp_gather_decompress_split": [_P, _P, _U64, _U64, _U64, _U64, _P, _P, _P, _U64, _P],
     "ibp_group_create": [ctypes.POINTER(ctypes.c_void_p), _P, _P, _U32],
     "ibp_group_destroy": [_P],
@@ -221,6 +222,14 @@ def ibp_gather_decompress_ordered(store: int, dst, dst_stride_bytes: int, src, o
                                                        _ptr(workspace), workspace_bytes,
                                                        _stream(stream)),
            "ibp_gather_decompress_ordered")
+
+
+def ibp_group_gather_decompress_ordered(group: int, dst, dst_row_stride: int, ids, batch: int,
+                                        workspace, workspace_bytes: int, stream=None) -> None:
+    _check(_lib_handle().ibp_group_gather_decompress_ordered(group, _ptr(dst), dst_row_stride,
+                                                             _ptr(ids), batch, _ptr(workspace),
+                                                             workspace_bytes, _stream(stream)),
+           "ibp_group_gather_decompress_ordered")
 
 
 def ibp_gather_decompress_cached(store: int, dst, dst_stride_bytes: int, host_src, cache_src,

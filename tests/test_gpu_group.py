@@ -151,3 +151,46 @@ def test_group_rejects_mixed_geometry():
     finally:
         for s in (a, b, c):
             s.close()
+
+
+def test_group_ordered_matches_group():
+    """The ordered group gather (items bucketed by store and region) writes the
+    plain group gather's bytes and status codes, an out-of-range id included."""
+    R, C, N, B = 512, 1024, 4000, 1500
+    stores, slots, tables = [], [], []
+    try:
+        for t in range(5):
+            rb = rows_u8(wl.dlrm_rows(N, R // 4, table=t, seed=7))
+            st, sl = _host_store(R, C, rb, wl.sample_ids(N, 50, seed=t), host=(t != 2))
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+        T = len(stores)
+        ids = np.stack([wl.zipf_ids(B, N, table=t, seed=8) for t in range(T)], axis=1)
+        ids[7, 3] = -4  # out of range in store 3
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            stride = T * R + 32
+            ref = torch.full((B, stride), 0x33, dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress(grp, ref, stride, to_dev(ids), B)
+            codes = [s.status() for s in stores]
+            assert codes[3] == ibp.IBP_ERANGE
+            out = torch.full((B, stride), 0x33, dtype=torch.uint8, device=DEV)
+            ws = torch.empty(ibp.order_workspace_bytes(B * T), dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress_ordered(grp, out, stride, to_dev(ids), B, ws,
+                                                    ws.numel())
+            assert [s.status() for s in stores] == codes
+            assert torch.equal(out, ref)
+            o = out.cpu().numpy()
+            for t in range(T):
+                ok = ids[:, t] >= 0
+                assert np.array_equal(o[ok, t * R:(t + 1) * R], tables[t][ids[ok, t]]), t
+            with pytest.raises(ibp.IbpError) as e:
+                ibp.ibp_group_gather_decompress_ordered(grp, out, stride, to_dev(ids), B, ws,
+                                                        ws.numel() - 16)
+            assert e.value.status == ibp.IBP_EINVAL
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()
