@@ -96,12 +96,20 @@ class IbpStore:
         return out
 
     def gather(self, src: torch.Tensor, ids: torch.Tensor, out: Optional[torch.Tensor] = None,
-               offsets: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        """Rows ids[i] (device int64) from slots or a packed cache, into [len(ids), R]."""
+               offsets: Optional[torch.Tensor] = None, ordered: bool = False,
+               stream=None) -> torch.Tensor:
+        """Rows ids[i] (device int64) from slots or a packed cache, into [len(ids), R].
+        ordered=True buckets the ids by address first (for host stores beyond the
+        GPU's translation reach, ~20 GB); the rows come out in the same order."""
         n = ids.numel()
         if out is None:
             out = torch.empty((n, self.row_bytes), dtype=torch.uint8, device=ids.device)
-        ibp.ibp_gather_decompress(self.handle, out, src, offsets, ids, n, stream)
+        if ordered:
+            ws = torch.empty(ibp.order_workspace_bytes(n), dtype=torch.uint8, device=ids.device)
+            ibp.ibp_gather_decompress_ordered(self.handle, out, out.stride(0), src, offsets, ids,
+                                              n, ws, ws.numel(), stream)
+        else:
+            ibp.ibp_gather_decompress(self.handle, out, src, offsets, ids, n, stream)
         return out
 
     def pack(self, slots: torch.Tensor, stored: torch.Tensor,

@@ -35,6 +35,7 @@ def test_store_round_trip(host):
         ids = torch.from_numpy(wl.uniform_ids(3 * n, n, seed=2)).to(DEV)
         got = st.gather(slots, ids)
         assert np.array_equal(got.cpu().numpy(), rb[ids.cpu().numpy()])
+        assert torch.equal(st.gather(slots, ids, ordered=True), got)
         cache, offs = st.pack(slots.to(DEV) if host else slots, stored)
         assert np.array_equal(st.gather(cache, ids, offsets=offs[:-1]).cpu().numpy(),
                               rb[ids.cpu().numpy()])
