@@ -57,6 +57,8 @@ extern "C" {
 #define IBP_NOALLOC_MAX_ROW_BYTES 8192u
 #define IBP_MAX_TUNE_CANDIDATES 8u
 #define IBP_MAX_GROUP_STORES 64u
+/* device workspace bytes of the ordered gathers for n ids (or batch*T items) */
+#define IBP_ORDER_WORKSPACE_BYTES(n) (16ull * (uint64_t)(n) + 4096ull)
 
 typedef enum {
   IBP_OK = 0,
@@ -279,7 +281,10 @@ IBP_API ibp_status ibp_gather_decompress_split(const ibp_store* store, void* dst
                                                uint64_t n, ibp_stream_t stream);
 
 /* Gather-decompression in address order, for stores larger than the GPU's
- * reach into host memory: as ibp_gather_decompress_strided, but the ids are
+ * reach into host memory.  The pages have no counterpart: it is the gather of
+ * System Integration (GPU-initiated zero-copy reads of compressed tensors),
+ * scheduled for this GPU's address translation.  As
+ * ibp_gather_decompress_strided, but the ids are
  * first bucketed by the region of the store they address (1024 regions, a
  * counting sort in the workspace) and the rows decoded region by region, each
  * written to its own output row.  A GPU reads pinned host memory through
@@ -291,7 +296,6 @@ IBP_API ibp_status ibp_gather_decompress_split(const ibp_store* store, void* dst
  *              aligned, used during the call (stream-ordered)
  * Errors: as ibp_gather_decompress_strided; IBP_EINVAL for a missing or
  * short workspace, IBP_EALIGN for a misaligned one. */
-#define IBP_ORDER_WORKSPACE_BYTES(n) (16ull * (uint64_t)(n) + 4096ull)
 IBP_API ibp_status ibp_gather_decompress_ordered(const ibp_store* store, void* dst,
                                                  uint64_t dst_stride_bytes,
                                                  const void* host_or_dev_src,
