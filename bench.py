@@ -655,6 +655,7 @@ def run_kv(args, rank, world, torch, dist):
     prompt_ids = torch.from_numpy(
         (np.arange(B)[:, None] * T + np.arange(P)[None, :]).reshape(-1).astype(np.int64)).to(dev)
     check = None
+    kv_lengths = []  # each store's stored sizes, attached to it
     newrows = []  # rows of the decode tokens 1920..2047, kept on the GPU for the decode steps
     for layer in range(L):
         for kv in range(2):
@@ -671,6 +672,8 @@ def run_kv(args, rank, world, torch, dist):
             stored = torch.empty(rows_per, dtype=torch.int32, device=dev)
             ibp.ibp_compress(st, sl, xb, R, None, rows_per, stored)
             ratio_num += int(stored[:].view(B, T)[:, :P].sum().item())
+            ibp.ibp_store_set_lengths(st, stored)  # kept current by the decode-step compress
+            kv_lengths.append(stored)
             if layer == 0 and kv == 0:
                 check = xb.view(B, T, R)[:, :P].clone()
             newrows.append(xb.view(B, T, R)[:, P:].clone())
@@ -870,7 +873,7 @@ def run_weights(args, rank, world, torch, dist):
     t0 = time.time()
     g = torch.Generator(device=dev)
     stores, slots, stored_tot = [], [], 0
-    check = []
+    check, lengths = [], []
     for layer in range(L):
         for m, nr in enumerate(mats):
             g.manual_seed(args.seed * 1000003 + layer * 8 + m)
@@ -883,6 +886,8 @@ def run_weights(args, rank, world, torch, dist):
             stored = torch.empty(nr, dtype=torch.int32, device=dev)
             ibp.ibp_compress(st, sl, wb, R, None, nr, stored)
             stored_tot += int(stored.sum().item())
+            ibp.ibp_store_set_lengths(st, stored)  # whole streams in one fetch
+            lengths.append(stored)
             if layer == 0:
                 check.append(wb.clone())
             stores.append(st)

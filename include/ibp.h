@@ -280,6 +280,20 @@ IBP_API ibp_status ibp_gather_decompress_split(const ibp_store* store, void* dst
                                                const uint64_t* offsets, const int64_t* ids,
                                                uint64_t n, ibp_stream_t stream);
 
+/* Attach (or, with NULL, detach) a table of each slot's stored bytes: device
+ * uint32[n_rows], as ibp_compress writes to stored_bytes_out, owned by the
+ * caller and kept current by it.  With the table a decompression fetches each
+ * row's whole stream at once; without it the first fetch is the shortest
+ * stream any compressed row can have and rows whose raw chunks made theirs
+ * longer need a second round trip (over the host link, a second wait).  The
+ * pages keep only the raw bitmap on the GPU; the table is 4 bytes per row of
+ * HBM.  A wrong entry costs time, not bytes: fetches are clamped to
+ * [shortest stream, R] and the stream's own header decides what is decoded
+ * (a packed cache then needs R readable bytes after each row, as for corrupt
+ * streams).  Not for use while other calls run on the store.
+ * Errors: IBP_EINVAL (NULL store). */
+IBP_API ibp_status ibp_store_set_lengths(ibp_store* store, const uint32_t* lengths);
+
 /* Gather-decompression in address order, for stores larger than the GPU's
  * reach into host memory.  The pages have no counterpart: it is the gather of
  * System Integration (GPU-initiated zero-copy reads of compressed tensors),

@@ -24,6 +24,7 @@ struct ibp_store {
   uint32_t* h_scal;       // pinned host mirror of scal, filled after each derive
   cudaEvent_t props_ev;   // completes when h_scal is current
   std::atomic<int> props_ready{0};  // 1 once props_ev was seen complete (reset by derive)
+  const uint32_t* lengths = nullptr;  // caller's stored bytes per slot (device), or NULL
   uint64_t bitmap_words;
 };
 
@@ -150,6 +151,7 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.group_rows = split.group_rows;
   a.group_stride = split.group_stride;
   a.out_pos = out_pos;
+  a.lengths = s->lengths;
   return cu(ibp::launch_decode(a, host_props(s, st), s->sm_count, st));
 }
 
@@ -410,6 +412,12 @@ ibp_status ibp_gather_decompress_split(const ibp_store* s, void* dst, uint64_t g
   sp.group_stride = group_stride;
   return decode(s, dst, row_stride, src, offsets, ids, n, reinterpret_cast<cudaStream_t>(stream),
                 nullptr, nullptr, 0, sp);
+}
+
+ibp_status ibp_store_set_lengths(ibp_store* s, const uint32_t* lengths) {
+  if (!s) return IBP_EINVAL;
+  s->lengths = lengths;
+  return IBP_OK;
 }
 
 ibp_status ibp_gather_decompress_ordered(const ibp_store* s, void* dst, uint64_t dst_stride,

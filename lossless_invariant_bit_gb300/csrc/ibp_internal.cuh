@@ -59,6 +59,9 @@ struct DecodeArgs {
   // row i lands at dst + out_pos[i]*dst_stride; warps take 32-row chunks in
   // turn, so all of them sweep the sorted ids together
   const int64_t* out_pos;
+  // NULL, or each row id's stored bytes (in HBM): the first fetch then takes
+  // the whole stream, so rows with raw chunks need no second round trip
+  const uint32_t* lengths;
 };
 
 struct EncodeArgs {

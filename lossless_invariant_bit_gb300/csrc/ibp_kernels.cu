@@ -561,7 +561,10 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
       zero_row(drow, nvec, lane);
       continue;
     }
-    fetch_vectors(sbuf_sa, srow, 0u, min_vec, lane);
+    // the first fetch: the whole stream when its length is known, else the shortest one
+    const uint32_t first =
+        a.lengths ? min(max((__ldg(a.lengths + id) + 15u) >> 4, min_vec), nvec) : min_vec;
+    fetch_vectors(sbuf_sa, srow, 0u, first, lane);
     // chunk starts: exclusive scan of the chunk sizes, 32 chunks per pass
     uint32_t run = nch;
     for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
@@ -583,7 +586,7 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, WarpSmem L) {
       continue;
     }
     const uint32_t need_vec = (4u * words + 15u) >> 4;
-    if (need_vec > min_vec) fetch_vectors(sbuf_sa, srow, min_vec, need_vec, lane);
+    if (need_vec > first) fetch_vectors(sbuf_sa, srow, first, need_vec, lane);
     for (uint32_t v = lane; v < nvec; v += 32) {
       uint32_t o[4];
 #pragma unroll
@@ -778,7 +781,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   // ahead, so the loads complete while other rows are decoded.
   int64_t pid = 0, ppos = 0;
   uint64_t poff = 0;
-  uint32_t pbm = 0;
+  uint32_t pbm = 0, plen = 0;
   bool pin = false;
   auto step_ids = [&](uint32_t q) {
     const uint32_t t = 32u * q + lane;
@@ -793,6 +796,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
     if (pin && pid >= 0 && (uint64_t)pid < a.n_rows) {
       poff = source_offset(a, pid);
       pbm = __ldg(a.bitmap + (pid >> 5));
+      if (a.lengths) plen = __ldg(a.lengths + pid);
     }
   };
   auto step_store = [&](uint32_t q) {
@@ -813,8 +817,14 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
                           : !kSplit ? ri * a.dst_stride
                                     : (ri / a.group_rows) * a.group_stride +
                                           (ri % a.group_rows) * a.dst_stride;
-    rinfo[((q & 1u) << 5) + lane] = make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32),
-                                               (uint32_t)dsto, (uint32_t)(dsto >> 32));
+    // vectors of the first fetch: the raw row, the whole stream when its length
+    // is known, else the shortest stream; they ride in the top 12 bits of the
+    // output offset's high word (output offsets stay below 2^52)
+    const uint32_t nv = (fl & 2u) ? nvec
+                        : a.lengths ? min(max((plen + 15u) >> 4, min_vec), nvec) : min_vec;
+    rinfo[((q & 1u) << 5) + lane] =
+        make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32), (uint32_t)dsto,
+                   ((uint32_t)(dsto >> 32) & 0xFFFFFu) | (nv << 20));
   };
   // copy row tt into ring stage tt % S (one commit group, empty past the end);
   // rows of at most 2 KB: four predicated 16-byte copies per lane; larger
@@ -826,7 +836,7 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       const uint4 e = rinfo[tt & 63u];
       const uint32_t fl = e.x & 15u;
       if ((fl & 13u) == 1u) {
-        const uint32_t nv = (fl & 2u) ? nvec : min_vec;
+        const uint32_t nv = e.w >> 20;
         const uint8_t* src = src_lane + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u));
         const uint32_t sa = ring_sa + 4u * (tt % S) * F.sbuf_words;
 #pragma unroll
@@ -858,7 +868,8 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       const uint4 e = rinfo[t & 63u];
       const uint32_t fl = e.x & 15u;
       if (!(fl & 1u)) break;  // past the end of an ordered gather's last chunk
-      uint4* drow = reinterpret_cast<uint4*>(a.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
+      uint4* drow = reinterpret_cast<uint4*>(
+          a.dst + ((((uint64_t)(e.w & 0xFFFFFu)) << 32) | (uint64_t)e.z));
       uint32_t* sb = ring + (t % S) * F.sbuf_words;
       constexpr bool split = kSplit;
       if (fl & 12u) {
@@ -930,11 +941,12 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         break;
       }
       const uint32_t need_vec = (4u * words + 15u) >> 4;
-      if (need_vec > min_vec) {  // the raw chunks made the stream longer: second fetch
+      const uint32_t fetched = e.w >> 20;
+      if (need_vec > fetched) {  // the raw chunks made the stream longer: second fetch
         // (every copy issued before any is awaited: one round trip, not one per 512 bytes)
         const uint4* src = reinterpret_cast<const uint4*>(
             a.src + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u)));
-        fetch_vectors(static_cast<uint32_t>(__cvta_generic_to_shared(sb)), src, min_vec,
+        fetch_vectors(static_cast<uint32_t>(__cvta_generic_to_shared(sb)), src, fetched,
                       need_vec, lane);
       }
       __syncwarp();

@@ -56,6 +56,7 @@ _SIGS = {
     "ibp_pack": [_P, _P, _P, _P, _P, _U64, _P],
     "ibp_gather_decompress_cached": [_P, _P, _U64, _P, _P, _U64, _P, _P, _U64, _P],
     "ibp_gather_decompress_ordered": [_P, _P, _U64, _P, _P, _P, _U64, _P, _U64, _P],
+    "ibp_store_set_lengths": [_P, _P],
     "ibp_group_gather_decompress_ordered": [_P, _P, _U64, _P, _U64, _P, _U64, _P],
     "ibp_gather_decompress_split": [_P, _P, _U64, _U64, _U64, _U64, _P, _P, _P, _U64, _P],
     "ibp_group_create": [ctypes.POINTER(ctypes.c_void_p), _P, _P, _U32],
@@ -208,6 +209,11 @@ def ibp_gather_decompress_split(store: int, dst, group_rows: int, group_stride: 
                                                      _ptr(offsets), _ptr(ids), n,
                                                      _stream(stream)),
            "ibp_gather_decompress_split")
+
+
+def ibp_store_set_lengths(store: int, lengths) -> None:
+    """Attach each slot's stored bytes (device uint32/int32 [n_rows]) or detach (None)."""
+    _check(_lib_handle().ibp_store_set_lengths(store, _ptr(lengths)), "ibp_store_set_lengths")
 
 
 def order_workspace_bytes(n: int) -> int:

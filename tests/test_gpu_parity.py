@@ -674,3 +674,33 @@ def test_ordered_gather_checks_its_workspace(stores):
         ibp.ibp_gather_decompress_ordered(st.h, buf, 512, buf, None, ids, 64,
                                           buf.data_ptr() + 8, ibp.order_workspace_bytes(64))
     assert e.value.status == ibp.IBP_EALIGN
+
+
+@pytest.mark.parametrize("R,C", [(8192, 256), (2048, 256), (1024, 64), (400, 100)])
+def test_length_table_changes_nothing_but_fetches(stores, R, C):
+    """With the slots' stored sizes attached, gathers from host slots (fast and
+    generic decoders; rows with raw chunks) return the same bytes as without;
+    wrong entries (too short, too long) still decode correctly."""
+    N = 1200 if R >= 2048 else 3000
+    b = (wl.kv_rows(0, 1, 2, range(N // 2)).view(np.uint8).reshape(-1, R)[:N] if R == 8192
+         else wl.fuzz_rows(N, R, seed=R))
+    N = len(b)
+    st = stores(R, C, N)
+    d = to_dev(b)
+    ibp.ibp_build_meta(st.h, d, R, None, N, 95, 100)
+    slots = torch.zeros((N, st.slot), dtype=torch.uint8, pin_memory=True)
+    stored = torch.zeros(N, dtype=torch.int32, device=DEV)
+    ibp.ibp_compress(st.h, slots, d, R, None, N, stored)
+    torch.cuda.synchronize()
+    ids = to_dev(np.random.default_rng(R).integers(0, N, size=2 * N).astype(np.int64))
+    ref = torch.empty((2 * N, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress(st.h, ref, slots, None, ids, 2 * N)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(ref.cpu().numpy(), b[ids.cpu().numpy()])
+    for lens in (stored, torch.zeros_like(stored), torch.full_like(stored, 1 << 20)):
+        ibp.ibp_store_set_lengths(st.h, lens)
+        out = torch.empty_like(ref)
+        ibp.ibp_gather_decompress(st.h, out, slots, None, ids, 2 * N)
+        assert st.status() == ibp.IBP_OK
+        assert torch.equal(out, ref)
+    ibp.ibp_store_set_lengths(st.h, None)
