@@ -1,0 +1,159 @@
+"""Threshold builder against the brute-force optimum Mask on tiny inputs (CPU).
+
+The pages' preprocessing (gist.science explainer, Methodology > Core
+Algorithm > Preprocessing) marks a bit invariant when it holds one value in at
+least a fraction T of the analysed tensors; they leave T to the user.  A
+threshold Mask is not the smallest store in general: what a row costs depends
+on which chunks match, and on word rounding.  This file measures how far the
+best threshold falls from the best Mask of all, on rows small enough to try
+every Mask.
+
+Each case has 32·W bit positions of three kinds:
+  * fixed: one value in every row.  Putting such a bit in the Mask never breaks
+    a match and never lengthens a stream, so every optimum may include it;
+  * noise: flipped in exactly half of the rows, so no threshold T > 1/2 keeps it;
+  * free (a few): flipped with probabilities 0.02 .. 0.5.
+The brute force tries all 3^b (Mask, Bitval) choices over the b free bits (out,
+in with 0, in with 1), with fixed bits in and noise bits out.  Every threshold
+Mask lies in that family, so the family's optimum bounds them all from below.
+
+Asserted: each threshold Mask of the full grid (every majority count k/n,
+k > n/2) lies in the family; the optimum is no larger than any of them; the
+optimum's stored rows decode back.  Reported, not asserted: the gap of the best
+grid threshold, of the default candidate set, and of T = 0.95 alone
+(`python -m tests.test_builder_optimum 30` from the repository root prints
+the table over 30 seeds per geometry).
+"""
+import itertools
+import sys
+
+import numpy as np
+import pytest
+
+from oracle import ref_c
+
+N_ROWS = 48
+CANDIDATES = [(9, 10), (95, 100), (99, 100), (999, 1000), (1, 1)]
+GEOMETRIES = [(4, 4, 20), (4, 8, 24), (4, 16, 60), (8, 32, 90)]  # (W words, C bytes, noise bits)
+
+
+def make_case(seed, W, noise, nfree=8, n=N_ROWS):
+    g = np.random.default_rng(7000 + seed)
+    base = g.integers(0, 1 << 32, size=W, dtype=np.uint64).astype(np.uint32)
+    order = g.permutation(32 * W)
+    free = sorted(int(x) for x in order[:nfree])
+    noisy = sorted(int(x) for x in order[nfree:nfree + noise])
+    rows = np.tile(base, (n, 1))
+    for pos in free:
+        p = float(g.choice([0.02, 0.05, 0.1, 0.2, 0.3, 0.5]))
+        flip = g.random(n) < p
+        rows[flip, pos // 32] ^= np.uint32(1 << (pos % 32))
+    for pos in noisy:
+        flip = g.permutation(n) < n // 2  # exactly half of the rows
+        rows[flip, pos // 32] ^= np.uint32(1 << (pos % 32))
+    return rows, base, free, noisy
+
+
+def stored_total(rows, C, mask, bitval):
+    n, W = rows.shape
+    R = 4 * W
+    slots = np.zeros((n, R), np.uint8)
+    bm = np.zeros((n + 31) // 32, np.uint32)
+    st = ref_c.compress_batch(rows.view(np.uint8).reshape(n, R), C, mask, bitval, slots, bm,
+                              nthreads=1)
+    return int(st.astype(np.int64).sum()), slots, bm, st
+
+
+def _bit(pos):
+    return pos // 32, np.uint32(1 << (pos % 32))
+
+
+def brute_force(rows, C, base, free, noisy):
+    W = rows.shape[1]
+    fixed = np.full(W, 0xFFFFFFFF, np.uint32)
+    for pos in free + noisy:
+        w, b = _bit(pos)
+        fixed[w] &= ~b
+    best = None
+    for states in itertools.product((0, 1, 2), repeat=len(free)):
+        mask = fixed.copy()
+        bitval = base & fixed
+        for pos, s in zip(free, states):
+            w, b = _bit(pos)
+            if s:
+                mask[w] |= b
+            if s == 2:
+                bitval[w] |= b
+        tot = stored_total(rows, C, mask, bitval)[0]
+        if best is None or tot < best[0]:
+            best = (tot, mask, bitval)
+    return best, fixed
+
+
+def measure(seed, W, C, noise):
+    rows, base, free, noisy = make_case(seed, W, noise)
+    n = len(rows)
+    rb = rows.view(np.uint8).reshape(n, 4 * W)
+    (opt, m_opt, b_opt), fixed = brute_force(rows, C, base, free, noisy)
+    grid = {}
+    for k in range(n // 2 + 1, n + 1):
+        m, b = ref_c.build_meta(rb, k, n)
+        grid[k] = (stored_total(rows, C, m, b)[0], m, b)
+    cands = []
+    for num, den in CANDIDATES:
+        m, b = ref_c.build_meta(rb, num, den)
+        cands.append(stored_total(rows, C, m, b)[0])
+    return dict(rows=rows, base=base, free=free, noisy=noisy, fixed=fixed, opt=opt,
+                m_opt=m_opt, b_opt=b_opt, grid=grid, cands=cands, raw=n * 4 * W)
+
+
+@pytest.mark.parametrize("seed", range(3))
+@pytest.mark.parametrize("W,C,noise", GEOMETRIES)
+def test_threshold_masks_bounded_by_brute_force(seed, W, C, noise):
+    r = measure(seed, W, C, noise)
+    fixed, base = r["fixed"], r["base"]
+    noise_mask = np.zeros(W, np.uint32)
+    for pos in r["noisy"]:
+        w, b = _bit(pos)
+        noise_mask[w] |= b
+    for k, (tot, m, b) in r["grid"].items():
+        # in the family: every fixed bit in with its value, every noise bit out
+        assert np.array_equal(m & fixed, fixed), k
+        assert np.array_equal(b & fixed, base & fixed), k
+        assert not np.any(m & noise_mask), k
+        assert r["opt"] <= tot, k
+    assert r["opt"] <= min(r["cands"]) <= r["raw"]
+    # the optimum's stored rows decode back to the rows
+    n, R = len(r["rows"]), 4 * W
+    _, slots, bm, st = stored_total(r["rows"], C, r["m_opt"], r["b_opt"])
+    out, bad = ref_c.decompress_batch(slots, bm, R, C, r["m_opt"], r["b_opt"], n=n, slot_stride=R)
+    assert bad == 0
+    assert np.array_equal(out, r["rows"].view(np.uint8).reshape(n, R))
+    print(f"seed {seed} W {W} C {C}: optimum {r['opt']} B, best grid threshold "
+          f"{min(v[0] for v in r['grid'].values())} B, candidates {min(r['cands'])} B, "
+          f"T=0.95 {r['cands'][1]} B, raw {r['raw']} B")
+
+
+def _report(n_seeds):
+    rows = []
+    for W, C, noise in GEOMETRIES:
+        hit = [0, 0, 0]
+        gaps = [[], [], []]
+        for seed in range(n_seeds):
+            r = measure(seed, W, C, noise)
+            sizes = [min(v[0] for v in r["grid"].values()), min(r["cands"]), r["cands"][1]]
+            for j, s in enumerate(sizes):
+                hit[j] += s == r["opt"]
+                gaps[j].append(s / r["opt"] - 1.0)
+        rows.append((W, C, noise, hit, [(float(np.mean(g)), float(np.max(g))) for g in gaps]))
+    print(f"{n_seeds} seeds per geometry, {N_ROWS} rows; per column: cases at the optimum, "
+          f"mean / max excess over it")
+    print("| R | C | noise bits | best grid threshold | candidates | T = 0.95 |")
+    print("|---|---|---|---|---|---|")
+    for W, C, noise, hit, g in rows:
+        cells = [f"{h}/{n_seeds}, {m * 100:.1f} % / {x * 100:.1f} %" for h, (m, x) in zip(hit, g)]
+        print(f"| {4 * W} B | {C} B | {noise} | " + " | ".join(cells) + " |")
+
+
+if __name__ == "__main__":
+    _report(int(sys.argv[1]) if len(sys.argv) > 1 else 30)
