@@ -9,6 +9,7 @@ when its rows are contiguous), compressed slots live in pinned host memory
     st = IbpStore(row_bytes=512, chunk_bytes=1024, n_rows=len(rows))
     st.build(rows_gpu, sample_ids=sample)           # Mask/Bitval from a sample
     slots, stored = st.compress(rows_gpu)           # pinned host slots
+    st.set_lengths(stored)                          # optional: one fetch per row
     batch = st.gather(slots, ids_gpu)               # [len(ids), 512] on the GPU
 """
 from __future__ import annotations
@@ -33,12 +34,15 @@ class IbpStore:
         self.row_bytes, self.chunk_bytes, self.n_rows = row_bytes, chunk_bytes, n_rows
         self.handle = ibp.ibp_store_create(row_bytes, chunk_bytes, n_rows, slot_bytes)
         self.slot_bytes = ibp.ibp_store_get_info(self.handle).slot_bytes
+        self._lengths = None  # the attached length table, kept alive while the library reads it
 
     # -- lifetime
     def close(self) -> None:
         if self.handle:
+            ibp.ibp_store_set_lengths(self.handle, None)
             ibp.ibp_store_destroy(self.handle)
             self.handle = None
+            self._lengths = None
 
     def __enter__(self) -> "IbpStore":
         return self
@@ -82,6 +86,16 @@ class IbpStore:
         ibp.ibp_compress(self.handle, slots, rows, rows.stride(0), slot_ids, rows.shape[0],
                          stored, stream)
         return slots, stored
+
+    def set_lengths(self, stored: Optional[torch.Tensor]) -> None:
+        """Attach each slot's stored bytes (the int32 [n_rows] that compress()
+        returns, on the device) so that decoders fetch a row's whole stream at
+        once; None detaches.  The store keeps a reference while it is attached."""
+        if stored is not None and (stored.numel() != self.n_rows or stored.element_size() != 4
+                                   or not stored.is_cuda or not stored.is_contiguous()):
+            raise ValueError("lengths must be a contiguous 4-byte device tensor of n_rows entries")
+        ibp.ibp_store_set_lengths(self.handle, stored)
+        self._lengths = stored
 
     # -- decompression
     def decompress(self, src: torch.Tensor, n: Optional[int] = None,

@@ -36,6 +36,12 @@ def test_store_round_trip(host):
         got = st.gather(slots, ids)
         assert np.array_equal(got.cpu().numpy(), rb[ids.cpu().numpy()])
         assert torch.equal(st.gather(slots, ids, ordered=True), got)
+        st.set_lengths(stored)  # whole-stream fetches: same rows
+        assert torch.equal(st.gather(slots, ids), got)
+        assert torch.equal(st.gather(slots, ids, ordered=True), got)
+        st.set_lengths(None)
+        with pytest.raises(ValueError):
+            st.set_lengths(stored[:-1])
         cache, offs = st.pack(slots.to(DEV) if host else slots, stored)
         assert np.array_equal(st.gather(cache, ids, offsets=offs[:-1]).cpu().numpy(),
                               rb[ids.cpu().numpy()])
