@@ -14,7 +14,7 @@ the end-to-end number through the C ABI with host buffers, the raw-gather
 baseline, clocks, and the CPU oracle timed on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sparse|tiny]
+                    [--workload sparse|tiny|kv|dlrm|dense|weights|sweep|transfers|large]
 """
 from __future__ import annotations
 
@@ -1257,6 +1257,132 @@ def run_dlrm(args, rank, world, torch, dist):
     return res
 
 
+def line_bytes(stored: np.ndarray) -> np.ndarray:
+    """Link bytes of reading `stored` bytes from a 128-byte boundary: whole
+    lines, then a tail that costs 32, 64 or 128 bytes (measured by the
+    transfers workload's read_granularity)."""
+    full, r = np.divmod(np.asarray(stored, np.int64), 128)
+    tail = np.select([r == 0, r <= 32, r <= 64], [0, 32, 64], 128)
+    return full * 128 + tail
+
+
+def run_dense(args, rank, world, torch, dist):
+    """Dense GNN (the pages' Table 1 dense row): 2,000,000 x 128 fp32 features
+    ~ N(0, 0.1^2) in pinned host slots (1 GB), Mask/Bitval from a 1 % sample at
+    T = 0.95, chunk 256 B, 1 KB and 4 KB (1 KB and 4 KB give identical streams:
+    one chunk per 512-byte row).  A step gathers one two-hop mini-batch, the
+    sorted unique union of 1024 seeds, 15 neighbours each and 10 of each of
+    those (uniform random graph).  Per chunk size: ratio, delivered GB/s, its
+    fraction of link / ratio, and the speedup over the uncompressed gather of
+    the same ids; the value is the 1 KB point."""
+    from lossless_invariant_bit_gb300 import dist as ibpdist
+    from lossless_invariant_bit_gb300 import ibp
+    from lossless_invariant_bit_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    hbm = measured_peaks()["hbm_gbs"]
+    NR, R = args.rows, 512
+    steps, warm = max(3, min(args.steps, 200)), max(3, min(args.warmup, 10))
+    rows = np.empty((NR, 128), np.float32)
+    wl.dense_gnn_rows(NR, 128, seed=args.seed, out=rows)
+    rb = rows.view(np.uint8)
+    d_rows = torch.from_numpy(rb).to(dev)
+    raw_host = torch.empty((NR, R), dtype=torch.uint8, pin_memory=True)
+    raw_host.copy_(torch.from_numpy(rb))
+    slots = torch.empty((NR, R), dtype=torch.uint8, pin_memory=True)
+    link = _link_probe(torch, ibp, raw_host, stream, sp, dev)
+    log("link probe: %.1f GB/s host->HBM" % link)
+    sample = torch.from_numpy(wl.sample_ids(NR, 10, seed=args.seed)).to(dev)
+    pool = 8
+    ids_np = [wl.two_hop_ids(NR, seed=args.seed, batch=ibpdist.batch_seed(rank, b))
+              for b in range(pool)]
+    ids_dev = [torch.from_numpy(x).to(dev) for x in ids_np]
+    nmax = max(len(x) for x in ids_np)
+    out = torch.empty((nmax, R), dtype=torch.uint8, device=dev)
+    stored = torch.empty(NR, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches = 0
+
+    def timed(fn):
+        nonlocal launches
+        for b in range(warm):
+            fn(b)
+        evs = []
+        for b in range(warm, warm + steps):
+            flush.zero_()  # L2 flush, outside the timed events
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(b)
+            e1.record(stream)
+            evs.append((e0, e1, b % pool))
+        torch.cuda.synchronize()
+        launches += steps
+        t = sum(a.elapsed_time(c) / 1e3 for a, c, _ in evs)
+        return sum(len(ids_np[i]) for _, _, i in evs) * R / t / 1e9
+
+    with ClockSampler(dev.index) as clk:
+        raw_gbs = timed(lambda b: ibp.ibp_gather_copy(out, raw_host, R, R, ids_dev[b % pool],
+                                                      len(ids_np[b % pool]), NR, sp))
+        log("uncompressed gather: %.1f GB/s" % raw_gbs)
+        points = []
+        for C in (256, 1024, 4096):
+            st = ibp.ibp_store_create(R, C, NR, 0)
+            ibp.ibp_build_meta(st, d_rows, R, sample, len(sample), 95, 100)
+            ibp.ibp_compress(st, slots, d_rows, R, None, NR, stored)
+            torch.cuda.synchronize()
+            assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+            st_np = stored.cpu().numpy().astype(np.int64)
+            ratio = sum(float(st_np[x].sum()) for x in ids_np) / (sum(len(x) for x in ids_np) * R)
+            gbs = timed(lambda b: ibp.ibp_gather_decompress(st, out, slots, None, ids_dev[b % pool],
+                                                            len(ids_np[b % pool]), sp))
+            assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+            last = (warm + steps - 1) % pool
+            pick = np.random.default_rng(C).choice(len(ids_np[last]), 2000, replace=False)
+            ok = bool(np.array_equal(out[torch.from_numpy(pick).to(dev)].cpu().numpy(),
+                                     rb[ids_np[last][pick]]))
+            ideal = min(hbm, link / ratio)
+            # what the link carries: whole 128-byte lines, a line's tail read
+            # costing 32, 64 or 128 bytes (the transfers workload's
+            # read_granularity); a 452-byte stream costs as much as a raw row
+            line_ratio = sum(float(line_bytes(st_np[x]).sum()) for x in ids_np) / (
+                sum(len(x) for x in ids_np) * R)
+            gran = min(hbm, link / line_ratio)
+            points.append({"chunk_bytes": C, "ratio": round(ratio, 5), "gbs": round(gbs, 2),
+                           "roofline_peak": round(ideal, 2), "frac": round(gbs / ideal, 4),
+                           "link_line_bytes_per_row_byte": round(line_ratio, 5),
+                           "granular_peak": round(gran, 2),
+                           "frac_of_granular_peak": round(gbs / gran, 4),
+                           "speedup_vs_raw_gather": round(gbs / raw_gbs, 3),
+                           "parity_sampled_rows_ok": ok})
+            log("dense C=%d: ratio %.4f  %.1f GB/s  %.3f of link/ratio  %.3f of the line-granular "
+                "ceiling  %.3fx raw" % (C, ratio, gbs, gbs / ideal, gbs / gran, gbs / raw_gbs))
+            ibp.ibp_store_destroy(st)
+    head = next(p for p in points if p["chunk_bytes"] == 1024)
+    n_avg = statistics.mean(len(x) for x in ids_np)
+    return {
+        "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
+        "value": head["gbs"], "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": round(n_avg * R / head["gbs"] / 1e6, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (seeded numpy: dense GNN features N(0, 0.1^2); two-hop mini-batches "
+                "on a uniform random graph)",
+        "config": {"workload": "dense GNN gather-decompress: %d x 128 fp32 rows in pinned host "
+                               "slots, 1%% sample, T=0.95; two-hop mini-batches of %.0f unique "
+                               "ids on average; value is the 1 KB chunk point" % (NR, n_avg),
+                   "l2": "flushed between steps (256 MB write, outside the timed events)"},
+        "link_gbs": round(link, 2), "raw_gather_gbs": round(raw_gbs, 2),
+        "roofline": {"bound": "link", "achieved": head["gbs"], "peak": head["roofline_peak"],
+                     "unit": "GB/s", "frac": head["frac"], "traffic": None,
+                     "kernel": "k_decode_fast<true, mode, small> (ibp_gather_decompress)"},
+        "chunks": points,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+
+
 def _link_probe(torch, ibp, host, stream, sp, dev):
     """Best of 5 aligned zero-copy copies of a pinned host buffer into HBM, GB/s."""
     pbytes = (host.numel() // 16) * 16
@@ -1655,7 +1781,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--workload", default="sparse",
                     choices=["sparse", "tiny", "kv", "dlrm", "transfers", "sweep", "weights",
-                             "large"])
+                             "large", "dense"])
     ap.add_argument("--dlrm-dim", type=int, default=128, choices=[128, 256, 512])
     ap.add_argument("--dlrm-rows", type=int, default=1_000_000)
     ap.add_argument("--kv-layers", type=int, default=32)
@@ -1693,7 +1819,7 @@ def main():
         dist.barrier()
     run = {"tiny": run_tiny, "kv": run_kv, "dlrm": run_dlrm, "transfers": run_transfers,
            "sweep": run_sweep, "weights": run_weights,
-           "large": run_large}.get(args.workload, run_ours)
+           "large": run_large, "dense": run_dense}.get(args.workload, run_ours)
     res = run(args, rank, world, torch, dist)
     if args.workload == "sparse" and not args.no_cache_path:
         # the HBM cache path of the same metric, reported beside the host path
