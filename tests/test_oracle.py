@@ -372,3 +372,47 @@ def test_pack_slots_layout():
         got = py.decompress(bytes(packed[offs[i]:offs[i] + stored[i]]), raw, R, C, list(mask),
                             list(bitval))
         assert got == rows[i].tobytes()
+
+
+def test_id_indexed_paths_match_their_definitions():
+    """The id lists of the batch calls mean what they say: a build over sample
+    ids is the build over rows[ids] (repeats counted, n = the sample's size),
+    compressing into slot ids is compressing in order and moving each slot,
+    and a gather is the dense decode indexed by ids."""
+    n, R, C = 300, 96, 32
+    rows = wl.fuzz_rows(n, R, seed=12)
+    g = np.random.default_rng(12)
+    ids = g.integers(0, n, size=80).astype(np.int64)  # unsorted, with repeats
+    m_s, b_s = ref_c.build_meta(rows, 9, 10, sample_ids=ids)
+    m_g, b_g = ref_c.build_meta(rows[ids], 9, 10)
+    mp, bp = py.build_meta([rows[i].tobytes() for i in ids], 9, 10)
+    assert np.array_equal(m_s, m_g) and np.array_equal(b_s, b_g)
+    assert list(m_s) == mp and list(b_s) == bp
+    # a bit set in exactly the sampled rows is invariant one over the sample
+    # (and would be invariant zero if n counted every stored row)
+    marked = np.zeros((200, 4), np.uint32)
+    sample = np.arange(0, 200, 10, dtype=np.int64)
+    marked[sample, 0] = 1
+    m1, b1 = ref_c.build_meta(marked.view(np.uint8), 9, 10, sample_ids=sample)
+    assert (m1[0] & 1) and (b1[0] & 1)
+    # slot ids: the same stored bytes, sizes and raw bits, at the slots named
+    slots = np.zeros((n, R), np.uint8)
+    bitmap = np.zeros((n + 31) // 32, np.uint32)
+    stored = ref_c.compress_batch(rows, C, m_s, b_s, slots, bitmap)
+    perm = g.permutation(2 * n)[:n].astype(np.int64)  # into a store of 2n slots
+    slots2 = np.zeros((2 * n, R), np.uint8)
+    bitmap2 = np.zeros((2 * n + 31) // 32, np.uint32)
+    stored2 = ref_c.compress_batch(rows, C, m_s, b_s, slots2, bitmap2, slot_ids=perm)
+    assert np.array_equal(stored2, stored)
+    raw = np.unpackbits(bitmap.view(np.uint8), bitorder="little")[:n]
+    raw2 = np.unpackbits(bitmap2.view(np.uint8), bitorder="little")[:2 * n]
+    assert np.array_equal(raw2[perm], raw)
+    assert raw2.sum() == raw.sum()  # no other slot marked
+    for i in range(n):
+        assert np.array_equal(slots2[perm[i], :stored[i]], slots[i, :stored[i]])
+    # gather: the dense decode indexed by ids (repeats included)
+    dense, bad = ref_c.decompress_batch(slots, bitmap, R, C, m_s, b_s, n=n, slot_stride=R)
+    assert bad == 0 and np.array_equal(dense, rows)
+    got, bad = ref_c.decompress_batch(slots2, bitmap2, R, C, m_s, b_s, ids=perm[ids],
+                                      slot_stride=R)
+    assert bad == 0 and np.array_equal(got, rows[ids])
