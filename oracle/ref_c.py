@@ -34,33 +34,38 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def bind(L):
+    """Declare the argument and return types of the oracle's functions on a
+    loaded copy of it (the test suite also loads deliberately broken builds)."""
+    L.ibp_ref_build_meta.argtypes = [_u8p, ctypes.c_uint64, ctypes.c_uint32, _i64p,
+                                     ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
+                                     _u32p, _u32p]
+    L.ibp_ref_build_meta.restype = ctypes.c_int
+    L.ibp_ref_compress_row.argtypes = [_u8p, ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p,
+                                       _u8p, _intp, _u64p]
+    L.ibp_ref_compress_row.restype = ctypes.c_uint32
+    L.ibp_ref_decompress_row.argtypes = [_u8p, ctypes.c_uint32, ctypes.c_int, ctypes.c_uint32,
+                                         ctypes.c_uint32, _u32p, _u32p, _u8p]
+    L.ibp_ref_decompress_row.restype = ctypes.c_int
+    L.ibp_ref_compress_batch.argtypes = [_u8p, ctypes.c_uint64, ctypes.c_uint64, _i64p, _u8p,
+                                         ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
+                                         _u32p, _u32p, _u32p, _u32p, ctypes.c_int]
+    L.ibp_ref_compress_batch.restype = ctypes.c_uint64
+    L.ibp_ref_decompress_batch.argtypes = [_u8p, _u64p, ctypes.c_uint64, ctypes.c_uint32,
+                                           _u32p, _i64p, ctypes.c_uint64, ctypes.c_uint32,
+                                           ctypes.c_uint32, _u32p, _u32p, _u8p,
+                                           ctypes.c_uint64, ctypes.c_int]
+    L.ibp_ref_decompress_batch.restype = ctypes.c_uint64
+    L.ibp_ref_max_threads.argtypes = []
+    L.ibp_ref_max_threads.restype = ctypes.c_int
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_LIB)
-        L.ibp_ref_build_meta.argtypes = [_u8p, ctypes.c_uint64, ctypes.c_uint32, _i64p,
-                                         ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
-                                         _u32p, _u32p]
-        L.ibp_ref_build_meta.restype = ctypes.c_int
-        L.ibp_ref_compress_row.argtypes = [_u8p, ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p,
-                                           _u8p, _intp, _u64p]
-        L.ibp_ref_compress_row.restype = ctypes.c_uint32
-        L.ibp_ref_decompress_row.argtypes = [_u8p, ctypes.c_uint32, ctypes.c_int, ctypes.c_uint32,
-                                             ctypes.c_uint32, _u32p, _u32p, _u8p]
-        L.ibp_ref_decompress_row.restype = ctypes.c_int
-        L.ibp_ref_compress_batch.argtypes = [_u8p, ctypes.c_uint64, ctypes.c_uint64, _i64p, _u8p,
-                                             ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
-                                             _u32p, _u32p, _u32p, _u32p, ctypes.c_int]
-        L.ibp_ref_compress_batch.restype = ctypes.c_uint64
-        L.ibp_ref_decompress_batch.argtypes = [_u8p, _u64p, ctypes.c_uint64, ctypes.c_uint32,
-                                               _u32p, _i64p, ctypes.c_uint64, ctypes.c_uint32,
-                                               ctypes.c_uint32, _u32p, _u32p, _u8p,
-                                               ctypes.c_uint64, ctypes.c_int]
-        L.ibp_ref_decompress_batch.restype = ctypes.c_uint64
-        L.ibp_ref_max_threads.argtypes = []
-        L.ibp_ref_max_threads.restype = ctypes.c_int
-        _lib = L
+        _lib = bind(ctypes.CDLL(_LIB))
     return _lib
 
 
