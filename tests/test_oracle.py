@@ -33,7 +33,7 @@ def b2w(b):
 
 
 # ------------------------------------------------------------ worked examples
-@pytest.mark.parametrize("name", golden_io.names("e1") + golden_io.names("e2") + golden_io.names("e4"))
+@pytest.mark.parametrize("name", golden_io.names("e1") + golden_io.names("e2") + golden_io.names("e4") + golden_io.names("e5"))
 @pytest.mark.parametrize("impl", ["py", "c"])
 def test_golden_compress(name, impl):
     g = golden_io.load(name)

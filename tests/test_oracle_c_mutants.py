@@ -81,7 +81,7 @@ def _c_pins():
         if not ok:
             failed.append(name)
 
-    for name in golden_io.names("e1") + golden_io.names("e2") + golden_io.names("e4"):
+    for name in golden_io.names("e1") + golden_io.names("e2") + golden_io.names("e4") + golden_io.names("e5"):
         g = golden_io.load(name)
 
         def golden(g=g):

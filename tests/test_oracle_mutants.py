@@ -66,7 +66,7 @@ def _pins(m):
     """Run the pins against oracle module `m`; return the names that fail."""
     failed = []
     # hand-worked compression examples
-    for name in golden_io.names("e1") + golden_io.names("e2") + golden_io.names("e4"):
+    for name in golden_io.names("e1") + golden_io.names("e2") + golden_io.names("e4") + golden_io.names("e5"):
         g = golden_io.load(name)
         try:
             stored, raw, bits = m.compress(w2b(g["row"]), g["C"], g["mask"], g["bitval"])
