@@ -52,7 +52,9 @@ def measured_peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) over the timed region."""
+    """nvidia-smi samples (200 ms) over the timed region, plus one sample
+    taken just before it starts and one just after it ends, so that a region
+    shorter than the sampling period still carries a clock record."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -63,7 +65,17 @@ class ClockSampler:
         self.proc = None
         self.lines = []
 
+    def _once(self):
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                               timeout=10)
+            return [ln.strip() for ln in r.stdout.splitlines() if ln.strip()]
+        except (OSError, subprocess.TimeoutExpired):
+            return []
+
     def __enter__(self):
+        self.lines.extend(self._once())  # edge sample: just before the region
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
@@ -87,6 +99,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.t.join(timeout=2)
+        self.lines.extend(self._once())  # edge sample: just after the region
 
     def summary(self):
         sm, mx, reasons = [], None, set()

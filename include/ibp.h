@@ -157,12 +157,17 @@ IBP_API ibp_status ibp_build_meta_tuned(ibp_store* store, const void* rows, uint
  *   rows, row_stride, sample_ids, n, thr_num, thr_den  as for ibp_build_meta
  *   row_bytes    R, a multiple of 16, at most IBP_NOALLOC_MAX_ROW_BYTES
  *                (larger rows are rejected with IBP_EINVAL)
- *   mask_out, bitval_out  device uint32[R/4] each, written by the call
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call clears and reuses the same array, so calls whose work
- * overlaps on the GPU (other streams, other host threads) race and give wrong
- * results: serialise them.  Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA. */
+ *   mask_out, bitval_out  device uint32[R/4] each (4-byte aligned), written
+ *                by the call; sample_ids, when given, is 8-byte aligned
+ * Each call outside a stream capture looks up the array's device address
+ * with the current device (after a cudaDeviceReset, or in another context of
+ * that device, the array lives elsewhere); a call being captured uses the
+ * address the last uncaptured call on that device saw, so make one call on a
+ * device before capturing any (a capture with none before it returns
+ * IBP_EINVAL).  Every call clears and reuses the same array, so calls whose
+ * work overlaps on the GPU (other streams, other host threads) race and give
+ * wrong results: serialise them.  Errors: IBP_EINVAL, IBP_EALIGN (rows,
+ * row_stride, the outputs or sample_ids misaligned), IBP_ECUDA. */
 IBP_API ibp_status ibp_build_meta_noalloc(const void* rows, uint64_t row_stride,
                                           uint32_t row_bytes, const int64_t* sample_ids,
                                           uint64_t n, uint32_t thr_num, uint32_t thr_den,
@@ -199,7 +204,12 @@ IBP_API ibp_status ibp_compress(ibp_store* store, void* dst_slots, const void* s
  * properties have reached the host (after any such call that follows the
  * Mask/Bitval build and a synchronisation of its stream; earlier captures
  * run the slower forms that read them on the device); the builder calls may
- * not be captured. */
+ * not be captured.  A captured call keeps the store properties of the
+ * Mask/Bitval current at capture time: replayed after the Mask/Bitval was
+ * rebuilt or set again, it finds a newer generation of the store on the
+ * device, sets IBP_EINVAL in the status word and zero-fills its output rows
+ * (decompression) or writes nothing (compression).  Capture again after every
+ * Mask/Bitval change. */
 IBP_API ibp_status ibp_decompress(const ibp_store* store, void* dst, const void* src,
                           const uint64_t* offsets, uint64_t n, ibp_stream_t stream);
 
@@ -227,9 +237,12 @@ IBP_API ibp_status ibp_gather_decompress_strided(const ibp_store* store, void* d
  * into every store, e.g. the per-table lookups of a DLRM batch (the review's
  * DLRM embedding-lookup integration).  Rows must be <= 2 KB with chunks a
  * multiple of 16 bytes, slots <= 64 KB.  Waits for the stores' pending
- * Mask/Bitval builds; a store whose Mask/Bitval changes later needs a new
- * group.  Allocates device memory.  Errors: IBP_EINVAL, IBP_EALIGN,
- * IBP_ENOMEM, IBP_ECUDA. */
+ * Mask/Bitval builds and takes each store's properties and its length table
+ * (ibp_store_set_lengths) as they are now: a store whose Mask/Bitval changes
+ * later needs a new group (until then its lookups set IBP_EINVAL in its
+ * status word and are zero-filled), and so does one whose length table is
+ * attached or detached later.  Allocates device memory.  Errors: IBP_EINVAL,
+ * IBP_EALIGN, IBP_ENOMEM, IBP_ECUDA. */
 IBP_API ibp_status ibp_group_create(ibp_group** out, ibp_store* const* stores,
                                     const void* const* srcs, uint32_t n);
 

@@ -98,6 +98,7 @@ ibp::HostProps host_props(const ibp_store* s, cudaStream_t st) {
   }
   const volatile uint32_t* h = s->h_scal;
   hp.known = true;
+  hp.gen = h[9];
   hp.min_bits = h[0];
   hp.max_runs = h[1];
   hp.uniform = h[3] != 0;
@@ -517,6 +518,10 @@ ibp_status ibp_group_create(ibp_group** out, ibp_store* const* stores, const voi
     g.ush = hp.ush;
     g.ubv = hp.ubv;
     g.ukeep = hp.ukeep;
+    g.scal = s->scal;
+    g.lengths = s->lengths;
+    g.gen = hp.gen;
+    g.pad[0] = g.pad[1] = g.pad[2] = 0;
   }
   ibp_group* grp = nullptr;
   if (e == IBP_OK) {

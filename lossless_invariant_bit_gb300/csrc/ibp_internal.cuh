@@ -18,7 +18,10 @@ namespace ibp {
 //   scal          [0] min_bits = nch + sum(ckeep), [1] max runs of one word's nm,
 //                 [2] meta valid flag, [3] uniform flag (all words share ~Mask
 //                 and Bitval, <= 2 runs), [4] run0, [5] run1, [6] s0 | s1 << 8,
-//                 [7] Bitval, [8] kept bits per word (of the uniform word)
+//                 [7] Bitval, [8] kept bits per word (of the uniform word),
+//                 [9] generation: bumped by every derive (every Mask/Bitval
+//                 build or install), so a launch whose store properties were
+//                 fixed on the host can tell that they are out of date
 struct MetaView {
   const uint32_t* mask;
   const uint32_t* bitval;
@@ -79,6 +82,7 @@ struct EncodeArgs {
   uint64_t slot;
   uint32_t* stored_out;
   uint32_t um0, um1, ush, ubv, ukeep;  // uniform store (the k_encode<true> form)
+  uint32_t gen;       // store generation the uniform parameters belong to
   uint32_t chunk_lg;  // log2 of the rows a warp takes at a time: 5 (32 rows, one
                       // raw-bitmap word) or 0 (one row; bitmap bits set by atomics)
 };
@@ -111,6 +115,7 @@ enum { kModeRuntime = 0, kModeUniform = 1, kModeRun2 = 2, kModeNet5 = 3, kModeUn
 struct HostProps {
   bool known;
   bool uniform;
+  uint32_t gen;  // generation of the derive these properties come from
   uint32_t min_bits, max_runs;
   uint32_t um0, um1, ush, ubv, ukeep;  // uniform word: run masks, s0 | s1 << 8, Bitval, keep
 };
@@ -118,7 +123,9 @@ struct HostProps {
 // Launch parameters of the fast decoder: shared-memory layout (in words:
 // descriptor table and group table per CTA, then per warp a ring of S
 // single-row stream buffers and the chunk starts) and the store properties of
-// the specialised modes.
+// the specialised modes, with the generation they belong to (a launch replayed
+// from a CUDA graph after the Mask/Bitval changed sees a newer one on the
+// device, reports IBP_EINVAL and zero-fills its rows).
 struct FastParams {
   uint32_t table_words;
   uint32_t gtab_words;
@@ -127,6 +134,7 @@ struct FastParams {
   uint32_t S;
   uint32_t min_bits;
   uint32_t um0, um1, ush, ubv, ukeep;
+  uint32_t gen;
 };
 
 // One store of a fused multi-store gather (all stores share R and C).
@@ -143,7 +151,12 @@ struct GroupEntry {
   uint32_t min_vec;        // 16-byte vectors of the shortest compressed stream
   uint32_t can_pack;       // some compressed row can exist
   uint32_t um0, um1, ush, ubv, ukeep;  // uniform stores
+  const uint32_t* scal;    // the store's scalars: its current generation at scal[9]
+  const uint32_t* lengths; // NULL, or each slot's stored bytes (the store's length table)
+  uint32_t gen;            // generation the fields above were read at
+  uint32_t pad[3];
 };
+static_assert(sizeof(GroupEntry) % 16 == 0, "group entries are staged as 16-byte vectors");
 
 struct GroupArgs {
   const GroupEntry* entries;

@@ -391,6 +391,7 @@ __global__ void __launch_bounds__(1024) k_derive(uint32_t* mask, uint32_t* bitva
     scal[0] = nch + s_sum;
     scal[1] = s_runs;
     scal[2] = 1;
+    scal[9] += 1u;  // a new generation of the store's tables
   }
 }
 
@@ -737,13 +738,17 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
   const uint32_t min_words = (min_bits + 31u) >> 5;
   const bool can_pack = 4u * min_words < R;
   const uint32_t min_vec = min((4u * min_words + 15u) >> 4, nvec);
+  // the specialised modes carry store properties fixed on the host; a launch
+  // replayed (from a CUDA graph) after the Mask/Bitval changed must not use them
+  const bool stale = kMode != kModeRuntime && __ldg(a.m.scal + 9) != F.gen;
 
   uint4* tab = reinterpret_cast<uint4*>(smem);
   uint32_t* gtab = smem + F.table_words;
   uint32_t* uparm = gtab + F.gtab_words;  // uniform-store parameters (runtime mode)
   uint32_t* ring = uparm + 8 + wid * F.warp_words;
   // row info ring, two 32-row chunks: {offset | flags (lo, hi), output offset (lo, hi)}
-  // flags (low 4 bits, offsets are 16-byte aligned): 1 present, 2 raw, 4 bad id, 8 misaligned
+  // flags (low 4 bits, offsets are 16-byte aligned): 1 present, 2 raw, 4 bad id,
+  // 8 misaligned, 4|8 store properties out of date
   uint4* rinfo = reinterpret_cast<uint4*>(ring + S * F.sbuf_words);
   uint32_t* cinfo = ring + S * F.sbuf_words + 256;
   {
@@ -803,7 +808,9 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
     uint32_t fl = 0;
     uint64_t off = 0;
     if (pin) {
-      if (pid < 0 || (uint64_t)pid >= a.n_rows || poff == kBadSource) {
+      if (stale) {
+        fl = 1u | 12u;
+      } else if (pid < 0 || (uint64_t)pid >= a.n_rows || poff == kBadSource) {
         fl = 1u | 4u;
       } else if (poff & 15u) {
         fl = 1u | 8u;
@@ -873,7 +880,10 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
       uint32_t* sb = ring + (t % S) * F.sbuf_words;
       constexpr bool split = kSplit;
       if (fl & 12u) {
-        if (lane == 0) set_status(a.status, (fl & 4u) ? IBP_ERANGE : IBP_EALIGN);
+        if (lane == 0)
+          set_status(a.status, (fl & 12u) == 12u ? IBP_EINVAL
+                               : (fl & 4u)       ? IBP_ERANGE
+                                                 : IBP_EALIGN);
         if (split)
           for (uint32_t v = lane; v < nvec; v += 32)
             *split_group(drow, gtab, v, a.chunk_stride) = make_uint4(0, 0, 0, 0);
@@ -1000,11 +1010,18 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
   constexpr uint32_t S = kRingStages;
   GroupEntry* ent = reinterpret_cast<GroupEntry*>(smem);
   const uint32_t ent_words = T * (uint32_t)(sizeof(GroupEntry) / 4);
+  // stores whose Mask/Bitval changed since the group read their properties
+  // (a launch replayed from a CUDA graph): their items report IBP_EINVAL
+  __shared__ uint32_t s_stale[IBP_MAX_GROUP_STORES / 32];
   {
     const uint4* src = reinterpret_cast<const uint4*>(g.entries);
     uint4* dstv = reinterpret_cast<uint4*>(smem);
     for (uint32_t v = threadIdx.x; v < ent_words / 4u; v += blockDim.x) dstv[v] = __ldg(src + v);
+    if (threadIdx.x < IBP_MAX_GROUP_STORES / 32) s_stale[threadIdx.x] = 0u;
   }
+  __syncthreads();
+  for (uint32_t t = threadIdx.x; t < T; t += blockDim.x)
+    if (__ldg(ent[t].scal + 9) != ent[t].gen) atomicOr(&s_stale[t >> 5], 1u << (t & 31u));
   uint32_t* ring = smem + ent_words + wid * g.warp_words;
   uint4* rinfo = reinterpret_cast<uint4*>(ring + S * g.sbuf_words);
   uint32_t* cinfo = ring + S * g.sbuf_words + 256;
@@ -1027,7 +1044,7 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
 
   int64_t pid = 0;
   uint64_t poff = 0, pitem = 0;
-  uint32_t pbm = 0, pt = 0;
+  uint32_t pbm = 0, pt = 0, plen = 0;
   bool pin = false;
   auto step_ids = [&](uint32_t q) {
     const uint32_t t = 32u * q + lane;
@@ -1043,13 +1060,16 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
     if (pin && pid >= 0 && (uint64_t)pid < ent[pt].n_rows) {
       poff = (uint64_t)pid * ent[pt].slot;
       pbm = __ldg(ent[pt].bitmap + (pid >> 5));
+      if (ent[pt].lengths) plen = __ldg(ent[pt].lengths + pid);
     }
   };
   auto step_store = [&](uint32_t q) {
     uint32_t fl = 0;
     uint64_t off = 0;
     if (pin) {
-      if (pid < 0 || (uint64_t)pid >= ent[pt].n_rows) {
+      if ((s_stale[pt >> 5] >> (pt & 31u)) & 1u) {
+        fl = 1u | 12u;
+      } else if (pid < 0 || (uint64_t)pid >= ent[pt].n_rows) {
         fl = 1u | 4u;
       } else {
         fl = 1u | (((pbm >> (pid & 31)) & 1u) << 1);
@@ -1057,8 +1077,15 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
       }
     }
     const uint64_t dsto = (pitem / T) * g.dst_row_stride + (uint64_t)pt * R;
-    rinfo[((q & 1u) << 5) + lane] = make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32) | (pt << 24),
-                                               (uint32_t)dsto, (uint32_t)(dsto >> 32));
+    // vectors of the first fetch (the raw row; the whole stream when the store
+    // has a length table; else the shortest stream) ride in the top 12 bits of
+    // the output offset's high word (output offsets stay below 2^52)
+    const GroupEntry& en = ent[pt];
+    const uint32_t nv = (fl & 2u) ? nvec
+                        : en.lengths ? min(max((plen + 15u) >> 4, en.min_vec), nvec) : en.min_vec;
+    rinfo[((q & 1u) << 5) + lane] =
+        make_uint4((uint32_t)off | fl, (uint32_t)(off >> 32) | (pt << 24), (uint32_t)dsto,
+                   ((uint32_t)(dsto >> 32) & 0xFFFFFu) | (nv << 20));
   };
   const uint32_t ring_sa = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + 16u * lane;
   auto issue = [&](uint32_t tt) {
@@ -1067,7 +1094,7 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
       const uint32_t fl = e.x & 15u;
       if ((fl & 13u) == 1u) {
         const GroupEntry& en = ent[e.y >> 24];
-        const uint32_t nv = (fl & 2u) ? nvec : en.min_vec;
+        const uint32_t nv = e.w >> 20;
         const uint8_t* src = en.src + 16u * lane +
                              ((((uint64_t)(e.y & 0xFFFFFFu)) << 32) | (uint64_t)(e.x & ~15u));
         const uint32_t sa = ring_sa + 4u * (tt & (S - 1u)) * g.sbuf_words;
@@ -1101,10 +1128,11 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
       const uint32_t fl = e.x & 15u;
       if (!(fl & 1u)) break;  // past the end of an ordered gather's last chunk
       const GroupEntry& en = ent[e.y >> 24];
-      uint4* drow = reinterpret_cast<uint4*>(g.dst + ((((uint64_t)e.w) << 32) | (uint64_t)e.z));
+      uint4* drow = reinterpret_cast<uint4*>(
+          g.dst + ((((uint64_t)(e.w & 0xFFFFFu)) << 32) | (uint64_t)e.z));
       uint32_t* sb = ring + (t & (S - 1u)) * g.sbuf_words;
       if (fl & 12u) {
-        if (lane == 0) set_status(en.status, IBP_ERANGE);
+        if (lane == 0) set_status(en.status, (fl & 12u) == 12u ? IBP_EINVAL : IBP_ERANGE);
         zero_row(drow, nvec, lane);
         break;
       }
@@ -1146,10 +1174,11 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
           break;
         }
         const uint32_t need_vec = (4u * words + 15u) >> 4;
-        if (need_vec > en.min_vec) {
+        const uint32_t fetched = e.w >> 20;
+        if (need_vec > fetched) {  // the raw chunks made the stream longer: second fetch
           const uint4* src = reinterpret_cast<const uint4*>(
               en.src + ((((uint64_t)(e.y & 0xFFFFFFu)) << 32) | (uint64_t)(e.x & ~15u)));
-          fetch_vectors(static_cast<uint32_t>(__cvta_generic_to_shared(sb)), src, en.min_vec,
+          fetch_vectors(static_cast<uint32_t>(__cvta_generic_to_shared(sb)), src, fetched,
                         need_vec, lane);
         }
         __syncwarp();
@@ -1226,6 +1255,13 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
   const uint32_t nvec = R >> 4;
   const uint64_t wpb = blockDim.x >> 5;
   const uint64_t stride = (uint64_t)gridDim.x * wpb;
+  // the uniform parameters were fixed on the host for one generation of the
+  // store's tables; a launch replayed (from a CUDA graph) after the Mask/Bitval
+  // changed writes nothing and reports IBP_EINVAL
+  if (kUni && __ldg(a.m.scal + 9) != a.gen) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(a.status, IBP_EINVAL);
+    return;
+  }
 
   // A warp takes rpc consecutive rows at a time: 32 for large batches with
   // identity slots (the warp owns one raw-bitmap word and writes it once,
@@ -1957,6 +1993,7 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   F.ush = hp.ush;
   F.ubv = hp.ubv;
   F.ukeep = hp.ukeep;
+  F.gen = hp.gen;
   // 8 warps per CTA; rows above 2 KB take as many as their rings leave room for
   int warps = 8;
   size_t smem = 4ull * (F.table_words + F.gtab_words + 8 + (uint64_t)warps * F.warp_words);
@@ -2067,6 +2104,7 @@ cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count
     u.ush = hp.ush;
     u.ubv = hp.ubv;
     u.ukeep = hp.ukeep;
+    u.gen = hp.gen;
     return launch_encode_t<true>(u, sm_count, st);
   }
   return launch_encode_t<false>(a, sm_count, st);

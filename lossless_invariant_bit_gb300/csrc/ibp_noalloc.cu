@@ -22,19 +22,31 @@ namespace {
 
 constexpr int kMaxDevices = 256;
 std::mutex g_setup_mu;
-uint32_t* g_counts_addr[kMaxDevices] = {};  // device address of the array, per device
+uint32_t* g_counts_addr[kMaxDevices] = {};  // last looked-up device address, per device
 
 // The array's name in host code is only a host-side stand-in; the kernels
-// need its device address, looked up once per device with that device current.
-ibp_status counts_on(int dev, uint32_t** out) {
+// need its device address, looked up with the device current.  Outside a
+// stream capture the lookup runs on every call (it is cheap once the module
+// is loaded, and after a cudaDeviceReset, or in another context of the same
+// device, the array lives at another address); a call being captured cannot
+// make the lookup and takes the address the last uncaptured call on this
+// device saw.
+ibp_status counts_on(int dev, cudaStream_t st, uint32_t** out) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return IBP_ECUDA;
+  }
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (g_counts_addr[dev] == nullptr) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_counts) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return IBP_ECUDA;
     }
     g_counts_addr[dev] = static_cast<uint32_t*>(p);
+  } else if (g_counts_addr[dev] == nullptr) {
+    return IBP_EINVAL;  // no uncaptured call on this device yet
   }
   *out = g_counts_addr[dev];
   return IBP_OK;
@@ -54,15 +66,19 @@ extern "C" ibp_status ibp_build_meta_noalloc(const void* rows, uint64_t row_stri
   if (thr_den == 0 || thr_num > thr_den || 2ull * thr_num <= thr_den) return IBP_EINVAL;
   if ((reinterpret_cast<uintptr_t>(rows) & 15u) || (row_stride & 15u) || row_stride < row_bytes)
     return IBP_EALIGN;
+  // the kernels store whole 32-bit words to the outputs and read 64-bit ids
+  if (((reinterpret_cast<uintptr_t>(mask_out) | reinterpret_cast<uintptr_t>(bitval_out)) & 3u) ||
+      (reinterpret_cast<uintptr_t>(sample_ids) & 7u))
+    return IBP_EALIGN;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return IBP_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return IBP_EINVAL;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return IBP_ECUDA;
-  uint32_t* counts = nullptr;
-  ibp_status e = counts_on(dev, &counts);
-  if (e != IBP_OK) return e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* counts = nullptr;
+  ibp_status e = counts_on(dev, st, &counts);
+  if (e != IBP_OK) return e;
   const uint32_t W = row_bytes / 4;
   // the array keeps the previous call's counts: clear the part this call uses
   if (cudaMemsetAsync(counts, 0, 32ull * W * sizeof(uint32_t), st) != cudaSuccess)

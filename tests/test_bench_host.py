@@ -51,3 +51,15 @@ def test_line_bytes_follow_the_measured_size_classes():
         costs.append(int(c[0]))
     assert costs == [32, 64, 128, 160, 192, 256]
     assert b.line_bytes(np.array([0, 4, 452, 512, 513])).tolist() == [0, 32, 512, 512, 544]
+
+
+def test_clock_sampler_without_nvidia_smi_records_nothing():
+    """Where nvidia-smi is missing (this CPU-only check), entering and leaving
+    the sampler, edge samples included, raises nothing and records no sample."""
+    b = _bench()
+    import shutil
+    if shutil.which("nvidia-smi"):
+        return
+    with b.ClockSampler(0) as c:
+        pass
+    assert c.summary()["samples"] == 0

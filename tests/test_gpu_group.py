@@ -194,3 +194,67 @@ def test_group_ordered_matches_group():
     finally:
         for s in stores:
             s.close()
+
+
+def test_group_length_tables_and_a_rebuilt_store():
+    """2 KB rows at 1 KB chunks: about half the rows carry one raw chunk, so
+    their streams are longer than the shortest one.  With each store's length
+    table attached before the group is made, the first fetch takes the whole
+    stream; the output is the same.  A store whose Mask/Bitval is rebuilt
+    after the group was made reports IBP_EINVAL and its lookups are
+    zero-filled; the other stores are unaffected."""
+    T, N, B, dim, C = 5, 4000, 1500, 512, 1024
+    R = dim * 4
+    stores, slots, tables, lengths = [], [], [], []
+    try:
+        for t in range(T):
+            rb = rows_u8(wl.dlrm_rows(N, dim, table=t, seed=7))
+            st = Store(R, C, N)
+            d = torch.from_numpy(rb).to(DEV)
+            smp = torch.from_numpy(wl.sample_ids(N, 100, seed=t)).to(DEV)
+            ibp.ibp_build_meta(st.h, d, R, smp, smp.numel(), 95, 100)
+            sl = torch.empty((N, st.slot), dtype=torch.uint8, pin_memory=True)
+            ln = torch.empty(N, dtype=torch.int32, device=DEV)
+            ibp.ibp_compress(st.h, sl, d, R, None, N, ln)
+            torch.cuda.synchronize()
+            ibp.ibp_store_set_lengths(st.h, ln)
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+            lengths.append(ln)
+        ln_np = lengths[0].cpu().numpy()
+        min_bytes = int(ln_np[ln_np < R].min())
+        assert (ln_np[ln_np < R] > min_bytes).mean() > 0.2  # many rows need more than the shortest stream
+        ids = np.stack([wl.zipf_ids(B, N, table=t, seed=3) for t in range(T)], axis=1)
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            out = torch.full((B, T, R), 0xCC, dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress(grp, out, T * R, to_dev(ids), B)
+            for s in stores:
+                assert s.status() == ibp.IBP_OK
+            o = out.cpu().numpy()
+            for t in range(T):
+                assert np.array_equal(o[:, t], tables[t][ids[:, t]]), t
+            ws = torch.empty(ibp.order_workspace_bytes(B * T), dtype=torch.uint8, device=DEV)
+            out2 = torch.zeros_like(out)
+            ibp.ibp_group_gather_decompress_ordered(grp, out2, T * R, to_dev(ids), B, ws,
+                                                    ws.numel())
+            assert torch.equal(out, out2)
+            # store 2 gets a new Mask/Bitval: the group's copy of its properties is stale
+            d2 = torch.from_numpy(tables[2]).to(DEV)
+            ibp.ibp_build_meta(stores[2].h, d2, R, None, N, 1, 1)
+            torch.cuda.synchronize()
+            out.fill_(0xCC)
+            ibp.ibp_group_gather_decompress(grp, out, T * R, to_dev(ids), B)
+            assert stores[2].status() == ibp.IBP_EINVAL
+            for t in (0, 1, 3, 4):
+                assert stores[t].status() == ibp.IBP_OK
+            o = out.cpu().numpy()
+            assert not o[:, 2].any()
+            for t in (0, 1, 3, 4):
+                assert np.array_equal(o[:, t], tables[t][ids[:, t]]), t
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()

@@ -117,7 +117,6 @@ def test_compress_and_decompress_fuzz(stores, R, C):
     assert np.array_equal(stored, ref_st)
     assert np.array_equal(st.bitmap(), ref_bm)
     assert_streams_equal(slots.cpu().numpy(), ref_sl, ref_st)
-    assert 0 < ref_bm.sum() or True
     out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
     ibp.ibp_decompress(st.h, out, slots, None, n)
     assert st.status() == ibp.IBP_OK

@@ -331,3 +331,64 @@ def test_decode_step_captured_in_a_cuda_graph():
             assert np.array_equal(out.cpu().numpy(), expect), step
     finally:
         st.close()
+
+
+def test_graph_replayed_after_a_rebuild_reports_einval():
+    """A decompression and a compression captured in a CUDA graph keep the
+    store properties of the Mask/Bitval current at capture.  Replayed after
+    the Mask/Bitval was rebuilt, they must not decode or pack with them: the
+    decompression zero-fills its rows and the compression writes nothing,
+    both setting IBP_EINVAL.  A fresh capture works again."""
+    rows, _ = wl.tiny_rows(seed=21, n_rows=2048, raw_frac=0.01)
+    rb = rows_u8(rows)
+    n, R, C = rb.shape[0], rb.shape[1], 256
+    st = Store(R, C, n, R)
+    try:
+        d = torch.from_numpy(rb).to(DEV)
+        ibp.ibp_build_meta(st.h, d, R, None, n, 95, 100)
+        slots = torch.zeros((n, R), dtype=torch.uint8, device=DEV)
+        ibp.ibp_compress(st.h, slots, d, R, None, n, None)
+        torch.cuda.synchronize()  # the store's properties reach the host
+        out = torch.zeros((n, R), dtype=torch.uint8, device=DEV)
+        slots2 = torch.zeros_like(slots)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # warm-up of the specialised forms
+            ibp.ibp_decompress(st.h, out, slots, None, n, side)
+            ibp.ibp_compress(st.h, slots2, d, R, None, n, None, side)
+        torch.cuda.synchronize()
+        assert st.status() == ibp.IBP_OK
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            sp = torch.cuda.current_stream()
+            ibp.ibp_decompress(st.h, out, slots, None, n, sp)
+            ibp.ibp_compress(st.h, slots2, d, R, None, n, None, sp)
+        out.zero_()
+        slots2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert st.status() == ibp.IBP_OK
+        assert np.array_equal(out.cpu().numpy(), rb)
+        assert torch.equal(slots2, slots)
+        # a rebuild (another threshold) starts a new generation of the store's tables
+        ibp.ibp_build_meta(st.h, d, R, None, n, 1, 1)
+        torch.cuda.synchronize()
+        out.fill_(0x5A)
+        slots2.fill_(0x77)
+        g.replay()
+        torch.cuda.synchronize()
+        assert st.status() == ibp.IBP_EINVAL
+        assert not out.any(), "stale replay must zero-fill its rows"
+        assert bool((slots2 == 0x77).all()), "stale replay must not write slots"
+        # uncaptured calls and a new capture use the new tables
+        ibp.ibp_compress(st.h, slots, d, R, None, n, None)
+        torch.cuda.synchronize()
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2):
+            ibp.ibp_decompress(st.h, out, slots, None, n, torch.cuda.current_stream())
+        g2.replay()
+        torch.cuda.synchronize()
+        assert st.status() == ibp.IBP_OK
+        assert np.array_equal(out.cpu().numpy(), rb)
+    finally:
+        st.close()

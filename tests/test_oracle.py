@@ -374,6 +374,32 @@ def test_pack_slots_layout():
         assert got == rows[i].tobytes()
 
 
+def test_packed_cache_golden():
+    """Hand-worked packed cache (tests/golden/e6_packed_cache.txt): the
+    stored words and raw bits of three rows (both chunks packed, one chunk
+    raw, a raw row), and the 16-byte rounded offsets they pack at."""
+    g = golden_io.load("e6_packed_cache.txt")
+    R, C = g["R"], g["C"]
+    mask = np.array(g["mask"], np.uint32)
+    bitval = np.array(g["bitval"], np.uint32)
+    rows = np.stack([np.array(g["row%d" % i], np.uint32) for i in range(3)]).view(np.uint8)
+    slots = np.full((3, R), 0xEE, np.uint8)
+    bitmap = np.zeros(1, np.uint32)
+    stored = ref_c.compress_batch(rows, C, mask, bitval, slots, bitmap, nthreads=1)
+    for i in range(3):
+        want = np.array(g["stored%d" % i], np.uint32).view(np.uint8)
+        assert int(stored[i]) == len(want), i
+        assert np.array_equal(slots[i, :len(want)], want), i
+        assert (int(bitmap[0]) >> i) & 1 == g["rawbits"][i], i
+        got = py.compress(rows[i].tobytes(), C, list(mask), list(bitval))
+        assert got[0] == want.tobytes() and int(got[1]) == g["rawbits"][i], i
+    packed, offs = ref_c.pack_slots(slots, stored)
+    assert [int(o) for o in offs] == g["offsets"]
+    for i in range(3):
+        want = np.array(g["stored%d" % i], np.uint32).view(np.uint8)
+        assert np.array_equal(packed[offs[i]:offs[i] + len(want)], want), i
+
+
 def test_id_indexed_paths_match_their_definitions():
     """The id lists of the batch calls mean what they say: a build over sample
     ids is the build over rows[ids] (repeats counted, n = the sample's size),
