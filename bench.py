@@ -467,6 +467,10 @@ def run_ours(args, rank, world, torch, dist):
     # --- CPU baseline: the oracle on the host cores, one batch (rank 0, N = 1)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(store, ids_np, ibp)
+        # the oracle's rows for 2000 ids of the last timed batch against the
+        # GPU's, the generated rows and the oracle's compression of them
+        leg = oracle_leg(ibp, store.st, store.slots, R, store.C, ids_np[last][pick], got, want)
+        result["cpu_baseline"]["parity_oracle_ok"] = leg["parity_oracle_ok"]
 
     # --- the chunk-aware builder: the threshold chosen from the sample itself
     if not args.no_tuned:
@@ -575,6 +579,28 @@ def run_tiny(args, rank, world, torch, dist):
         dist.barrier()
     assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
     parity_ok = bool(torch.equal(out, d_rows))
+    # cpu_baseline leg: the oracle decodes the first 8192 rows (two replicas)
+    # from a host copy of the packed cache; its rows against the GPU's
+    from oracle import ref_c
+    k_or = 2 * per
+    mask = np.zeros(R // 4, np.uint32)
+    bitval = np.zeros(R // 4, np.uint32)
+    ibp.ibp_meta_get(st, mask, bitval)
+    bitmap = np.zeros((n + 31) // 32, np.uint32)
+    ibp.ibp_bitmap_get(st, bitmap)
+    offs_np = offs[:k_or + 1].cpu().numpy().view(np.uint64)
+    cache_np = cache[:int(offs_np[-1]) + R].cpu().numpy()
+    threads = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    orows, obad = ref_c.decompress_batch(cache_np, bitmap, R, C, mask, bitval, n=k_or,
+                                         offsets=offs_np[:k_or], nthreads=threads)
+    t_or = time.perf_counter() - t0
+    leg = {"value": round(k_or * R / t_or / 1e9, 4), "unit": "GB/s", "cores": threads,
+           "kind": "oracle",
+           "sample": "the first %d rows of the packed cache decoded by the oracle C decoder "
+                     "(OpenMP over rows, %.2f s)" % (k_or, t_or),
+           "parity_oracle_ok": bool(obad == 0 and np.array_equal(orows, out[:k_or].cpu().numpy())
+                                    and np.array_equal(orows, rb[:k_or]))}
     t_total = sum(times)
     t_total = ibpdist.max_over_ranks(t_total, dist, dev)
     value = n * R * args.steps * world / t_total / 1e9
@@ -636,6 +662,7 @@ def run_tiny(args, rank, world, torch, dist):
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": n * R},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
+        "cpu_baseline": leg,
     }
     ibp.ibp_store_destroy(st)
     return res
@@ -713,6 +740,15 @@ def run_kv(args, rank, world, torch, dist):
     ibp.ibp_gather_decompress(stores[0], out, slots[0], None, ids, n, sp)
     torch.cuda.synchronize()
     parity_ok = bool(torch.equal(out, check))
+    # cpu_baseline leg: the oracle decodes 2048 sampled rows of layer 0's K
+    # store from the same host slots (its rows against the GPU's and the
+    # generated ones; its compression against the stored bytes)
+    pick = np.sort(np.random.default_rng(3).choice(n, 2048, replace=False))
+    ids_np = prompt_ids.cpu().numpy()
+    leg = oracle_leg(ibp, stores[0], slots[0], R, C, ids_np[pick],
+                     out.view(-1, R)[torch.from_numpy(pick).to(dev)].cpu().numpy(),
+                     check.reshape(-1, R)[torch.from_numpy(pick).to(dev)].cpu().numpy(),
+                     note="; layer 0 K store, prompt rows")
     evs = []
     with ClockSampler(dev.index) as clk:
         for b in range(args.steps):
@@ -854,6 +890,7 @@ def run_kv(args, rank, world, torch, dist):
         "gpu_launches": 2 * L * args.steps,
         "clocks": clk.summary(),
         "decode_steps": decode,
+        "cpu_baseline": leg,
         "attention_layout": {"value": round(att_gbs, 3), "unit": "GB/s", "steps": asteps,
                              "frac": round(att_gbs / roof, 4), "parity_layer0_ok": att_ok,
                              "note": "the same 64 gathers per step written as [20, 32, 1920, "
@@ -1104,6 +1141,7 @@ def run_dlrm(args, rank, world, torch, dist):
     g = torch.Generator(device=dev)
     stored_sum = []
     check_rows = []
+    lengths = []  # each table's stored sizes, attached to its store (length table)
     batches = [np.stack([wl.zipf_ids(B, N, table=t, seed=args.seed * 1000 + bb)
                          for t in range(Tn)], axis=1) for bb in range(min(args.pool, 4))]
     for t in range(Tn):
@@ -1115,6 +1153,8 @@ def run_dlrm(args, rank, world, torch, dist):
         sl = torch.empty((N, R), dtype=torch.uint8, pin_memory=True)
         stored = torch.empty(N, dtype=torch.int32, device=dev)
         ibp.ibp_compress(st, sl, x, R, None, N, stored)
+        ibp.ibp_store_set_lengths(st, stored)
+        lengths.append(stored)
         stored_sum.append(stored.to(torch.int64).cpu().numpy())
         # the rows the last batch looks up in this table, for the parity check
         check_rows.append(x[torch.from_numpy(batches[-1][:, t]).to(dev)].cpu())
@@ -1199,16 +1239,28 @@ def run_dlrm(args, rank, world, torch, dist):
     torch.cuda.synchronize()
     ordered_same = bool(torch.equal(out, out_o))
     oev = []
-    for b in range(args.steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step_ordered(b)
-        e1.record(stream)
-        oev.append((e0, e1))
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk_o:
+        for b in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step_ordered(b)
+            e1.record(stream)
+            oev.append((e0, e1))
+        torch.cuda.synchronize()
     for st in stores:
         assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    # cpu_baseline leg: the oracle decodes sampled lookups of the last batch in
+    # three tables from the same host slots; its rows must equal the GPU's and
+    # the tables' rows, and its compression of those rows the stored bytes
+    step_ordered(pool - 1)
+    torch.cuda.synchronize()
+    o_np = out_o.cpu().numpy()
+    pick = np.random.default_rng(5).choice(B, 1024, replace=False)
+    legs = []
+    for t in (0, Tn // 2, Tn - 1):
+        legs.append(oracle_leg(ibp, stores[t], slots[t], R, C, batches[pool - 1][pick, t],
+                               o_np[pick, t], check_rows[t].numpy()[pick]))
     ibp.ibp_group_destroy(grp)
     otimes = [a.elapsed_time(c) / 1e3 for a, c in oev]
     plain_gbs = B * Tn * R * len(times) / sum(times) / 1e9
@@ -1246,6 +1298,7 @@ def run_dlrm(args, rank, world, torch, dist):
                                "slots, chunk 1 KB, 1%% sample, T=0.95; batch 8192 Zipf(1.05) ids "
                                "per table -> [8192, 26, %d], ordered fused gather" % (N, dim, dim),
                    "row_bytes": R, "launches_per_step": 4,
+                   "length_tables": "each table's stored sizes attached (one fetch per row)",
                    "l2": "flushed between steps (256 MB write, outside the timed events)"},
         "ratio": round(ratio, 5), "ratio_distinct_rows": round(ratio_unique, 5),
         "link_gbs": round(link, 2),
@@ -1263,10 +1316,19 @@ def run_dlrm(args, rank, world, torch, dist):
                      "kernel": "k_gather_group, ordered (ibp_group_gather_decompress_ordered: "
                                "three bucketing kernels and the gather)"},
         "gpu_launches": 4 * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk_o.summary(),
+        "cpu_baseline": {
+            "value": round(len(legs) * 1024 * R / sum(len(pick) * R / (l["value"] * 1e9)
+                                                       for l in legs) / 1e9, 4),
+            "unit": "GB/s", "cores": legs[0]["cores"], "kind": "oracle",
+            "sample": "1024 lookups of the last batch in tables 0, %d and %d decoded by the "
+                      "oracle C decoder from the same host slots" % (Tn // 2, Tn - 1),
+            "parity_oracle_ok": all(l["parity_oracle_ok"] for l in legs)},
     }
     for st in stores:
+        ibp.ibp_store_set_lengths(st, None)
         ibp.ibp_store_destroy(st)
+    del lengths
     return res
 
 
@@ -1354,8 +1416,12 @@ def run_dense(args, rank, world, torch, dist):
             assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
             last = (warm + steps - 1) % pool
             pick = np.random.default_rng(C).choice(len(ids_np[last]), 2000, replace=False)
-            ok = bool(np.array_equal(out[torch.from_numpy(pick).to(dev)].cpu().numpy(),
-                                     rb[ids_np[last][pick]]))
+            got_pick = out[torch.from_numpy(pick).to(dev)].cpu().numpy()
+            ok = bool(np.array_equal(got_pick, rb[ids_np[last][pick]]))
+            if C == 1024:  # cpu_baseline leg of the headline chunk size
+                leg = oracle_leg(ibp, st, slots, R, C, ids_np[last][pick], got_pick,
+                                 rb[ids_np[last][pick]],
+                                 note="; 2000 ids of the last timed mini-batch")
             ideal = min(hbm, link / ratio)
             # what the link carries: whole 128-byte lines, a line's tail read
             # costing 32, 64 or 128 bytes (the transfers workload's
@@ -1393,6 +1459,7 @@ def run_dense(args, rank, world, torch, dist):
         "chunks": points,
         "gpu_launches": launches,
         "clocks": clk.summary(),
+        "cpu_baseline": leg,
     }
 
 
@@ -1733,6 +1800,58 @@ def cpu_baseline(store, batches, ibp, seconds=1.5):
                       "decoder, OpenMP over rows" % (k, len(batches[0]), dt)}
 
 
+def oracle_leg(ibp, st, slots, R, C, ids, gpu_rows, raw_rows=None, threads=None,
+               note=""):
+    """The cpu_baseline leg of a sub-result: the oracle decodes rows `ids` of
+    the same host slots on the host cores (timed), and its rows are compared
+    byte for byte with the GPU's output for those ids (gpu_rows) and, when
+    given, with the rows the store was compressed from (raw_rows), whose
+    oracle compression must also equal the stored bytes in the slots."""
+    from oracle import ref_c
+    W = R // 4
+    info = ibp.ibp_store_get_info(st)
+    mask = np.zeros(W, np.uint32)
+    bitval = np.zeros(W, np.uint32)
+    ibp.ibp_meta_get(st, mask, bitval)
+    bitmap = np.zeros((info.n_rows + 31) // 32, np.uint32)
+    ibp.ibp_bitmap_get(st, bitmap)
+    threads = threads or len(os.sched_getaffinity(0))
+    slots_np = slots.numpy() if hasattr(slots, "numpy") else slots
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    t0 = time.perf_counter()
+    out, bad = ref_c.decompress_batch(slots_np, bitmap, R, C, mask, bitval, ids=ids,
+                                      slot_stride=int(info.slot_bytes), nthreads=threads)
+    dt = time.perf_counter() - t0
+    ok = bad == 0 and np.array_equal(out, gpu_rows)
+    if raw_rows is not None:
+        ok = ok and np.array_equal(out, raw_rows)
+        # the oracle's own compression of the same rows: stored bytes and raw bits
+        k = min(len(ids), 512)
+        ref_sl = np.zeros((k, int(info.slot_bytes)), np.uint8)
+        ref_bm = np.zeros((k + 31) // 32, np.uint32)
+        ref_st = ref_c.compress_batch(np.ascontiguousarray(raw_rows[:k]), C, mask, bitval, ref_sl,
+                                      ref_bm, nthreads=threads)
+        sl2 = slots_np.reshape(info.n_rows, -1)
+        for j in range(k):
+            i = int(ids[j])
+            ok = ok and bool(((bitmap[i >> 5] >> (i & 31)) & 1) == ((ref_bm[j >> 5] >> (j & 31)) & 1))
+            ok = ok and np.array_equal(sl2[i, :ref_st[j]], ref_sl[j, :ref_st[j]])
+    return {"value": round(len(ids) * R / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d rows of this workload decoded by the oracle C decoder (OpenMP over "
+                      "rows, %.2f s)%s" % (len(ids), dt, note),
+            "parity_oracle_ok": bool(ok)}
+
+
+def free_host_cache(torch):
+    """Return cached pinned host blocks and device blocks between workloads."""
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    if hasattr(torch._C, "_host_emptyCache"):
+        torch._C._host_emptyCache()
+
+
 def run_reference(args, rank, world, torch):
     """The oracle as it stands, on the host cores, same workload and metric."""
     from lossless_invariant_bit_gb300 import workloads as wl
@@ -1807,6 +1926,8 @@ def main():
                     help="skip the HBM cache-front sub-result of the default workload")
     ap.add_argument("--no-cache-path", action="store_true",
                     help="skip the HBM cache-path sub-result of the default workload")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the dense GNN, DLRM and KV sub-results of the default workload")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -1841,8 +1962,35 @@ def main():
         t = run_tiny(sub, rank, world, torch, dist)
         res["cache_path"] = {k: t[k] for k in ("value", "unit", "steps", "ms_per_step", "ratio",
                                                "parity_all_rows_ok", "single_batch_us", "roofline", "e2e",
-                                               "clocks")}
+                                               "clocks", "cpu_baseline")}
         res["cache_path"]["config"] = t["config"]["workload"]
+    if args.workload == "sparse" and not args.no_configs:
+        # the other workloads of the metric at their full sizes, each with its
+        # own roofline, clock record and oracle leg (sub-results of this line)
+        keep = ("value", "unit", "steps", "warmup", "ms_per_step", "ratio", "link_gbs",
+                "roofline", "clocks", "cpu_baseline", "gpu_launches")
+        subs = [("dense_gnn", run_dense, {}), ("dlrm_dim128", run_dlrm, {"dlrm_dim": 128}),
+                ("dlrm_dim512", run_dlrm, {"dlrm_dim": 512}), ("kv_fetch", run_kv, {})]
+        for key, fn, over in subs:
+            free_host_cache(torch)
+            sub = argparse.Namespace(**vars(args))
+            sub.steps, sub.warmup = min(args.steps, 20), max(3, min(args.warmup, 5))
+            for k_, v_ in over.items():
+                setattr(sub, k_, v_)
+            t0 = time.time()
+            r = fn(sub, rank, world, torch, dist)
+            d = {k_: r[k_] for k_ in keep if k_ in r}
+            d["config"] = r["config"]
+            for k_ in ("parity_all_lookups_ok", "parity_layer0_ok", "chunks", "fused_unordered",
+                       "per_store_launches", "ratio_distinct_rows", "raw_gather_gbs",
+                       "attention_layout", "decode_steps"):
+                if k_ in r:
+                    d[k_] = r[k_]
+            d["wall_s"] = round(time.time() - t0, 1)
+            res[key] = d
+            log("%s: %.1f GB/s (%.3f of its roofline) in %.0f s" % (
+                key, r["value"], r["roofline"]["frac"], time.time() - t0))
+        free_host_cache(torch)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if dist:
