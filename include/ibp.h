@@ -59,6 +59,10 @@ extern "C" {
 #define IBP_MAX_GROUP_STORES 64u
 /* device workspace bytes of the ordered gathers for n ids (or batch*T items) */
 #define IBP_ORDER_WORKSPACE_BYTES(n) (16ull * (uint64_t)(n) + 4096ull)
+/* device workspace bytes of ibp_project_compress for m rows of R bytes */
+#define IBP_PROJECT_WORKSPACE_BYTES(m, R) \
+  ((((uint64_t)(m) * ((uint64_t)(R) / 16ull) + 255ull) / 256ull) * 256ull + \
+   (uint64_t)(m) * (uint64_t)(R))
 
 typedef enum {
   IBP_OK = 0,
@@ -360,6 +364,41 @@ IBP_API ibp_status ibp_gather_decompress_cached(const ibp_store* store, void* ds
 IBP_API ibp_status ibp_pack(const ibp_store* store, void* dst_packed, uint64_t* offsets_out,
                             const void* src_slots, const uint32_t* stored_bytes, uint64_t n,
                             ibp_stream_t stream);
+
+/* K/V projection with the compressor in its epilogue (the review's LLM
+ * paragraph: the K/V of each decode token are compressed on the GPU with the
+ * Mask/Bitval built from the prompt's K/V, and offloaded to host memory).
+ * Computes Y = X W^T (+ bias) on the tensor cores, fp32 accumulation, and
+ * compresses each row of Y into its slot as ibp_compress would: the GEMM's
+ * epilogue tests each tile of a row against the Mask/Bitval and gathers its
+ * kept bits; a second kernel, launched behind it on the same stream
+ * (programmatic dependent launch), places them in each row's stream.
+ *   x          device [m, k_dim] 16-bit values, row-major (the tokens' inputs)
+ *   k_dim      contraction length, a multiple of 64
+ *   w          device [N, k_dim] 16-bit values, row-major (a K or V projection
+ *              weight, one output channel per row), N = R / 2
+ *   bias       NULL or device [N] values of the same type (16-byte aligned)
+ *   dtype      0: fp16 inputs, weights, bias and output; 1: bf16
+ *   y          device [m, N] output (R bytes per row): the projection itself,
+ *              rounded to the 16-bit type; the compressed rows are exactly
+ *              ibp_compress applied to these rows
+ *   dst_slots, slot_ids, stored_bytes_out  as for ibp_compress (row r of Y
+ *              goes to slot slot_ids[r], or r when slot_ids is NULL)
+ *   workspace  device memory of IBP_PROJECT_WORKSPACE_BYTES(m, R) bytes,
+ *              16-byte aligned, used during the call (stream-ordered)
+ * The store's chunks must be 256 bytes (one head of 128 16-bit values) and R
+ * a multiple of 256.  Reads the store's current Mask/Bitval on the device (no
+ * store properties are fixed on the host).  Errors: IBP_EINVAL (geometry,
+ * dtype, k_dim, workspace, m above 65535 * 128), IBP_EALIGN, IBP_ERANGE,
+ * IBP_ECUDA; a slot id out of range sets IBP_ERANGE in the status word (that
+ * row's slot is not written), and a device wait that gave up sets
+ * IBP_ETIMEOUT. */
+IBP_API ibp_status ibp_project_compress(ibp_store* store, const void* x, uint64_t m,
+                                        uint64_t k_dim, const void* w, const void* bias,
+                                        uint32_t dtype, void* y, void* dst_slots,
+                                        const int64_t* slot_ids, uint32_t* stored_bytes_out,
+                                        void* workspace, uint64_t workspace_bytes,
+                                        ibp_stream_t stream);
 
 /* Copy the store's Mask and Bitval (R/4 words each) to host arrays.  Synchronous. */
 IBP_API ibp_status ibp_meta_get(const ibp_store* store, uint32_t* mask_host, uint32_t* bitval_host);

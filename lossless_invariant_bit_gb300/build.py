@@ -1,7 +1,7 @@
 """Build libibp.so in-tree with nvcc for sm_103a (GB300).
 
 The translation units (kernels, C-ABI, allocation-free builder, transfer
-baselines) compile in parallel, then link into a
+baselines, projection with the compressor in its epilogue) compile in parallel, then link into a
 shared library beside this file.  The CUDA runtime is linked statically, so
 the library loads without any other CUDA library on the path.
 """
@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libibp.so")
-SOURCES = ["ibp_kernels.cu", "ibp_api.cu", "ibp_noalloc.cu", "ibp_transfer.cu"]
+SOURCES = ["ibp_kernels.cu", "ibp_api.cu", "ibp_noalloc.cu", "ibp_transfer.cu", "ibp_project.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -26,17 +26,51 @@ struct ibp_store {
   std::atomic<int> props_ready{0};  // 1 once props_ev was seen complete (reset by derive)
   const uint32_t* lengths = nullptr;  // caller's stored bytes per slot (device), or NULL
   uint64_t bitmap_words;
+  // the last source pointer a decode saw, with bit 0 set when it was pinned
+  // host memory (a pointer query costs more host time than a small launch)
+  std::atomic<uintptr_t> src_kind{0};
 };
 
 struct ibp_group {
   uint32_t T, R, C, W, wpc, nch;
   int device, sm_count;
+  uint32_t host_src;  // some store's slots are pinned host memory
   ibp::GroupEntry* entries;  // device copy, one per store
 };
+
+namespace ibp {
+
+bool host_pointer(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
+}  // namespace ibp
 
 namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Whether `src` is pinned host memory, remembered per store for the last
+// source seen.  Only the launch shape depends on it.  A stream being captured
+// makes no pointer query: an unseen source counts as device memory there.
+bool source_is_host(const ibp_store* s, const void* src, cudaStream_t st) {
+  const uintptr_t v = s->src_kind.load(std::memory_order_relaxed);
+  if ((v & ~(uintptr_t)1) == reinterpret_cast<uintptr_t>(src)) return (v & 1u) != 0;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return false;
+  }
+  const bool host = ibp::host_pointer(src);
+  const_cast<ibp_store*>(s)->src_kind.store(reinterpret_cast<uintptr_t>(src) | (host ? 1u : 0u),
+                                            std::memory_order_relaxed);
+  return host;
+}
 
 inline ibp_status cu(cudaError_t e) { return e == cudaSuccess ? IBP_OK : IBP_ECUDA; }
 
@@ -153,6 +187,7 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.group_stride = split.group_stride;
   a.out_pos = out_pos;
   a.lengths = s->lengths;
+  a.host_src = source_is_host(s, src, st) ? 1u : 0u;
   return cu(ibp::launch_decode(a, host_props(s, st), s->sm_count, st));
 }
 
@@ -537,6 +572,9 @@ ibp_status ibp_group_create(ibp_group** out, ibp_store* const* stores, const voi
     grp->nch = s0->nch;
     grp->device = s0->device;
     grp->sm_count = s0->sm_count;
+    grp->host_src = 0;
+    for (uint32_t t = 0; t < n; ++t)
+      if (ibp::host_pointer(srcs[t])) grp->host_src = 1;
     if (cudaMalloc(&grp->entries, sizeof(ibp::GroupEntry) * n) != cudaSuccess) {
       cudaGetLastError();
       e = IBP_ENOMEM;
@@ -587,6 +625,7 @@ ibp_status ibp_group_gather_decompress(const ibp_group* g, void* dst, uint64_t d
   a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
   a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u);
   a.order = nullptr;
+  a.host_src = g->host_src;
   return cu(ibp::launch_group(a, g->sm_count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -626,7 +665,57 @@ ibp_status ibp_group_gather_decompress_ordered(const ibp_group* g, void* dst,
   a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
   a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u);
   a.order = order;
+  a.host_src = g->host_src;
   return cu(ibp::launch_group(a, g->sm_count, st));
+}
+
+ibp_status ibp_project_compress(ibp_store* s, const void* x, uint64_t m, uint64_t k_dim,
+                                const void* w, const void* bias, uint32_t dtype, void* y,
+                                void* dst_slots, const int64_t* slot_ids,
+                                uint32_t* stored_bytes_out, void* workspace,
+                                uint64_t workspace_bytes, ibp_stream_t stream) {
+  if (!s) return IBP_EINVAL;
+  if (m == 0) return IBP_OK;
+  if (!x || !w || !y || !dst_slots || !workspace) return IBP_EINVAL;
+  if (dtype > 1u || k_dim == 0 || (k_dim % 64u) != 0 || k_dim > (1ull << 31)) return IBP_EINVAL;
+  // one chunk = one 128-column tile of 16-bit values
+  if (s->C != 256u || (s->R % 256u) != 0) return IBP_EINVAL;
+  if (!slot_ids && m > s->n_rows) return IBP_ERANGE;
+  if (m > 65535ull * 128ull) return IBP_EINVAL;  // row tiles in one grid dimension
+  if (workspace_bytes < IBP_PROJECT_WORKSPACE_BYTES(m, s->R)) return IBP_EINVAL;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(dst_slots) ||
+      !aligned16(workspace) || (bias && !aligned16(bias)) ||
+      (reinterpret_cast<uintptr_t>(slot_ids) & 7u) ||
+      (reinterpret_cast<uintptr_t>(stored_bytes_out) & 3u))
+    return IBP_EALIGN;
+  ibp_status e = on_device(s);
+  if (e != IBP_OK) return e;
+  ibp::ProjectArgs a;
+  a.mask = s->mask;
+  a.bitval = s->bitval;
+  a.nm = s->nm;
+  a.mv = s->mv;
+  a.ckeep = s->ckeep;
+  a.bitmap = s->bitmap;
+  a.status = s->status;
+  a.W = s->W;
+  a.nch = s->nch;
+  a.bf16 = dtype;
+  a.m = m;
+  a.k_dim = k_dim;
+  a.bias = bias;
+  a.y = static_cast<uint8_t*>(y);
+  a.dst = static_cast<uint8_t*>(dst_slots);
+  a.slot = s->slot;
+  a.slot_ids = slot_ids;
+  a.n_rows = s->n_rows;
+  a.stored_out = stored_bytes_out;
+  // workspace: a participation flag per (row, tile), up to 4 tiles per chunk,
+  // then the staged kept bits (R bytes per row)
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.flags = reinterpret_cast<uint32_t*>(ws);
+  a.staged = reinterpret_cast<uint32_t*>(ws + ((m * (s->R / 16u) + 255u) / 256u) * 256u);
+  return cu(ibp::launch_project(a, x, w, s->sm_count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ibp_status ibp_meta_get(const ibp_store* s, uint32_t* mask_host, uint32_t* bitval_host) {

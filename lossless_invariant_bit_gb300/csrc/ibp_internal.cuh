@@ -65,6 +65,7 @@ struct DecodeArgs {
   // NULL, or each row id's stored bytes (in HBM): the first fetch then takes
   // the whole stream, so rows with raw chunks need no second round trip
   const uint32_t* lengths;
+  uint32_t host_src;  // src is pinned host memory (sets the launch shape only)
 };
 
 struct EncodeArgs {
@@ -169,9 +170,43 @@ struct GroupArgs {
   uint32_t sbuf_words;
   uint32_t warp_words;
   const int64_t* order;     // NULL, or the items in address order (ordered gather)
+  uint32_t host_src;        // some store's slots are pinned host memory (launch shape only)
 };
 
+// K/V projection with the compressor in its epilogue (ibp_project_compress):
+// Y[m, N] = X[m, k_dim] W[N, k_dim]^T (+ bias), 16-bit in and out, in tiles
+// of 128 rows x (128 / seg) columns (N = nch * 128: a chunk is 1, 2 or 4
+// tiles), then each row of Y compressed into its slot.
+struct ProjectArgs {
+  const uint32_t* mask;     // the store's Mask, Bitval, ~Mask, move masks, kept bits per chunk
+  const uint32_t* bitval;
+  const uint32_t* nm;
+  const uint32_t* mv;
+  const uint32_t* ckeep;
+  uint32_t* bitmap;
+  uint32_t* status;
+  uint32_t W, nch;          // row words (R / 4) and chunks (R / 256)
+  uint32_t bf16;            // 1: bf16 values, 0: fp16
+  uint64_t m, k_dim;        // rows (tokens) and the contraction length (multiple of 64)
+  const void* bias;         // NULL or [N] values of the output type
+  uint8_t* y;               // [m, R bytes]: the projection's output
+  uint8_t* dst;             // slots (host-mapped or device)
+  uint64_t slot;            // slot stride
+  const int64_t* slot_ids;  // NULL: row r -> slot r
+  uint64_t n_rows;
+  uint32_t* stored_out;     // NULL or [m]
+  uint32_t* flags;          // [m, tiles]: every word of the (row, tile) matches the Mask
+  uint32_t* staged;         // [m, tiles, 64 / seg] packed kept bits of matching tiles
+};
+
+cudaError_t launch_project(const ProjectArgs& a, const void* x, const void* w, int sm_count,
+                           cudaStream_t st);
+
 cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st);
+uint64_t launch_blocks(uint64_t n, uint64_t full, uint64_t warps, uint64_t rpw, bool host,
+                       bool ordered);
+// Whether p points into pinned host memory (false when unknown).
+bool host_pointer(const void* p);
 bool fast_geometry(uint32_t R, uint32_t C);
 
 WarpSmem decode_smem(uint32_t W, uint32_t nch);

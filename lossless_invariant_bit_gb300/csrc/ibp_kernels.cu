@@ -1548,6 +1548,196 @@ __global__ void __launch_bounds__(256, 3) k_encode(EncodeArgs a, WarpSmem L) {
 }
 
 // ------------------------------------------------------------------------
+// Compression of rows above 2 KB, one CTA per row: the CTA's threads stage
+// the row in shared memory together and split its 16-byte groups between
+// them for the mismatch test and the packing, so a row costs a few memory
+// round trips instead of one warp walking 4-32 KB alone (a decode step's
+// handful of 8 KB K/V rows took ~25 us per call that way).  Same steps and
+// output as k_encode.
+// ------------------------------------------------------------------------
+template <bool kUni>
+__global__ void __launch_bounds__(256) k_encode_rows(EncodeArgs a) {
+  extern __shared__ __align__(16) uint32_t smem[];
+  __shared__ uint32_t s_words;
+  const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
+  const uint32_t nvec = R >> 4, G = W >> 2;
+  const uint32_t tid = threadIdx.x, T = blockDim.x, lane = tid & 31u, wid = tid >> 5;
+  uint32_t* xbuf = smem;           // the row: W words
+  uint32_t* obuf = xbuf + W;       // the packed stream: W + 8 words
+  uint32_t* cinfo = obuf + W + 8;  // per chunk: mismatch flag, then start | p << 31
+  // uniform parameters fixed on the host for an older Mask/Bitval (a launch
+  // replayed from a CUDA graph): write nothing, report IBP_EINVAL
+  if (kUni && __ldg(a.m.scal + 9) != a.gen) {
+    if (tid == 0 && blockIdx.x == 0) set_status(a.status, IBP_EINVAL);
+    return;
+  }
+  const bool by_group = (wpc & 3u) == 0u;
+  const uint32_t msk = ~(a.um0 | a.um1);
+  const uint32_t G4 = (G + 3u) & ~3u;
+  const uint32_t xs_sa = static_cast<uint32_t>(__cvta_generic_to_shared(xbuf));
+  auto put = [&](uint32_t v, uint32_t bit, uint32_t nbits) {
+    const uint32_t q = bit >> 5, sh = bit & 31u;
+    atomicOr(obuf + q, v << sh);
+    if (sh != 0u && sh + nbits > 32u) atomicOr(obuf + q + 1, v >> (32u - sh));
+  };
+  for (uint64_t i = blockIdx.x; i < a.n; i += gridDim.x) {
+    const int64_t slot = a.slot_ids ? __ldg(a.slot_ids + i) : (int64_t)i;
+    if (slot < 0 || (uint64_t)slot >= a.n_rows) {  // the same for every thread
+      if (tid == 0) {
+        set_status(a.status, IBP_ERANGE);
+        if (a.stored_out) a.stored_out[i] = 0;
+      }
+      continue;
+    }
+    const uint8_t* src = a.src + i * a.src_stride;
+    for (uint32_t v = tid; v < nvec; v += T)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(xs_sa + 16u * v),
+                   "l"(src + 16u * v));
+    cp_async_commit();
+    for (uint32_t k = tid; k < nch; k += T) cinfo[k] = 0;
+    cp_async_wait_n<0>();
+    __syncthreads();
+    // chunks with a Mask mismatch
+    if (by_group) {
+      for (uint32_t g = tid; g < G; g += T) {
+        const uint4 x4 = *reinterpret_cast<const uint4*>(xbuf + 4u * g);
+        uint32_t d;
+        if (kUni) {
+          d = ((x4.x & msk) ^ a.ubv) | ((x4.y & msk) ^ a.ubv) | ((x4.z & msk) ^ a.ubv) |
+              ((x4.w & msk) ^ a.ubv);
+        } else {
+          const uint4 m4 = __ldg(reinterpret_cast<const uint4*>(a.m.mask) + g);
+          const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(a.m.bitval) + g);
+          d = ((x4.x & m4.x) ^ b4.x) | ((x4.y & m4.y) ^ b4.y) | ((x4.z & m4.z) ^ b4.z) |
+              ((x4.w & m4.w) ^ b4.w);
+        }
+        if (d) cinfo[__ldg(a.gtab + g) & 0xFFFFu] = 1u;
+      }
+    } else {
+      for (uint32_t w = tid; w < W; w += T) {
+        const uint32_t m = kUni ? msk : __ldg(a.m.mask + w);
+        const uint32_t b = kUni ? a.ubv : __ldg(a.m.bitval + w);
+        if ((xbuf[w] & m) != b) cinfo[__ldg(a.m.kr + w) & 0xFFFFu] = 1u;
+      }
+    }
+    __syncthreads();
+    if (wid == 0) {  // participation, chunk sizes -> starts, stream words
+      uint32_t run = nch;
+      for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
+        const uint32_t k = k0 + lane;
+        uint32_t size = 0, p = 0;
+        if (k < nch) {
+          const uint32_t full = 32u * min(wpc, W - k * wpc);
+          const uint32_t keep = __ldg(a.m.ckeep + k);
+          p = (cinfo[k] == 0u && keep < full) ? 1u : 0u;
+          size = p ? keep : full;
+        }
+        const uint32_t incl = warp_inclusive_scan(size, lane);
+        if (k < nch) cinfo[k] = (run + incl - size) | (p << 31);
+        run += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) s_words = (run + 31u) >> 5;
+    }
+    __syncthreads();
+    const uint32_t words = s_words;
+    const bool raw = 4u * words >= R;
+    uint4* dslot = reinterpret_cast<uint4*>(a.dst + (uint64_t)slot * a.slot);
+    if (raw) {
+      for (uint32_t v = tid; v < nvec; v += T)
+        dslot[v] = *reinterpret_cast<const uint4*>(xbuf + 4u * v);
+    } else {
+      const uint32_t padded = (words + 3u) & ~3u;
+      for (uint32_t z = tid; z < padded + 4u; z += T) obuf[z] = 0;
+      __syncthreads();
+      for (uint32_t k = tid; k < nch; k += T)
+        if (cinfo[k] >> 31) atomicOr(obuf + (k >> 5), 1u << (k & 31u));
+      for (uint32_t g = tid; by_group && g < G; g += T) {
+        const uint32_t gd = __ldg(a.gtab + g);
+        const uint32_t k = gd & 0xFFFFu;
+        const uint32_t ci = cinfo[k];
+        const uint32_t start = ci & 0x7FFFFFFFu;
+        const uint4 x4 = *reinterpret_cast<const uint4*>(xbuf + 4u * g);
+        const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+        if (ci >> 31) {  // packed chunk: word w's kept bits at its all-packed offset + delta
+          if (kUni) {
+            uint32_t bit = start + (gd >> 16) * a.ukeep;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t v = ((xs[e] & a.um0) >> (a.ush & 31u)) |
+                                 ((xs[e] & a.um1) >> (a.ush >> 8));
+              if (a.ukeep) put(v, bit, a.ukeep);
+              bit += a.ukeep;
+            }
+          } else {
+            const uint32_t delta = start - __ldg(a.gtab + G4 + k);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint4 t0 = __ldg(a.t5 + (2u * (uint32_t)e) * G + g);
+              const uint4 t1 = __ldg(a.t5 + (2u * (uint32_t)e + 1u) * G + g);
+              uint32_t x = xs[e] & t1.y;  // the kept bits, gathered to the low end
+              uint32_t t = x & t0.x;
+              x = (x ^ t) | (t >> 1);
+              t = x & t0.y;
+              x = (x ^ t) | (t >> 2);
+              t = x & t0.z;
+              x = (x ^ t) | (t >> 4);
+              t = x & t0.w;
+              x = (x ^ t) | (t >> 8);
+              t = x & t1.x;
+              x = (x ^ t) | (t >> 16);
+              const uint32_t nb = __popc(t1.y);
+              if (nb) put(x, t1.w + delta, nb);
+            }
+          }
+        } else {  // raw chunk: the 4 words verbatim
+          uint32_t bit = start + ((gd >> 16) << 5);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            put(xs[e], bit, 32u);
+            bit += 32u;
+          }
+        }
+      }
+      for (uint32_t w = tid; !by_group && w < W; w += T) {
+        const uint32_t krw = __ldg(a.m.kr + w);  // chunk | word in chunk << 16
+        const uint32_t ci = cinfo[krw & 0xFFFFu];
+        const bool packed = (ci >> 31) != 0u;
+        uint32_t v = xbuf[w];
+        uint32_t nbits = 32;
+        uint32_t bit;
+        if (kUni) {
+          bit = (ci & 0x7FFFFFFFu) + (krw >> 16) * (packed ? a.ukeep : 32u);
+          if (packed) {
+            v = ((v & a.um0) >> (a.ush & 31u)) | ((v & a.um1) >> (a.ush >> 8));
+            nbits = a.ukeep;
+          }
+        } else {
+          bit = (ci & 0x7FFFFFFFu) + (packed ? __ldg(a.m.pre + w) : ((krw >> 16) << 5));
+          if (packed) {
+            const uint32_t keepm = __ldg(a.m.nm + w);
+            v = gather_bits(v & keepm, a.m.mv, W, w);
+            nbits = __popc(keepm);
+          }
+        }
+        if (nbits) put(v, bit, nbits);
+      }
+      __syncthreads();
+      for (uint32_t v = tid; 4u * v < padded; v += T)
+        dslot[v] = *reinterpret_cast<const uint4*>(obuf + 4u * v);
+    }
+    if (tid == 0) {
+      const uint32_t bitm = 1u << ((uint64_t)slot & 31u);
+      if (raw)
+        atomicOr(a.bitmap + ((uint64_t)slot >> 5), bitm);
+      else
+        atomicAnd(a.bitmap + ((uint64_t)slot >> 5), ~bitm);
+      if (a.stored_out) a.stored_out[i] = raw ? R : 4u * words;
+    }
+    __syncthreads();  // the buffers are refilled for the next row
+  }
+}
+
+// ------------------------------------------------------------------------
 // Aligned zero-copy copy (the review's GPU aligned transfer): consecutive
 // lanes take consecutive 16-byte vectors, so every warp load covers four
 // whole 128-byte lines; eight loads per thread are in flight before the
@@ -1978,6 +2168,29 @@ int max_smem_optin() {
 }
 }  // namespace
 
+// CTAs for a gather of n rows (or items) by persistent warps, `full` CTAs
+// filling the GPU:
+//   - ordered gathers take 32-row chunks in turn, as many CTAs as fit (a grid
+//     cut to sweep the sorted list in more rounds, so that the warps stay
+//     within a smaller address range at a time, measured slower: 192 against
+//     243 GB/s on 26 tables of 2 KB rows, 53 GB of host slots);
+//   - other gathers from pinned host memory spread the rows over every SM (a
+//     few rows per warp: the link's latency wants many rows in flight, and
+//     a few thousand rows would otherwise sit on a few SMs);
+//   - from HBM, at least `rpw` rows per warp (one resolve chunk: measured best
+//     for batches of a few thousand rows), else as many CTAs as fit.
+uint64_t launch_blocks(uint64_t n, uint64_t full, uint64_t warps, uint64_t rpw, bool host,
+                       bool ordered) {
+  if (ordered) return (n + 32ull * warps - 1) / (32ull * warps);
+  if (host) {
+    uint64_t r = (n + full * warps - 1) / (full * warps);
+    if (r > 32) r = 32;
+    if (r < 1) r = 1;
+    return (n + r * warps - 1) / (r * warps);
+  }
+  return (n + rpw * warps - 1) / (rpw * warps);
+}
+
 template <bool kIds, int kMode, bool kBig, bool kSplit>
 cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, cudaStream_t st) {
   FastParams F;
@@ -2008,11 +2221,8 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   auto kern = k_decode_fast<kIds, kMode, kBig, kSplit>;
   const int bps = blocks_per_sm(kern, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  // rows per warp at least 32 (one resolve chunk; measured best for batches of
-  // a few thousand rows up to 2 KB) or, above 2 KB, 8 (a few thousand such
-  // rows still spread over every SM); else as many CTAs as fit
-  const uint64_t rpw = kBig ? 8ull : 32ull;
-  const uint64_t need = (a.n + rpw * warps - 1) / (rpw * warps);
+  const uint64_t need = launch_blocks(a.n, blocks, (uint64_t)warps, kBig ? 8ull : 32ull,
+                                      a.host_src != 0u, kIds && a.out_pos != nullptr);
   if (blocks > need) blocks = need;
   kern<<<(uint32_t)blocks, 32 * warps, smem, st>>>(a, F);
   return cudaGetLastError();
@@ -2086,12 +2296,24 @@ cudaError_t launch_encode_v(const EncodeArgs& a, int sm_count, cudaStream_t st) 
 }
 
 template <bool kUni>
+cudaError_t launch_encode_rows(const EncodeArgs& a, int sm_count, cudaStream_t st) {
+  const uint32_t W = a.m.W;
+  const size_t smem = 4ull * (2ull * W + 8ull + ((a.m.nch + 3u) & ~3u));
+  const int threads = 256;
+  const int bps = blocks_per_sm(k_encode_rows<kUni>, threads, smem);
+  uint64_t blocks = (uint64_t)sm_count * bps;
+  if (blocks > a.n) blocks = a.n;
+  k_encode_rows<kUni><<<(uint32_t)blocks, threads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <bool kUni>
 cudaError_t launch_encode_t(const EncodeArgs& a, int sm_count, cudaStream_t st) {
   const uint32_t nvec = a.m.R >> 4;
   if (nvec <= 32u) return launch_encode_v<kUni, 1>(a, sm_count, st);
   if (nvec <= 64u) return launch_encode_v<kUni, 2>(a, sm_count, st);
   if (nvec <= 128u) return launch_encode_v<kUni, 4>(a, sm_count, st);
-  return launch_encode_v<kUni, 0>(a, sm_count, st);
+  return launch_encode_rows<kUni>(a, sm_count, st);  // rows above 2 KB: a CTA per row
 }
 
 cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count,
@@ -2136,7 +2358,8 @@ cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st) {
   const size_t smem = 4ull * (g.T * (sizeof(GroupEntry) / 4) + (uint64_t)warps * g.warp_words);
   const int bps = blocks_per_sm(k_gather_group, 32 * warps, smem);
   uint64_t blocks = (uint64_t)sm_count * bps;
-  const uint64_t need = (g.n_items + 8ull * warps - 1) / (8ull * warps);
+  const uint64_t need = launch_blocks(g.n_items, blocks, (uint64_t)warps, 8ull, g.host_src != 0u,
+                                      g.order != nullptr);
   if (blocks > need) blocks = need;
   k_gather_group<<<(uint32_t)blocks, 32 * warps, smem, st>>>(g);
   return cudaGetLastError();

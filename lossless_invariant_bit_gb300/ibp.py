@@ -71,6 +71,7 @@ _SIGS = {
     "ibp_gather_copy": [_P, _P, _U64, _U32, _P, _U64, _U64, _P],
     "ibp_gather_copy_dma": [_P, _P, _U64, _U32, _P, _U64, _U64, _P],
     "ibp_gather_copy_staged": [_P, _P, _U64, _U32, _P, _U64, _U64, _P, _P],
+    "ibp_project_compress": [_P, _P, _U64, _U64, _P, _P, _U32, _P, _P, _P, _P, _P, _U64, _P],
 }
 
 
@@ -214,6 +215,24 @@ def ibp_gather_decompress_split(store: int, dst, group_rows: int, group_stride: 
 def ibp_store_set_lengths(store: int, lengths) -> None:
     """Attach each slot's stored bytes (device uint32/int32 [n_rows]) or detach (None)."""
     _check(_lib_handle().ibp_store_set_lengths(store, _ptr(lengths)), "ibp_store_set_lengths")
+
+
+def project_workspace_bytes(m: int, row_bytes: int) -> int:
+    """IBP_PROJECT_WORKSPACE_BYTES(m, R) of include/ibp.h."""
+    m, R = int(m), int(row_bytes)
+    return (m * (R // 16) + 255) // 256 * 256 + m * R
+
+
+def ibp_project_compress(store: int, x, m: int, k_dim: int, w, bias, dtype: int, y, dst_slots,
+                         slot_ids, stored_bytes_out, workspace, workspace_bytes: int,
+                         stream=None) -> None:
+    """Y = X W^T (+ bias) on the tensor cores, each row of Y compressed into
+    its slot in the same launch (dtype 0: fp16, 1: bf16)."""
+    _check(_lib_handle().ibp_project_compress(store, _ptr(x), m, k_dim, _ptr(w), _ptr(bias),
+                                              dtype, _ptr(y), _ptr(dst_slots), _ptr(slot_ids),
+                                              _ptr(stored_bytes_out), _ptr(workspace),
+                                              workspace_bytes, _stream(stream)),
+           "ibp_project_compress")
 
 
 def order_workspace_bytes(n: int) -> int:

@@ -91,3 +91,17 @@ def test_binding_raises_on_error(lib):
     with pytest.raises(ibp.IbpError) as ei:
         ibp.ibp_store_create(1000, 256, 10)
     assert ei.value.status == ibp.IBP_EINVAL
+
+
+def test_project_compress_host_checks(lib):
+    """The fused projection rejects a missing store on the host, and its
+    workspace size is the header's formula: a 4-byte participation flag per
+    (row, tile), up to four tiles per 256-byte chunk (rounded to 256 bytes),
+    then R bytes of staged kept bits per row."""
+    assert lib.ibp_project_compress(None, 16, 20, 4096, 16, None, 0, 16, 16, None, None, 16,
+                                    1 << 20, None) == ibp.IBP_EINVAL
+    # m = 20 rows of 8 KB (32 chunks, up to 128 tiles): 20*128*4 = 10240 + 20*8192
+    assert ibp.project_workspace_bytes(20, 8192) == 10240 + 163840
+    # m = 300: 300*512 = 153600 bytes of flags (a multiple of 256)
+    assert ibp.project_workspace_bytes(300, 8192) == 153600 + 300 * 8192
+    assert ibp.project_workspace_bytes(3, 256) == 256 + 768
