@@ -696,6 +696,7 @@ ibp_status ibp_project_compress(ibp_store* s, const void* x, uint64_t m, uint64_
   a.nm = s->nm;
   a.mv = s->mv;
   a.ckeep = s->ckeep;
+  a.pre = s->pre;
   a.bitmap = s->bitmap;
   a.status = s->status;
   a.W = s->W;

@@ -183,6 +183,7 @@ struct ProjectArgs {
   const uint32_t* nm;
   const uint32_t* mv;
   const uint32_t* ckeep;
+  const uint32_t* pre;      // kept bits of the earlier words of each word's chunk
   uint32_t* bitmap;
   uint32_t* status;
   uint32_t W, nch;          // row words (R / 4) and chunks (R / 256)

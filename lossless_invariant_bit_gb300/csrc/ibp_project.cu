@@ -47,6 +47,19 @@
 namespace ibp {
 namespace {
 
+// Most tiles a chunk is cut into for small batches (1, 2 or 4).
+#ifndef IBP_PROJECT_MAX_SEG
+#define IBP_PROJECT_MAX_SEG 4u
+#endif
+// Most stages in the ring (fewer when the stages are larger).
+#ifndef IBP_PROJECT_MAX_STAGES
+#define IBP_PROJECT_MAX_STAGES 16u
+#endif
+// Accumulators in tensor memory, taken by the k-blocks in turn (1, 2 or 4).
+#ifndef IBP_PROJECT_ACCUMULATORS
+#define IBP_PROJECT_ACCUMULATORS 4u
+#endif
+
 constexpr uint32_t kPjBM = 128;           // rows per tile (the MMA's M)
 constexpr uint32_t kPjBK = 64;            // K elements per stage: one 128-byte row
 constexpr uint32_t kPjRing = 200u * 1024u;  // shared-memory bytes of the stage ring
@@ -60,11 +73,20 @@ template <int kSeg, int kAR>
 struct PjShape {
   static constexpr uint32_t BN = 128u / kSeg;             // columns per tile
   static constexpr uint32_t WPT = 64u / kSeg;             // row words per tile
-  static constexpr uint32_t A = (uint32_t)kAR * 128u;     // bytes of X per stage
-  static constexpr uint32_t B = BN * 128u;                // bytes of W per stage
-  static constexpr uint32_t S0 = kPjRing / (A + B);
-  static constexpr uint32_t S = S0 > 16u ? 16u : S0;      // stages
-  static constexpr uint32_t TMEM = BN < 32u ? 32u : BN;   // accumulator columns
+  static constexpr uint32_t A = (uint32_t)kAR * 128u;     // bytes of X per k-block
+  static constexpr uint32_t B = BN * 128u;                // bytes of W per k-block
+  // k-blocks per stage: one TMA copy of each operand fetches them all (a
+  // copy has a cost of its own besides its bytes: with one k-block per
+  // stage, narrow tiles streamed W at the same k-blocks per second whatever
+  // their width)
+  static constexpr uint32_t KB = (A + B) <= 12288u ? 4u : (A + B) <= 24576u ? 2u : 1u;
+  static constexpr uint32_t SA = KB * A, SB = KB * B;     // bytes per stage
+  static constexpr uint32_t S0 = kPjRing / (SA + SB);
+  static constexpr uint32_t S = S0 > IBP_PROJECT_MAX_STAGES ? IBP_PROJECT_MAX_STAGES : S0;
+  // independent accumulators the k-blocks take in turn: consecutive MMAs into
+  // one accumulator wait for each other, and a narrow tile's MMAs are short
+  static constexpr uint32_t ACC = IBP_PROJECT_ACCUMULATORS;
+  static constexpr uint32_t TMEM = ACC * BN;             // accumulator columns (<= 512)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -88,30 +110,38 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-// Wait for the phase of `parity` to complete, for at most ~2 s.
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(a), "r"(parity), "r"(1000000u)
+      : "memory");
+  return done != 0u;
+}
+
+// Wait for the phase of `parity` to complete, for at most ~2 s (the clock is
+// read only once the first test has failed).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_addr(bar);
+  if (mbar_try(a, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity), "r"(1000000u)
-        : "memory");
-    if (done) return true;
+    if (mbar_try(a, parity)) return true;
     if (global_ns() - t0 > 2000000000ull) return false;
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t x, int32_t y) {
+// One TMA copy of a 3-D box {64 elements, rows, k-blocks} into shared memory
+// (coordinates: element 0, first row, first k-block), completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t row, int32_t kblock) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(0), "r"(row), "r"(kblock)
       : "memory");
 }
 
@@ -189,8 +219,8 @@ __global__ void __launch_bounds__(128, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
-  uint8_t* s_x = smem;                // P::S tiles of X (kAR rows each)
-  uint8_t* s_w = smem + P::S * P::A;  // P::S tiles of W (BN rows each)
+  uint8_t* s_x = smem;                 // P::S stages of X: KB tiles of kAR rows each
+  uint8_t* s_w = smem + P::S * P::SA;  // P::S stages of W: KB tiles of BN rows each
   uint32_t* s_meta = reinterpret_cast<uint32_t*>(smem + kPjRing);
   uint64_t* full = reinterpret_cast<uint64_t*>(s_meta + kPjMetaWords);
   uint64_t* empty = full + P::S;
@@ -238,32 +268,41 @@ __global__ void __launch_bounds__(128, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *s_tmem;
 
+  const uint32_t st_n = (kb_n + P::KB - 1) / P::KB;  // stages to fill
   if (warp == 0 && lane == 0) {  // producer
-    for (uint32_t kb = 0; kb < kb_n; ++kb) {
-      const uint32_t s = kb % P::S, round = kb / P::S;
+    for (uint32_t ks = 0; ks < st_n; ++ks) {
+      const uint32_t s = ks % P::S, round = ks / P::S;
       if (round > 0 && !mbar_wait(empty + s, (round - 1u) & 1u)) {
         atomicExch(s_fail, 1u);
         break;
       }
       if (*reinterpret_cast<volatile uint32_t*>(s_fail)) break;
-      mbar_expect_tx(full + s, P::A + P::B);
-      tma_load_2d(s_x + s * P::A, &tmap_x, full + s, (int32_t)(kb * kPjBK), (int32_t)m0);
-      tma_load_2d(s_w + s * P::B, &tmap_w, full + s, (int32_t)(kb * kPjBK), (int32_t)n0);
+      // k-blocks past the end of K read as zero (and are not multiplied)
+      mbar_expect_tx(full + s, P::SA + P::SB);
+      tma_load_3d(s_x + s * P::SA, &tmap_x, full + s, (int32_t)m0, (int32_t)(ks * P::KB));
+      tma_load_3d(s_w + s * P::SB, &tmap_w, full + s, (int32_t)n0, (int32_t)(ks * P::KB));
     }
   } else if (warp == 1 && lane == 0) {  // MMA issuer
     const uint32_t idesc = mma_idesc(a.bf16, P::BN);
-    for (uint32_t kb = 0; kb < kb_n; ++kb) {
-      const uint32_t s = kb % P::S, round = kb / P::S;
+    for (uint32_t ks = 0; ks < st_n; ++ks) {
+      const uint32_t s = ks % P::S, round = ks / P::S;
       if (!mbar_wait(full + s, round & 1u)) {
         atomicExch(s_fail, 1u);
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t xa = smem_addr(s_x + s * P::A), wa = smem_addr(s_w + s * P::B);
 #pragma unroll
-      for (uint32_t kk = 0; kk < kPjBK / 16u; ++kk)
-        mma_f16(tmem, sw128_desc(xa + 32u * kk), sw128_desc(wa + 32u * kk), idesc,
-                (kb | kk) != 0u ? 1u : 0u);
+      for (uint32_t j = 0; j < P::KB; ++j) {
+        const uint32_t kb = ks * P::KB + j;
+        if (kb >= kb_n) break;
+        const uint32_t xa = smem_addr(s_x + s * P::SA + j * P::A);
+        const uint32_t wa = smem_addr(s_w + s * P::SB + j * P::B);
+        const uint32_t acc = kb % P::ACC;  // this k-block's accumulator
+#pragma unroll
+        for (uint32_t kk = 0; kk < kPjBK / 16u; ++kk)
+          mma_f16(tmem + acc * P::BN, sw128_desc(xa + 32u * kk), sw128_desc(wa + 32u * kk),
+                  idesc, (kb >= P::ACC || kk != 0u) ? 1u : 0u);
+      }
       mma_commit(empty + s);  // the stage is free once these MMAs have read it
     }
     mma_commit(done);  // every MMA issued so far has completed
@@ -278,18 +317,21 @@ __global__ void __launch_bounds__(128, 1)
   const uint64_t row = (uint64_t)m0 + 32u * warp + lane;
   const bool valid = ok && row < a.m;
   uint32_t x[P::WPT];  // the row's tile: BN 16-bit values, two per word
+  const uint32_t used = kb_n < P::ACC ? kb_n : P::ACC;  // accumulators written
 #pragma unroll
   for (uint32_t j = 0; j < P::BN / 32u; ++j) {
-    uint32_t r[32];
-    if (ok) {
-      tmem_ld32(tmem + ((32u * warp) << 16) + 32u * j, r);
-    } else {
+    float f[32];
 #pragma unroll
-      for (uint32_t i = 0; i < 32u; ++i) r[i] = 0u;
+    for (uint32_t i = 0; i < 32u; ++i) f[i] = 0.f;
+    for (uint32_t q = 0; ok && q < used; ++q) {  // the accumulators' sum
+      uint32_t r[32];
+      tmem_ld32(tmem + ((32u * warp) << 16) + q * P::BN + 32u * j, r);
+#pragma unroll
+      for (uint32_t i = 0; i < 32u; ++i) f[i] += __uint_as_float(r[i]);
     }
 #pragma unroll
     for (uint32_t i = 0; i < 16u; ++i) {
-      float lo = __uint_as_float(r[2u * i]), hi = __uint_as_float(r[2u * i + 1u]);
+      float lo = f[2u * i], hi = f[2u * i + 1u];
       if (a.bias) {
         const uint32_t bw = __ldg(reinterpret_cast<const uint32_t*>(a.bias) + w0 + 16u * j + i);
         lo += to_float((uint16_t)(bw & 0xFFFFu), a.bf16);
@@ -354,22 +396,26 @@ __global__ void __launch_bounds__(128, 1)
 __global__ void __launch_bounds__(128) k_project_assemble(ProjectArgs a, uint32_t seg) {
   extern __shared__ __align__(16) uint32_t sm[];
   __shared__ uint32_t s_words;
+  __shared__ int64_t s_slot;
   // wait for the projection grid: its staged bits, flags and Y are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t W = a.W, nch = a.nch, R = 4u * W, ntiles = nch * seg, wpt = 64u / seg;
   const uint32_t tid = threadIdx.x, T = blockDim.x, lane = tid & 31u;
   const uint64_t r = blockIdx.x;
-  uint32_t* src = sm;                            // W words: each chunk's source
-  uint32_t* out = src + W;                       // W + 8 words: the stream
-  uint32_t* seg_keep = out + W + 8u;             // kept bits of each tile (ntiles)
-  uint32_t* seg_start = seg_keep + ntiles;       // stream offset of each tile's bits
-  uint32_t* cst = seg_start + ntiles;            // per chunk: start | p << 31
-  for (uint32_t i = tid; i < ntiles; i += T) seg_keep[i] = 0;
-  __syncthreads();
-  for (uint32_t w = tid; w < W; w += T) {
-    const uint32_t k = __popc(__ldg(a.nm + w));
-    if (k) atomicAdd(seg_keep + w / wpt, k);
+  uint32_t* src = sm;                       // W words: each chunk's source
+  uint32_t* out = src + W;                  // W + 8 words: the stream
+  uint32_t* seg_keep = out + W + 8u;        // kept bits of each tile (ntiles)
+  uint32_t* seg_start = seg_keep + ntiles;  // each tile's flag, then its stream offset
+  uint32_t* cst = seg_start + ntiles;       // per chunk: start | p << 31
+  // every tile's flag and kept bits (from the chunk-relative prefix of kept
+  // bits), and the slot: one round of independent loads
+  for (uint32_t ti = tid; ti < ntiles; ti += T) {
+    const uint32_t c = ti / seg, h = ti % seg, w = 64u * c + h * wpt;
+    const uint32_t hi = h + 1u < seg ? __ldg(a.pre + w + wpt) : __ldg(a.ckeep + c);
+    seg_keep[ti] = hi - __ldg(a.pre + w);
+    seg_start[ti] = __ldcg(a.flags + r * ntiles + ti);
   }
+  if (tid == 0) s_slot = a.slot_ids ? __ldg(a.slot_ids + r) : (int64_t)r;
   __syncthreads();
   if (tid < 32u) {  // participation, chunk sizes -> starts (a warp scan)
     uint32_t run = nch;
@@ -379,7 +425,7 @@ __global__ void __launch_bounds__(128) k_project_assemble(ProjectArgs a, uint32_
       if (c < nch) {
         const uint32_t keep = __ldg(a.ckeep + c);
         p = keep < 2048u ? 1u : 0u;
-        for (uint32_t h = 0; h < seg; ++h) p &= __ldcg(a.flags + r * ntiles + c * seg + h);
+        for (uint32_t h = 0; h < seg; ++h) p &= seg_start[c * seg + h];
         size = p ? keep : 2048u;
       }
       uint32_t incl = size;
@@ -403,7 +449,7 @@ __global__ void __launch_bounds__(128) k_project_assemble(ProjectArgs a, uint32_
   __syncthreads();
   const uint32_t words = s_words;
   const bool raw = 4u * words >= R;
-  const int64_t slot = a.slot_ids ? __ldg(a.slot_ids + r) : (int64_t)r;
+  const int64_t slot = s_slot;
   if (slot < 0 || (uint64_t)slot >= a.n_rows) {
     if (tid == 0) {
       set_status(a.status, IBP_ERANGE);
@@ -495,18 +541,20 @@ EncodeTiledFn encode_fn() {
   return g_encode;
 }
 
-// A 2-D map of a row-major [rows, k] matrix of 16-bit values, boxes of
-// box_rows rows x 64 elements (128 bytes) with the 128-byte swizzle; rows past
-// the end read as zero.
+// A 3-D map of a row-major [rows, k] matrix of 16-bit values seen as
+// {64 elements, rows, k / 64 k-blocks} (the k-blocks 128 bytes apart), boxes
+// of {64, box_rows, box_kb} with the 128-byte swizzle: box_kb K-major tiles
+// of box_rows x 64 one after another.  Rows and k-blocks past the end read as
+// zero.
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k, uint32_t box_rows,
-              uint32_t bf16) {
+              uint32_t box_kb, uint32_t bf16) {
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
-  const cuuint64_t dims[2] = {k, rows};
-  const cuuint64_t strides[1] = {k * 2u};
-  const cuuint32_t box[2] = {kPjBK, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return f(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+  const cuuint64_t dims[3] = {kPjBK, rows, k / kPjBK};
+  const cuuint64_t strides[2] = {k * 2u, kPjBK * 2u};
+  const cuuint32_t box[3] = {kPjBK, box_rows, box_kb};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return f(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -516,8 +564,8 @@ template <int kSeg, int kAR>
 cudaError_t launch_shape(const ProjectArgs& a, const void* x, const void* w, cudaStream_t st) {
   using P = PjShape<kSeg, kAR>;
   CUtensorMap mx, mw;
-  if (!make_map(&mx, x, a.m, a.k_dim, (uint32_t)kAR, a.bf16) ||
-      !make_map(&mw, w, (uint64_t)a.nch * 128u, a.k_dim, P::BN, a.bf16))
+  if (!make_map(&mx, x, a.m, a.k_dim, (uint32_t)kAR, P::KB, a.bf16) ||
+      !make_map(&mw, w, (uint64_t)a.nch * 128u, a.k_dim, P::BN, P::KB, a.bf16))
     return cudaErrorInvalidValue;
   auto kern = k_project_compress<kSeg, kAR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -559,7 +607,8 @@ cudaError_t launch_project(const ProjectArgs& a, const void* x, const void* w, i
   if (mtiles > 65535u || a.m > 0x7FFFFFFFull) return cudaErrorInvalidValue;
   // narrower tiles while the grid would leave most SMs idle
   uint32_t seg = 1;
-  while (seg < 4u && (uint64_t)a.nch * seg * mtiles < (uint64_t)sm_count) seg *= 2u;
+  while (seg < IBP_PROJECT_MAX_SEG && (uint64_t)a.nch * seg * mtiles < (uint64_t)sm_count)
+    seg *= 2u;
   const bool few = a.m <= 32u;  // one row tile, at most 32 rows of X to load
   if (seg == 1u) return few ? launch_shape<1, 32>(a, x, w, st) : launch_shape<1, 128>(a, x, w, st);
   if (seg == 2u) return few ? launch_shape<2, 32>(a, x, w, st) : launch_shape<2, 128>(a, x, w, st);
