@@ -872,6 +872,7 @@ def run_kv(args, rank, world, torch, dist):
                        "parity_layer0_ok": ok})
         del outh
     del newrows
+    proj = kv_decode_projection(torch, ibp, dev, stream, sp, seed=args.seed)
     res = {
         "metric": "IBP decompressed GB/s delivered (host & HBM) and % of link/HBM roofline",
         "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -890,6 +891,7 @@ def run_kv(args, rank, world, torch, dist):
         "gpu_launches": 2 * L * args.steps,
         "clocks": clk.summary(),
         "decode_steps": decode,
+        "decode_projection": proj,
         "cpu_baseline": leg,
         "attention_layout": {"value": round(att_gbs, 3), "unit": "GB/s", "steps": asteps,
                              "frac": round(att_gbs / roof, 4), "parity_layer0_ok": att_ok,
@@ -899,6 +901,105 @@ def run_kv(args, rank, world, torch, dist):
     for st in stores:
         ibp.ibp_store_destroy(st)
     return res
+
+
+def kv_decode_projection(torch, ibp, dev, stream, sp, seed=0, reps=50):
+    """A decode step's K (or V) projection of one layer, OPT-6.7B shape: the
+    20 new tokens' hidden states [20, 4096] fp16 times a 4096 x 4096 fp16
+    weight (+ bias), each output row (one token's K: 8 KB) compressed into
+    its host slot.  Fused (ibp_project_compress: tensor-core GEMM with the
+    compressor in its epilogue) against the unfused pair (cuBLAS through
+    torch, then ibp_compress).  The store's Mask/Bitval comes from the
+    prompt's 20 x 1920 projected rows; weight rows carry per-channel
+    log-normal scales with 2 % outlier channels x20, so the projected K/V
+    follow the KV workload's recipe (N(0, 1) times per-channel scales).
+    Parity: the fused slots, stored sizes and raw bits equal ibp_compress of
+    the fused Y, and the oracle's compression of 20 rows equals both."""
+    from oracle import ref_c
+    B, P, T, CH = 20, 1920, 2048, 4096
+    R, C = CH * 2, 256
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed * 7 + 11)
+    scale = torch.exp(0.5 * torch.randn(CH, generator=g, device=dev))
+    scale[torch.randperm(CH, generator=g, device=dev)[:int(round(0.02 * CH))]] *= 20.0
+    w = (torch.randn((CH, CH), generator=g, device=dev) * (scale[:, None] / CH ** 0.5)).half()
+    bias = (torch.randn(CH, generator=g, device=dev) * 0.05 * scale).half()
+    rows = B * T
+    st = ibp.ibp_store_create(R, C, rows, R)
+    xp = torch.randn((B * P, CH), generator=g, device=dev).half()
+    yp = torch.nn.functional.linear(xp, w, bias)
+    pid = torch.from_numpy((np.arange(B)[:, None] * T + np.arange(P)[None, :]).reshape(-1)).to(dev)
+    ibp.ibp_build_meta(st, yp.view(torch.uint8), R, None, B * P, 95, 100)
+    slots = torch.empty((rows, R), dtype=torch.uint8, pin_memory=True)
+    slots2 = torch.empty((rows, R), dtype=torch.uint8, pin_memory=True)
+    ibp.ibp_compress(st, slots, yp.view(torch.uint8), R, pid, B * P, None)
+    del xp, yp
+    x = torch.randn((B, CH), generator=g, device=dev).half()
+    sid = torch.from_numpy((np.arange(B) * T + P).astype(np.int64)).to(dev)
+    y = torch.empty((B, CH), dtype=torch.float16, device=dev)
+    stored = torch.empty(B, dtype=torch.int32, device=dev)
+    stored2 = torch.empty(B, dtype=torch.int32, device=dev)
+    wsb = ibp.project_workspace_bytes(B, R)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def fused():
+        ibp.ibp_project_compress(st, x, B, CH, w, bias, 0, y, slots, sid, stored, ws, wsb, sp)
+
+    def unfused():
+        yu = torch.nn.functional.linear(x, w, bias)
+        ibp.ibp_compress(st, slots2, yu, R, sid, B, stored2, sp)
+
+    def timeit(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()  # the 32 MB weight comes from HBM, as in a decode step
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    with ClockSampler(dev.index) as clk:
+        t_f = timeit(fused)
+        t_u = timeit(unfused)
+        t_g = timeit(lambda: torch.nn.functional.linear(x, w, bias))
+    assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    # parity: the fused result against ibp_compress of the fused Y, and the oracle
+    fused()
+    ibp.ibp_compress(st, slots2, y, R, sid, B, stored2, sp)
+    torch.cuda.synchronize()
+    assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    sid_np = sid.cpu().numpy()
+    st_f = stored.cpu().numpy().astype(np.uint32)
+    st_u = stored2.cpu().numpy().astype(np.uint32)
+    s1, s2 = slots.numpy(), slots2.numpy()
+    same = bool(np.array_equal(st_f, st_u)) and all(
+        np.array_equal(s1[i, :st_f[j]], s2[i, :st_f[j]]) for j, i in enumerate(sid_np))
+    mask = np.zeros(R // 4, np.uint32)
+    bitval = np.zeros(R // 4, np.uint32)
+    ibp.ibp_meta_get(st, mask, bitval)
+    yb = y.view(torch.uint8).cpu().numpy().reshape(B, R)
+    ref_sl = np.zeros((B, R), np.uint8)
+    ref_bm = np.zeros(1, np.uint32)
+    ref_st = ref_c.compress_batch(yb, C, mask, bitval, ref_sl, ref_bm)
+    oracle_ok = bool(np.array_equal(ref_st, st_f)) and all(
+        np.array_equal(s1[i, :ref_st[j]], ref_sl[j, :ref_st[j]]) for j, i in enumerate(sid_np))
+    ibp.ibp_store_destroy(st)
+    return {"fused_us": round(t_f, 2), "unfused_us": round(t_u, 2), "gemm_us": round(t_g, 2),
+            "fused_speedup": round(t_u / t_f, 3),
+            "weight_gbs_fused": round(CH * CH * 2 / t_f / 1e3, 1),
+            "rows_stored_bytes": [int(v) for v in st_f],
+            "parity_vs_unfused_ok": same, "parity_oracle_ok": oracle_ok,
+            "clocks": clk.summary(),
+            "note": "one (layer, K) projection of a decode step: 20 x 4096 fp16 times 4096 x "
+                    "4096 (+ bias); fused ibp_project_compress vs cuBLAS (torch) + ibp_compress; "
+                    "a step has 64 such calls (32 layers x K, V); L2 flushed before each"}
 
 
 def run_weights(args, rank, world, torch, dist):
@@ -1196,6 +1297,28 @@ def run_dlrm(args, rank, world, torch, dist):
         assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
     per_store_times = [a.elapsed_time(c) / 1e3 for a, c in evs]
     per_store_gbs = B * Tn * R * len(per_store_times) / sum(per_store_times) / 1e9
+    # the uncompressed transfer of the same lookups over the same host memory:
+    # 26 raw gathers of R bytes from the same slot addresses (the slots are R
+    # bytes apart), the review's Table 1 baseline for this workload
+    raw_out = torch.empty((Tn, B, R), dtype=torch.uint8, device=dev)
+
+    def step_raw(b):
+        ids = ids_dev[b % pool]
+        for t in range(Tn):
+            ibp.ibp_gather_copy(raw_out[t], slots[t], R, R, ids[t], B, N, sp)
+    for b in range(args.warmup):
+        step_raw(b)
+    rev = []
+    for b in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step_raw(b)
+        e1.record(stream)
+        rev.append((e0, e1))
+    torch.cuda.synchronize()
+    raw_gbs = B * Tn * R * len(rev) / sum(a.elapsed_time(c) / 1e3 for a, c in rev) / 1e9
+    del raw_out
 
     # the same batches through one fused launch over all 26 tables
     grp = ibp.ibp_group_create(stores, slots)
@@ -1309,6 +1432,10 @@ def run_dlrm(args, rank, world, torch, dist):
         "per_store_launches": {"value": round(per_store_gbs, 3), "unit": "GB/s",
                                "launches_per_step": Tn,
                                "note": "26 ibp_gather_decompress_strided calls per batch"},
+        "raw_gather_per_table": {"value": round(raw_gbs, 3), "unit": "GB/s",
+                                 "speedup_of_ordered_ibp": round(value / world / raw_gbs, 3),
+                                 "note": "26 uncompressed ibp_gather_copy calls per batch over "
+                                         "the same slot addresses (R bytes per lookup)"},
         "roofline": {"bound": "link", "achieved": round(value / world, 2), "peak": round(roof, 2),
                      "unit": "GB/s", "frac": round(value / world / roof, 4), "traffic": None,
                      "peak_is": "min(HBM, link / stored bytes of the batch's distinct rows per "
@@ -1983,7 +2110,8 @@ def main():
             d["config"] = r["config"]
             for k_ in ("parity_all_lookups_ok", "parity_layer0_ok", "chunks", "fused_unordered",
                        "per_store_launches", "ratio_distinct_rows", "raw_gather_gbs",
-                       "attention_layout", "decode_steps"):
+                       "attention_layout", "decode_steps", "decode_projection",
+                       "raw_gather_per_table"):
                 if k_ in r:
                     d[k_] = r[k_]
             d["wall_s"] = round(time.time() - t0, 1)

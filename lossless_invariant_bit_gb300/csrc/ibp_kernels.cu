@@ -846,11 +846,20 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
         const uint32_t nv = e.w >> 20;
         const uint8_t* src = src_lane + ((((uint64_t)e.y) << 32) | (uint64_t)(e.x & ~15u));
         const uint32_t sa = ring_sa + 4u * (tt % S) * F.sbuf_words;
+        // one copy per lane covers a stream of up to 512 bytes (measured: the
+        // HBM cache path, 324-byte streams, 3 % faster than four predicated
+        // copies per lane; a 64-bit window read of 3 stream words per 4 output
+        // words measured 3 % slower than the per-word reads, and 5 CTAs per SM
+        // instead of 4 4 % slower)
+        if (lane < nv)
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(src));
+        if (nv > 32u) {  // streams above 512 bytes (and raw rows above 512 bytes)
 #pragma unroll
-        for (uint32_t j = 0; j < (kBig ? 16u : 4u); ++j)
-          if (lane + 32u * j < nv)
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * j),
-                         "l"(src + 512u * j));
+          for (uint32_t j = 1; j < (kBig ? 16u : 4u); ++j)
+            if (lane + 32u * j < nv)
+              asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(sa + 512u * j),
+                           "l"(src + 512u * j));
+        }
       }
     }
     cp_async_commit();

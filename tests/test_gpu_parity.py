@@ -703,3 +703,51 @@ def test_length_table_changes_nothing_but_fetches(stores, R, C):
         assert st.status() == ibp.IBP_OK
         assert torch.equal(out, ref)
     ibp.ibp_store_set_lengths(st.h, None)
+
+
+@pytest.mark.parametrize("keep,pos", [(1, 31), (4, 0), (7, 23), (10, 13), (11, 5)])
+def test_uniform_single_run_decoder_with_raw_chunks(stores, keep, pos):
+    """Every word keeps one run of `keep` bits at bit `pos` (the uniform,
+    single-run store form; runs of up to 10 bits take a 64-bit window of the
+    stream per 4 words).  Some rows carry a raw chunk (a word missing its
+    Mask) ahead of packed ones, some are raw throughout; decoded from device
+    slots, pinned host slots and a packed cache, the rows come back and the
+    stored bytes equal the oracle's."""
+    R, C, n = 1024, 256, 3000
+    W = R // 4
+    run = ((1 << keep) - 1) << pos
+    rng = np.random.default_rng(keep * 100 + pos)
+    mask = np.full(W, ~run & 0xFFFFFFFF, np.uint32)
+    bitval = np.full(W, int(rng.integers(0, 1 << 32)) & int(mask[0]), np.uint32)
+    rows = (bitval[None, :] | (rng.integers(0, 1 << 32, (n, W), dtype=np.uint32) & run))
+    rows = rows.astype(np.uint32)
+    for i in range(0, n, 7):  # a raw chunk: one word misses the Mask
+        c = int(rng.integers(0, R // C))
+        low = int(mask[0]) & -int(mask[0])  # the lowest Mask bit
+        rows[i, c * (C // 4) + int(rng.integers(0, C // 4))] ^= np.uint32(low)
+    rows[5::97] = rng.integers(0, 1 << 32, rows[5::97].shape, dtype=np.uint32)  # raw rows
+    b = rows.view(np.uint8).reshape(n, R)
+    st = stores(R, C, n)
+    st.set_meta(mask, bitval)
+    torch.cuda.synchronize()
+    d = to_dev(b)
+    slots, stored = gpu_compress(st, d, n)
+    ref_sl, ref_bm, ref_st = oracle_slots(b, C, mask, bitval, st.slot)
+    assert np.array_equal(stored, ref_st)
+    assert_streams_equal(slots.cpu().numpy(), ref_sl, ref_st)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_decompress(st.h, out, slots, None, n)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
+    host = to_pinned(slots.cpu().numpy())
+    ids = rng.integers(0, n, 5000).astype(np.int64)
+    outg = torch.empty((len(ids), R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress(st.h, outg, host, None, to_dev(ids), len(ids))
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(outg.cpu().numpy(), b[ids])
+    packed_ref, offs_ref = ref_c.pack_slots(ref_sl, ref_st)
+    cache = to_dev(np.concatenate([packed_ref, np.zeros(R, np.uint8)]))
+    out.zero_()
+    ibp.ibp_decompress(st.h, out, cache, to_dev(offs_ref[:n]), n)
+    assert st.status() == ibp.IBP_OK
+    assert np.array_equal(out.cpu().numpy(), b)
