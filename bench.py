@@ -651,7 +651,7 @@ def run_tiny(args, rank, world, torch, dist):
                      "frac": round(moved / hbm, 4),
                      # dram read + write of a 48-replica launch (profiles/
                      # k_decode_fast_tiny_cache.md) scaled to this launch's rows
-                     "traffic": round(211.01e6 * n / (48 * 4096)),
+                     "traffic": round(211.45e6 * n / (48 * 4096)),
                      "traffic_is": "dram__bytes_read.sum + dram__bytes_write.sum from ncu, "
                                    "scaled from a 196,608-row capture (part of the output is "
                                    "still in L2 when the kernel ends)",
@@ -994,8 +994,17 @@ def kv_decode_projection(torch, ibp, dev, stream, sp, seed=0, reps=50, tokens=20
     oracle_ok = bool(np.array_equal(ref_st, st_f)) and all(
         np.array_equal(s1[i, :ref_st[j]], ref_sl[j, :ref_st[j]]) for j, i in enumerate(sid_np))
     ibp.ibp_store_destroy(st)
+    wbytes = CH * CH * 2 + B * CH * 2  # the weight, and X: the kernel's algorithmic reads
+    hbm = measured_peaks()["hbm_gbs"]
     return {"tokens": B, "fused_us": round(t_f, 2), "unfused_us": round(t_u, 2),
             "gemm_us": round(t_g, 2),
+            "roofline": {"bound": "hbm", "achieved": round(wbytes / t_f / 1e3, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(wbytes / t_f / 1e3 / hbm, 4),
+                         # dram__bytes_read.sum of one 20-token launch of
+                         # k_project_compress<4, 32> (profiles/
+                         # k_project_compress_kv_decode.md); null at other sizes
+                         "traffic": 33.82e6 if B == 20 else None,
+                         "kernel": "k_project_compress + k_project_assemble (whole call)"},
             "fused_speedup": round(t_u / t_f, 3),
             "weight_gbs_fused": round(CH * CH * 2 / t_f / 1e3, 1),
             "ratio": round(float(st_f.sum()) / (B * R), 5),
