@@ -66,7 +66,6 @@ constexpr uint32_t kPjRing = 200u * 1024u;  // shared-memory bytes of the stage 
 // shared memory: 1 KB alignment slack, the ring, the tile's metadata (8 x 64
 // words at most: mask, bitval, ~mask, 5 move masks), barriers
 constexpr uint32_t kPjMetaWords = 8u * 64u;
-constexpr uint32_t kPjSmem = 1024u + kPjRing + 4u * kPjMetaWords + 512u;
 
 // Shape of one instance: kSeg tiles per chunk, kAR rows of X loaded per stage.
 template <int kSeg, int kAR>
@@ -83,6 +82,11 @@ struct PjShape {
   static constexpr uint32_t SA = KB * A, SB = KB * B;     // bytes per stage
   static constexpr uint32_t S0 = kPjRing / (SA + SB);
   static constexpr uint32_t S = S0 > IBP_PROJECT_MAX_STAGES ? IBP_PROJECT_MAX_STAGES : S0;
+  static constexpr uint32_t RING = S * (SA + SB);         // bytes of the ring
+  // dynamic shared memory: 1 KB alignment slack, the ring, the tile's
+  // metadata, the barriers (only what this shape uses: a smaller carve-out
+  // of shared memory)
+  static constexpr uint32_t SMEM = 1024u + RING + 4u * kPjMetaWords + 512u;
   // independent accumulators the k-blocks take in turn: consecutive MMAs into
   // one accumulator wait for each other, and a narrow tile's MMAs are short
   static constexpr uint32_t ACC = IBP_PROJECT_ACCUMULATORS;
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(128, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
   uint8_t* s_x = smem;                 // P::S stages of X: KB tiles of kAR rows each
   uint8_t* s_w = smem + P::S * P::SA;  // P::S stages of W: KB tiles of BN rows each
-  uint32_t* s_meta = reinterpret_cast<uint32_t*>(smem + kPjRing);
+  uint32_t* s_meta = reinterpret_cast<uint32_t*>(smem + P::RING);
   uint64_t* full = reinterpret_cast<uint64_t*>(s_meta + kPjMetaWords);
   uint64_t* empty = full + P::S;
   uint64_t* done = empty + P::S;
@@ -247,6 +251,9 @@ __global__ void __launch_bounds__(128, 1)
       s_meta[(3u + st) * P::WPT + i] = __ldg(a.mv + st * W + w);
   }
   if (threadIdx.x == 0) {
+    // the tensor maps' descriptors, fetched while the CTA sets up
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
     for (uint32_t s = 0; s < P::S; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
@@ -569,10 +576,10 @@ cudaError_t launch_shape(const ProjectArgs& a, const void* x, const void* w, cud
     return cudaErrorInvalidValue;
   auto kern = k_project_compress<kSeg, kAR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kPjSmem);
+                                       (int)P::SMEM);
   if (e != cudaSuccess) return e;
   const uint64_t mtiles = (a.m + kPjBM - 1) / kPjBM;
-  kern<<<dim3(a.nch * kSeg, (uint32_t)mtiles), 128, kPjSmem, st>>>(mx, mw, a);
+  kern<<<dim3(a.nch * kSeg, (uint32_t)mtiles), 128, P::SMEM, st>>>(mx, mw, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the row assembly, launched behind the projection (programmatic dependent
