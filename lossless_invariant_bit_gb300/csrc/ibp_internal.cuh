@@ -59,8 +59,8 @@ struct DecodeArgs {
   uint64_t group_rows;
   uint64_t group_stride;
   // ordered gather (out_pos != NULL): ids come sorted by address region and
-  // row i lands at dst + out_pos[i]*dst_stride; warps take 32-row chunks in
-  // turn, so all of them sweep the sorted ids together
+  // row i lands at dst + out_pos[i]*dst_stride; each warp takes a contiguous
+  // share of the sorted ids, so each SM reads a narrow address range
   const int64_t* out_pos;
   // NULL, or each row id's stored bytes (in HBM): the first fetch then takes
   // the whole stream, so rows with raw chunks need no second round trip
