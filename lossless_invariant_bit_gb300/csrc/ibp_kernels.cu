@@ -1048,7 +1048,12 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
   int64_t pid = 0;
   uint64_t poff = 0, pitem = 0;
   uint32_t pbm = 0, pt = 0, plen = 0;
-  bool pin = false;
+  bool pin = false, pdup = false;
+  // an ordered gather's list has the lookups of one row next to each other
+  // (Zipf batches repeat rows): an item that repeats the warp's previous item
+  // is copied from that item's output row instead of fetched again
+  int64_t carry_id = -1;
+  uint32_t carry_t = 0xFFFFFFFFu;
   auto step_ids = [&](uint32_t q) {
     const uint32_t t = 32u * q + lane;
     const uint64_t ri = row_index(t);
@@ -1057,6 +1062,19 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
       pitem = ordered ? (uint64_t)__ldg(g.order + ri) : ri;
       pid = __ldg(g.ids + pitem);
       pt = (uint32_t)(pitem % T);
+    }
+    if (ordered) {
+      const int64_t key_id = pin ? pid : -1;
+      const uint32_t key_t = pin ? pt : 0xFFFFFFFFu;
+      int64_t prev_id = __shfl_up_sync(kFull, key_id, 1);
+      uint32_t prev_t = __shfl_up_sync(kFull, key_t, 1);
+      if (lane == 0) {
+        prev_id = carry_id;
+        prev_t = carry_t;
+      }
+      pdup = pin && key_id >= 0 && prev_t == key_t && prev_id == key_id;
+      carry_id = __shfl_sync(kFull, key_id, 31);
+      carry_t = __shfl_sync(kFull, key_t, 31);
     }
   };
   auto step_loads = [&]() {
@@ -1074,6 +1092,8 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
         fl = 1u | 12u;
       } else if (pid < 0 || (uint64_t)pid >= ent[pt].n_rows) {
         fl = 1u | 4u;
+      } else if (pdup) {
+        fl = 7u;  // 1 | 2 | 4: a repeat of the previous item (never a fetch)
       } else {
         fl = 1u | (((pbm >> (pid & 31)) & 1u) << 1);
         off = poff;
@@ -1117,6 +1137,7 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
     step_store(q);
   }
   __syncwarp();
+  const uint4* prev_row = nullptr;  // output row of the warp's previous item
   for (uint32_t t = 0; t + 1u < S; ++t) issue(t);
 #pragma unroll 1
   for (uint32_t t = 0; t < cnt; ++t) {
@@ -1134,6 +1155,12 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
       uint4* drow = reinterpret_cast<uint4*>(
           g.dst + ((((uint64_t)(e.w & 0xFFFFFu)) << 32) | (uint64_t)e.z));
       uint32_t* sb = ring + (t & (S - 1u)) * g.sbuf_words;
+      const uint4* from_row = prev_row;
+      prev_row = drow;
+      if (fl == 7u) {  // the previous item's row (written by this warp just before)
+        for (uint32_t v = lane; v < nvec; v += 32) drow[v] = __ldcg(from_row + v);
+        break;
+      }
       if (fl & 12u) {
         if (lane == 0) set_status(en.status, (fl & 12u) == 12u ? IBP_EINVAL : IBP_ERANGE);
         zero_row(drow, nvec, lane);
