@@ -1508,6 +1508,58 @@ def line_bytes(stored: np.ndarray) -> np.ndarray:
     return full * 128 + tail
 
 
+def sector_bytes(start: np.ndarray, stored: np.ndarray) -> np.ndarray:
+    """32-byte sectors touched by reading `stored` bytes from byte `start`."""
+    start = np.asarray(start, np.int64)
+    end = start + np.asarray(stored, np.int64)
+    return (-(-end // 32) - start // 32) * 32
+
+
+def dense_packed_host(torch, ibp, st, slots, stored, NR, R, ids_np, ids_dev, out, rb, timed,
+                      link, raw_gbs, sp, dev):
+    """The same store packed into pinned host memory: each row's stored bytes
+    at a 16-byte offset (the packed layout of the HBM cache, System
+    Integration), gathered through the offsets form of ibp_gather_decompress.
+    Against the slot store (every stream from a 128-byte boundary) it trades
+    line-aligned starts for no padding; the sector count says what the link
+    would carry if it moved 32-byte sectors."""
+    offs = torch.empty(NR + 1, dtype=torch.int64, device=dev)
+    ibp.ibp_pack(st, None, offs, slots, stored, NR, sp)
+    total = int(offs[NR].item())
+    packed_dev = torch.empty(total, dtype=torch.uint8, device=dev)
+    ibp.ibp_pack(st, packed_dev, offs, slots, stored, NR, sp)
+    packed = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    packed.copy_(packed_dev)
+    del packed_dev
+    torch.cuda.synchronize()
+    assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    gbs = timed(lambda b: ibp.ibp_gather_decompress(st, out, packed, offs, ids_dev[b % len(ids_np)],
+                                                    len(ids_np[b % len(ids_np)]), sp))
+    assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    x = ids_np[-1]
+    ibp.ibp_gather_decompress(st, out, packed, offs, ids_dev[-1], len(x), sp)
+    torch.cuda.synchronize()
+    assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    ok = bool(np.array_equal(out[:len(x)].cpu().numpy(), rb[x]))
+    st_np = stored.cpu().numpy().astype(np.int64)
+    off_np = offs[:NR].cpu().numpy()
+    nb = sum(len(i) for i in ids_np) * R
+    sec_packed = sum(float(sector_bytes(off_np[i], st_np[i]).sum()) for i in ids_np) / nb
+    sec_slots = sum(float(sector_bytes(0, st_np[i]).sum()) for i in ids_np) / nb
+    line_slots = sum(float(line_bytes(st_np[i]).sum()) for i in ids_np) / nb
+    log("dense C=1024, packed host store (%.0f MB): %.1f GB/s  %.3fx raw; sectors per row byte "
+        "%.4f packed / %.4f slots; link lines per row byte (slots) %.4f"
+        % (total / 1e6, gbs, gbs / raw_gbs, sec_packed, sec_slots, line_slots))
+    del packed
+    return {"chunk_bytes": 1024, "store_bytes": total, "gbs": round(gbs, 2),
+            "speedup_vs_raw_gather": round(gbs / raw_gbs, 3),
+            "frac_of_link_over_sector_ratio": round(gbs / (link / sec_packed), 4),
+            "sector_bytes_per_row_byte": round(sec_packed, 5),
+            "slot_store_sector_bytes_per_row_byte": round(sec_slots, 5),
+            "slot_store_line_bytes_per_row_byte": round(line_slots, 5),
+            "parity_batch_ok": ok}
+
+
 def run_dense(args, rank, world, torch, dist):
     """Dense GNN (the pages' Table 1 dense row): 2,000,000 x 128 fp32 features
     ~ N(0, 0.1^2) in pinned host slots (1 GB), Mask/Bitval from a 1 % sample at
@@ -1605,6 +1657,9 @@ def run_dense(args, rank, world, torch, dist):
                            "parity_sampled_rows_ok": ok})
             log("dense C=%d: ratio %.4f  %.1f GB/s  %.3f of link/ratio  %.3f of the line-granular "
                 "ceiling  %.3fx raw" % (C, ratio, gbs, gbs / ideal, gbs / gran, gbs / raw_gbs))
+            if C == 1024:
+                packed_point = dense_packed_host(torch, ibp, st, slots, stored, NR, R, ids_np,
+                                                 ids_dev, out, rb, timed, link, raw_gbs, sp, dev)
             ibp.ibp_store_destroy(st)
     head = next(p for p in points if p["chunk_bytes"] == 1024)
     n_avg = statistics.mean(len(x) for x in ids_np)
@@ -1624,6 +1679,7 @@ def run_dense(args, rank, world, torch, dist):
                      "unit": "GB/s", "frac": head["frac"], "traffic": None,
                      "kernel": "k_decode_fast<true, mode, small> (ibp_gather_decompress)"},
         "chunks": points,
+        "packed_host_store": packed_point,
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "cpu_baseline": leg,

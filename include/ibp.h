@@ -58,7 +58,7 @@ extern "C" {
 #define IBP_MAX_TUNE_CANDIDATES 8u
 #define IBP_MAX_GROUP_STORES 64u
 /* device workspace bytes of the ordered gathers for n ids (or batch*T items) */
-#define IBP_ORDER_WORKSPACE_BYTES(n) (16ull * (uint64_t)(n) + 4096ull)
+#define IBP_ORDER_WORKSPACE_BYTES(n) (20ull * (uint64_t)(n) + 65536ull)
 /* device workspace bytes of ibp_project_compress for m rows of R bytes */
 #define IBP_PROJECT_WORKSPACE_BYTES(m, R) \
   ((((uint64_t)(m) * ((uint64_t)(R) / 16ull) + 255ull) / 256ull) * 256ull + \
@@ -265,13 +265,18 @@ IBP_API ibp_status ibp_group_gather_decompress(const ibp_group* group, void* dst
 
 /* As ibp_group_gather_decompress, in address order (see
  * ibp_gather_decompress_ordered): the batch*T items are bucketed by store
- * and by region within it, then decoded bucket by bucket, each to its own
- * place in dst.  For groups whose slots together exceed the GPU's reach into
- * host memory (DLRM tables of 1-2 KB rows: 26-53 GB).
+ * and by region within it, each bucket of up to 2048 items is sorted by row
+ * id, and the list is decoded in contiguous shares of equal cost (a lookup
+ * that fetches a row counts as eight that repeat the row before it), each
+ * item to its own place in dst.  Repeated lookups of a row (Zipf batches)
+ * next to each other are fetched and decoded once: the repeats are stored
+ * from the decoded copy.  For groups whose slots together exceed the GPU's
+ * reach into host memory (DLRM tables of 1-2 KB rows: 26-53 GB), and for
+ * batches that repeat rows.
  *   workspace  device memory of IBP_ORDER_WORKSPACE_BYTES(batch*T) bytes,
  *              16-byte aligned
  * Errors: as ibp_group_gather_decompress; IBP_EINVAL for a missing or short
- * workspace, IBP_EALIGN for a misaligned one. */
+ * workspace or batch*T above 2^32 - 1, IBP_EALIGN for a misaligned one. */
 IBP_API ibp_status ibp_group_gather_decompress_ordered(const ibp_group* group, void* dst,
                                                        uint64_t dst_row_stride,
                                                        const int64_t* ids, uint64_t batch,

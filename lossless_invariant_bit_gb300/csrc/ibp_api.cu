@@ -623,8 +623,9 @@ ibp_status ibp_group_gather_decompress(const ibp_group* g, void* dst, uint64_t d
   a.dst = static_cast<uint8_t*>(dst);
   a.dst_row_stride = dst_row_stride;
   a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
-  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u);
+  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u) + g->W;
   a.order = nullptr;
+  a.shares = nullptr;
   a.host_src = g->host_src;
   return cu(ibp::launch_group(a, g->sm_count, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -639,14 +640,22 @@ ibp_status ibp_group_gather_decompress_ordered(const ibp_group* g, void* dst,
   if (!aligned16(dst) || (dst_row_stride & 15u) || dst_row_stride < (uint64_t)g->T * g->R)
     return IBP_EALIGN;
   const uint64_t n_items = batch * g->T;
+  if (n_items > 0xFFFFFFFFull) return IBP_EINVAL;
   if (!workspace || workspace_bytes < IBP_ORDER_WORKSPACE_BYTES(n_items)) return IBP_EINVAL;
   if (!aligned16(workspace)) return IBP_EALIGN;
   int d = -1;
   if (cudaGetDevice(&d) != cudaSuccess) return IBP_ECUDA;
   if (d != g->device) return IBP_EINVAL;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int64_t* order = static_cast<int64_t*>(workspace);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(order + 2 * n_items);
+  // workspace: the item order (8 bytes per item), each item's cost prefix
+  // within its bucket (4 per item), the warp shares (at most n/32 + 9 words),
+  // then the bucket counters and the bucket costs (4 KB each)
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int64_t* order = reinterpret_cast<int64_t*>(ws);
+  uint32_t* wpre = reinterpret_cast<uint32_t*>(ws + 8ull * n_items);
+  uint32_t* shares = reinterpret_cast<uint32_t*>(ws + 12ull * n_items);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + IBP_ORDER_WORKSPACE_BYTES(n_items) - 8192ull);
+  uint32_t* cost = hist + ibp::kOrderBuckets;
   ibp_status e = cu(cudaMemsetAsync(hist, 0, 4ull * ibp::kOrderBuckets, st));
   if (e != IBP_OK) return e;
   e = cu(ibp::launch_order_items(g->entries, g->T, ids, n_items, order, hist, g->sm_count, st));
@@ -663,10 +672,11 @@ ibp_status ibp_group_gather_decompress_ordered(const ibp_group* g, void* dst,
   a.dst = static_cast<uint8_t*>(dst);
   a.dst_row_stride = dst_row_stride;
   a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
-  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u);
+  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u) + g->W;
   a.order = order;
+  a.shares = nullptr;
   a.host_src = g->host_src;
-  return cu(ibp::launch_group(a, g->sm_count, st));
+  return cu(ibp::launch_group_ordered(a, hist, wpre, cost, shares, g->sm_count, st));
 }
 
 ibp_status ibp_project_compress(ibp_store* s, const void* x, uint64_t m, uint64_t k_dim,

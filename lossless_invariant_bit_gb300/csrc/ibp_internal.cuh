@@ -170,6 +170,7 @@ struct GroupArgs {
   uint32_t sbuf_words;
   uint32_t warp_words;
   const int64_t* order;     // NULL, or the items in address order (ordered gather)
+  const uint32_t* shares;   // NULL, or warp w's items order[shares[w] .. shares[w+1])
   uint32_t host_src;        // some store's slots are pinned host memory (launch shape only)
 };
 
@@ -242,6 +243,15 @@ cudaError_t launch_order_ids(const int64_t* ids, uint64_t n, uint64_t n_rows, in
 cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int64_t* ids,
                                uint64_t n_items, int64_t* order_out, uint32_t* hist,
                                int sm_count, cudaStream_t st);
+// The ordered group gather after launch_order_items: each bucket of g.order
+// sorted by row id (repeats of a row side by side), the list cut into warp
+// shares of equal cost (an item that fetches a row costs as much as several
+// repeats), then the gather.  hist: the bucket ends launch_order_items left;
+// wpre: n_items words; cost: kOrderBuckets words; shares: n_items / 32 + 9
+// words at least.
+cudaError_t launch_group_ordered(GroupArgs g, const uint32_t* hist, uint32_t* wpre,
+                                 uint32_t* cost, uint32_t* shares, int sm_count,
+                                 cudaStream_t st);
 cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count,
                           cudaStream_t st);
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,

@@ -1032,16 +1032,20 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
   uint32_t* ring = smem + ent_words + wid * g.warp_words;
   uint4* rinfo = reinterpret_cast<uint4*>(ring + S * g.sbuf_words);
   uint32_t* cinfo = ring + S * g.sbuf_words + 256;
+  // the warp's last decoded row, kept while the next items repeat it
+  uint4* lastrow = reinterpret_cast<uint4*>(cinfo + ((nch + 3u) & ~3u));
   __syncthreads();
   const uint32_t nhw = (nch + 31u) >> 5;
   const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
                                                                  : ((1u << (nch & 31u)) - 1u);
-  // contiguous item shares (of the address-sorted list, for an ordered gather)
+  // contiguous item shares: of the sorted list, as cut for an ordered gather
+  // (equal numbers of distinct rows), else equal numbers of items
   const uint64_t nw = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t gw = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
   const bool ordered = g.order != nullptr;
-  const uint64_t r0 = g.n_items * gw / nw;
-  const uint32_t cnt = (uint32_t)(g.n_items * (gw + 1) / nw - r0);
+  const uint64_t r0 = g.shares ? (uint64_t)__ldg(g.shares + gw) : g.n_items * gw / nw;
+  const uint32_t cnt = (uint32_t)((g.shares ? (uint64_t)__ldg(g.shares + gw + 1)
+                                            : g.n_items * (gw + 1) / nw) - r0);
   if (cnt == 0) return;
   auto row_index = [&](uint32_t t) -> uint64_t { return r0 + t; };  // the warp's t-th item
 
@@ -1051,7 +1055,7 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
   bool pin = false, pdup = false;
   // an ordered gather's list has the lookups of one row next to each other
   // (Zipf batches repeat rows): an item that repeats the warp's previous item
-  // is copied from that item's output row instead of fetched again
+  // is not fetched; its row is stored from the warp's copy of the last one
   int64_t carry_id = -1;
   uint32_t carry_t = 0xFFFFFFFFu;
   auto step_ids = [&](uint32_t q) {
@@ -1137,7 +1141,6 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
     step_store(q);
   }
   __syncwarp();
-  const uint4* prev_row = nullptr;  // output row of the warp's previous item
   for (uint32_t t = 0; t + 1u < S; ++t) issue(t);
 #pragma unroll 1
   for (uint32_t t = 0; t < cnt; ++t) {
@@ -1155,26 +1158,32 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
       uint4* drow = reinterpret_cast<uint4*>(
           g.dst + ((((uint64_t)(e.w & 0xFFFFFu)) << 32) | (uint64_t)e.z));
       uint32_t* sb = ring + (t & (S - 1u)) * g.sbuf_words;
-      const uint4* from_row = prev_row;
-      prev_row = drow;
-      if (fl == 7u) {  // the previous item's row (written by this warp just before)
-        for (uint32_t v = lane; v < nvec; v += 32) drow[v] = __ldcg(from_row + v);
+      if (fl == 7u) {  // a repeat: the row this warp decoded last (each lane its own groups)
+        for (uint32_t v = lane; v < nvec; v += 32) drow[v] = lastrow[v];
         break;
       }
+      // the next item repeats this one: keep the row (set only in an ordered
+      // gather, where the item after a repeat's first lookup is flagged)
+      const bool keep = t + 1u < cnt && (rinfo[(t + 1u) & 63u].x & 15u) == 7u;
       if (fl & 12u) {
         if (lane == 0) set_status(en.status, (fl & 12u) == 12u ? IBP_EINVAL : IBP_ERANGE);
         zero_row(drow, nvec, lane);
+        if (keep) zero_row(lastrow, nvec, lane);
         break;
       }
       if (fl & 2u) {
         uint4* dp = drow + lane;
-        for (uint32_t v = lane; v < nvec; v += 32, dp += 32)
-          *dp = *reinterpret_cast<const uint4*>(sb + 4u * v);
+        for (uint32_t v = lane; v < nvec; v += 32, dp += 32) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sb + 4u * v);
+          *dp = x;
+          if (keep) lastrow[v] = x;
+        }
         break;
       }
       if (!en.can_pack) {
         if (lane == 0) set_status(en.status, IBP_ECORRUPT);
         zero_row(drow, nvec, lane);
+        if (keep) zero_row(lastrow, nvec, lane);
         break;
       }
       const uint32_t mode = en.mode;
@@ -1201,6 +1210,7 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
           if (lane == 0) set_status(en.status, IBP_ECORRUPT);
           __syncwarp();
           zero_row(drow, nvec, lane);
+          if (keep) zero_row(lastrow, nvec, lane);
           break;
         }
         const uint32_t need_vec = (4u * words + 15u) >> 4;
@@ -1227,10 +1237,11 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
           packed = (ci >> 31) != 0u;
           delta = start - __ldg(cstat + k);
         }
+        uint4 val;
         if (!packed) {
           const uint32_t bit = start + ((gd >> 16) << 5);
           const uint32_t q = bit >> 5;
-          *dp = make_uint4(__funnelshift_r(sb[q], sb[q + 1], bit), __funnelshift_r(sb[q + 1], sb[q + 2], bit),
+          val = make_uint4(__funnelshift_r(sb[q], sb[q + 1], bit), __funnelshift_r(sb[q + 1], sb[q + 2], bit),
                            __funnelshift_r(sb[q + 2], sb[q + 3], bit), __funnelshift_r(sb[q + 3], sb[q + 4], bit));
         } else if (uni) {
           uint32_t bit = nch + 4u * gi * en.ukeep + delta;
@@ -1242,10 +1253,12 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
             o[x] = ((v << (en.ush & 31u)) & en.um0) | ((v << (en.ush >> 8)) & en.um1) | en.ubv;
             bit += en.ukeep;
           }
-          *dp = make_uint4(o[0], o[1], o[2], o[3]);
+          val = make_uint4(o[0], o[1], o[2], o[3]);
         } else {
-          *dp = decode_group(en.tab, sb, gi, G, delta, net5);
+          val = decode_group(en.tab, sb, gi, G, delta, net5);
         }
+        *dp = val;
+        if (keep) lastrow[gi] = val;
       }
     } while (false);
     __syncwarp();
@@ -2103,6 +2116,218 @@ __global__ void __launch_bounds__(256) k_order_items_scatter(const GroupEntry* e
     order[atomicAdd(cursor + item_bucket(ent, T, bpt, ids, i), 1u)] = (int64_t)i;
 }
 
+// Largest bucket grouped in shared memory (larger ones keep the scatter's order).
+constexpr uint32_t kGroupCap = 2048;
+constexpr uint32_t kGroupHash = 2 * kGroupCap;  // hash slots (load at most 1/2)
+// Cost of an item that fetches a row, in units of an item that repeats the
+// row before it (stored from the warp's copy: no fetch, no decode), for
+// cutting the list into warp shares of equal cost.
+constexpr uint32_t kFetchWeight = 8;
+// dynamic shared memory of k_order_items_group: hash keys, slot counters,
+// items and their slots before and after grouping
+constexpr size_t kGroupSmem = 8ull * kGroupHash + 4ull * kGroupHash + 2ull * 4ull * kGroupCap +
+                              2ull * 2ull * kGroupCap;
+
+// One CTA per bucket of the ordered group list: the bucket's lookups of each
+// row brought next to each other (each item's row id inserted into a hash
+// table in shared memory, then the items counting-sorted by their row's hash
+// slot: the rows in hash order, their lookups side by side).  Each item's
+// cost (a row's first item kFetchWeight, its repeats 1), the cost of the
+// bucket's earlier items in wpre, the bucket's total in cost.  ends: bucket
+// ends in order (the scatter's cursors).  A bucket above kGroupCap items
+// keeps its order, every item costing kFetchWeight (cost = its item count;
+// wpre unused).
+__global__ void __launch_bounds__(256) k_order_items_group(const int64_t* ids,
+                                                           const uint32_t* ends,
+                                                           int64_t* order, uint32_t* wpre,
+                                                           uint32_t* cost) {
+  extern __shared__ __align__(16) unsigned long long gsm[];
+  unsigned long long* hkey = gsm;                                    // kGroupHash
+  uint32_t* hcnt = reinterpret_cast<uint32_t*>(hkey + kGroupHash);  // kGroupHash
+  uint32_t* item = hcnt + kGroupHash;                                // kGroupCap
+  uint32_t* item2 = item + kGroupCap;                                // kGroupCap
+  uint16_t* slot = reinterpret_cast<uint16_t*>(item2 + kGroupCap);  // kGroupCap
+  uint16_t* slot2 = slot + kGroupCap;                                // kGroupCap
+  __shared__ uint32_t wsum[8];
+  constexpr unsigned long long kEmpty = 0x8000000000000000ull;
+  const uint32_t b = blockIdx.x, tid = threadIdx.x, lane = tid & 31u, wid = tid >> 5;
+  const uint32_t nt = blockDim.x;
+  const uint32_t start = b ? ends[b - 1] : 0u, nb = ends[b] - start;
+  if (nb == 0u || nb > kGroupCap) {
+    if (tid == 0) cost[b] = nb;
+    return;
+  }
+  uint32_t hs = 4u;  // hash slots: a power of two at least twice the items
+  while (hs < 2u * nb) hs <<= 1;
+  uint32_t lg = 0;
+  while ((1u << lg) < hs) ++lg;
+  for (uint32_t i = tid; i < hs; i += nt) {
+    hkey[i] = kEmpty;
+    hcnt[i] = 0u;
+  }
+  __syncthreads();
+  // each item's row into the table (linear probing; a row's lookups share a slot)
+  for (uint32_t j = tid; j < nb; j += nt) {
+    const int64_t it = order[start + j];
+    const int64_t id = __ldg(ids + it);
+    const unsigned long long k =
+        (unsigned long long)id == kEmpty ? kEmpty + 1ull : (unsigned long long)id;
+    uint32_t h = (uint32_t)((k * 0x9E3779B97F4A7C15ull) >> (64u - lg));
+    for (uint32_t probe = 0; probe < hs; ++probe) {
+      const unsigned long long prev = atomicCAS(hkey + h, kEmpty, k);
+      if (prev == kEmpty || prev == k) break;
+      h = (h + 1u) & (hs - 1u);
+    }
+    item[j] = (uint32_t)it;
+    slot[j] = (uint16_t)h;
+    atomicAdd(hcnt + h, 1u);
+  }
+  __syncthreads();
+  // slot starts: an exclusive scan of the counts (hs / nt slots per thread)
+  const uint32_t per = (hs + nt - 1u) / nt, s0 = tid * per;
+  uint32_t sum = 0;
+  for (uint32_t q = 0; q < per; ++q)
+    if (s0 + q < hs) sum += hcnt[s0 + q];
+  uint32_t incl = sum;
+#pragma unroll
+  for (uint32_t d = 1; d < 32u; d <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31u) wsum[wid] = incl;
+  __syncthreads();
+  uint32_t base = 0;
+  for (uint32_t w = 0; w < wid; ++w) base += wsum[w];
+  uint32_t run = base + incl - sum;
+  for (uint32_t q = 0; q < per; ++q) {
+    if (s0 + q < hs) {
+      const uint32_t c = hcnt[s0 + q];
+      hcnt[s0 + q] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (uint32_t j = tid; j < nb; j += nt) {
+    const uint32_t p = atomicAdd(hcnt + slot[j], 1u);
+    item2[p] = item[j];
+    slot2[p] = slot[j];
+  }
+  __syncthreads();
+  // costs in the new order: a position starts a row when its slot differs
+  // from the one before; 8 consecutive positions per thread
+  const uint32_t j0 = tid * 8u;
+  uint32_t wts = 0, csum = 0;
+#pragma unroll
+  for (uint32_t q = 0; q < 8u; ++q) {
+    const uint32_t j = j0 + q;
+    if (j < nb) {
+      const uint32_t w = (j == 0u || slot2[j] != slot2[j - 1u]) ? kFetchWeight : 1u;
+      wts |= w << (4u * q);
+      csum += w;
+    }
+  }
+  __syncthreads();  // wsum is reused
+  incl = csum;
+#pragma unroll
+  for (uint32_t d = 1; d < 32u; d <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31u) wsum[wid] = incl;
+  __syncthreads();
+  uint32_t cbase = 0, total = 0;
+  for (uint32_t w = 0; w < (nt >> 5); ++w) {
+    if (w < wid) cbase += wsum[w];
+    total += wsum[w];
+  }
+  uint32_t r = cbase + incl - csum;
+#pragma unroll
+  for (uint32_t q = 0; q < 8u; ++q) {
+    const uint32_t j = j0 + q;
+    if (j < nb) {
+      order[start + j] = (int64_t)item2[j];
+      wpre[start + j] = r;
+      r += (wts >> (4u * q)) & 15u;
+    }
+  }
+  if (tid == 0) cost[b] = total;
+}
+
+static_assert(kOrderBuckets == 4u * 256u, "k_order_shares scans 4 bucket costs per thread");
+
+// Warp shares of the grouped list with equal costs: share w starts at the
+// item whose cost interval holds floor(w * total / nw); shares[nw] = n.  A
+// share may start on a repeat (its first item then fetches the row again).
+// One warp per share (nw + 1 warps); each CTA first scans the bucket costs.
+__global__ void __launch_bounds__(256) k_order_shares(const uint32_t* ends, const uint32_t* cost,
+                                                      const uint32_t* wpre, uint32_t nw,
+                                                      uint32_t n, uint32_t* shares) {
+  __shared__ unsigned long long pre[kOrderBuckets];
+  __shared__ unsigned long long wsum[8];
+  const uint32_t tid = threadIdx.x, lane = tid & 31u, wid = tid >> 5;
+  // bucket costs, 4 per thread, and their exclusive scan
+  unsigned long long c[4], sum = 0;
+#pragma unroll
+  for (uint32_t q = 0; q < 4u; ++q) {
+    const uint32_t bk = 4u * tid + q;
+    const uint32_t nb = ends[bk] - (bk ? ends[bk - 1u] : 0u);
+    c[q] = nb > kGroupCap ? (unsigned long long)kFetchWeight * nb : (unsigned long long)cost[bk];
+    sum += c[q];
+  }
+  unsigned long long incl = sum;
+#pragma unroll
+  for (uint32_t d = 1; d < 32u; d <<= 1) {
+    const unsigned long long v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31u) wsum[wid] = incl;
+  __syncthreads();
+  unsigned long long run = 0, total = 0;
+  for (uint32_t w = 0; w < 8u; ++w) {
+    if (w < wid) run += wsum[w];
+    total += wsum[w];
+  }
+  run += incl - sum;
+#pragma unroll
+  for (uint32_t q = 0; q < 4u; ++q) {
+    pre[4u * tid + q] = run;
+    run += c[q];
+  }
+  __syncthreads();
+  const uint32_t w = blockIdx.x * 8u + wid;
+  if (w > nw) return;
+  if (w == nw) {
+    if (lane == 0) shares[w] = n;
+    return;
+  }
+  const unsigned long long k = (unsigned long long)w * total / nw;
+  // the last bucket whose cost starts at or before k (it holds k)
+  uint32_t lo = 0, hi = kOrderBuckets - 1u;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi + 1u) >> 1;
+    if (pre[mid] <= k) lo = mid; else hi = mid - 1u;
+  }
+  const uint32_t start = lo ? ends[lo - 1u] : 0u, nbl = ends[lo] - start;
+  const unsigned long long off = k - pre[lo];
+  uint32_t j;
+  if (nbl > kGroupCap) {
+    j = (uint32_t)(off / kFetchWeight);
+  } else {  // the last item whose cost starts at or before off: a 32-way search
+    uint32_t a = 0, span = nbl;  // the answer lies in [a, a + span)
+    while (span > 1u) {
+      const uint32_t step = (span + 31u) >> 5;
+      const uint32_t cand = a + lane * step;
+      const bool le = cand < a + span && __ldg(wpre + start + cand) <= off;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, le);  // lane 0 always true
+      const uint32_t last = 31u - __clz(m);
+      a += last * step;
+      span = min(step, span - last * step);
+    }
+    j = a;
+  }
+  if (lane == 0) shares[w] = start + j;
+}
+
 }  // namespace
 
 cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int64_t* ids,
@@ -2382,17 +2607,50 @@ cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uin
   return cudaGetLastError();
 }
 
-cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st) {
-  if (g.n_items == 0) return cudaSuccess;
-  const int warps = 8;
-  const size_t smem = 4ull * (g.T * (sizeof(GroupEntry) / 4) + (uint64_t)warps * g.warp_words);
-  const int bps = blocks_per_sm(k_gather_group, 32 * warps, smem);
+static size_t group_smem(const GroupArgs& g, int warps) {
+  return 4ull * (g.T * (sizeof(GroupEntry) / 4) + (uint64_t)warps * g.warp_words);
+}
+
+static uint64_t group_blocks(const GroupArgs& g, int sm_count, int warps) {
+  const int bps = blocks_per_sm(k_gather_group, 32 * warps, group_smem(g, warps));
   uint64_t blocks = (uint64_t)sm_count * bps;
   const uint64_t need = launch_blocks(g.n_items, blocks, (uint64_t)warps, 8ull, g.host_src != 0u,
                                       g.order != nullptr);
-  if (blocks > need) blocks = need;
-  k_gather_group<<<(uint32_t)blocks, 32 * warps, smem, st>>>(g);
+  return blocks > need ? need : blocks;
+}
+
+static cudaError_t launch_group_blocks(const GroupArgs& g, uint64_t blocks, int warps,
+                                       cudaStream_t st) {
+  k_gather_group<<<(uint32_t)blocks, 32 * warps, group_smem(g, warps), st>>>(g);
   return cudaGetLastError();
+}
+
+cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st) {
+  if (g.n_items == 0) return cudaSuccess;
+  const int warps = 8;
+  return launch_group_blocks(g, group_blocks(g, sm_count, warps), warps, st);
+}
+
+cudaError_t launch_group_ordered(GroupArgs g, const uint32_t* hist, uint32_t* wpre,
+                                 uint32_t* cost, uint32_t* shares, int sm_count,
+                                 cudaStream_t st) {
+  if (g.n_items == 0) return cudaSuccess;
+  if (g.n_items > 0xFFFFFFFFull) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(k_order_items_group,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kGroupSmem);
+  if (e != cudaSuccess) return e;
+  k_order_items_group<<<kOrderBuckets, 256, kGroupSmem, st>>>(
+      g.ids, hist, const_cast<int64_t*>(g.order), wpre, cost);
+  const int warps = 8;
+  const uint64_t blocks = group_blocks(g, sm_count, warps);
+  const uint32_t nw = (uint32_t)(blocks * warps);
+  k_order_shares<<<(nw + 1u + 7u) / 8u, 256, 0, st>>>(hist, cost, wpre, nw,
+                                                      (uint32_t)g.n_items, shares);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  g.shares = shares;
+  return launch_group_blocks(g, blocks, warps, st);
 }
 
 cudaError_t launch_link_copy(uint4* dst, const uint4* src, uint64_t nvec, int sm_count,

@@ -236,8 +236,8 @@ def ibp_project_compress(store: int, x, m: int, k_dim: int, w, bias, dtype: int,
 
 
 def order_workspace_bytes(n: int) -> int:
-    """Bytes of workspace ibp_gather_decompress_ordered needs for n ids."""
-    return 16 * int(n) + 4096
+    """Bytes of workspace the ordered gathers need for n ids (items)."""
+    return 20 * int(n) + 65536
 
 
 def ibp_gather_decompress_ordered(store: int, dst, dst_stride_bytes: int, src, offsets, ids,

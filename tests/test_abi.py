@@ -54,7 +54,7 @@ def test_host_side_argument_checks(lib):
                                            None) == ibp.IBP_EINVAL
     assert lib.ibp_gather_decompress_ordered(None, 16, 16, 16, None, 16, 1, 16, 4112,
                                              None) == ibp.IBP_EINVAL
-    assert ibp.order_workspace_bytes(10) == 16 * 10 + 4096
+    assert ibp.order_workspace_bytes(10) == 20 * 10 + 65536
     assert lib.ibp_store_set_lengths(None, 16) == ibp.IBP_EINVAL
     # a cache front needs both its map and its cache, the cache 16-byte aligned
     assert lib.ibp_gather_decompress_cached(None, 16, 16, 16, 16, 1, None, 16, 1, None) == ibp.IBP_EINVAL

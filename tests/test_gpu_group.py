@@ -258,3 +258,73 @@ def test_group_length_tables_and_a_rebuilt_store():
     finally:
         for s in stores:
             s.close()
+
+
+def test_group_ordered_repeats_large_buckets_and_errors():
+    """The ordered group gather over heavy repeats: every item equals the plain
+    group gather's (bytes and status codes) and the rows.  Store 0 (dense,
+    uniform, host) has one row whose stream is corrupt, looked up 2600 times:
+    its bucket is above the 2048 items sorted in shared memory and stays in
+    scatter order, and the repeats of a corrupt row are zero-filled like the
+    row.  Store 1 (network mode, host) has a hot row whose repeats span warp
+    shares; store 2 (two-run mode, HBM) has out-of-range ids repeated next to
+    each other; store 3 (all raw, HBM) takes the raw path with repeats.  A
+    batch of 3 leaves most warps an empty share."""
+    R, C, N, B = 512, 64, 3000, 6000
+    g = np.random.default_rng(11)
+    stores, slots, tables = [], [], []
+    try:
+        dense = rows_u8(wl.dense_gnn_rows(N, seed=13))
+        fuzz = wl.fuzz_rows(N, R, seed=14)
+        tiny = rows_u8(wl.tiny_rows(seed=15, n_rows=N, dim=R // 4, raw_frac=0.02)[0])
+        for rb, host in [(dense, True), (fuzz, True), (tiny, False)]:
+            st, sl = _host_store(R, C, rb, host=host)
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+        st = Store(R, C, N)  # all raw: a store whose Mask was never built
+        sl = torch.empty((N, st.slot), dtype=torch.uint8, device=DEV)
+        ibp.ibp_compress(st.h, sl, torch.from_numpy(fuzz).to(DEV), R, None, N, None)
+        stores.append(st)
+        slots.append(sl)
+        tables.append(fuzz)
+        torch.cuda.synchronize()
+        # a packed row of store 0 made corrupt: every chunk flagged raw in its header
+        bm = stores[0].bitmap()
+        packed = [i for i in range(N) if not (int(bm[i >> 5]) >> (i & 31)) & 1]
+        bad = packed[len(packed) // 2]
+        slots[0][bad, :4] = 0
+        T = len(stores)
+        ids = np.stack([wl.zipf_ids(B, N, table=t, seed=16) for t in range(T)], axis=1)
+        ids[g.choice(B, 2600, replace=False), 0] = bad
+        ids[g.choice(B, 900, replace=False), 1] = int(ids[0, 1])
+        ids[100:140, 2] = N + 5
+        ids[200:230, 2] = -1
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            for b in (B, 3):
+                sub = np.ascontiguousarray(ids[:b])
+                ref = torch.full((b, T, R), 0xCC, dtype=torch.uint8, device=DEV)
+                ibp.ibp_group_gather_decompress(grp, ref, T * R, to_dev(sub), b)
+                codes = [s.status() for s in stores]
+                out = torch.full((b, T, R), 0x33, dtype=torch.uint8, device=DEV)
+                ws = torch.empty(ibp.order_workspace_bytes(b * T), dtype=torch.uint8,
+                                 device=DEV)
+                ibp.ibp_group_gather_decompress_ordered(grp, out, T * R, to_dev(sub), b, ws,
+                                                        ws.numel())
+                assert [s.status() for s in stores] == codes, b
+                assert torch.equal(out, ref), b
+                o = out.cpu().numpy()
+                for t in range(T):
+                    x = sub[:, t]
+                    ok = (x >= 0) & (x < N) & ~((t == 0) & (x == bad))
+                    assert np.array_equal(o[ok, t], tables[t][x[ok]]), (b, t)
+                    assert not o[~ok, t].any(), (b, t)
+                if b == B:
+                    assert codes[0] == ibp.IBP_ECORRUPT and codes[2] == ibp.IBP_ERANGE
+                    assert codes[1] == ibp.IBP_OK and codes[3] == ibp.IBP_OK
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()
