@@ -1029,6 +1029,7 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
   __syncthreads();
   for (uint32_t t = threadIdx.x; t < T; t += blockDim.x)
     if (__ldg(ent[t].scal + 9) != ent[t].gen) atomicOr(&s_stale[t >> 5], 1u << (t & 31u));
+
   uint32_t* ring = smem + ent_words + wid * g.warp_words;
   uint4* rinfo = reinterpret_cast<uint4*>(ring + S * g.sbuf_words);
   uint32_t* cinfo = ring + S * g.sbuf_words + 256;
@@ -2042,6 +2043,10 @@ __global__ void __launch_bounds__(256) k_order_count(const int64_t* ids, uint64_
 // counts -> exclusive starts, in place (one block of kOrderBuckets threads)
 __global__ void __launch_bounds__(1024) k_order_scan(uint32_t* hist) {
   __shared__ uint32_t part[kOrderBuckets];
+  // behind the count (programmatic dependent launch in the group path; a
+  // plain launch makes both instructions no-ops)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t t = threadIdx.x;
   const uint32_t v = hist[t];
   part[t] = v;
@@ -2096,6 +2101,7 @@ __global__ void __launch_bounds__(256) k_order_items_count(const GroupEntry* ent
                                                            const int64_t* ids, uint64_t n,
                                                            uint32_t* hist) {
   __shared__ uint32_t h[kOrderBuckets];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t bpt = kOrderBuckets / T;
   for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) h[b] = 0;
   __syncthreads();
@@ -2110,6 +2116,8 @@ __global__ void __launch_bounds__(256) k_order_items_count(const GroupEntry* ent
 __global__ void __launch_bounds__(256) k_order_items_scatter(const GroupEntry* ent, uint32_t T,
                                                              const int64_t* ids, uint64_t n,
                                                              uint32_t* cursor, int64_t* order) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t bpt = kOrderBuckets / T;
   for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (uint64_t)gridDim.x * blockDim.x)
@@ -2124,9 +2132,8 @@ constexpr uint32_t kGroupHash = 2 * kGroupCap;  // hash slots (load at most 1/2)
 // cutting the list into warp shares of equal cost.
 constexpr uint32_t kFetchWeight = 8;
 // dynamic shared memory of k_order_items_group: hash keys, slot counters,
-// items and their slots before and after grouping
-constexpr size_t kGroupSmem = 8ull * kGroupHash + 4ull * kGroupHash + 2ull * 4ull * kGroupCap +
-                              2ull * 2ull * kGroupCap;
+// and each position's slot after grouping (4 CTAs per SM)
+constexpr size_t kGroupSmem = 8ull * kGroupHash + 4ull * kGroupHash + 2ull * kGroupCap;
 
 // One CTA per bucket of the ordered group list: the bucket's lookups of each
 // row brought next to each other (each item's row id inserted into a hash
@@ -2136,7 +2143,7 @@ constexpr size_t kGroupSmem = 8ull * kGroupHash + 4ull * kGroupHash + 2ull * 4ul
 // bucket's earlier items in wpre, the bucket's total in cost.  ends: bucket
 // ends in order (the scatter's cursors).  A bucket above kGroupCap items
 // keeps its order, every item costing kFetchWeight (cost = its item count;
-// wpre unused).
+// wpre unused).  Launched behind the scatter (programmatic dependent launch).
 __global__ void __launch_bounds__(256) k_order_items_group(const int64_t* ids,
                                                            const uint32_t* ends,
                                                            int64_t* order, uint32_t* wpre,
@@ -2144,14 +2151,13 @@ __global__ void __launch_bounds__(256) k_order_items_group(const int64_t* ids,
   extern __shared__ __align__(16) unsigned long long gsm[];
   unsigned long long* hkey = gsm;                                    // kGroupHash
   uint32_t* hcnt = reinterpret_cast<uint32_t*>(hkey + kGroupHash);  // kGroupHash
-  uint32_t* item = hcnt + kGroupHash;                                // kGroupCap
-  uint32_t* item2 = item + kGroupCap;                                // kGroupCap
-  uint16_t* slot = reinterpret_cast<uint16_t*>(item2 + kGroupCap);  // kGroupCap
-  uint16_t* slot2 = slot + kGroupCap;                                // kGroupCap
+  uint16_t* slot2 = reinterpret_cast<uint16_t*>(hcnt + kGroupHash);  // kGroupCap
   __shared__ uint32_t wsum[8];
   constexpr unsigned long long kEmpty = 0x8000000000000000ull;
+  constexpr uint32_t kPer = kGroupCap / 256u;  // items per thread at most
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t b = blockIdx.x, tid = threadIdx.x, lane = tid & 31u, wid = tid >> 5;
-  const uint32_t nt = blockDim.x;
   const uint32_t start = b ? ends[b - 1] : 0u, nb = ends[b] - start;
   if (nb == 0u || nb > kGroupCap) {
     if (tid == 0) cost[b] = nb;
@@ -2161,30 +2167,38 @@ __global__ void __launch_bounds__(256) k_order_items_group(const int64_t* ids,
   while (hs < 2u * nb) hs <<= 1;
   uint32_t lg = 0;
   while ((1u << lg) < hs) ++lg;
-  for (uint32_t i = tid; i < hs; i += nt) {
+  for (uint32_t i = tid; i < hs; i += 256u) {
     hkey[i] = kEmpty;
     hcnt[i] = 0u;
   }
   __syncthreads();
-  // each item's row into the table (linear probing; a row's lookups share a slot)
-  for (uint32_t j = tid; j < nb; j += nt) {
-    const int64_t it = order[start + j];
-    const int64_t id = __ldg(ids + it);
-    const unsigned long long k =
-        (unsigned long long)id == kEmpty ? kEmpty + 1ull : (unsigned long long)id;
-    uint32_t h = (uint32_t)((k * 0x9E3779B97F4A7C15ull) >> (64u - lg));
-    for (uint32_t probe = 0; probe < hs; ++probe) {
-      const unsigned long long prev = atomicCAS(hkey + h, kEmpty, k);
-      if (prev == kEmpty || prev == k) break;
-      h = (h + 1u) & (hs - 1u);
+  // each item's row into the table (linear probing; a row's lookups share a
+  // slot); item j = tid + 256 q is held in registers
+  uint32_t it[kPer], sl[kPer];
+#pragma unroll
+  for (uint32_t q = 0; q < kPer; ++q) {
+    const uint32_t j = tid + 256u * q;
+    it[q] = 0u;
+    sl[q] = 0u;
+    if (j < nb) {
+      const int64_t item = order[start + j];
+      const int64_t id = __ldg(ids + item);
+      const unsigned long long k =
+          (unsigned long long)id == kEmpty ? kEmpty + 1ull : (unsigned long long)id;
+      uint32_t h = (uint32_t)((k * 0x9E3779B97F4A7C15ull) >> (64u - lg));
+      for (uint32_t probe = 0; probe < hs; ++probe) {
+        const unsigned long long prev = atomicCAS(hkey + h, kEmpty, k);
+        if (prev == kEmpty || prev == k) break;
+        h = (h + 1u) & (hs - 1u);
+      }
+      it[q] = (uint32_t)item;
+      sl[q] = h;
+      atomicAdd(hcnt + h, 1u);
     }
-    item[j] = (uint32_t)it;
-    slot[j] = (uint16_t)h;
-    atomicAdd(hcnt + h, 1u);
   }
   __syncthreads();
-  // slot starts: an exclusive scan of the counts (hs / nt slots per thread)
-  const uint32_t per = (hs + nt - 1u) / nt, s0 = tid * per;
+  // slot starts: an exclusive scan of the counts (hs / 256 slots per thread)
+  const uint32_t per = (hs + 255u) / 256u, s0 = tid * per;
   uint32_t sum = 0;
   for (uint32_t q = 0; q < per; ++q)
     if (s0 + q < hs) sum += hcnt[s0 + q];
@@ -2207,10 +2221,14 @@ __global__ void __launch_bounds__(256) k_order_items_group(const int64_t* ids,
     }
   }
   __syncthreads();
-  for (uint32_t j = tid; j < nb; j += nt) {
-    const uint32_t p = atomicAdd(hcnt + slot[j], 1u);
-    item2[p] = item[j];
-    slot2[p] = slot[j];
+  // every read of the bucket's old order happened before the first barrier
+#pragma unroll
+  for (uint32_t q = 0; q < kPer; ++q) {
+    if (tid + 256u * q < nb) {
+      const uint32_t p = atomicAdd(hcnt + sl[q], 1u);
+      order[start + p] = (int64_t)it[q];
+      slot2[p] = (uint16_t)sl[q];
+    }
   }
   __syncthreads();
   // costs in the new order: a position starts a row when its slot differs
@@ -2236,7 +2254,7 @@ __global__ void __launch_bounds__(256) k_order_items_group(const int64_t* ids,
   if (lane == 31u) wsum[wid] = incl;
   __syncthreads();
   uint32_t cbase = 0, total = 0;
-  for (uint32_t w = 0; w < (nt >> 5); ++w) {
+  for (uint32_t w = 0; w < 8u; ++w) {
     if (w < wid) cbase += wsum[w];
     total += wsum[w];
   }
@@ -2245,7 +2263,6 @@ __global__ void __launch_bounds__(256) k_order_items_group(const int64_t* ids,
   for (uint32_t q = 0; q < 8u; ++q) {
     const uint32_t j = j0 + q;
     if (j < nb) {
-      order[start + j] = (int64_t)item2[j];
       wpre[start + j] = r;
       r += (wts >> (4u * q)) & 15u;
     }
@@ -2264,6 +2281,7 @@ __global__ void __launch_bounds__(256) k_order_shares(const uint32_t* ends, cons
                                                       uint32_t n, uint32_t* shares) {
   __shared__ unsigned long long pre[kOrderBuckets];
   __shared__ unsigned long long wsum[8];
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // behind the grouping kernel
   const uint32_t tid = threadIdx.x, lane = tid & 31u, wid = tid >> 5;
   // bucket costs, 4 per thread, and their exclusive scan
   unsigned long long c[4], sum = 0;
@@ -2330,6 +2348,25 @@ __global__ void __launch_bounds__(256) k_order_shares(const uint32_t* ends, cons
 
 }  // namespace
 
+// A launch that may start while the stream's previous kernel finishes
+// (programmatic dependent launch): the kernel waits for that kernel's results
+// with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_behind(void (*kern)(KArgs...), uint32_t grid, uint32_t block, size_t smem,
+                          cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int64_t* ids,
                                uint64_t n_items, int64_t* order_out, uint32_t* hist,
                                int sm_count, cudaStream_t st) {
@@ -2339,10 +2376,10 @@ cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int6
   const uint64_t need = (n_items + 255) / 256;
   if (blocks > need) blocks = need;
   k_order_items_count<<<(uint32_t)blocks, 256, 0, st>>>(entries, T, ids, n_items, hist);
-  k_order_scan<<<1, kOrderBuckets, 0, st>>>(hist);
-  k_order_items_scatter<<<(uint32_t)blocks, 256, 0, st>>>(entries, T, ids, n_items, hist,
-                                                          order_out);
-  return cudaGetLastError();
+  cudaError_t e = launch_behind(k_order_scan, 1u, kOrderBuckets, 0, st, hist);
+  if (e != cudaSuccess) return e;
+  return launch_behind(k_order_items_scatter, (uint32_t)blocks, 256u, 0, st, entries, T, ids,
+                       n_items, hist, order_out);
 }
 
 cudaError_t launch_count_ones(const CountArgs& a, int sm_count, cudaStream_t st) {
@@ -2640,16 +2677,18 @@ cudaError_t launch_group_ordered(GroupArgs g, const uint32_t* hist, uint32_t* wp
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kGroupSmem);
   if (e != cudaSuccess) return e;
-  k_order_items_group<<<kOrderBuckets, 256, kGroupSmem, st>>>(
-      g.ids, hist, const_cast<int64_t*>(g.order), wpre, cost);
+  e = launch_behind(k_order_items_group, kOrderBuckets, 256u, kGroupSmem, st, g.ids, hist,
+                    const_cast<int64_t*>(g.order), wpre, cost);
+  if (e != cudaSuccess) return e;
   const int warps = 8;
   const uint64_t blocks = group_blocks(g, sm_count, warps);
   const uint32_t nw = (uint32_t)(blocks * warps);
-  k_order_shares<<<(nw + 1u + 7u) / 8u, 256, 0, st>>>(hist, cost, wpre, nw,
-                                                      (uint32_t)g.n_items, shares);
-  e = cudaGetLastError();
+  e = launch_behind(k_order_shares, (nw + 1u + 7u) / 8u, 256u, 0, st, (const uint32_t*)hist,
+                    (const uint32_t*)cost, (const uint32_t*)wpre, nw, (uint32_t)g.n_items, shares);
   if (e != cudaSuccess) return e;
   g.shares = shares;
+  // the gather is a plain launch: started early (behind the share kernel) its
+  // CTAs, sized to fill the SMs, measured 3x slower on 2 KB rows
   return launch_group_blocks(g, blocks, warps, st);
 }
 
