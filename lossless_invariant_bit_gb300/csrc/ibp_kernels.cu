@@ -2097,31 +2097,61 @@ __device__ __forceinline__ uint32_t item_bucket(const GroupEntry* ent, uint32_t 
   return t * bpt + r;
 }
 
+// The items are visited table by table (x = t * batch + b is item b*T + t),
+// so that the 256 items of a CTA come from one or two tables and touch a few
+// dozen buckets: the CTA adds up its counts in shared memory and sends one
+// global atomic per bucket it touched.  (Visited in item order, the bucket
+// of a table's hottest rows took a returning global atomic per lookup, more
+// than a thousand in a row on one address.)
+__device__ __forceinline__ uint64_t table_major_item(uint64_t x, uint32_t T, uint64_t batch) {
+  return (x % batch) * T + x / batch;
+}
+
 __global__ void __launch_bounds__(256) k_order_items_count(const GroupEntry* ent, uint32_t T,
                                                            const int64_t* ids, uint64_t n,
                                                            uint32_t* hist) {
   __shared__ uint32_t h[kOrderBuckets];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t bpt = kOrderBuckets / T;
+  const uint64_t batch = n / T;
   for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) h[b] = 0;
   __syncthreads();
-  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (uint64_t)gridDim.x * blockDim.x)
-    atomicAdd(&h[item_bucket(ent, T, bpt, ids, i)], 1u);
+  for (uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n;
+       x += (uint64_t)gridDim.x * blockDim.x)
+    atomicAdd(&h[item_bucket(ent, T, bpt, ids, table_major_item(x, T, batch))], 1u);
   __syncthreads();
   for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x)
     if (h[b]) atomicAdd(hist + b, h[b]);
 }
 
+// One item per thread (the grid covers the n items), in table-major order:
+// a rank within the CTA's items of the same bucket (shared memory), one
+// global atomic per bucket the CTA touched for its base, the item at base +
+// rank.  cursor: each bucket's next free position (the scanned counts).
 __global__ void __launch_bounds__(256) k_order_items_scatter(const GroupEntry* ent, uint32_t T,
                                                              const int64_t* ids, uint64_t n,
                                                              uint32_t* cursor, int64_t* order) {
+  __shared__ uint32_t lc[kOrderBuckets];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t bpt = kOrderBuckets / T;
-  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (uint64_t)gridDim.x * blockDim.x)
-    order[atomicAdd(cursor + item_bucket(ent, T, bpt, ids, i), 1u)] = (int64_t)i;
+  const uint64_t batch = n / T;
+  for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) lc[b] = 0;
+  const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool has = x < n;
+  uint64_t item = 0;
+  uint32_t bk = 0, rank = 0;
+  __syncthreads();
+  if (has) {
+    item = table_major_item(x, T, batch);
+    bk = item_bucket(ent, T, bpt, ids, item);
+    rank = atomicAdd(&lc[bk], 1u);
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the scanned cursors
+  for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x)
+    if (lc[b]) lc[b] = atomicAdd(cursor + b, lc[b]);
+  __syncthreads();
+  if (has) order[lc[bk] + rank] = (int64_t)item;
 }
 
 // Largest bucket grouped in shared memory (larger ones keep the scatter's order).
@@ -2372,13 +2402,15 @@ cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int6
                                int sm_count, cudaStream_t st) {
   if (n_items == 0) return cudaSuccess;
   if (T == 0 || T > kOrderBuckets) return cudaErrorInvalidValue;
+  const uint64_t need = (n_items + 255) / 256;  // the scatter: one item per thread
+  if (need > 0x7FFFFFFFull) return cudaErrorInvalidValue;
   uint64_t blocks = (uint64_t)sm_count * 4;
-  const uint64_t need = (n_items + 255) / 256;
   if (blocks > need) blocks = need;
   k_order_items_count<<<(uint32_t)blocks, 256, 0, st>>>(entries, T, ids, n_items, hist);
   cudaError_t e = launch_behind(k_order_scan, 1u, kOrderBuckets, 0, st, hist);
   if (e != cudaSuccess) return e;
-  return launch_behind(k_order_items_scatter, (uint32_t)blocks, 256u, 0, st, entries, T, ids,
+  const uint64_t sblocks = need;
+  return launch_behind(k_order_items_scatter, (uint32_t)sblocks, 256u, 0, st, entries, T, ids,
                        n_items, hist, order_out);
 }
 
