@@ -2030,6 +2030,7 @@ __device__ __forceinline__ uint32_t order_bucket(int64_t id, uint64_t n_rows) {
 __global__ void __launch_bounds__(256) k_order_count(const int64_t* ids, uint64_t n,
                                                      uint64_t n_rows, uint32_t* hist) {
   __shared__ uint32_t h[kOrderBuckets];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) h[b] = 0;
   __syncthreads();
   for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -2043,8 +2044,7 @@ __global__ void __launch_bounds__(256) k_order_count(const int64_t* ids, uint64_
 // counts -> exclusive starts, in place (one block of kOrderBuckets threads)
 __global__ void __launch_bounds__(1024) k_order_scan(uint32_t* hist) {
   __shared__ uint32_t part[kOrderBuckets];
-  // behind the count (programmatic dependent launch in the group path; a
-  // plain launch makes both instructions no-ops)
+  // behind the count (programmatic dependent launch)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t t = threadIdx.x;
@@ -2060,13 +2060,33 @@ __global__ void __launch_bounds__(1024) k_order_scan(uint32_t* hist) {
   hist[t] = part[t] - v;
 }
 
+// One id per thread (the grid covers the n ids): a rank among the CTA's ids
+// of the same bucket (shared memory), one global atomic per bucket the CTA
+// touched for its base (a bucket of hot rows takes one per CTA, not one per
+// lookup), the id and its position at base + rank.
 __global__ void __launch_bounds__(256) k_order_scatter(const int64_t* ids, uint64_t n,
                                                        uint64_t n_rows, uint32_t* cursor,
                                                        int64_t* ids_out, int64_t* pos_out) {
-  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (uint64_t)gridDim.x * blockDim.x) {
-    const int64_t id = __ldg(ids + i);
-    const uint32_t p = atomicAdd(cursor + order_bucket(id, n_rows), 1u);
+  __shared__ uint32_t lc[kOrderBuckets];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) lc[b] = 0;
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool has = i < n;
+  int64_t id = 0;
+  uint32_t bk = 0, rank = 0;
+  __syncthreads();
+  if (has) {
+    id = __ldg(ids + i);
+    bk = order_bucket(id, n_rows);
+    rank = atomicAdd(&lc[bk], 1u);
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the scanned cursors
+  for (uint32_t b = threadIdx.x; b < kOrderBuckets; b += blockDim.x)
+    if (lc[b]) lc[b] = atomicAdd(cursor + b, lc[b]);
+  __syncthreads();
+  if (has) {
+    const uint32_t p = lc[bk] + rank;
     ids_out[p] = id;
     pos_out[p] = (int64_t)i;
   }
@@ -2074,16 +2094,37 @@ __global__ void __launch_bounds__(256) k_order_scatter(const int64_t* ids, uint6
 
 }  // namespace
 
+// A launch that may start while the stream's previous kernel finishes
+// (programmatic dependent launch): the kernel waits for that kernel's results
+// with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_behind(void (*kern)(KArgs...), uint32_t grid, uint32_t block, size_t smem,
+                          cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_order_ids(const int64_t* ids, uint64_t n, uint64_t n_rows, int64_t* ids_out,
                              int64_t* pos_out, uint32_t* hist, int sm_count, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
+  const uint64_t need = (n + 255) / 256;  // the scatter: one id per thread
+  if (need > 0x7FFFFFFFull) return cudaErrorInvalidValue;
   uint64_t blocks = (uint64_t)sm_count * 4;
-  const uint64_t need = (n + 255) / 256;
   if (blocks > need) blocks = need;
   k_order_count<<<(uint32_t)blocks, 256, 0, st>>>(ids, n, n_rows, hist);
-  k_order_scan<<<1, kOrderBuckets, 0, st>>>(hist);
-  k_order_scatter<<<(uint32_t)blocks, 256, 0, st>>>(ids, n, n_rows, hist, ids_out, pos_out);
-  return cudaGetLastError();
+  cudaError_t e = launch_behind(k_order_scan, 1u, kOrderBuckets, 0, st, hist);
+  if (e != cudaSuccess) return e;
+  return launch_behind(k_order_scatter, (uint32_t)need, 256u, 0, st, ids, n, n_rows, hist,
+                       ids_out, pos_out);
 }
 
 namespace {
@@ -2377,25 +2418,6 @@ __global__ void __launch_bounds__(256) k_order_shares(const uint32_t* ends, cons
 }
 
 }  // namespace
-
-// A launch that may start while the stream's previous kernel finishes
-// (programmatic dependent launch): the kernel waits for that kernel's results
-// with griddepcontrol.wait.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_behind(void (*kern)(KArgs...), uint32_t grid, uint32_t block, size_t smem,
-                          cudaStream_t st, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(block, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 
 cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int64_t* ids,
                                uint64_t n_items, int64_t* order_out, uint32_t* hist,
