@@ -328,3 +328,39 @@ def test_group_ordered_repeats_large_buckets_and_errors():
     finally:
         for s in stores:
             s.close()
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_group_ordered_one_and_most_tables(T):
+    """The ordered group gather with one store (1024 buckets for it) and with
+    the most stores a group takes (16 buckets each): Zipf lookups, the plain
+    group gather's bytes and the rows."""
+    R, C, N, B = 512, 1024, 500, 300
+    stores, slots, tables = [], [], []
+    try:
+        for t in range(T):
+            rb = rows_u8(wl.dlrm_rows(N, R // 4, table=t, seed=21))
+            st, sl = _host_store(R, C, rb, host=(t % 3 != 1))
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+        ids = np.stack([wl.zipf_ids(B, N, table=t, seed=22) for t in range(T)], axis=1)
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            ref = torch.full((B, T, R), 0xCC, dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress(grp, ref, T * R, to_dev(ids), B)
+            out = torch.full((B, T, R), 0x33, dtype=torch.uint8, device=DEV)
+            ws = torch.empty(ibp.order_workspace_bytes(B * T), dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress_ordered(grp, out, T * R, to_dev(ids), B, ws,
+                                                    ws.numel())
+            for s in stores:
+                assert s.status() == ibp.IBP_OK
+            assert torch.equal(out, ref)
+            o = out.cpu().numpy()
+            for t in range(T):
+                assert np.array_equal(o[:, t], tables[t][ids[:, t]]), t
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()

@@ -751,3 +751,25 @@ def test_uniform_single_run_decoder_with_raw_chunks(stores, keep, pos):
     ibp.ibp_decompress(st.h, out, cache, to_dev(offs_ref[:n]), n)
     assert st.status() == ibp.IBP_OK
     assert np.array_equal(out.cpu().numpy(), b)
+
+
+def test_ordered_gather_zipf_batch(stores):
+    """A Zipf batch (hot rows looked up thousands of times, their bucket's ids
+    ranked within each CTA before one atomic per CTA) through the ordered
+    gather: the plain gather's bytes and the rows."""
+    N, R, C, n = 3000, 512, 256, 20000
+    b = wl.fuzz_rows(N, R, seed=77)
+    st = stores(R, C, N)
+    d = to_dev(b)
+    ibp.ibp_build_meta(st.h, d, R, None, N, 9, 10)
+    slots, _ = gpu_compress(st, d, N, host=True)
+    ids = wl.zipf_ids(n, N, alpha=1.2, seed=5)
+    assert np.bincount(ids).max() > 2000
+    ref = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress(st.h, ref, slots, None, to_dev(ids), n)
+    out = torch.empty((n, R), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(ibp.order_workspace_bytes(n), dtype=torch.uint8, device=DEV)
+    ibp.ibp_gather_decompress_ordered(st.h, out, R, slots, None, to_dev(ids), n, ws, ws.numel())
+    assert st.status() == ibp.IBP_OK
+    assert torch.equal(out, ref)
+    assert np.array_equal(out.cpu().numpy(), b[ids])
