@@ -650,13 +650,14 @@ def run_tiny(args, rank, world, torch, dist):
         "roofline": {"bound": "hbm", "achieved": round(moved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(moved / hbm, 4),
                      # dram read + write of a 48-replica launch (profiles/
-                     # k_decode_fast_tiny_cache.md) scaled to this launch's rows
-                     "traffic": round(211.45e6 * n / (48 * 4096)),
+                     # k_decode_tiles_tiny_cache.md) scaled to this launch's rows
+                     "traffic": round(210.52e6 * n / (48 * 4096)),
                      "traffic_is": "dram__bytes_read.sum + dram__bytes_write.sum from ncu, "
                                    "scaled from a 196,608-row capture (part of the output is "
                                    "still in L2 when the kernel ends)",
                      "peak_is": "HBM copy bandwidth, %s" % peaks["source"],
-                     "kernel": "k_decode_fast<false, uniform1, small> (ibp_decompress, packed offsets)",
+                     "kernel": "k_decode_tiles<uniform1> (ibp_decompress, packed offsets: "
+                               "bulk copies of 32-row tiles)",
                      "algorithmic_bytes_per_launch": int(stored_sum + n * R + 8 * n)},
         "e2e": {"value": round(n * R * e2e_steps / e2e_t / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": n * R},

@@ -199,7 +199,11 @@ IBP_API ibp_status ibp_compress(ibp_store* store, void* dst_slots, const void* s
  * contiguous.  A valid stream is read only within its own stored bytes
  * (rounded up to 16); a corrupt one is detected after reading at most R bytes
  * from its start (slot stores: within the slot), so a packed cache that may
- * hold corrupt data should keep R readable bytes after its last row.
+ * hold corrupt data should keep R readable bytes after its last row.  With
+ * offsets in GPU memory (src 16-byte aligned), where the starts of 32
+ * consecutive rows increase and each lies at most R bytes before the next
+ * (a cache written by ibp_pack), the bytes from each row's start to the
+ * next row's start are read: the tile's bytes in one bulk copy.
  * Errors: IBP_EINVAL, IBP_EALIGN, IBP_ECUDA; corrupt streams and misaligned
  * offsets set the status word.  Calls on one store from several host threads
  * are safe for decompression; building or setting the Mask/Bitval or the

@@ -998,6 +998,336 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
 }
 
 // ------------------------------------------------------------------------
+// Decompression of a packed cache in row order (ibp_decompress with offsets,
+// the source in GPU memory).  The stored bytes of rows r0 .. r0+31 lie back
+// to back when their offsets increase (a cache written by ibp_pack), so one
+// bulk copy (cp.async.bulk, completing on an mbarrier) brings a tile's bytes
+// into a shared-memory stage, and the warps decode its rows from there: no
+// per-row copies, commits or waits.  A producer warp fills kTileStages stages
+// ahead of kTileWarps decoding warps.  A row whose bytes are not all in the
+// stage -- the call's last row (its end is not known), a stream longer than
+// the bytes up to the next row's start, every row of a tile whose offsets are
+// out of order or not 16-byte aligned -- is read by its warp from global
+// memory, within its own stream as the other decoders read it; the output and
+// status codes are those of k_decode_fast.
+// ------------------------------------------------------------------------
+constexpr uint32_t kTileRows = 32;
+constexpr uint32_t kTileStages = 3;  // measured: 2 or 4 stages slower
+constexpr uint32_t kTileWarps = 8;  // decoding warps; one more produces
+
+struct TileInfo {
+  uint64_t off[kTileRows + 1];  // the rows' starts, then the end of the stage's bytes
+  uint32_t nr;                  // rows in the tile
+  uint32_t ok;                  // 1: the stage holds [off[0], off[nr])
+};
+
+__device__ __forceinline__ bool tile_bar_try(uint32_t a, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return done != 0u;
+}
+
+// Wait for the phase of `parity`, for at most ~2 s.
+__device__ __forceinline__ bool tile_bar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+  if (tile_bar_try(a, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (true) {
+    if (tile_bar_try(a, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 2000000000ull) return false;
+  }
+}
+
+// One row from its stream at sb (shared memory, 16-byte aligned), of which
+// `have` bytes are valid.  Returns 0 once the row is written (decoded, or
+// zero-filled with a status), else the bytes of stream it needs (> have).
+template <int kMode>
+__device__ __forceinline__ uint32_t tile_row(const DecodeArgs& a, const FastParams& F,
+                                             const uint4* tab, const uint32_t* gtab,
+                                             const uint32_t* uparm, uint32_t* cinfo,
+                                             const uint32_t* sb, uint32_t have, bool raw,
+                                             uint4* drow, uint32_t lane, bool can_pack,
+                                             bool net5, bool uni) {
+  const uint32_t R = a.m.R, W = a.m.W, wpc = a.m.wpc, nch = a.m.nch;
+  const uint32_t nvec = R >> 4, G = W >> 2;
+  if (raw) {
+    if (have < R) return R;
+    uint4* dp = drow + lane;
+    for (uint32_t v = lane; v < nvec; v += 32, dp += 32)
+      *dp = *reinterpret_cast<const uint4*>(sb + 4u * v);
+    return 0u;
+  }
+  if (!can_pack) {
+    if (lane == 0) set_status(a.status, IBP_ECORRUPT);
+    zero_row(drow, nvec, lane);
+    return 0u;
+  }
+  const uint32_t nhw = (nch + 31u) >> 5;
+  if (have < 4u * nhw) return 4u * nhw;
+  const uint32_t hexp = (lane + 1u < nhw || (nch & 31u) == 0u) ? 0xFFFFFFFFu
+                                                                 : ((1u << (nch & 31u)) - 1u);
+  const bool all_packed = nhw == 1u ? (sb[0] & hexp) == hexp
+                                    : __all_sync(kFull, lane >= nhw || (sb[lane] & hexp) == hexp);
+  if (all_packed) {
+    const uint32_t need = 4u * ((F.min_bits + 31u) >> 5);
+    if (have < need) return need;
+    uint4* dp = drow + lane;
+    for (uint32_t g = lane; g < G; g += 32, dp += 32)
+      *dp = decode_packed_group<kMode>(tab, sb, g, G, nch, 0u, net5, uni, F, uparm);
+    return 0u;
+  }
+  uint32_t run = nch;
+  for (uint32_t k0 = 0; k0 < nch; k0 += 32) {
+    const uint32_t k = k0 + lane;
+    uint32_t size = 0, pk = 0;
+    if (k < nch) {
+      pk = (sb[k >> 5] >> (k & 31u)) & 1u;
+      size = pk ? __ldg(a.m.ckeep + k) : 32u * min(wpc, W - k * wpc);
+    }
+    const uint32_t incl = warp_inclusive_scan(size, lane);
+    if (k < nch) cinfo[k] = (run + incl - size) | (pk << 31);
+    run += __shfl_sync(kFull, incl, 31);
+  }
+  const uint32_t words = (run + 31u) >> 5;
+  if (4u * words >= R || 4ull * words > a.avail) {
+    if (lane == 0) set_status(a.status, IBP_ECORRUPT);
+    __syncwarp();
+    zero_row(drow, nvec, lane);
+    return 0u;
+  }
+  if (have < 4u * words) return 4u * words;
+  __syncwarp();
+  const uint32_t* cstat = gtab + ((G + 3u) & ~3u);
+  for (uint32_t g = lane; g < G; g += 32) {
+    const uint32_t gd = gtab[g];
+    const uint32_t k = gd & 0xFFFFu;
+    const uint32_t ci = cinfo[k];
+    const uint32_t start = ci & 0x7FFFFFFFu;
+    uint4* dp = drow + g;
+    if (ci >> 31) {
+      *dp = decode_packed_group<kMode>(tab, sb, g, G, nch, start - cstat[k], net5, uni, F, uparm);
+    } else {
+      const uint32_t bit = start + ((gd >> 16) << 5);
+      const uint32_t q = bit >> 5;
+      *dp = make_uint4(__funnelshift_r(sb[q], sb[q + 1], bit),
+                       __funnelshift_r(sb[q + 1], sb[q + 2], bit),
+                       __funnelshift_r(sb[q + 2], sb[q + 3], bit),
+                       __funnelshift_r(sb[q + 3], sb[q + 4], bit));
+    }
+  }
+  return 0u;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(32 * (kTileWarps + 1), 3) k_decode_tiles(DecodeArgs a,
+                                                                           FastParams F,
+                                                                           uint32_t stage_bytes) {
+  extern __shared__ __align__(16) uint32_t smem[];
+  const uint32_t lane = threadIdx.x & 31u, wid = threadIdx.x >> 5;
+  const uint32_t R = a.m.R, W = a.m.W, nch = a.m.nch;
+  const uint32_t nvec = R >> 4, G = W >> 2;
+  const uint32_t min_bits = kMode == kModeRuntime ? __ldg(a.m.scal) : F.min_bits;
+  const bool net5 = kMode == kModeNet5 || (kMode == kModeRuntime && __ldg(a.m.scal + 1) > 2u);
+  const bool uni = kMode == kModeUniform || kMode == kModeUniform1 ||
+                   (kMode == kModeRuntime && __ldg(a.m.scal + 3) != 0u);
+  const uint32_t min_words = (min_bits + 31u) >> 5;
+  const bool can_pack = 4u * min_words < R;
+  const uint32_t min_vec = min((4u * min_words + 15u) >> 4, nvec);
+  const bool stale = kMode != kModeRuntime && __ldg(a.m.scal + 9) != F.gen;
+  FastParams P = F;
+  P.min_bits = min_bits;  // the runtime mode reads it on the device
+  (void)G;
+
+  uint4* tab = reinterpret_cast<uint4*>(smem);
+  uint32_t* gtab = smem + F.table_words;
+  uint32_t* uparm = gtab + F.gtab_words;
+  TileInfo* info = reinterpret_cast<TileInfo*>(uparm + 8);
+  uint64_t* full = reinterpret_cast<uint64_t*>(info + kTileStages);
+  uint64_t* empty = full + kTileStages;
+  uint32_t* s_fail = reinterpret_cast<uint32_t*>(empty + kTileStages);
+  const uint32_t scr_words = W + 16u;
+  uint32_t* scratch = s_fail + 4;                         // kTileWarps x scr_words
+  uint32_t* cinfo_all = scratch + kTileWarps * scr_words;  // kTileWarps x nch (rounded)
+  const uint32_t nch4 = (nch + 3u) & ~3u;
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(cinfo_all + kTileWarps * nch4) + 127u) & ~uintptr_t(127));
+  {
+    if (F.table_words && !uni) {
+      const uint4* t = net5 ? a.t5 : a.t2;
+      const uint32_t nv = net5 ? 2u * W : W;
+      for (uint32_t v = threadIdx.x; v < nv; v += blockDim.x) tab[v] = __ldg(t + v);
+    }
+    for (uint32_t g = threadIdx.x; g < F.gtab_words; g += blockDim.x) gtab[g] = __ldg(a.gtab + g);
+    if (kMode == kModeRuntime && threadIdx.x < 8) uparm[threadIdx.x] = __ldg(a.m.scal + 4 + threadIdx.x);
+    if (threadIdx.x == 0) {
+      for (uint32_t st = 0; st < kTileStages; ++st) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(full + st))),
+                     "r"(1u)
+                     : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(empty + st))),
+                     "r"(kTileWarps)
+                     : "memory");
+      }
+      s_fail[0] = 0u;  // a wait gave up
+      s_fail[1] = 0u;  // tiles the producer issued
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  }
+  __syncthreads();
+
+  const uint64_t ntiles = (a.n + kTileRows - 1) / kTileRows;
+  const uint64_t t0 = ntiles * blockIdx.x / gridDim.x;
+  const uint32_t cnt = (uint32_t)(ntiles * (blockIdx.x + 1) / gridDim.x - t0);
+  const uint64_t cap = (uint64_t)stage_bytes - 64u;  // bytes a stage takes (64 bytes of slack)
+
+  if (wid == kTileWarps) {  // producer
+    for (uint32_t k = 0; k < cnt; ++k) {
+      const uint32_t s = k % kTileStages, round = k / kTileStages;
+      if (round > 0 && !tile_bar_wait(empty + s, (round - 1u) & 1u)) {
+        if (lane == 0) atomicExch(s_fail, 1u);
+        break;
+      }
+      if (*reinterpret_cast<volatile uint32_t*>(s_fail)) break;
+      const uint64_t r0 = (t0 + k) * kTileRows;
+      const uint32_t nr = (uint32_t)min((uint64_t)kTileRows, a.n - r0);
+      const bool has_next = r0 + nr < a.n;
+      uint64_t o = 0, oe = 0;
+      if (lane < nr) o = __ldg(a.offsets + r0 + lane);
+      if (lane == 0 && has_next) oe = __ldg(a.offsets + r0 + nr);
+      oe = __shfl_sync(kFull, oe, 0);
+      const uint64_t base = __shfl_sync(kFull, o, 0);
+      const uint64_t last = __shfl_sync(kFull, o, nr - 1u);
+      const uint64_t end = has_next ? oe : last;  // the call's last row: its end is unknown
+      const uint64_t nxt = __shfl_down_sync(kFull, o, 1);
+      // each start 16-byte aligned and at most R bytes before the next: the
+      // copy then reads only bytes the decoders may read (R from a row's start)
+      const uint64_t to = lane + 1u == nr ? end : nxt;
+      const bool in_order = lane >= nr || ((o & 15u) == 0u && o <= to && to - o <= R);
+      const bool ok = __all_sync(kFull, in_order) && (end & 15u) == 0u && end - base <= cap;
+      TileInfo& ti = info[s];
+      if (lane < nr) ti.off[lane] = o;
+      if (lane == 0) {
+        ti.off[nr] = end;
+        ti.nr = nr;
+        ti.ok = ok ? 1u : 0u;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t fb = static_cast<uint32_t>(__cvta_generic_to_shared(full + s));
+        const uint32_t bytes = ok ? (uint32_t)(end - base) : 0u;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                     "r"(bytes)
+                     : "memory");
+        if (bytes)
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+              "%2, [%3];" ::"r"(static_cast<uint32_t>(
+                                  __cvta_generic_to_shared(stages + (size_t)s * stage_bytes))),
+              "l"(a.src + base), "r"(bytes), "r"(fb)
+              : "memory");
+        s_fail[1] = k + 1u;  // tiles issued
+      }
+    }
+  } else {  // decoding warps
+    uint32_t* scr = scratch + wid * scr_words;
+    uint32_t* cinfo = cinfo_all + wid * nch4;
+    static_assert(kTileRows == 32u, "a tile's raw bits are one bitmap word");
+    // the raw bits of the tile (rows 32k .. 32k+31: one bitmap word), loaded
+    // a tile ahead
+    uint32_t bm_next = cnt ? __ldg(a.bitmap + t0) : 0u;
+    for (uint32_t k = 0; k < cnt; ++k) {
+      const uint32_t s = k % kTileStages;
+      const uint32_t bm = bm_next;
+      if (k + 1u < cnt) bm_next = __ldg(a.bitmap + t0 + k + 1u);
+      if (!tile_bar_wait(full + s, (k / kTileStages) & 1u)) {
+        if (lane == 0) atomicExch(s_fail, 1u);
+        break;
+      }
+      if (*reinterpret_cast<volatile uint32_t*>(s_fail)) break;
+      const TileInfo& ti = info[s];
+      const uint32_t nr = ti.nr;
+      const bool ok = ti.ok != 0u;
+      const uint64_t base = ti.off[0], end = ti.off[nr];
+      const uint32_t* stage = reinterpret_cast<const uint32_t*>(stages + (size_t)s * stage_bytes);
+      const uint64_t r0 = (t0 + k) * kTileRows;
+      for (uint32_t j = wid; j < nr; j += kTileWarps) {
+        const uint64_t i = r0 + j;
+        uint4* drow = reinterpret_cast<uint4*>(a.dst + i * a.dst_stride);
+        const uint64_t o = ti.off[j];
+        if (stale) {
+          if (lane == 0) set_status(a.status, IBP_EINVAL);
+          zero_row(drow, nvec, lane);
+          continue;
+        }
+        if (o & 15u) {
+          if (lane == 0) set_status(a.status, IBP_EALIGN);
+          zero_row(drow, nvec, lane);
+          continue;
+        }
+        const bool raw = (bm >> j) & 1u;
+        uint32_t need = 0xFFFFFFFFu;
+        if (ok) {
+          const uint64_t h = end - o;
+          need = tile_row<kMode>(a, P, tab, gtab, uparm, cinfo, stage + ((o - base) >> 2),
+                                 h > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)h, raw, drow, lane,
+                                 can_pack, net5, uni);
+        }
+        if (need == 0u) continue;
+        // from global memory: the first fetch as the other decoders take it
+        // (the raw row, the stream's length when a length table is attached,
+        // else the shortest stream), then the rest of the stream if it needs it
+        const uint4* src = reinterpret_cast<const uint4*>(a.src + o);
+        uint4* sv = reinterpret_cast<uint4*>(scr);
+        uint32_t nv = raw ? nvec
+                          : a.lengths ? min(max((__ldg(a.lengths + i) + 15u) >> 4, min_vec), nvec)
+                                      : min_vec;
+        __syncwarp();
+        for (uint32_t v = lane; v < nv; v += 32) sv[v] = src[v];
+        __syncwarp();
+        need = tile_row<kMode>(a, P, tab, gtab, uparm, cinfo, scr, 16u * nv, raw, drow, lane,
+                               can_pack, net5, uni);
+        if (need == 0u) continue;
+        const uint32_t nv2 = min((need + 15u) >> 4, nvec);
+        for (uint32_t v = nv + lane; v < nv2; v += 32) sv[v] = src[v];
+        __syncwarp();
+        tile_row<kMode>(a, P, tab, gtab, uparm, cinfo, scr, 16u * nv2, raw, drow, lane, can_pack,
+                        net5, uni);
+      }
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(empty + s)))
+                     : "memory");
+    }
+  }
+  __syncthreads();
+  if (*reinterpret_cast<volatile uint32_t*>(s_fail)) {
+    // a wait gave up: report it and let the copies in flight land before the
+    // CTA's shared memory goes away (each with its own bounded wait)
+    if (threadIdx.x == 0) {
+      set_status(a.status, IBP_ETIMEOUT);
+      // a stage is refilled only after its tile was decoded: the last
+      // kTileStages tiles issued are the only copies that can be in flight
+      const uint32_t issued = s_fail[1];
+      for (uint32_t k = issued > kTileStages ? issued - kTileStages : 0u; k < issued; ++k)
+        tile_bar_wait(full + (k % kTileStages), (k / kTileStages) & 1u);
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------------
 // Fused multi-store gather (a batch of lookups into several stores of one
 // geometry -- the 26 embedding tables of a DLRM batch -- in one launch, so
 // small per-table batches still fill the GPU).  Item i = b*T + t looks up
@@ -2574,6 +2904,50 @@ cudaError_t launch_fast(const DecodeArgs& a, const HostProps& hp, int sm_count, 
   return cudaGetLastError();
 }
 
+// The tile decoder for a packed cache read in row order; cudaErrorNotSupported
+// when its stages do not fit (the caller then takes k_decode_fast).
+template <int kMode>
+cudaError_t launch_tiles(const DecodeArgs& a, const HostProps& hp, int sm_count,
+                         cudaStream_t st) {
+  FastParams F = {};
+  const uint32_t W = a.m.W, nch = a.m.nch;
+  F.table_words = (kMode == kModeUniform || kMode == kModeUniform1) ? 0u : 8u * W;
+  F.gtab_words = (((W >> 2) + 3u) & ~3u) + ((nch + 3u) & ~3u);
+  F.min_bits = hp.min_bits;
+  F.um0 = hp.um0;
+  F.um1 = hp.um1;
+  F.ush = hp.ush;
+  F.ubv = hp.ubv;
+  F.ukeep = hp.ukeep;
+  F.gen = hp.gen;
+  // a stage takes up to 16 KB of stream bytes (a tile above that is read
+  // row by row): three stages and three CTAs per SM for rows of 1 KB
+  const uint32_t stage_bytes = ((min(kTileRows * a.m.R, 16384u) + 64u) + 127u) & ~127u;
+  const size_t fixed = 4ull * (F.table_words + F.gtab_words + 8) + sizeof(TileInfo) * kTileStages +
+                       16ull * kTileStages + 16ull +
+                       4ull * kTileWarps * ((W + 16u) + ((nch + 3u) & ~3u)) + 128ull;
+  const size_t smem = fixed + (size_t)kTileStages * stage_bytes;
+  if (smem > (size_t)max_smem_optin()) return cudaErrorNotSupported;
+  auto kern = k_decode_tiles<kMode>;
+  const int threads = 32 * (int)(kTileWarps + 1);
+  const int bps = blocks_per_sm(kern, threads, smem);
+  if (bps < 1) return cudaErrorNotSupported;
+  const uint64_t ntiles = (a.n + kTileRows - 1) / kTileRows;
+  uint64_t blocks = (uint64_t)sm_count * bps;
+  if (blocks > ntiles) blocks = ntiles;
+  kern<<<(uint32_t)blocks, threads, smem, st>>>(a, F, stage_bytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tiles_mode(const DecodeArgs& a, const HostProps& hp, int sm_count,
+                              cudaStream_t st) {
+  if (!hp.known) return launch_tiles<kModeRuntime>(a, hp, sm_count, st);
+  if (hp.uniform && hp.um1 == 0u) return launch_tiles<kModeUniform1>(a, hp, sm_count, st);
+  if (hp.uniform) return launch_tiles<kModeUniform>(a, hp, sm_count, st);
+  if (hp.max_runs <= 2u) return launch_tiles<kModeRun2>(a, hp, sm_count, st);
+  return launch_tiles<kModeNet5>(a, hp, sm_count, st);
+}
+
 template <bool kIds, bool kBig, bool kSplit = false>
 cudaError_t launch_fast_mode(const DecodeArgs& a, const HostProps& hp, int sm_count,
                              cudaStream_t st) {
@@ -2597,9 +2971,18 @@ cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count
   // rows up to 2 KB take the fast decoder from HBM and from host memory alike
   // (its cp.async copies use the .ca form: measured, the L2-only .cg form
   // reads host memory over the link at 60 % of the rate)
-  if (a.t2 && fast_geometry(a.m.R, a.m.wpc * 4u))
+  if (a.t2 && fast_geometry(a.m.R, a.m.wpc * 4u)) {
+    // a packed cache in GPU memory read in row order: whole tiles of rows by
+    // bulk copies (the source 16-byte aligned, as the copies need)
+    if (!a.ids && a.offsets && !a.host_src && !a.cache_map &&
+        (reinterpret_cast<uintptr_t>(a.src) & 15u) == 0u) {
+      const cudaError_t e = launch_tiles_mode(a, hp, sm_count, st);
+      if (e != cudaErrorNotSupported) return e;
+      cudaGetLastError();
+    }
     return a.ids ? launch_fast_mode<true, false>(a, hp, sm_count, st)
                  : launch_fast_mode<false, false>(a, hp, sm_count, st);
+  }
   // rows of 2-8 KB: the same pipeline with longer copies and, where the rings
   // need it, fewer warps per CTA
   if (a.t2 && a.m.R <= 8192u && (a.m.wpc & 3u) == 0u)

@@ -773,3 +773,69 @@ def test_ordered_gather_zipf_batch(stores):
     assert st.status() == ibp.IBP_OK
     assert torch.equal(out, ref)
     assert np.array_equal(out.cpu().numpy(), b[ids])
+
+
+def test_packed_cache_tiles_match_the_row_gather(stores):
+    """ibp_decompress of a packed HBM cache reads whole tiles of rows with bulk
+    copies when the offsets allow it.  Every case must give the bytes and the
+    status of the same rows gathered one by one (ids 0..n-1, the fast
+    gather), which reads each row within its own stream:
+    - offsets in order, over a ragged last tile;
+    - a tile whose offsets run backwards;
+    - a row whose start is more than R bytes before the next;
+    - streams whose header claims more bytes than the row was packed into,
+      mid-tile and on a tile's last row (they run into the next row);
+    - a header whose stream would exceed R (corrupt)."""
+    rows, _ = wl.tiny_rows(seed=9, n_rows=3000, raw_frac=0.02)
+    b = rows_u8(rows)
+    n, R, C = len(b), 1024, 256
+    st = stores(R, C, n)
+    d = to_dev(b)
+    ibp.ibp_build_meta(st.h, d, R, None, n, 95, 100)
+    slots, stored = gpu_compress(st, d, n)
+    offs = torch.zeros(n + 1, dtype=torch.int64, device=DEV)
+    ibp.ibp_pack(st.h, None, offs, slots, to_dev(stored.astype(np.int32)), n)
+    total = int(offs[-1].item())
+    cache = torch.zeros(total + 4 * R, dtype=torch.uint8, device=DEV)
+    ibp.ibp_pack(st.h, cache, offs, slots, to_dev(stored.astype(np.int32)), n)
+    base = offs[:n].cpu().numpy().astype(np.int64)
+    assert st.status() == ibp.IBP_OK
+    packed_rows = np.flatnonzero(stored == stored[stored < R].min())
+    ids = to_dev(np.arange(n, dtype=np.int64))
+
+    def both(o):
+        out = torch.full((n, R), 0x5A, dtype=torch.uint8, device=DEV)
+        ibp.ibp_decompress(st.h, out, cache, to_dev(o.astype(np.uint64)), n)
+        s1 = st.status()
+        ref = torch.full((n, R), 0x5A, dtype=torch.uint8, device=DEV)
+        ibp.ibp_gather_decompress(st.h, ref, cache, to_dev(o.astype(np.uint64)), ids, n)
+        s2 = st.status()
+        assert s1 == s2
+        assert torch.equal(out, ref)
+        return out.cpu().numpy(), s1
+
+    o, s = both(base)
+    assert s == ibp.IBP_OK and np.array_equal(o, b)
+    back = base.copy()
+    back[64:96] = base[64:96][::-1]  # tile 2 backwards
+    back[200] = base[900]            # row 200 far from its neighbours
+    o, s = both(back)
+    assert s == ibp.IBP_OK
+    want = np.arange(n)
+    want[64:96] = want[64:96][::-1]
+    want[200] = 900
+    assert np.array_equal(o, b[want])
+    # headers of all-packed rows changed: one claims a raw chunk (a longer
+    # stream, still below R), one claims every chunk raw (above R: corrupt)
+    hdr = cache.view(torch.int32)
+    mid, last, bad = packed_rows[packed_rows % 32 == 5][0], packed_rows[packed_rows % 32 == 31][0], \
+        packed_rows[packed_rows % 32 == 12][0]
+    for r, value in ((mid, 0b1011), (last, 0b0111), (bad, 0)):
+        w = int(base[r]) // 4
+        hdr[w] = (int(hdr[w].item()) & ~0xF) | value
+    o, s = both(base)
+    assert s == ibp.IBP_ECORRUPT
+    assert not o[bad].any()
+    keep = np.ones(n, bool)
+    keep[[mid, last, bad]] = False
+    assert np.array_equal(o[keep], b[keep])
