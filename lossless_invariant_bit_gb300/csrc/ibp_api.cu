@@ -649,12 +649,14 @@ ibp_status ibp_group_gather_decompress_ordered(const ibp_group* g, void* dst,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // workspace: the item order (8 bytes per item), each item's cost prefix
   // within its bucket (4 per item), the warp shares (at most n/32 + 9 words),
-  // then the bucket counters and the bucket costs (4 KB each)
+  // then the bucket counters and the bucket costs (4 bytes per bucket each)
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int64_t* order = reinterpret_cast<int64_t*>(ws);
   uint32_t* wpre = reinterpret_cast<uint32_t*>(ws + 8ull * n_items);
   uint32_t* shares = reinterpret_cast<uint32_t*>(ws + 12ull * n_items);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + IBP_ORDER_WORKSPACE_BYTES(n_items) - 8192ull);
+  static_assert(8ull * ibp::kOrderBuckets <= 32768ull, "bucket arrays in the workspace's tail");
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + IBP_ORDER_WORKSPACE_BYTES(n_items) -
+                                               8ull * ibp::kOrderBuckets);
   uint32_t* cost = hist + ibp::kOrderBuckets;
   ibp_status e = cu(cudaMemsetAsync(hist, 0, 4ull * ibp::kOrderBuckets, st));
   if (e != IBP_OK) return e;

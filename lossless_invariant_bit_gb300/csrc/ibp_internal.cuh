@@ -235,7 +235,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const HostProps& hp, int sm_count
 // Bucket the ids by address region (a counting sort on id * kOrderBuckets /
 // n_rows): ids_out, in bucket order, and pos_out, each id's index in ids.
 // hist: kOrderBuckets zeroed counters.
-constexpr uint32_t kOrderBuckets = 1024;
+#ifndef IBP_ORDER_BUCKETS
+#define IBP_ORDER_BUCKETS 1024u
+#endif
+constexpr uint32_t kOrderBuckets = IBP_ORDER_BUCKETS;
 cudaError_t launch_order_ids(const int64_t* ids, uint64_t n, uint64_t n_rows, int64_t* ids_out,
                              int64_t* pos_out, uint32_t* hist, int sm_count, cudaStream_t st);
 // The same for a group's items (b, t): bucket t * (kOrderBuckets / T) plus the

@@ -2372,22 +2372,35 @@ __global__ void __launch_bounds__(256) k_order_count(const int64_t* ids, uint64_
 }
 
 // counts -> exclusive starts, in place (one block of kOrderBuckets threads)
+// (1024 threads, kOrderBuckets / 1024 consecutive counters each)
 __global__ void __launch_bounds__(1024) k_order_scan(uint32_t* hist) {
-  __shared__ uint32_t part[kOrderBuckets];
+  constexpr uint32_t kPer = kOrderBuckets / 1024u;
+  static_assert(kPer * 1024u == kOrderBuckets, "whole counters per thread");
+  __shared__ uint32_t part[1024];
   // behind the count (programmatic dependent launch)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t t = threadIdx.x;
-  const uint32_t v = hist[t];
+  uint32_t c[kPer], v = 0;
+#pragma unroll
+  for (uint32_t q = 0; q < kPer; ++q) {
+    c[q] = hist[kPer * t + q];
+    v += c[q];
+  }
   part[t] = v;
   __syncthreads();
-  for (uint32_t d = 1; d < kOrderBuckets; d <<= 1) {
+  for (uint32_t d = 1; d < 1024u; d <<= 1) {
     const uint32_t x = t >= d ? part[t - d] : 0u;
     __syncthreads();
     part[t] += x;
     __syncthreads();
   }
-  hist[t] = part[t] - v;
+  uint32_t run = part[t] - v;
+#pragma unroll
+  for (uint32_t q = 0; q < kPer; ++q) {
+    hist[kPer * t + q] = run;
+    run += c[q];
+  }
 }
 
 // One id per thread (the grid covers the n ids): a rank among the CTA's ids
@@ -2451,7 +2464,7 @@ cudaError_t launch_order_ids(const int64_t* ids, uint64_t n, uint64_t n_rows, in
   uint64_t blocks = (uint64_t)sm_count * 4;
   if (blocks > need) blocks = need;
   k_order_count<<<(uint32_t)blocks, 256, 0, st>>>(ids, n, n_rows, hist);
-  cudaError_t e = launch_behind(k_order_scan, 1u, kOrderBuckets, 0, st, hist);
+  cudaError_t e = launch_behind(k_order_scan, 1u, 1024u, 0, st, hist);
   if (e != cudaSuccess) return e;
   return launch_behind(k_order_scatter, (uint32_t)need, 256u, 0, st, ids, n, n_rows, hist,
                        ids_out, pos_out);
@@ -2671,7 +2684,8 @@ __global__ void __launch_bounds__(256) k_order_items_group(const int64_t* ids,
   if (tid == 0) cost[b] = total;
 }
 
-static_assert(kOrderBuckets == 4u * 256u, "k_order_shares scans 4 bucket costs per thread");
+constexpr uint32_t kSharePer = kOrderBuckets / 256u;  // bucket costs per thread
+static_assert(kSharePer * 256u == kOrderBuckets, "k_order_shares: whole buckets per thread");
 
 // Warp shares of the grouped list with equal costs: share w starts at the
 // item whose cost interval holds floor(w * total / nw); shares[nw] = n.  A
@@ -2684,11 +2698,11 @@ __global__ void __launch_bounds__(256) k_order_shares(const uint32_t* ends, cons
   __shared__ unsigned long long wsum[8];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // behind the grouping kernel
   const uint32_t tid = threadIdx.x, lane = tid & 31u, wid = tid >> 5;
-  // bucket costs, 4 per thread, and their exclusive scan
-  unsigned long long c[4], sum = 0;
+  // bucket costs, kSharePer per thread, and their exclusive scan
+  unsigned long long c[kSharePer], sum = 0;
 #pragma unroll
-  for (uint32_t q = 0; q < 4u; ++q) {
-    const uint32_t bk = 4u * tid + q;
+  for (uint32_t q = 0; q < kSharePer; ++q) {
+    const uint32_t bk = kSharePer * tid + q;
     const uint32_t nb = ends[bk] - (bk ? ends[bk - 1u] : 0u);
     c[q] = nb > kGroupCap ? (unsigned long long)kFetchWeight * nb : (unsigned long long)cost[bk];
     sum += c[q];
@@ -2708,8 +2722,8 @@ __global__ void __launch_bounds__(256) k_order_shares(const uint32_t* ends, cons
   }
   run += incl - sum;
 #pragma unroll
-  for (uint32_t q = 0; q < 4u; ++q) {
-    pre[4u * tid + q] = run;
+  for (uint32_t q = 0; q < kSharePer; ++q) {
+    pre[kSharePer * tid + q] = run;
     run += c[q];
   }
   __syncthreads();
@@ -2759,7 +2773,7 @@ cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int6
   uint64_t blocks = (uint64_t)sm_count * 4;
   if (blocks > need) blocks = need;
   k_order_items_count<<<(uint32_t)blocks, 256, 0, st>>>(entries, T, ids, n_items, hist);
-  cudaError_t e = launch_behind(k_order_scan, 1u, kOrderBuckets, 0, st, hist);
+  cudaError_t e = launch_behind(k_order_scan, 1u, 1024u, 0, st, hist);
   if (e != cudaSuccess) return e;
   const uint64_t sblocks = need;
   return launch_behind(k_order_items_scatter, (uint32_t)sblocks, 256u, 0, st, entries, T, ids,
