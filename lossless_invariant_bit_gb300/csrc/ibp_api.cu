@@ -74,6 +74,20 @@ bool source_is_host(const ibp_store* s, const void* src, cudaStream_t st) {
 
 inline ibp_status cu(cudaError_t e) { return e == cudaSuccess ? IBP_OK : IBP_ECUDA; }
 
+// Test hook of the bounded waits (read once): IBP_DEBUG_WITHHOLD_TILE=k makes
+// the tile decoder's producer withhold tile k, so the warps waiting for it give
+// up after ~2 s and the call reports IBP_ETIMEOUT.  Unset: no tile withheld.
+uint64_t withheld_tile() {
+  static const uint64_t tile = [] {
+    const char* v = std::getenv("IBP_DEBUG_WITHHOLD_TILE");
+    if (!v || !*v) return ~0ull;
+    char* end = nullptr;
+    const unsigned long long t = std::strtoull(v, &end, 10);
+    return (end && *end == '\0') ? (uint64_t)t : ~0ull;
+  }();
+  return tile;
+}
+
 // Calls on a store run on the device it was created on.
 ibp_status on_device(const ibp_store* s) {
   int d = -1;
@@ -188,6 +202,7 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   a.out_pos = out_pos;
   a.lengths = s->lengths;
   a.host_src = source_is_host(s, src, st) ? 1u : 0u;
+  a.withhold_tile = withheld_tile();
   return cu(ibp::launch_decode(a, host_props(s, st), s->sm_count, st));
 }
 

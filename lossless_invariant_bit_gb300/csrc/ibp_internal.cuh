@@ -66,6 +66,9 @@ struct DecodeArgs {
   // the whole stream, so rows with raw chunks need no second round trip
   const uint32_t* lengths;
   uint32_t host_src;  // src is pinned host memory (sets the launch shape only)
+  // test hook of the bounded waits: the tile decoder's producer never
+  // releases this tile (~0: none; IBP_DEBUG_WITHHOLD_TILE in the environment)
+  uint64_t withhold_tile;
 };
 
 struct EncodeArgs {

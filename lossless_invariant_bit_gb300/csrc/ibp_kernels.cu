@@ -1223,6 +1223,7 @@ __global__ void __launch_bounds__(32 * (kTileWarps + 1), 3) k_decode_tiles(Decod
         ti.ok = ok ? 1u : 0u;
       }
       __syncwarp();
+      if (t0 + k == a.withhold_tile) continue;  // test hook: this tile is never released
       if (lane == 0) {
         const uint32_t fb = static_cast<uint32_t>(__cvta_generic_to_shared(full + s));
         const uint32_t bytes = ok ? (uint32_t)(end - base) : 0u;

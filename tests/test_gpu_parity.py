@@ -839,3 +839,54 @@ def test_packed_cache_tiles_match_the_row_gather(stores):
     keep = np.ones(n, bool)
     keep[[mid, last, bad]] = False
     assert np.array_equal(o[keep], b[keep])
+
+
+_WITHHELD_CHILD = r"""
+import numpy as np, torch
+from lossless_invariant_bit_gb300 import ibp
+from lossless_invariant_bit_gb300 import workloads as wl
+dev = torch.device("cuda:0")
+rows, _ = wl.tiny_rows(seed=3, n_rows=4096)
+b = rows.view(np.uint8).reshape(len(rows), -1)
+n, R, C = len(b), 1024, 256
+st = ibp.ibp_store_create(R, C, n, 0)
+d = torch.from_numpy(b).to(dev)
+ibp.ibp_build_meta(st, d, R, None, n, 95, 100)
+info = ibp.ibp_store_get_info(st)
+slots = torch.zeros((n, info.slot_bytes), dtype=torch.uint8, device=dev)
+stored = torch.zeros(n, dtype=torch.int32, device=dev)
+ibp.ibp_compress(st, slots, d, R, None, n, stored)
+offs = torch.zeros(n + 1, dtype=torch.int64, device=dev)
+ibp.ibp_pack(st, None, offs, slots, stored, n)
+cache = torch.zeros(int(offs[-1].item()) + R, dtype=torch.uint8, device=dev)
+ibp.ibp_pack(st, cache, offs, slots, stored, n)
+torch.cuda.synchronize()
+assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+out = torch.zeros((n, R), dtype=torch.uint8, device=dev)
+ibp.ibp_decompress(st, out, cache, offs, n)          # tile 5 is never released
+torch.cuda.synchronize()
+print("status", ibp.ibp_stream_status(st, reset=True))
+ids = torch.arange(n, dtype=torch.int64, device=dev)  # the ring decoder: no tiles
+ibp.ibp_gather_decompress(st, out, cache, offs, ids, n)
+torch.cuda.synchronize()
+print("after", ibp.ibp_stream_status(st, reset=True), bool(np.array_equal(out.cpu().numpy(), b)))
+"""
+
+
+def test_tile_decoder_wait_gives_up_and_the_context_stays_usable():
+    """The tile decoder's waits are bounded.  A test hook
+    (IBP_DEBUG_WITHHOLD_TILE, read once per process) makes the producer never
+    release one tile: the warps waiting for it give up after ~2 s, the call
+    reports IBP_ETIMEOUT, and the next call in the same process decodes every
+    row.  Run in a child process so the hook touches no other test."""
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, IBP_DEBUG_WITHHOLD_TILE="5")
+    r = subprocess.run([sys.executable, "-c", _WITHHELD_CHILD], env=env, capture_output=True,
+                       text=True, timeout=600,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = dict(l.split(" ", 1) for l in r.stdout.strip().splitlines() if " " in l)
+    assert int(lines["status"]) == ibp.IBP_ETIMEOUT
+    assert lines["after"] == "%d True" % ibp.IBP_OK
