@@ -271,7 +271,7 @@ IBP_API ibp_status ibp_group_gather_decompress(const ibp_group* group, void* dst
  * ibp_gather_decompress_ordered): the batch*T items are bucketed by store
  * and by region within it, each bucket of up to 2048 items is sorted by row
  * id, and the list is decoded in contiguous shares of equal cost (a lookup
- * that fetches a row counts as eight that repeat the row before it), each
+ * that fetches a row counts as four that repeat the row before it), each
  * item to its own place in dst.  Repeated lookups of a row (Zipf batches)
  * next to each other are fetched and decoded once: the repeats are stored
  * from the decoded copy.  For groups whose slots together exceed the GPU's
