@@ -3127,11 +3127,10 @@ cudaError_t launch_group_ordered(GroupArgs g, const uint32_t* hist, uint32_t* wp
                                  cudaStream_t st) {
   if (g.n_items == 0) return cudaSuccess;
   if (g.n_items > 0xFFFFFFFFull) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(k_order_items_group,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kGroupSmem);
-  if (e != cudaSuccess) return e;
-  e = launch_behind(k_order_items_group, kOrderBuckets, 256u, kGroupSmem, st, g.ids, hist,
+  // sets the kernel's shared-memory limit once (cached), so the call stays
+  // capturable in a CUDA graph
+  blocks_per_sm(k_order_items_group, 256, kGroupSmem);
+  cudaError_t e = launch_behind(k_order_items_group, kOrderBuckets, 256u, kGroupSmem, st, g.ids, hist,
                     const_cast<int64_t*>(g.order), wpre, cost);
   if (e != cudaSuccess) return e;
   const int warps = 8;

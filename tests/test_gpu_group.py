@@ -364,3 +364,69 @@ def test_group_ordered_one_and_most_tables(T):
     finally:
         for s in stores:
             s.close()
+
+
+def test_ordered_group_and_packed_decode_in_a_cuda_graph():
+    """The ordered group gather (five kernels chained by programmatic
+    dependent launch, then the gather) and the packed-cache decode (bulk
+    copies on mbarriers) captured once in a CUDA graph and replayed with new
+    lookups: every replay returns the rows."""
+    R, C, N, B, T = 512, 1024, 3000, 700, 3
+    stores, slots, tables = [], [], []
+    try:
+        for t in range(T):
+            rb = rows_u8(wl.dlrm_rows(N, R // 4, table=t, seed=31))
+            st, sl = _host_store(R, C, rb, host=(t != 1))
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+        # a packed HBM cache of store 0
+        st0 = stores[0]
+        stored = torch.zeros(N, dtype=torch.int32, device=DEV)
+        d0 = torch.from_numpy(tables[0]).to(DEV)
+        s0 = torch.zeros((N, st0.slot), dtype=torch.uint8, device=DEV)
+        ibp.ibp_compress(st0.h, s0, d0, R, None, N, stored)
+        offs = torch.zeros(N + 1, dtype=torch.int64, device=DEV)
+        ibp.ibp_pack(st0.h, None, offs, s0, stored, N)
+        cache = torch.zeros(int(offs[-1].item()) + R, dtype=torch.uint8, device=DEV)
+        ibp.ibp_pack(st0.h, cache, offs, s0, stored, N)
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            ids = torch.zeros((B, T), dtype=torch.int64, device=DEV)
+            out = torch.zeros((B, T, R), dtype=torch.uint8, device=DEV)
+            ws = torch.empty(ibp.order_workspace_bytes(B * T), dtype=torch.uint8, device=DEV)
+            dec = torch.zeros((N, R), dtype=torch.uint8, device=DEV)
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):  # warm-up: launch shapes and store properties known
+                ibp.ibp_group_gather_decompress_ordered(grp, out, T * R, ids, B, ws, ws.numel(),
+                                                        side)
+                ibp.ibp_decompress(st0.h, dec, cache, offs, N, side)
+            torch.cuda.synchronize()
+            for s in stores:
+                assert s.status() == ibp.IBP_OK
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                sp = torch.cuda.current_stream()
+                ibp.ibp_group_gather_decompress_ordered(grp, out, T * R, ids, B, ws, ws.numel(),
+                                                        sp)
+                ibp.ibp_decompress(st0.h, dec, cache, offs, N, sp)
+            for step in range(3):
+                z = np.stack([wl.zipf_ids(B, N, table=t, seed=40 + step) for t in range(T)],
+                             axis=1)
+                ids.copy_(torch.from_numpy(z))
+                out.zero_()
+                dec.zero_()
+                g.replay()
+                torch.cuda.synchronize()
+                for s in stores:
+                    assert s.status() == ibp.IBP_OK, step
+                o = out.cpu().numpy()
+                for t in range(T):
+                    assert np.array_equal(o[:, t], tables[t][z[:, t]]), (step, t)
+                assert np.array_equal(dec.cpu().numpy(), tables[0]), step
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()
