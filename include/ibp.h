@@ -401,7 +401,11 @@ IBP_API ibp_status ibp_pack(const ibp_store* store, void* dst_packed, uint64_t* 
  * dtype, k_dim, workspace, m above 65535 * 128), IBP_EALIGN, IBP_ERANGE,
  * IBP_ECUDA; a slot id out of range sets IBP_ERANGE in the status word (that
  * row's slot is not written), and a device wait that gave up sets
- * IBP_ETIMEOUT. */
+ * IBP_ETIMEOUT.
+ * The call may be captured into a CUDA graph after one uncaptured call of the
+ * same shape on the device (it sets the kernels' shared-memory limits once);
+ * a replay reads x, w, bias and the store's tables at the addresses given at
+ * capture. */
 IBP_API ibp_status ibp_project_compress(ibp_store* store, const void* x, uint64_t m,
                                         uint64_t k_dim, const void* w, const void* bias,
                                         uint32_t dtype, void* y, void* dst_slots,

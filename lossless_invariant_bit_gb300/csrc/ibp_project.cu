@@ -567,6 +567,34 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k, uin
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Raise a kernel's dynamic shared-memory limit to `smem` once per device (a
+// call being captured into a CUDA graph then sets nothing).
+cudaError_t smem_limit(const void* fn, size_t smem) {
+  struct Seen {
+    const void* fn;
+    int dev;
+    size_t smem;
+  };
+  static std::mutex mu;
+  static Seen seen[64];
+  static int n_seen = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_seen; ++i)
+    if (seen[i].fn == fn && seen[i].dev == dev && seen[i].smem >= smem) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n_seen; ++i)
+    if (seen[i].fn == fn && seen[i].dev == dev) {
+      seen[i].smem = smem;
+      return cudaSuccess;
+    }
+  if (n_seen < 64) seen[n_seen++] = Seen{fn, dev, smem};
+  return cudaSuccess;
+}
+
 template <int kSeg, int kAR>
 cudaError_t launch_shape(const ProjectArgs& a, const void* x, const void* w, cudaStream_t st) {
   using P = PjShape<kSeg, kAR>;
@@ -575,8 +603,7 @@ cudaError_t launch_shape(const ProjectArgs& a, const void* x, const void* w, cud
       !make_map(&mw, w, (uint64_t)a.nch * 128u, a.k_dim, P::BN, P::KB, a.bf16))
     return cudaErrorInvalidValue;
   auto kern = k_project_compress<kSeg, kAR>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)P::SMEM);
+  cudaError_t e = smem_limit(reinterpret_cast<const void*>(kern), P::SMEM);
   if (e != cudaSuccess) return e;
   const uint64_t mtiles = (a.m + kPjBM - 1) / kPjBM;
   kern<<<dim3(a.nch * kSeg, (uint32_t)mtiles), 128, P::SMEM, st>>>(mx, mw, a);
@@ -589,7 +616,7 @@ cudaError_t launch_shape(const ProjectArgs& a, const void* x, const void* w, cud
   const size_t smem = 4ull * (2ull * a.W + 8ull + 2ull * ntiles + ((a.nch + 3u) & ~3u));
   auto asmk = k_project_assemble;
   if (smem > 48u * 1024u) {
-    e = cudaFuncSetAttribute(asmk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = smem_limit(reinterpret_cast<const void*>(asmk), smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};

@@ -181,3 +181,54 @@ def test_project_compress_rejects_bad_geometry():
         assert e.value.status == ibp.IBP_EINVAL
     finally:
         st.close()
+
+
+def test_project_compress_captured_in_a_cuda_graph():
+    """A decode step's projection captured once in a CUDA graph (the two
+    kernels, the second launched behind the first) and replayed with new
+    inputs: every replay writes the bytes an uncaptured call writes for the
+    same inputs (Y, stored bytes, sizes, raw bits)."""
+    m, K, N, R = 20, 4096, 4096, 8192
+    dtype = torch.float16
+    w, b = _weights(N, K, dtype, seed=77)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(78)
+    xp = torch.randn((512, K), generator=g, device=DEV).to(dtype)
+    yp = (xp.float() @ w.float().T + b.float()).to(dtype).contiguous()
+    n_rows = 64
+    st = Store(R, 256, n_rows, R)
+    try:
+        ibp.ibp_build_meta(st.h, yp.view(torch.uint8), R, None, 512, 95, 100)
+        x = torch.zeros((m, K), dtype=dtype, device=DEV)
+        y = torch.empty((m, N), dtype=dtype, device=DEV)
+        slots = torch.zeros((n_rows, R), dtype=torch.uint8, device=DEV)
+        stored = torch.zeros(m, dtype=torch.int32, device=DEV)
+        wsb = ibp.project_workspace_bytes(m, R)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # warm-up: kernel limits set, store properties known
+            ibp.ibp_project_compress(st.h, x, m, K, w, b, 0, y, slots, None, stored, ws, wsb, side)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            ibp.ibp_project_compress(st.h, x, m, K, w, b, 0, y, slots, None, stored, ws, wsb,
+                                     torch.cuda.current_stream())
+        for step in range(3):
+            xs = torch.randn((m, K), generator=g, device=DEV).to(dtype)
+            x.copy_(xs)
+            slots.zero_()
+            gr.replay()
+            torch.cuda.synchronize()
+            assert st.status() == ibp.IBP_OK
+            got = (y.clone(), slots[:m].clone(), stored.clone(), st.bitmap().copy())
+            slots.zero_()
+            ibp.ibp_project_compress(st.h, xs, m, K, w, b, 0, y, slots, None, stored, ws, wsb)
+            torch.cuda.synchronize()
+            assert st.status() == ibp.IBP_OK
+            assert torch.equal(got[0], y), step
+            assert torch.equal(got[1], slots[:m]), step
+            assert torch.equal(got[2], stored), step
+            assert np.array_equal(got[3], st.bitmap()), step
+    finally:
+        st.close()
