@@ -1007,13 +1007,14 @@ __global__ void __launch_bounds__(256, IBP_FAST_MIN_BLOCKS(kMode)) k_decode_fast
 // ahead of kTileWarps decoding warps.  A row whose bytes are not all in the
 // stage -- the call's last row (its end is not known), a stream longer than
 // the bytes up to the next row's start, every row of a tile whose offsets are
-// out of order or not 16-byte aligned -- is read by its warp from global
-// memory, within its own stream as the other decoders read it; the output and
-// status codes are those of k_decode_fast.
+// out of order, not 16-byte aligned, more than R bytes apart, or span more
+// than a stage's 16 KB -- is read by its warp from global memory, within its
+// own stream as the other decoders read it; the output and status codes are
+// those of k_decode_fast.
 // ------------------------------------------------------------------------
 constexpr uint32_t kTileRows = 32;
 constexpr uint32_t kTileStages = 3;  // measured: 2 or 4 stages slower
-constexpr uint32_t kTileWarps = 8;  // decoding warps; one more produces
+constexpr uint32_t kTileWarps = 8;  // decoding warps (one more produces); 12 or 16 measured slower
 
 struct TileInfo {
   uint64_t off[kTileRows + 1];  // the rows' starts, then the end of the stage's bytes
