@@ -1461,7 +1461,7 @@ def run_dlrm(args, rank, world, torch, dist):
         "config": {"workload": "DLRM lookup: 26 tables x %d rows x dim %d fp32 in pinned host "
                                "slots, chunk 1 KB, 1%% sample, T=0.95; batch 8192 Zipf(1.05) ids "
                                "per table -> [8192, 26, %d], ordered fused gather" % (N, dim, dim),
-                   "row_bytes": R, "launches_per_step": 4,
+                   "row_bytes": R, "launches_per_step": 6,
                    "length_tables": "each table's stored sizes attached (one fetch per row)",
                    "l2": "flushed between steps (256 MB write, outside the timed events)"},
         "ratio": round(ratio, 5), "ratio_distinct_rows": round(ratio_unique, 5),
@@ -1482,8 +1482,9 @@ def run_dlrm(args, rank, world, torch, dist):
                      "peak_is": "min(HBM, link / stored bytes of the batch's distinct rows per "
                                 "delivered byte): repeats of a row can come from the GPU's caches",
                      "kernel": "k_gather_group, ordered (ibp_group_gather_decompress_ordered: "
-                               "three bucketing kernels and the gather)"},
-        "gpu_launches": 4 * args.steps,
+                               "three bucketing kernels, the grouping and share kernels, "
+                               "and the gather)"},
+        "gpu_launches": 6 * args.steps,
         "clocks": clk_o.summary(),
         "cpu_baseline": {
             "value": round(len(legs) * 1024 * R / sum(len(pick) * R / (l["value"] * 1e9)
