@@ -677,15 +677,21 @@ __device__ __forceinline__ uint4 decode_packed_group(const uint4* tab, const uin
                                                      uint32_t g, uint32_t G, uint32_t nch,
                                                      uint32_t delta, bool net5, bool uni,
                                                      const FastParams& F, const uint32_t* up) {
-  if (kMode == kModeUniform1) {  // one run: a shift and a mask per word
-    uint32_t bit = nch + 4u * g * F.ukeep + delta;
+  if (kMode == kModeUniform1) {  // one run: a funnel shift and a mask per word
+    // The window starts ush bits before the word's kept bits, so they land at
+    // the run's place [ush, ush + ukeep) without a second shift.  For a
+    // stream's first word (bit < ush) the window takes its low word from the
+    // shared-memory word before the stream: every stream buffer has other
+    // shared memory in front of it, and those bits fall below ush, outside
+    // the mask.
+    int bit = (int)(nch + 4u * g * F.ukeep + delta) - (int)(F.ush & 31u);
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t q = bit >> 5;
-      const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], bit);
-      o[e] = ((x << (F.ush & 31u)) & F.um0) | F.ubv;
-      bit += F.ukeep;
+      const int q = bit >> 5;  // -1 at the least
+      const uint32_t x = __funnelshift_r(sb[q], sb[q + 1], (uint32_t)bit);
+      o[e] = (x & F.um0) | F.ubv;
+      bit += (int)F.ukeep;
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
   }
@@ -2373,11 +2379,10 @@ __global__ void __launch_bounds__(256) k_order_count(const int64_t* ids, uint64_
     if (h[b]) atomicAdd(hist + b, h[b]);
 }
 
-// counts -> exclusive starts, in place (one block of kOrderBuckets threads)
-// (1024 threads, kOrderBuckets / 1024 consecutive counters each)
+// counts -> exclusive starts, in place: one block of 1024 threads,
+// ceil(kOrderBuckets / 1024) consecutive counters each
 __global__ void __launch_bounds__(1024) k_order_scan(uint32_t* hist) {
-  constexpr uint32_t kPer = kOrderBuckets / 1024u;
-  static_assert(kPer * 1024u == kOrderBuckets, "whole counters per thread");
+  constexpr uint32_t kPer = (kOrderBuckets + 1023u) / 1024u;
   __shared__ uint32_t part[1024];
   // behind the count (programmatic dependent launch)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -2386,7 +2391,7 @@ __global__ void __launch_bounds__(1024) k_order_scan(uint32_t* hist) {
   uint32_t c[kPer], v = 0;
 #pragma unroll
   for (uint32_t q = 0; q < kPer; ++q) {
-    c[q] = hist[kPer * t + q];
+    c[q] = kPer * t + q < kOrderBuckets ? hist[kPer * t + q] : 0u;
     v += c[q];
   }
   part[t] = v;
@@ -2400,7 +2405,7 @@ __global__ void __launch_bounds__(1024) k_order_scan(uint32_t* hist) {
   uint32_t run = part[t] - v;
 #pragma unroll
   for (uint32_t q = 0; q < kPer; ++q) {
-    hist[kPer * t + q] = run;
+    if (kPer * t + q < kOrderBuckets) hist[kPer * t + q] = run;
     run += c[q];
   }
 }
