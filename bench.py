@@ -651,7 +651,7 @@ def run_tiny(args, rank, world, torch, dist):
                      "frac": round(moved / hbm, 4),
                      # dram read + write of a 48-replica launch (profiles/
                      # k_decode_tiles_tiny_cache.md) scaled to this launch's rows
-                     "traffic": round(210.52e6 * n / (48 * 4096)),
+                     "traffic": round(210.11e6 * n / (48 * 4096)),
                      "traffic_is": "dram__bytes_read.sum + dram__bytes_write.sum from ncu, "
                                    "scaled from a 196,608-row capture (part of the output is "
                                    "still in L2 when the kernel ends)",
