@@ -264,7 +264,7 @@ def test_group_ordered_repeats_large_buckets_and_errors():
     """The ordered group gather over heavy repeats: every item equals the plain
     group gather's (bytes and status codes) and the rows.  Store 0 (dense,
     uniform, host) has one row whose stream is corrupt, looked up 2600 times:
-    its bucket is above the 2048 items sorted in shared memory and stays in
+    its bucket is above the 2048 items grouped in shared memory and stays in
     scatter order, and the repeats of a corrupt row are zero-filled like the
     row.  Store 1 (network mode, host) has a hot row whose repeats span warp
     shares; store 2 (two-run mode, HBM) has out-of-range ids repeated next to
@@ -323,6 +323,44 @@ def test_group_ordered_repeats_large_buckets_and_errors():
                 if b == B:
                     assert codes[0] == ibp.IBP_ECORRUPT and codes[2] == ibp.IBP_ERANGE
                     assert codes[1] == ibp.IBP_OK and codes[3] == ibp.IBP_OK
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()
+
+
+@pytest.mark.parametrize("B", [16384, 20000])
+def test_group_ordered_large_batches(B):
+    """Batches of 16384 and 20000 rows over two stores (one in host memory,
+    one in HBM): Zipf lookups with a row repeated 3000 times, whose bucket
+    holds more items than are grouped in shared memory; the plain group
+    gather's bytes and the rows."""
+    R, C, N, T = 512, 1024, 6000, 2
+    stores, slots, tables = [], [], []
+    try:
+        for t in range(T):
+            rb = rows_u8(wl.dlrm_rows(N, R // 4, table=t, seed=51))
+            st, sl = _host_store(R, C, rb, host=(t == 0))
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+        ids = np.stack([wl.zipf_ids(B, N, table=t, seed=52) for t in range(T)], axis=1)
+        ids[np.random.default_rng(53).choice(B, 3000, replace=False), 1] = 17
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            ref = torch.full((B, T, R), 0xCC, dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress(grp, ref, T * R, to_dev(ids), B)
+            out = torch.full((B, T, R), 0x33, dtype=torch.uint8, device=DEV)
+            ws = torch.empty(ibp.order_workspace_bytes(B * T), dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_gather_decompress_ordered(grp, out, T * R, to_dev(ids), B, ws,
+                                                    ws.numel())
+            for s in stores:
+                assert s.status() == ibp.IBP_OK
+            assert torch.equal(out, ref)
+            o = out.cpu().numpy()
+            for t in range(T):
+                assert np.array_equal(o[:, t], tables[t][ids[:, t]]), t
         finally:
             ibp.ibp_group_destroy(grp)
     finally:
