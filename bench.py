@@ -887,7 +887,12 @@ def run_kv(args, rank, world, torch, dist):
                    "l2": "flushed between steps (256 MB write, outside the timed events)"},
         "ratio": round(ratio, 5), "link_gbs": round(link, 2), "parity_layer0_ok": parity_ok,
         "roofline": {"bound": "link", "achieved": round(value / world, 2), "peak": round(roof, 2),
-                     "unit": "GB/s", "frac": round(value / world / roof, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(value / world / roof, 4),
+                     # host-link read sectors of one (layer, K|V) fetch of 38,400 rows (ncu,
+                     # profiles/k_decode_fast_kv_dense_link.md): every launch reads as many
+                     "traffic": 310.93e6,
+                     "traffic_is": "host-link (sysmem) read bytes of one launch from ncu "
+                                   "(1.002 x its stored bytes)",
                      "kernel": "k_decode_fast<true, mode, big> (ibp_gather_decompress, 8 KB rows)"},
         "gpu_launches": 2 * L * args.steps,
         "clocks": clk.summary(),
@@ -1478,7 +1483,13 @@ def run_dlrm(args, rank, world, torch, dist):
                                  "note": "26 uncompressed ibp_gather_copy calls per batch over "
                                          "the same slot addresses (R bytes per lookup)"},
         "roofline": {"bound": "link", "achieved": round(value / world, 2), "peak": round(roof, 2),
-                     "unit": "GB/s", "frac": round(value / world / roof, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(value / world / roof, 4),
+                     # host-link read sectors of the first timed k_gather_group launch at this
+                     # size (ncu, profiles/k_gather_group_dlrm.md); null at other sizes
+                     "traffic": ({128: 48.39e6, 512: 191.52e6}.get(dim)
+                                 if (N, B, Tn, args.seed) == (1_000_000, 8192, 26, 0) else None),
+                     "traffic_is": "host-link (sysmem) read bytes of one k_gather_group launch "
+                                   "from ncu",
                      "peak_is": "min(HBM, link / stored bytes of the batch's distinct rows per "
                                 "delivered byte): repeats of a row can come from the GPU's caches",
                      "kernel": "k_gather_group, ordered (ibp_group_gather_decompress_ordered: "
@@ -1678,7 +1689,13 @@ def run_dense(args, rank, world, torch, dist):
                    "l2": "flushed between steps (256 MB write, outside the timed events)"},
         "link_gbs": round(link, 2), "raw_gather_gbs": round(raw_gbs, 2),
         "roofline": {"bound": "link", "achieved": head["gbs"], "peak": head["roofline_peak"],
-                     "unit": "GB/s", "frac": head["frac"], "traffic": None,
+                     "unit": "GB/s", "frac": head["frac"],
+                     # host-link read sectors of a 1 KB-chunk launch (ncu, 138,395 ids of a
+                     # 400,000-row store: 15.03 sectors per id, profiles/
+                     # k_decode_fast_kv_dense_link.md) scaled to this run's mean batch
+                     "traffic": round(2080214 * 32 / 138395 * n_avg),
+                     "traffic_is": "host-link (sysmem) read bytes per launch from ncu, scaled "
+                                   "by the ids of a batch",
                      "kernel": "k_decode_fast<true, mode, small> (ibp_gather_decompress)"},
         "chunks": points,
         "packed_host_store": packed_point,
