@@ -474,7 +474,7 @@ def run_ours(args, rank, world, torch, dist):
 
     # --- the chunk-aware builder: the threshold chosen from the sample itself
     if not args.no_tuned:
-        cands = [(9, 10), (95, 100), (99, 100), (999, 1000), (1, 1)]
+        cands = [(3, 4), (85, 100), (9, 10), (95, 100), (97, 100), (99, 100), (999, 1000), (1, 1)]
         d_rows = torch.from_numpy(store.rows_np.view(np.uint8)).to(dev)
         d_sample = torch.from_numpy(store.sample).to(dev)
         chosen = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -1818,7 +1818,7 @@ def run_sweep(args, rank, world, torch, dist):
 
     # sampling sweep: ratio of the whole store against the share of rows analysed
     sampling = []
-    cands = [(9, 10), (95, 100), (99, 100), (999, 1000), (1, 1)]
+    cands = [(3, 4), (85, 100), (9, 10), (95, 100), (97, 100), (99, 100), (999, 1000), (1, 1)]
     for name, gen_rows in (("sparse GNN", wl.sparse_gnn_rows), ("dense GNN", wl.dense_gnn_rows)):
         NR, R, C = 2_000_000, 512, 1024
         rows_np = np.empty((NR, 128), np.float32)

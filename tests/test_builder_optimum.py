@@ -33,7 +33,11 @@ import pytest
 from oracle import ref_c
 
 N_ROWS = 48
-CANDIDATES = [(9, 10), (95, 100), (99, 100), (999, 1000), (1, 1)]
+# the chunk-aware builder's default candidates (it prices up to eight): over 30
+# seeds per geometry they reach the optimum in 94 of 120 cases, against 74 for
+# the five thresholds 0.9, 0.95, 0.99, 0.999, 1
+CANDIDATES = [(3, 4), (85, 100), (9, 10), (95, 100), (97, 100), (99, 100), (999, 1000), (1, 1)]
+T095 = CANDIDATES.index((95, 100))
 GEOMETRIES = [(4, 4, 20), (4, 8, 24), (4, 16, 60), (8, 32, 90)]  # (W words, C bytes, noise bits)
 
 
@@ -131,7 +135,7 @@ def test_threshold_masks_bounded_by_brute_force(seed, W, C, noise):
     assert np.array_equal(out, r["rows"].view(np.uint8).reshape(n, R))
     print(f"seed {seed} W {W} C {C}: optimum {r['opt']} B, best grid threshold "
           f"{min(v[0] for v in r['grid'].values())} B, candidates {min(r['cands'])} B, "
-          f"T=0.95 {r['cands'][1]} B, raw {r['raw']} B")
+          f"T=0.95 {r['cands'][T095]} B, raw {r['raw']} B")
 
 
 def _report(n_seeds):
@@ -141,7 +145,7 @@ def _report(n_seeds):
         gaps = [[], [], []]
         for seed in range(n_seeds):
             r = measure(seed, W, C, noise)
-            sizes = [min(v[0] for v in r["grid"].values()), min(r["cands"]), r["cands"][1]]
+            sizes = [min(v[0] for v in r["grid"].values()), min(r["cands"]), r["cands"][T095]]
             for j, s in enumerate(sizes):
                 hit[j] += s == r["opt"]
                 gaps[j].append(s / r["opt"] - 1.0)
