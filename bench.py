@@ -1419,6 +1419,53 @@ def run_dlrm(args, rank, world, torch, dist):
         torch.cuda.synchronize()
     for st in stores:
         assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    # the same ordered gathers with each batch's plan made one step ahead: a
+    # step gathers batch b (planned during the step before) while a second
+    # stream plans batch b + 1; the step ends when both are done, and the plan
+    # starts no earlier than the step (two workspaces in turn)
+    wsb = ibp.order_workspace_bytes(B * Tn)
+    pws = [torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in range(2)]
+    out_p = torch.empty_like(out)
+    ps = torch.cuda.Stream(device=dev)
+    planned = [torch.cuda.Event(), torch.cuda.Event()]
+    gathered = [torch.cuda.Event(), torch.cuda.Event()]
+    ps.wait_stream(stream)
+    ibp.ibp_group_order_plan(grp, ids2d[0], B, pws[0], wsb, ps.cuda_stream)
+    planned[0].record(ps)
+
+    def step_piped(b, start=None):
+        k = b % 2
+        stream.wait_event(planned[k])
+        ibp.ibp_group_gather_decompress_planned(grp, out_p, Tn * R, ids2d[b % pool], B, pws[k],
+                                                wsb, sp)
+        gathered[k].record(stream)
+        if start is not None:
+            ps.wait_event(start)
+        ps.wait_event(gathered[1 - k])  # the previous step's gather read that workspace
+        ibp.ibp_group_order_plan(grp, ids2d[(b + 1) % pool], B, pws[1 - k], wsb, ps.cuda_stream)
+        planned[1 - k].record(ps)
+        stream.wait_event(planned[1 - k])
+
+    for b in range(args.warmup):
+        step_piped(b)
+    torch.cuda.synchronize()
+    pev = []
+    with ClockSampler(dev.index) as clk_p:
+        for b in range(args.warmup, args.warmup + args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step_piped(b, start=e0)
+            e1.record(stream)
+            pev.append((e0, e1))
+        torch.cuda.synchronize()
+    for st in stores:
+        assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    lastp = (args.warmup + args.steps - 1) % pool
+    step_ordered(lastp)
+    torch.cuda.synchronize()
+    piped_same = bool(torch.equal(out_p, out_o))
+    ptimes = [a.elapsed_time(c) / 1e3 for a, c in pev]
     # cpu_baseline leg: the oracle decodes sampled lookups of the last batch in
     # three tables from the same host slots; its rows must equal the GPU's and
     # the tables' rows, and its compression of those rows the stored bytes
@@ -1433,7 +1480,10 @@ def run_dlrm(args, rank, world, torch, dist):
     ibp.ibp_group_destroy(grp)
     otimes = [a.elapsed_time(c) / 1e3 for a, c in oev]
     plain_gbs = B * Tn * R * len(times) / sum(times) / 1e9
-    t_total = ibpdist.max_over_ranks(sum(otimes), dist, dev)
+    ordered_gbs = B * Tn * R * len(otimes) / sum(otimes) / 1e9
+    # the line's value: the pipelined steps (each gathers one batch and plans
+    # the next one)
+    t_total = ibpdist.max_over_ranks(sum(ptimes), dist, dev)
     value = B * Tn * R * args.steps * world / t_total / 1e9
     ratio = statistics.mean(
         sum(float(stored_sum[t][batches[b % pool][:, t]].sum()) for t in range(Tn)) / (B * Tn * R)
@@ -1465,16 +1515,25 @@ def run_dlrm(args, rank, world, torch, dist):
         "data": "synthetic (seeded torch generator on the GPU: N(0, 0.01^2) embedding tables)",
         "config": {"workload": "DLRM lookup: 26 tables x %d rows x dim %d fp32 in pinned host "
                                "slots, chunk 1 KB, 1%% sample, T=0.95; batch 8192 Zipf(1.05) ids "
-                               "per table -> [8192, 26, %d], ordered fused gather" % (N, dim, dim),
+                               "per table -> [8192, 26, %d], ordered fused gather with each "
+                               "batch's plan made one step ahead on a second stream"
+                               % (N, dim, dim),
                    "row_bytes": R, "launches_per_step": 6,
                    "length_tables": "each table's stored sizes attached (one fetch per row)",
                    "l2": "flushed between steps (256 MB write, outside the timed events)"},
         "ratio": round(ratio, 5), "ratio_distinct_rows": round(ratio_unique, 5),
         "link_gbs": round(link, 2),
-        "parity_all_lookups_ok": bool(parity_ok and fused_ok and ordered_same),
+        "parity_all_lookups_ok": bool(parity_ok and fused_ok and ordered_same and piped_same),
         "fused_unordered": {"value": round(plain_gbs, 3), "unit": "GB/s",
                             "frac": round(plain_gbs / roof, 4),
                             "note": "ibp_group_gather_decompress: items in batch order"},
+        "ordered_one_call": {"value": round(ordered_gbs, 3), "unit": "GB/s",
+                             "frac": round(ordered_gbs / roof, 4),
+                             "ms_per_step": round(statistics.mean(otimes) * 1e3, 4),
+                             "clocks": clk_o.summary(), "launches_per_step": 6,
+                             "note": "ibp_group_gather_decompress_ordered: each batch planned "
+                                     "and gathered in one call on one stream"},
+        "pipelined_same_rows_as_one_call": piped_same,
         "per_store_launches": {"value": round(per_store_gbs, 3), "unit": "GB/s",
                                "launches_per_step": Tn,
                                "note": "26 ibp_gather_decompress_strided calls per batch"},
@@ -1492,11 +1551,12 @@ def run_dlrm(args, rank, world, torch, dist):
                                    "from ncu",
                      "peak_is": "min(HBM, link / stored bytes of the batch's distinct rows per "
                                 "delivered byte): repeats of a row can come from the GPU's caches",
-                     "kernel": "k_gather_group, ordered (ibp_group_gather_decompress_ordered: "
-                               "three bucketing kernels, the grouping and share kernels, "
-                               "and the gather)"},
+                     "kernel": "k_gather_group, planned (ibp_group_gather_decompress_planned, "
+                               "leaving each SM room for a grouping CTA; the next batch's plan: "
+                               "three bucketing kernels, the grouping and share kernels, on a "
+                               "second stream)"},
         "gpu_launches": 6 * args.steps,
-        "clocks": clk_o.summary(),
+        "clocks": clk_p.summary(),
         "cpu_baseline": {
             "value": round(len(legs) * 1024 * R / sum(len(pick) * R / (l["value"] * 1e9)
                                                        for l in legs) / 1e9, 4),
@@ -2225,9 +2285,10 @@ def main():
             d = {k_: r[k_] for k_ in keep if k_ in r}
             d["config"] = r["config"]
             for k_ in ("parity_all_lookups_ok", "parity_layer0_ok", "chunks", "fused_unordered",
+                       "ordered_one_call", "pipelined_same_rows_as_one_call",
                        "per_store_launches", "ratio_distinct_rows", "raw_gather_gbs",
                        "attention_layout", "decode_steps", "decode_projection",
-                       "raw_gather_per_table"):
+                       "raw_gather_per_table", "packed_host_store"):
                 if k_ in r:
                     d[k_] = r[k_]
             d["wall_s"] = round(time.time() - t0, 1)

@@ -287,6 +287,35 @@ IBP_API ibp_status ibp_group_gather_decompress_ordered(const ibp_group* group, v
                                                        void* workspace, uint64_t workspace_bytes,
                                                        ibp_stream_t stream);
 
+/* ibp_group_gather_decompress_ordered in two calls, so that a batch's plan
+ * (its bucketing, grouping and warp shares: a chain of short latency-bound
+ * launches) runs ahead, e.g. on a second stream while the previous batch is
+ * gathered (a DLRM loop knows its next batch's ids).  The output equals
+ * ibp_group_gather_decompress_ordered's.
+ *
+ * ibp_group_order_plan writes the plan of ids [batch, T] into workspace
+ * (IBP_ORDER_WORKSPACE_BYTES(batch*T) bytes, 16-byte aligned), including a
+ * stamp of batch*T and the warp shares.  ibp_group_gather_decompress_planned
+ * then gathers ids (the same device array, unchanged since the plan) into dst
+ * as the ordered call would, with as many CTAs per SM as leave room for one
+ * CTA of the plan's grouping kernel, so that another stream's plan runs
+ * beside it.  The caller orders the two calls (same stream,
+ * or an event) and keeps one workspace per batch in flight: a plan must not
+ * overwrite a workspace a gather still reads.  A planned gather whose
+ * workspace holds no plan for batch*T items writes nothing and sets
+ * IBP_EINVAL in the status word of the group's first store; a plan made for
+ * other ids of the same size still gives the right rows, in a worse order.
+ * Errors: as ibp_group_gather_decompress_ordered. */
+IBP_API ibp_status ibp_group_order_plan(const ibp_group* group, const int64_t* ids,
+                                        uint64_t batch, void* workspace,
+                                        uint64_t workspace_bytes, ibp_stream_t stream);
+IBP_API ibp_status ibp_group_gather_decompress_planned(const ibp_group* group, void* dst,
+                                                       uint64_t dst_row_stride,
+                                                       const int64_t* ids, uint64_t batch,
+                                                       const void* workspace,
+                                                       uint64_t workspace_bytes,
+                                                       ibp_stream_t stream);
+
 /* Gather-decompression into a layout that splits each row by chunks (the
  * KV-cache fetch of System Integration, decompressed straight into the
  * attention layout): output row i = g*group_rows + r puts its chunk k (C

@@ -206,6 +206,71 @@ ibp_status decode(const ibp_store* s, void* dst, uint64_t dst_stride, const void
   return cu(ibp::launch_decode(a, host_props(s, st), s->sm_count, st));
 }
 
+
+// The gather arguments of a group call (no order, shares or plan stamp).
+ibp::GroupArgs group_args(const ibp_group* g, const int64_t* ids, uint64_t batch, void* dst,
+                          uint64_t dst_row_stride) {
+  ibp::GroupArgs a;
+  a.entries = g->entries;
+  a.T = g->T;
+  a.R = g->R;
+  a.W = g->W;
+  a.wpc = g->wpc;
+  a.nch = g->nch;
+  a.ids = ids;
+  a.n_items = batch * g->T;
+  a.dst = static_cast<uint8_t*>(dst);
+  a.dst_row_stride = dst_row_stride;
+  a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
+  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u) + g->W;
+  a.order = nullptr;
+  a.shares = nullptr;
+  a.host_src = g->host_src;
+  a.plan_stamp = nullptr;
+  return a;
+}
+
+// The ordered gathers' workspace: the item order (8 bytes per item), each
+// item's cost prefix within its bucket (4 per item), the warp shares (at most
+// n/32 + 9 words), then in the 64 KB tail a plan's stamp (4 words) and the
+// bucket counters and the bucket costs (4 bytes per bucket each) at its end.
+struct OrderWorkspace {
+  int64_t* order;
+  uint32_t* wpre;
+  uint32_t* shares;
+  uint32_t* stamp;
+  uint32_t* hist;
+  uint32_t* cost;
+};
+
+OrderWorkspace order_workspace(void* workspace, uint64_t n_items) {
+  static_assert(8ull * ibp::kOrderBuckets + 16ull <= 32768ull,
+                "bucket arrays and stamp in the workspace's tail");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  OrderWorkspace w;
+  w.order = reinterpret_cast<int64_t*>(ws);
+  w.wpre = reinterpret_cast<uint32_t*>(ws + 8ull * n_items);
+  w.shares = reinterpret_cast<uint32_t*>(ws + 12ull * n_items);
+  w.hist = reinterpret_cast<uint32_t*>(ws + IBP_ORDER_WORKSPACE_BYTES(n_items) -
+                                       8ull * ibp::kOrderBuckets);
+  w.cost = w.hist + ibp::kOrderBuckets;
+  w.stamp = w.hist - 4;
+  return w;
+}
+
+// Arguments of the ordered group calls, checked on the host.
+ibp_status check_ordered(const ibp_group* g, const int64_t* ids, uint64_t n_items,
+                         const void* workspace, uint64_t workspace_bytes) {
+  if (!ids) return IBP_EINVAL;
+  if (n_items > 0xFFFFFFFFull) return IBP_EINVAL;
+  if (!workspace || workspace_bytes < IBP_ORDER_WORKSPACE_BYTES(n_items)) return IBP_EINVAL;
+  if (!aligned16(workspace)) return IBP_EALIGN;
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) return IBP_ECUDA;
+  if (d != g->device) return IBP_EINVAL;
+  return IBP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -626,22 +691,7 @@ ibp_status ibp_group_gather_decompress(const ibp_group* g, void* dst, uint64_t d
   int d = -1;
   if (cudaGetDevice(&d) != cudaSuccess) return IBP_ECUDA;
   if (d != g->device) return IBP_EINVAL;
-  ibp::GroupArgs a;
-  a.entries = g->entries;
-  a.T = g->T;
-  a.R = g->R;
-  a.W = g->W;
-  a.wpc = g->wpc;
-  a.nch = g->nch;
-  a.ids = ids;
-  a.n_items = batch * g->T;
-  a.dst = static_cast<uint8_t*>(dst);
-  a.dst_row_stride = dst_row_stride;
-  a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
-  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u) + g->W;
-  a.order = nullptr;
-  a.shares = nullptr;
-  a.host_src = g->host_src;
+  const ibp::GroupArgs a = group_args(g, ids, batch, dst, dst_row_stride);
   return cu(ibp::launch_group(a, g->sm_count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -655,45 +705,60 @@ ibp_status ibp_group_gather_decompress_ordered(const ibp_group* g, void* dst,
   if (!aligned16(dst) || (dst_row_stride & 15u) || dst_row_stride < (uint64_t)g->T * g->R)
     return IBP_EALIGN;
   const uint64_t n_items = batch * g->T;
-  if (n_items > 0xFFFFFFFFull) return IBP_EINVAL;
-  if (!workspace || workspace_bytes < IBP_ORDER_WORKSPACE_BYTES(n_items)) return IBP_EINVAL;
-  if (!aligned16(workspace)) return IBP_EALIGN;
-  int d = -1;
-  if (cudaGetDevice(&d) != cudaSuccess) return IBP_ECUDA;
-  if (d != g->device) return IBP_EINVAL;
+  ibp_status e = check_ordered(g, ids, n_items, workspace, workspace_bytes);
+  if (e != IBP_OK) return e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // workspace: the item order (8 bytes per item), each item's cost prefix
-  // within its bucket (4 per item), the warp shares (at most n/32 + 9 words),
-  // then the bucket counters and the bucket costs (4 bytes per bucket each)
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int64_t* order = reinterpret_cast<int64_t*>(ws);
-  uint32_t* wpre = reinterpret_cast<uint32_t*>(ws + 8ull * n_items);
-  uint32_t* shares = reinterpret_cast<uint32_t*>(ws + 12ull * n_items);
-  static_assert(8ull * ibp::kOrderBuckets <= 32768ull, "bucket arrays in the workspace's tail");
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + IBP_ORDER_WORKSPACE_BYTES(n_items) -
-                                               8ull * ibp::kOrderBuckets);
-  uint32_t* cost = hist + ibp::kOrderBuckets;
-  ibp_status e = cu(cudaMemsetAsync(hist, 0, 4ull * ibp::kOrderBuckets, st));
+  const OrderWorkspace w = order_workspace(workspace, n_items);
+  e = cu(cudaMemsetAsync(w.hist, 0, 4ull * ibp::kOrderBuckets, st));
   if (e != IBP_OK) return e;
-  e = cu(ibp::launch_order_items(g->entries, g->T, ids, n_items, order, hist, g->sm_count, st));
+  e = cu(ibp::launch_order_items(g->entries, g->T, ids, n_items, w.order, w.hist, g->sm_count,
+                                 st));
   if (e != IBP_OK) return e;
-  ibp::GroupArgs a;
-  a.entries = g->entries;
-  a.T = g->T;
-  a.R = g->R;
-  a.W = g->W;
-  a.wpc = g->wpc;
-  a.nch = g->nch;
-  a.ids = ids;
-  a.n_items = n_items;
-  a.dst = static_cast<uint8_t*>(dst);
-  a.dst_row_stride = dst_row_stride;
-  a.sbuf_words = ((g->W + 8u) + 3u) & ~3u;
-  a.warp_words = 4u * a.sbuf_words + 256u + ((g->nch + 3u) & ~3u) + g->W;
-  a.order = order;
-  a.shares = nullptr;
-  a.host_src = g->host_src;
-  return cu(ibp::launch_group_ordered(a, hist, wpre, cost, shares, g->sm_count, st));
+  ibp::GroupArgs a = group_args(g, ids, batch, dst, dst_row_stride);
+  a.order = w.order;
+  return cu(ibp::launch_group_ordered(a, w.hist, w.wpre, w.cost, w.shares, g->sm_count, st));
+}
+
+ibp_status ibp_group_order_plan(const ibp_group* g, const int64_t* ids, uint64_t batch,
+                                void* workspace, uint64_t workspace_bytes, ibp_stream_t stream) {
+  if (!g) return IBP_EINVAL;
+  if (batch == 0) return IBP_OK;
+  const uint64_t n_items = batch * g->T;
+  ibp_status e = check_ordered(g, ids, n_items, workspace, workspace_bytes);
+  if (e != IBP_OK) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const OrderWorkspace w = order_workspace(workspace, n_items);
+  e = cu(cudaMemsetAsync(w.hist, 0, 4ull * ibp::kOrderBuckets, st));
+  if (e != IBP_OK) return e;
+  e = cu(ibp::launch_order_items(g->entries, g->T, ids, n_items, w.order, w.hist, g->sm_count,
+                                 st));
+  if (e != IBP_OK) return e;
+  ibp::GroupArgs a = group_args(g, ids, batch, nullptr, 0);
+  a.order = w.order;
+  const uint64_t blocks = ibp::group_gather_blocks(a, g->sm_count, ibp::group_planned_per_sm(a));
+  return cu(ibp::launch_group_plan(a, w.hist, w.wpre, w.cost, w.shares, (uint32_t)(8u * blocks),
+                                   w.stamp, st));
+}
+
+ibp_status ibp_group_gather_decompress_planned(const ibp_group* g, void* dst,
+                                               uint64_t dst_row_stride, const int64_t* ids,
+                                               uint64_t batch, const void* workspace,
+                                               uint64_t workspace_bytes, ibp_stream_t stream) {
+  if (!g) return IBP_EINVAL;
+  if (batch == 0) return IBP_OK;
+  if (!dst || !ids) return IBP_EINVAL;
+  if (!aligned16(dst) || (dst_row_stride & 15u) || dst_row_stride < (uint64_t)g->T * g->R)
+    return IBP_EALIGN;
+  const uint64_t n_items = batch * g->T;
+  ibp_status e = check_ordered(g, ids, n_items, workspace, workspace_bytes);
+  if (e != IBP_OK) return e;
+  const OrderWorkspace w = order_workspace(const_cast<void*>(workspace), n_items);
+  ibp::GroupArgs a = group_args(g, ids, batch, dst, dst_row_stride);
+  a.order = w.order;
+  a.shares = w.shares;
+  a.plan_stamp = w.stamp;
+  const uint64_t blocks = ibp::group_gather_blocks(a, g->sm_count, ibp::group_planned_per_sm(a));
+  return cu(ibp::launch_group_gather(a, blocks, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ibp_status ibp_project_compress(ibp_store* s, const void* x, uint64_t m, uint64_t k_dim,

@@ -175,7 +175,12 @@ struct GroupArgs {
   const int64_t* order;     // NULL, or the items in address order (ordered gather)
   const uint32_t* shares;   // NULL, or warp w's items order[shares[w] .. shares[w+1])
   uint32_t host_src;        // some store's slots are pinned host memory (launch shape only)
+  // NULL, or the stamp a plan made ahead left in its workspace: {kPlanMagic,
+  // n_items, shares}; a gather whose stamp differs writes nothing and sets
+  // IBP_EINVAL in store 0's status word
+  const uint32_t* plan_stamp;
 };
+constexpr uint32_t kPlanMagic = 0x49425050u;
 
 // K/V projection with the compressor in its epilogue (ibp_project_compress):
 // Y[m, N] = X[m, k_dim] W[N, k_dim]^T (+ bias), 16-bit in and out, in tiles
@@ -258,6 +263,21 @@ cudaError_t launch_order_items(const GroupEntry* entries, uint32_t T, const int6
 cudaError_t launch_group_ordered(GroupArgs g, const uint32_t* hist, uint32_t* wpre,
                                  uint32_t* cost, uint32_t* shares, int sm_count,
                                  cudaStream_t st);
+// The two halves of launch_group_ordered, for a plan made ahead of its gather
+// (ibp_group_order_plan, ibp_group_gather_decompress_planned):
+// group_gather_blocks: the gather's CTAs (at most max_per_sm per SM, 0 = as
+// many as fit), 8 warps each, one share per warp; launch_group_plan: the
+// grouping and share kernels for nw shares (stamp: NULL, or 3 words where the
+// share kernel writes {kPlanMagic, n_items, nw}); launch_group_gather: the
+// gather over g.order in g.shares.
+uint64_t group_gather_blocks(const GroupArgs& g, int sm_count, uint32_t max_per_sm);
+// CTAs per SM of a gather planned ahead: the most that leave room on each SM
+// (shared memory, registers, threads) for one CTA of the plan's grouping
+// kernel, so that the next batch's plan runs during the gather
+uint32_t group_planned_per_sm(const GroupArgs& g);
+cudaError_t launch_group_plan(GroupArgs g, const uint32_t* hist, uint32_t* wpre, uint32_t* cost,
+                              uint32_t* shares, uint32_t nw, uint32_t* stamp, cudaStream_t st);
+cudaError_t launch_group_gather(const GroupArgs& g, uint64_t blocks, cudaStream_t st);
 cudaError_t launch_encode(const EncodeArgs& a, const HostProps& hp, int sm_count,
                           cudaStream_t st);
 cudaError_t launch_pack(uint8_t* dst, uint64_t* offsets, const uint8_t* src, uint64_t slot,

@@ -1365,6 +1365,14 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
     if (threadIdx.x < IBP_MAX_GROUP_STORES / 32) s_stale[threadIdx.x] = 0u;
   }
   __syncthreads();
+  if (g.plan_stamp) {  // a plan made ahead: for this many items and shares?
+    const uint64_t nwarps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+    if (__ldg(g.plan_stamp) != kPlanMagic || __ldg(g.plan_stamp + 1) != (uint32_t)g.n_items ||
+        __ldg(g.plan_stamp + 2) != (uint32_t)nwarps) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) set_status(ent[0].status, IBP_EINVAL);
+      return;
+    }
+  }
   for (uint32_t t = threadIdx.x; t < T; t += blockDim.x)
     if (__ldg(ent[t].scal + 9) != ent[t].gen) atomicOr(&s_stale[t >> 5], 1u << (t & 31u));
 
@@ -1382,9 +1390,12 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
   const uint64_t nw = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t gw = (uint64_t)blockIdx.x * (blockDim.x >> 5) + wid;
   const bool ordered = g.order != nullptr;
-  const uint64_t r0 = g.shares ? (uint64_t)__ldg(g.shares + gw) : g.n_items * gw / nw;
-  const uint32_t cnt = (uint32_t)((g.shares ? (uint64_t)__ldg(g.shares + gw + 1)
-                                            : g.n_items * (gw + 1) / nw) - r0);
+  // (shares read from a workspace are clamped to the list)
+  const uint64_t r0 = g.shares ? min((uint64_t)__ldg(g.shares + gw), g.n_items)
+                               : g.n_items * gw / nw;
+  const uint64_t r1 = g.shares ? min((uint64_t)__ldg(g.shares + gw + 1), g.n_items)
+                               : g.n_items * (gw + 1) / nw;
+  const uint32_t cnt = (uint32_t)(r1 > r0 ? r1 - r0 : 0u);
   if (cnt == 0) return;
   auto row_index = [&](uint32_t t) -> uint64_t { return r0 + t; };  // the warp's t-th item
 
@@ -1403,6 +1414,9 @@ __global__ void __launch_bounds__(256, 3) k_gather_group(GroupArgs g) {
     pin = q < (cnt + 31u) / 32u && t < cnt && ri < g.n_items;
     if (pin) {
       pitem = ordered ? (uint64_t)__ldg(g.order + ri) : ri;
+      pin = pitem < g.n_items;  // an item of the list, as every plan makes it
+    }
+    if (pin) {
       pid = __ldg(g.ids + pitem);
       pt = (uint32_t)(pitem % T);
     }
@@ -2702,7 +2716,8 @@ static_assert(kSharePer * 256u == kOrderBuckets, "k_order_shares: whole buckets 
 // One warp per share (nw + 1 warps); each CTA first scans the bucket costs.
 __global__ void __launch_bounds__(256) k_order_shares(const uint32_t* ends, const uint32_t* cost,
                                                       const uint32_t* wpre, uint32_t nw,
-                                                      uint32_t n, uint32_t* shares) {
+                                                      uint32_t n, uint32_t* shares,
+                                                      uint32_t* stamp) {
   __shared__ unsigned long long pre[kOrderBuckets];
   __shared__ unsigned long long wsum[8];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // behind the grouping kernel
@@ -2739,7 +2754,14 @@ __global__ void __launch_bounds__(256) k_order_shares(const uint32_t* ends, cons
   const uint32_t w = blockIdx.x * 8u + wid;
   if (w > nw) return;
   if (w == nw) {
-    if (lane == 0) shares[w] = n;
+    if (lane == 0) {
+      shares[w] = n;
+      if (stamp) {  // the plan is complete once this kernel is
+        stamp[0] = kPlanMagic;
+        stamp[1] = n;
+        stamp[2] = nw;
+      }
+    }
     return;
   }
   const unsigned long long k = (unsigned long long)w * total / nw;
@@ -3128,27 +3150,87 @@ cudaError_t launch_group(const GroupArgs& g, int sm_count, cudaStream_t st) {
   return launch_group_blocks(g, group_blocks(g, sm_count, warps), warps, st);
 }
 
-cudaError_t launch_group_ordered(GroupArgs g, const uint32_t* hist, uint32_t* wpre,
-                                 uint32_t* cost, uint32_t* shares, int sm_count,
-                                 cudaStream_t st) {
+uint32_t group_planned_per_sm(const GroupArgs& g) {
+  struct Sm {
+    int dev = -1, smem = 0, regs = 0, reserved = 0, threads = 0;
+    int gather_regs = 0, group_regs = 0;
+    size_t gather_static = 0, group_static = 0;
+  };
+  static Sm c;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(g_cfg_mu);
+    if (c.dev != dev) {
+      Sm n;
+      n.dev = dev;
+      cudaDeviceGetAttribute(&n.smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+      cudaDeviceGetAttribute(&n.regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+      cudaDeviceGetAttribute(&n.reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+      cudaDeviceGetAttribute(&n.threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+      cudaFuncAttributes fa = {}, fg = {};
+      cudaFuncGetAttributes(&fa, k_gather_group);
+      cudaFuncGetAttributes(&fg, k_order_items_group);
+      cudaGetLastError();
+      n.gather_regs = fa.numRegs;
+      n.group_regs = fg.numRegs;
+      n.gather_static = fa.sharedSizeBytes;
+      n.group_static = fg.sharedSizeBytes;
+      c = n;
+    }
+  }
+  // registers are given out in units of 8 per thread
+  auto regs = [](int per_thread) { return (uint64_t)((per_thread + 7) / 8) * 8u * 256u; };
+  const size_t gsm = group_smem(g, 8);
+  const int kmax = blocks_per_sm(k_gather_group, 256, gsm);
+  const uint64_t gather_smem = gsm + c.gather_static + (uint64_t)c.reserved;
+  const uint64_t group_smem_b = kGroupSmem + c.group_static + (uint64_t)c.reserved;
+  for (int k = kmax; k > 1; --k)
+    if ((uint64_t)k * gather_smem + group_smem_b <= (uint64_t)c.smem &&
+        (uint64_t)k * regs(c.gather_regs) + regs(c.group_regs) <= (uint64_t)c.regs &&
+        (k + 1) * 256 <= c.threads)
+      return (uint32_t)k;
+  return 1u;
+}
+
+uint64_t group_gather_blocks(const GroupArgs& g, int sm_count, uint32_t max_per_sm) {
+  const uint64_t blocks = group_blocks(g, sm_count, 8);
+  const uint64_t cap = (uint64_t)sm_count * max_per_sm;
+  return max_per_sm && blocks > cap ? cap : blocks;
+}
+
+cudaError_t launch_group_plan(GroupArgs g, const uint32_t* hist, uint32_t* wpre, uint32_t* cost,
+                              uint32_t* shares, uint32_t nw, uint32_t* stamp, cudaStream_t st) {
   if (g.n_items == 0) return cudaSuccess;
-  if (g.n_items > 0xFFFFFFFFull) return cudaErrorInvalidValue;
+  if (g.n_items > 0xFFFFFFFFull || nw == 0) return cudaErrorInvalidValue;
   // sets the kernel's shared-memory limit once (cached), so the call stays
   // capturable in a CUDA graph
   blocks_per_sm(k_order_items_group, 256, kGroupSmem);
   cudaError_t e = launch_behind(k_order_items_group, kOrderBuckets, 256u, kGroupSmem, st, g.ids, hist,
                     const_cast<int64_t*>(g.order), wpre, cost);
   if (e != cudaSuccess) return e;
-  const int warps = 8;
-  const uint64_t blocks = group_blocks(g, sm_count, warps);
-  const uint32_t nw = (uint32_t)(blocks * warps);
-  e = launch_behind(k_order_shares, (nw + 1u + 7u) / 8u, 256u, 0, st, (const uint32_t*)hist,
-                    (const uint32_t*)cost, (const uint32_t*)wpre, nw, (uint32_t)g.n_items, shares);
+  return launch_behind(k_order_shares, (nw + 1u + 7u) / 8u, 256u, 0, st, (const uint32_t*)hist,
+                       (const uint32_t*)cost, (const uint32_t*)wpre, nw, (uint32_t)g.n_items,
+                       shares, stamp);
+}
+
+cudaError_t launch_group_gather(const GroupArgs& g, uint64_t blocks, cudaStream_t st) {
+  if (g.n_items == 0) return cudaSuccess;
+  // a plain launch: started early (behind the share kernel) its CTAs, sized
+  // to fill the SMs, measured 3x slower on 2 KB rows
+  return launch_group_blocks(g, blocks, 8, st);
+}
+
+cudaError_t launch_group_ordered(GroupArgs g, const uint32_t* hist, uint32_t* wpre,
+                                 uint32_t* cost, uint32_t* shares, int sm_count,
+                                 cudaStream_t st) {
+  if (g.n_items == 0) return cudaSuccess;
+  const uint64_t blocks = group_gather_blocks(g, sm_count, 0);
+  cudaError_t e =
+      launch_group_plan(g, hist, wpre, cost, shares, (uint32_t)(blocks * 8u), nullptr, st);
   if (e != cudaSuccess) return e;
   g.shares = shares;
-  // the gather is a plain launch: started early (behind the share kernel) its
-  // CTAs, sized to fill the SMs, measured 3x slower on 2 KB rows
-  return launch_group_blocks(g, blocks, warps, st);
+  return launch_group_gather(g, blocks, st);
 }
 
 cudaError_t launch_link_copy(uint4* dst, const uint4* src, uint64_t nvec, int sm_count,

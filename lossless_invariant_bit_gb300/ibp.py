@@ -58,6 +58,8 @@ _SIGS = {
     "ibp_gather_decompress_ordered": [_P, _P, _U64, _P, _P, _P, _U64, _P, _U64, _P],
     "ibp_store_set_lengths": [_P, _P],
     "ibp_group_gather_decompress_ordered": [_P, _P, _U64, _P, _U64, _P, _U64, _P],
+    "ibp_group_order_plan": [_P, _P, _U64, _P, _U64, _P],
+    "ibp_group_gather_decompress_planned": [_P, _P, _U64, _P, _U64, _P, _U64, _P],
     "ibp_gather_decompress_split": [_P, _P, _U64, _U64, _U64, _U64, _P, _P, _P, _U64, _P],
     "ibp_group_create": [ctypes.POINTER(ctypes.c_void_p), _P, _P, _U32],
     "ibp_group_destroy": [_P],
@@ -255,6 +257,21 @@ def ibp_group_gather_decompress_ordered(group: int, dst, dst_row_stride: int, id
                                                              _ptr(ids), batch, _ptr(workspace),
                                                              workspace_bytes, _stream(stream)),
            "ibp_group_gather_decompress_ordered")
+
+
+def ibp_group_order_plan(group: int, ids, batch: int, workspace, workspace_bytes: int,
+                         stream=None) -> None:
+    _check(_lib_handle().ibp_group_order_plan(group, _ptr(ids), batch, _ptr(workspace),
+                                              workspace_bytes, _stream(stream)),
+           "ibp_group_order_plan")
+
+
+def ibp_group_gather_decompress_planned(group: int, dst, dst_row_stride: int, ids, batch: int,
+                                        workspace, workspace_bytes: int, stream=None) -> None:
+    _check(_lib_handle().ibp_group_gather_decompress_planned(group, _ptr(dst), dst_row_stride,
+                                                             _ptr(ids), batch, _ptr(workspace),
+                                                             workspace_bytes, _stream(stream)),
+           "ibp_group_gather_decompress_planned")
 
 
 def ibp_gather_decompress_cached(store: int, dst, dst_stride_bytes: int, host_src, cache_src,

@@ -73,6 +73,9 @@ def test_host_side_argument_checks(lib):
     assert lib.ibp_group_create(ctypes.byref(grp), None, None, 1) == ibp.IBP_EINVAL
     assert lib.ibp_group_create(None, 16, 16, 1) == ibp.IBP_EINVAL
     assert lib.ibp_group_gather_decompress(None, 16, 512, 16, 1, None) == ibp.IBP_EINVAL
+    assert lib.ibp_group_order_plan(None, 16, 1, 16, 65556, None) == ibp.IBP_EINVAL
+    assert lib.ibp_group_gather_decompress_planned(None, 16, 512, 16, 1, 16, 65556,
+                                                   None) == ibp.IBP_EINVAL
     assert lib.ibp_group_destroy(None) == ibp.IBP_OK
     num = (ctypes.c_uint32 * 1)(95)
     den = (ctypes.c_uint32 * 1)(100)

@@ -330,6 +330,106 @@ def test_group_ordered_repeats_large_buckets_and_errors():
             s.close()
 
 
+def test_group_planned_gathers():
+    """A plan made ahead (ibp_group_order_plan) and its gather
+    (ibp_group_gather_decompress_planned) write the plain group gather's
+    bytes and status codes, an out-of-range id included:
+    - on one stream;
+    - three batches pipelined over two streams and two workspaces, each
+      batch's plan made while the previous batch is gathered;
+    - with a plan made for other ids of the same size (the rows are right);
+    - a workspace holding no plan, or a plan for another batch size: the
+      gather writes nothing and store 0 reports IBP_EINVAL."""
+    R, C, N, B = 512, 1024, 4000, 1500
+    stores, slots, tables = [], [], []
+    try:
+        for t in range(5):
+            rb = rows_u8(wl.dlrm_rows(N, R // 4, table=t, seed=61))
+            st, sl = _host_store(R, C, rb, wl.sample_ids(N, 50, seed=t), host=(t != 2))
+            stores.append(st)
+            slots.append(sl)
+            tables.append(rb)
+        T = len(stores)
+        batches = []
+        for k in range(3):
+            ids = np.stack([wl.zipf_ids(B, N, table=t, seed=62 + k) for t in range(T)], axis=1)
+            batches.append(ids)
+        batches[1][9, 3] = N + 2  # out of range in store 3
+        grp = ibp.ibp_group_create([s.h for s in stores], slots)
+        try:
+            wsb = ibp.order_workspace_bytes(B * T)
+            ws = [torch.zeros(wsb, dtype=torch.uint8, device=DEV) for _ in range(2)]
+            dev_ids = [to_dev(x) for x in batches]
+            refs, codes = [], []
+            for x in dev_ids:
+                ref = torch.full((B, T, R), 0xCC, dtype=torch.uint8, device=DEV)
+                ibp.ibp_group_gather_decompress(grp, ref, T * R, x, B)
+                refs.append(ref)
+                codes.append([s.status() for s in stores])
+            assert codes[1][3] == ibp.IBP_ERANGE and codes[0] == [ibp.IBP_OK] * T
+            # one stream
+            out = torch.full((B, T, R), 0x33, dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_order_plan(grp, dev_ids[1], B, ws[0], wsb)
+            ibp.ibp_group_gather_decompress_planned(grp, out, T * R, dev_ids[1], B, ws[0], wsb)
+            assert [s.status() for s in stores] == codes[1]
+            assert torch.equal(out, refs[1])
+            # pipelined: batch k+1 planned on a second stream while batch k is gathered
+            gs, ps = torch.cuda.Stream(), torch.cuda.Stream()
+            outs = [torch.full((B, T, R), 0x33, dtype=torch.uint8, device=DEV) for _ in range(3)]
+            planned = [torch.cuda.Event() for _ in range(3)]
+            gathered = [torch.cuda.Event() for _ in range(3)]
+            gs.wait_stream(torch.cuda.current_stream())
+            ps.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(ps):
+                ibp.ibp_group_order_plan(grp, dev_ids[0], B, ws[0], wsb, ps)
+                planned[0].record(ps)
+            for k in range(3):
+                with torch.cuda.stream(gs):
+                    gs.wait_event(planned[k])
+                    ibp.ibp_group_gather_decompress_planned(grp, outs[k], T * R, dev_ids[k], B,
+                                                            ws[k % 2], wsb, gs)
+                    gathered[k].record(gs)
+                if k + 1 < 3:
+                    with torch.cuda.stream(ps):
+                        if k >= 1:
+                            ps.wait_event(gathered[k - 1])  # its workspace is free again
+                        ibp.ibp_group_order_plan(grp, dev_ids[k + 1], B, ws[(k + 1) % 2], wsb, ps)
+                        planned[k + 1].record(ps)
+            torch.cuda.synchronize()
+            for k in range(3):
+                assert torch.equal(outs[k], refs[k]), k
+            assert [s.status() for s in stores] == [max(c) for c in zip(*codes)]
+            # a plan for batch 0's ids, gathered with batch 2's: right rows
+            ibp.ibp_group_order_plan(grp, dev_ids[0], B, ws[0], wsb)
+            out.fill_(0x33)
+            ibp.ibp_group_gather_decompress_planned(grp, out, T * R, dev_ids[2], B, ws[0], wsb)
+            assert [s.status() for s in stores] == [ibp.IBP_OK] * T
+            assert torch.equal(out, refs[2])
+            o = out.cpu().numpy()
+            for t in range(T):
+                assert np.array_equal(o[:, t], tables[t][batches[2][:, t]]), t
+            # no plan in the workspace, or one for another batch size
+            fresh = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+            other = torch.zeros(ibp.order_workspace_bytes(B * T), dtype=torch.uint8, device=DEV)
+            ibp.ibp_group_order_plan(grp, dev_ids[0][:B - 100].contiguous(), B - 100, other,
+                                     other.numel())
+            for w in (fresh, other):
+                out.fill_(0x33)
+                ibp.ibp_group_gather_decompress_planned(grp, out, T * R, dev_ids[2], B, w, wsb)
+                assert stores[0].status() == ibp.IBP_EINVAL
+                assert [s.status() for s in stores[1:]] == [ibp.IBP_OK] * (T - 1)
+                assert bool((out == 0x33).all())
+            with pytest.raises(ibp.IbpError) as e:
+                ibp.ibp_group_gather_decompress_planned(grp, out, T * R, dev_ids[2], B, ws[0],
+                                                        wsb - 16)
+            assert e.value.status == ibp.IBP_EINVAL
+        finally:
+            ibp.ibp_group_destroy(grp)
+    finally:
+        for s in stores:
+            s.close()
+
+
 @pytest.mark.parametrize("B", [16384, 20000])
 def test_group_ordered_large_batches(B):
     """Batches of 16384 and 20000 rows over two stores (one in host memory,
