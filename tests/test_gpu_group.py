@@ -508,7 +508,8 @@ def test_ordered_group_and_packed_decode_in_a_cuda_graph():
     """The ordered group gather (five kernels chained by programmatic
     dependent launch, then the gather) and the packed-cache decode (bulk
     copies on mbarriers) captured once in a CUDA graph and replayed with new
-    lookups: every replay returns the rows."""
+    lookups: every replay returns the rows.  So does a captured plan made
+    ahead with its planned gather."""
     R, C, N, B, T = 512, 1024, 3000, 700, 3
     stores, slots, tables = [], [], []
     try:
@@ -563,6 +564,30 @@ def test_ordered_group_and_packed_decode_in_a_cuda_graph():
                 for t in range(T):
                     assert np.array_equal(o[:, t], tables[t][z[:, t]]), (step, t)
                 assert np.array_equal(dec.cpu().numpy(), tables[0]), step
+            # a plan made ahead and its gather, captured after one uncaptured pair
+            with torch.cuda.stream(side):
+                ibp.ibp_group_order_plan(grp, ids, B, ws, ws.numel(), side)
+                ibp.ibp_group_gather_decompress_planned(grp, out, T * R, ids, B, ws, ws.numel(),
+                                                        side)
+            torch.cuda.synchronize()
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2):
+                sp = torch.cuda.current_stream()
+                ibp.ibp_group_order_plan(grp, ids, B, ws, ws.numel(), sp)
+                ibp.ibp_group_gather_decompress_planned(grp, out, T * R, ids, B, ws, ws.numel(),
+                                                        sp)
+            for step in range(2):
+                z = np.stack([wl.zipf_ids(B, N, table=t, seed=50 + step) for t in range(T)],
+                             axis=1)
+                ids.copy_(torch.from_numpy(z))
+                out.zero_()
+                g2.replay()
+                torch.cuda.synchronize()
+                for s in stores:
+                    assert s.status() == ibp.IBP_OK, step
+                o = out.cpu().numpy()
+                for t in range(T):
+                    assert np.array_equal(o[:, t], tables[t][z[:, t]]), (step, t)
         finally:
             ibp.ibp_group_destroy(grp)
     finally:
