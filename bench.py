@@ -1466,6 +1466,30 @@ def run_dlrm(args, rank, world, torch, dist):
     torch.cuda.synchronize()
     piped_same = bool(torch.equal(out_p, out_o))
     ptimes = [a.elapsed_time(c) / 1e3 for a, c in pev]
+    # the step's parts timed apart (each with the L2 flushed before it): the
+    # planned gather alone (its plan made once), the plan alone, and plan then
+    # gather on one stream
+    ibp.ibp_group_order_plan(grp, ids2d[0], B, pws[0], wsb, sp)
+    parts = {"gather_alone_us": [], "plan_alone_us": [], "plan_then_gather_us": []}
+    for name in parts:
+        for b in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if name != "gather_alone_us":
+                ibp.ibp_group_order_plan(grp, ids2d[b % pool], B, pws[0], wsb, sp)
+            if name != "plan_alone_us":
+                bb = 0 if name == "gather_alone_us" else b % pool
+                ibp.ibp_group_gather_decompress_planned(grp, out_p, Tn * R, ids2d[bb], B, pws[0],
+                                                        wsb, sp)
+            e1.record(stream)
+            parts[name].append((e0, e1))
+    torch.cuda.synchronize()
+    for st in stores:
+        assert ibp.ibp_stream_status(st, reset=True) == ibp.IBP_OK
+    parts = {k: round(statistics.mean(a.elapsed_time(c) * 1e3 for a, c in v), 1)
+             for k, v in parts.items()}
+    parts["pipelined_step_us"] = round(statistics.mean(ptimes) * 1e6, 1)
     # cpu_baseline leg: the oracle decodes sampled lookups of the last batch in
     # three tables from the same host slots; its rows must equal the GPU's and
     # the tables' rows, and its compression of those rows the stored bytes
@@ -1534,6 +1558,7 @@ def run_dlrm(args, rank, world, torch, dist):
                              "note": "ibp_group_gather_decompress_ordered: each batch planned "
                                      "and gathered in one call on one stream"},
         "pipelined_same_rows_as_one_call": piped_same,
+        "pipeline_parts": parts,
         "per_store_launches": {"value": round(per_store_gbs, 3), "unit": "GB/s",
                                "launches_per_step": Tn,
                                "note": "26 ibp_gather_decompress_strided calls per batch"},
@@ -2289,7 +2314,7 @@ def main():
             d = {k_: r[k_] for k_ in keep if k_ in r}
             d["config"] = r["config"]
             for k_ in ("parity_all_lookups_ok", "parity_layer0_ok", "chunks", "fused_unordered",
-                       "ordered_one_call", "pipelined_same_rows_as_one_call",
+                       "ordered_one_call", "pipelined_same_rows_as_one_call", "pipeline_parts",
                        "per_store_launches", "ratio_distinct_rows", "raw_gather_gbs",
                        "attention_layout", "decode_steps", "decode_projection",
                        "raw_gather_per_table", "packed_host_store"):
