@@ -305,6 +305,9 @@ IBP_API ibp_status ibp_group_gather_decompress_ordered(const ibp_group* group, v
  * workspace holds no plan for batch*T items writes nothing and sets
  * IBP_EINVAL in the status word of the group's first store; a plan made for
  * other ids of the same size still gives the right rows, in a worse order.
+ * Like the group's other calls, both may be captured into a CUDA graph once
+ * an uncaptured pair has run on the device (it sets the kernels' shared-memory
+ * limits and reads their resources).
  * Errors: as ibp_group_gather_decompress_ordered. */
 IBP_API ibp_status ibp_group_order_plan(const ibp_group* group, const int64_t* ids,
                                         uint64_t batch, void* workspace,
